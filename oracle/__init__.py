@@ -1,0 +1,147 @@
+"""Dense GEMM oracle (test infrastructure only).
+
+A plain, slow, obviously correct C = A.B in double precision, compiled from
+``gemm_oracle.c`` with gcc and reached through ctypes.  Only ``tests/``, the
+smoke check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may
+import this package; the product library never does, and this package imports
+nothing from it.
+
+What it computes: "Shared memory and tensor cores" (ml-compiler-from-scratch
+ch. 13) section 13.1 defines the GEMM as C = A @ B with 2*M*N*K flops; section
+13.8 fixes that tensor-core products are exact and sums are FP32.  The oracle
+forms the same exact products and sums them in fp64 (k ascending), so it is at
+least as accurate as any path under test.  BF16 inputs are passed as their raw
+16-bit patterns and widened exactly.
+
+Every function also returns D[i, j] = sum_k |A[i, k]| * |B[k, j]| on request,
+the per-entry scale used by the acceptance test max|C - C_ref| / D.
+
+Pins (tests/test_oracle.py): identity and permutation products, all-ones inputs
+(C == K everywhere), small-integer inputs against exact integer arithmetic, a
+second independent loop order at tiny sizes, float64 library matmul, and the
+BF16 widening against the library's own conversion.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libgemm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_ptr = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc, OpenMP, no -march flags)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+               "-std=c11", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        full = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
+        rows = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]
+        jik = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
+        for name, args in (("oracle_gemm_f32", full), ("oracle_gemm_bf16", full),
+                           ("oracle_gemm_rows_f32", rows), ("oracle_gemm_rows_bf16", rows),
+                           ("oracle_gemm_f32_jik", jik), ("oracle_gemm_bf16_jik", jik),
+                           ("oracle_widen_bf16", [_ptr, _ptr, _i64])):
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Host threads the oracle's OpenMP loops use."""
+    return int(_load().oracle_num_threads())
+
+
+def _as_operand(x: np.ndarray, bf16: bool) -> np.ndarray:
+    want = np.uint16 if bf16 else np.float32
+    if x.dtype != want:
+        raise TypeError(f"oracle operand must be {want.__name__}, got {x.dtype}")
+    if x.ndim != 2 or (x.size > 0 and x.shape[1] > 1 and x.strides[1] != x.itemsize):
+        raise ValueError("oracle operands are row-major 2-D arrays with unit inner stride")
+    return x
+
+
+def _ld(x: np.ndarray) -> int:
+    return x.strides[0] // x.itemsize if (x.shape[0] > 1 and x.size > 0) else max(x.shape[1], 1)
+
+
+def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = False):
+    """C = A.B in fp64 (and D = |A|.|B| if with_scale).
+
+    A: M x K, B: K x N, row-major, float32 or (bf16=True) uint16 BF16 patterns.
+    """
+    _as_operand(A, bf16), _as_operand(B, bf16)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    C = np.empty((M, N), np.float64)
+    D = np.empty((M, N), np.float64) if with_scale else None
+    fn = _load().oracle_gemm_bf16 if bf16 else _load().oracle_gemm_f32
+    fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), C.ctypes.data, max(N, 1),
+       D.ctypes.data if D is not None else None, max(N, 1))
+    return (C, D) if with_scale else C
+
+
+def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False):
+    """Rows `rows` of C = A.B and of D = |A|.|B|, each len(rows) x N, fp64."""
+    _as_operand(A, bf16), _as_operand(B, bf16)
+    M, K = A.shape
+    N = B.shape[1]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if r.size and (r.min() < 0 or r.max() >= M):
+        raise IndexError("row index out of range")
+    C = np.empty((r.size, N), np.float64)
+    D = np.empty((r.size, N), np.float64)
+    fn = _load().oracle_gemm_rows_bf16 if bf16 else _load().oracle_gemm_rows_f32
+    fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), r.ctypes.data, r.size,
+       C.ctypes.data, D.ctypes.data)
+    return C, D
+
+
+def gemm_jik(A: np.ndarray, B: np.ndarray, bf16: bool = False) -> np.ndarray:
+    """The same product with the j-i-k loop order (tiny sizes only)."""
+    _as_operand(A, bf16), _as_operand(B, bf16)
+    M, K = A.shape
+    N = B.shape[1]
+    C = np.empty((M, N), np.float64)
+    fn = _load().oracle_gemm_bf16_jik if bf16 else _load().oracle_gemm_f32_jik
+    fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), C.ctypes.data, max(N, 1))
+    return C
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """Exact value of each BF16 pattern, as fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_widen_bf16(b.ctypes.data, out.ctypes.data, b.size)
+    return out

@@ -1,0 +1,176 @@
+/*
+ * Dense GEMM oracle: C = A . B computed the plain way, in double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or
+ * calls this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark load it.  It shares no source with the CUDA path.
+ *
+ * What it computes follows "Shared memory and tensor cores" (ml-compiler-from-
+ * scratch ch. 13), section 13.1: a GEMM C = A @ B is 2*M*N*K floating-point
+ * operations, one multiply and one add per (i, j, k) triple, and nothing else.
+ * Section 13.8 of the same page fixes the precision contract of the tensor-core
+ * paths: products of the narrow inputs are formed exactly and summed in FP32.
+ * This oracle is stricter: every product of two FP32 or BF16 values is exact in
+ * IEEE double (24 + 24 significand bits < 53), and the sums are done in double,
+ * so the only rounding is that of a double-precision running sum.
+ *
+ * Layout: every matrix is row-major with a leading dimension in ELEMENTS
+ * (A is M x K with lda >= K, B is K x N with ldb >= N, C is M x N with ldc >= N).
+ * BF16 operands arrive as their raw 16-bit patterns and are widened exactly
+ * (a BF16 value is the top half of the FP32 with the same sign, exponent and
+ * first 7 mantissa bits).
+ *
+ * Besides C, every entry point can also return D[i][j] = sum_k |A[i][k]|*|B[k][j]|,
+ * the scale against which an error in C[i][j] is judged (max |dC| / D).
+ *
+ * Loop orders: the main routine runs i-k-j with a per-row accumulator and an
+ * OpenMP loop over rows.  A second, independent j-i-k routine exists only so the
+ * tests can brute-force one loop order against the other at tiny sizes.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no -march flags, so
+ * x86 and Arm hosts give the same bits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double widen_bf16(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One output row i of C (and optionally of D), k ascending, fp64 sums.
+ * a_at(k) and b_row(k) are expressed by the two element types below. */
+static void row_f32(int64_t i, int64_t N, int64_t K, const float *A, int64_t lda,
+                    const float *B, int64_t ldb, double *c, double *d)
+{
+    for (int64_t j = 0; j < N; ++j) c[j] = 0.0;
+    if (d) for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = (double)A[i * lda + k];
+        const float *b = B + k * ldb;
+        for (int64_t j = 0; j < N; ++j) c[j] += a * (double)b[j];
+        if (d) {
+            const double aa = fabs(a);
+            for (int64_t j = 0; j < N; ++j) d[j] += aa * fabs((double)b[j]);
+        }
+    }
+}
+
+static void row_bf16(int64_t i, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                     const uint16_t *B, int64_t ldb, double *c, double *d, double *bw)
+{
+    for (int64_t j = 0; j < N; ++j) c[j] = 0.0;
+    if (d) for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = widen_bf16(A[i * lda + k]);
+        const uint16_t *b = B + k * ldb;
+        for (int64_t j = 0; j < N; ++j) bw[j] = widen_bf16(b[j]);
+        for (int64_t j = 0; j < N; ++j) c[j] += a * bw[j];
+        if (d) {
+            const double aa = fabs(a);
+            for (int64_t j = 0; j < N; ++j) d[j] += aa * fabs(bw[j]);
+        }
+    }
+}
+
+/* Full C (M x N, leading dimension ldc) and optional D (leading dimension ldd). */
+void oracle_gemm_f32(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda, const float *B, int64_t ldb,
+                     double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i)
+        row_f32(i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL);
+}
+
+void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                      const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                      double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    #pragma omp parallel
+    {
+        double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i)
+            row_bf16(i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL, bw);
+        free(bw);
+    }
+}
+
+/* Only the rows listed in rows[0..nrows): C and D are dense nrows x N outputs.
+ * Used to check full-size problems where the whole product would take too long. */
+void oracle_gemm_rows_f32(int64_t M, int64_t N, int64_t K,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r)
+        row_f32(rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL);
+}
+
+void oracle_gemm_rows_bf16(int64_t M, int64_t N, int64_t K,
+                           const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                           const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    #pragma omp parallel
+    {
+        double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r)
+            row_bf16(rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL, bw);
+        free(bw);
+    }
+}
+
+/* Second loop order (j outer, then i, then k), single-threaded, for brute-force
+ * self-checks of the routine above on tiny sizes. */
+void oracle_gemm_f32_jik(int64_t M, int64_t N, int64_t K,
+                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                         double *C, int64_t ldc)
+{
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t i = 0; i < M; ++i) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                s += (double)A[i * lda + k] * (double)B[k * ldb + j];
+            C[i * ldc + j] = s;
+        }
+}
+
+void oracle_gemm_bf16_jik(int64_t M, int64_t N, int64_t K,
+                          const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                          double *C, int64_t ldc)
+{
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t i = 0; i < M; ++i) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                s += widen_bf16(A[i * lda + k]) * widen_bf16(B[k * ldb + j]);
+            C[i * ldc + j] = s;
+        }
+}
+
+/* Exact widening of n BF16 patterns, exposed so the tests can pin it. */
+void oracle_widen_bf16(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = widen_bf16(src[i]);
+}

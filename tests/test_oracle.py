@@ -1,0 +1,136 @@
+"""Pins for the fp64 GEMM oracle, each against something other than itself.
+
+No GPU.  Every check here is fixed by the mathematics of C = A.B ("Shared
+memory and tensor cores", ml-compiler-from-scratch ch. 13, section 13.1) or by
+an independent library routine: identity and permutation products, all-ones
+inputs, exact integer arithmetic, a second loop order, float64 matmul, and the
+library's own BF16 conversion.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array, make_operands
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _bf16_bits(x_float):
+    t = torch.as_tensor(np.asarray(x_float, dtype=np.float32)).to(torch.bfloat16)
+    return as_oracle_array(t).copy()
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (7, 13), (64, 33)])
+def test_identity_left(M, N):
+    rng = np.random.default_rng(1)
+    B = _f32(rng.standard_normal((M, N)))
+    C = oracle.gemm(np.eye(M, dtype=np.float32), B)
+    assert np.array_equal(C, B.astype(np.float64))
+
+
+def test_identity_right():
+    rng = np.random.default_rng(2)
+    A = _f32(rng.standard_normal((19, 23)))
+    C = oracle.gemm(A, np.eye(23, dtype=np.float32))
+    assert np.array_equal(C, A.astype(np.float64))
+
+
+def test_permutation():
+    rng = np.random.default_rng(3)
+    M, N = 37, 29
+    perm = rng.permutation(M)
+    P = np.zeros((M, M), np.float32)
+    P[np.arange(M), perm] = 1.0          # row i of P selects row perm[i] of B
+    B = _f32(rng.uniform(-1, 1, (M, N)))
+    C = oracle.gemm(P, B)
+    assert np.array_equal(C, B[perm].astype(np.float64))
+    # and the transposed permutation undoes it: a transposed-operand bug fails here
+    C2 = oracle.gemm(_f32(P.T), _f32(C))
+    assert np.array_equal(C2, B.astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (5, 9, 17), (33, 65, 129), (16, 16, 4096)])
+def test_all_ones_gives_K(M, N, K):
+    C, D = oracle.gemm(np.ones((M, K), np.float32), np.ones((K, N), np.float32), with_scale=True)
+    assert np.all(C == K) and np.all(D == K)
+
+
+def test_small_integers_exact_vs_integer_matmul():
+    rng = np.random.default_rng(4)
+    M, N, K = 45, 38, 300
+    Ai = rng.integers(-8, 9, (M, K))
+    Bi = rng.integers(-8, 9, (K, N))
+    C, D = oracle.gemm(_f32(Ai), _f32(Bi), with_scale=True)
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(D, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+def test_small_integers_exact_bf16():
+    rng = np.random.default_rng(5)
+    M, N, K = 31, 40, 257
+    Ai = rng.integers(-8, 9, (M, K))
+    Bi = rng.integers(-8, 9, (K, N))
+    C = oracle.gemm(_bf16_bits(Ai), _bf16_bits(Bi), bf16=True)
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (17, 16, 15), (16, 17, 17)])
+def test_second_loop_order_bit_equal(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    A = _f32(rng.standard_normal((M, K)))
+    B = _f32(rng.standard_normal((K, N)))
+    assert np.array_equal(oracle.gemm(A, B), oracle.gemm_jik(A, B))
+    Ab, Bb = _bf16_bits(A), _bf16_bits(B)
+    assert np.array_equal(oracle.gemm(Ab, Bb, bf16=True), oracle.gemm_jik(Ab, Bb, bf16=True))
+
+
+def test_against_float64_library_matmul():
+    rng = np.random.default_rng(6)
+    A = _f32(rng.standard_normal((64, 80)))
+    B = _f32(rng.standard_normal((80, 48)))
+    C, D = oracle.gemm(A, B, with_scale=True)
+    ref = (torch.from_numpy(A).double() @ torch.from_numpy(B).double()).numpy()
+    assert np.max(np.abs(C - ref) / D) < 1e-14
+
+
+def test_bf16_widening_matches_library_conversion():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen_bf16(bits)
+    lib = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], lib[~nan])
+    # a few fixed patterns: 1.0, -2.0, the largest finite value, +inf
+    assert list(oracle.widen_bf16(np.array([0x3F80, 0xC000, 0x7F7F, 0x7F80], np.uint16))) == [
+        1.0, -2.0, float(np.float32(3.3895313892515355e38)), float("inf")]
+
+
+def test_leading_dimensions_honoured():
+    A, B = make_operands(21, 18, 27, "fp32", "ints", 7, lda_pad=5, ldb_pad=3)
+    a, b = as_oracle_array(A), as_oracle_array(B)
+    assert a.strides[0] == (27 + 5) * 4 and b.strides[0] == (18 + 3) * 4
+    C = oracle.gemm(a, b)                 # the NaN padding must never be read
+    assert np.all(np.isfinite(C))
+    assert np.array_equal(C, np.ascontiguousarray(a).astype(np.int64) @ np.ascontiguousarray(b).astype(np.int64))
+
+
+def test_rows_variant_matches_full():
+    A, B = make_operands(50, 40, 60, "bf16", "normal", 8)
+    a, b = as_oracle_array(A), as_oracle_array(B)
+    C, D = oracle.gemm(a, b, bf16=True, with_scale=True)
+    rows = [0, 7, 49, 23]
+    Cr, Dr = oracle.gemm_rows(a, b, rows, bf16=True)
+    assert np.array_equal(Cr, C[rows]) and np.array_equal(Dr, D[rows])
+
+
+def test_empty_sum_and_empty_shapes():
+    C = oracle.gemm(np.zeros((4, 0), np.float32), np.zeros((0, 6), np.float32))
+    assert C.shape == (4, 6) and np.all(C == 0)
+    assert oracle.gemm(np.zeros((0, 3), np.float32), np.zeros((3, 5), np.float32)).shape == (0, 5)
+
+
+def test_threads_reported():
+    assert oracle.num_threads() >= 1

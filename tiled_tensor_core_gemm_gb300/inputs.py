@@ -1,0 +1,105 @@
+"""Seeded synthetic operands for the GEMM workloads.
+
+This module only draws random numbers and lays them out; it holds none of the
+GEMM's arithmetic, so both the CUDA path and the oracle can be fed from it.
+
+Recipe (the workloads are synthetic square and ragged GEMMs, as in the
+"Learn CuTeDSL" TFLOPS table and the ch. 13 traffic table):
+
+* one CPU ``torch.Generator`` seeded with the workload's seed; A (M x K) is
+  drawn first, then B (K x N), from the same generator;
+* ``uniform`` is U[-1, 1) = 2*rand - 1, ``normal`` is N(0, 1) via randn;
+* for BF16 operands the FP32 draw is rounded once to BF16 (round to nearest
+  even, the library's own ``.to(torch.bfloat16)``); those BF16 values are the
+  ground truth for every check;
+* ``ints`` draws integers uniformly from [-lo_hi, lo_hi], for the exactness
+  tests (every product and partial sum is then an exact small integer).
+
+Every array is row-major; ``ld_pad`` adds unused trailing columns so the
+leading dimension exceeds the logical width (the padding is filled with NaN so
+any read of it shows up in the result).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: str          # "fp32" | "tf32" | "bf16"  (the arithmetic path)
+    dist: str           # "uniform" | "normal"
+    seed: int
+
+
+# The five published workloads (shapes, distributions and seeds as stated there).
+C1_FP32_256 = Workload("fp32 256^3 U[-1,1] seed 0", 256, 256, 256, "fp32", "uniform", 0)
+C2_FP32_1024 = Workload("fp32 1024^3 U[-1,1] seed 1", 1024, 1024, 1024, "fp32", "uniform", 1)
+C2_TF32_1024 = Workload("tf32 1024^3 U[-1,1] seed 1", 1024, 1024, 1024, "tf32", "uniform", 1)
+C3_FP32_4096 = Workload("fp32 4096^3 N(0,1) seed 2", 4096, 4096, 4096, "fp32", "normal", 2)
+C3_TF32_4096 = Workload("tf32 4096^3 N(0,1) seed 2", 4096, 4096, 4096, "tf32", "normal", 2)
+C4_BF16_8192 = Workload("bf16 8192^3 N(0,1) seed 3", 8192, 8192, 8192, "bf16", "normal", 3)
+C5_BF16_RAGGED = tuple(
+    Workload(f"bf16 {m}x{n}x{k} U[-1,1] seed 4", m, n, k, "bf16", "uniform", 4)
+    for (m, n, k) in ((1000, 1000, 1000), (4097, 4095, 4099), (16384, 1024, 4096), (128, 8192, 8192))
+)
+
+
+def _draw(gen: torch.Generator, shape, dist: str, lo_hi: int = 8) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32)
+    if dist == "ints":
+        return torch.randint(-lo_hi, lo_hi + 1, shape, generator=gen).to(torch.float32)
+    if dist == "ones":
+        return torch.ones(shape, dtype=torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _pad(x: torch.Tensor, ld_pad: int) -> torch.Tensor:
+    if ld_pad == 0:
+        return x
+    rows, cols = x.shape
+    big = torch.full((rows, cols + ld_pad), float("nan"), dtype=x.dtype)
+    big[:, :cols] = x
+    return big[:, :cols]
+
+
+def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
+                  lda_pad: int = 0, ldb_pad: int = 0, lo_hi: int = 8):
+    """(A, B) as CPU torch tensors: float32 for fp32/tf32, bfloat16 for bf16.
+
+    The tensors may be views with a leading dimension larger than their width
+    (``*_pad``); use ``.stride(0)`` for the leading dimension.
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    a = _draw(gen, (M, K), dist, lo_hi)
+    b = _draw(gen, (K, N), dist, lo_hi)
+    if dtype == "bf16":
+        a = a.to(torch.bfloat16)
+        b = b.to(torch.bfloat16)
+    elif dtype not in ("fp32", "tf32"):
+        raise ValueError(f"unknown dtype {dtype!r}")
+    return _pad(a, lda_pad), _pad(b, ldb_pad)
+
+
+def workload_operands(w: Workload):
+    return make_operands(w.M, w.N, w.K, w.dtype, w.dist, w.seed)
+
+
+def as_oracle_array(t: torch.Tensor) -> np.ndarray:
+    """A CPU tensor as the numpy array the oracle takes (float32, or uint16 BF16 bits)."""
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(f"unsupported operand dtype {t.dtype}")
