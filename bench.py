@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the GEMM library on GB300.
+
+One step = one C = A.B through the C ABI (gemm_run) on the headline workload,
+a BF16-input GEMM with M = N = K = 8192 (N(0,1) operands rounded to BF16, seed
+3, FP32 accumulation and output) on the persistent tcgen05 path.  The FP32
+SIMT and TF32 tensor-core paths are timed on the 4096^3 FP32 workload in the
+same run and reported under "paths".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
+independent replica of the same GEMM (the path has no exchange step); value
+= all ranks' flops / the slowest rank's time.  --impl reference times the
+fp64 oracle on the host cores on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s at 4096³/8192³ (FP32, TF32, BF16) and % of GB300 dense peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129e6
+NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0}   # GB300 per-GPU dense, nominal
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers ---
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "sm_max_mhz")}, \
+            "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
+
+
+def source_digest() -> str:
+    """Digest of the kernel sources; profile figures taken from an older build are not reused."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_tensor_core_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[key]
+        if d.get("source_digest") == source_digest():
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling around a timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5
+            while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+                time.sleep(0.02)
+        except Exception:
+            self.proc = None
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        with open(self.file.name) as f:
+            text = f.read()
+        os.unlink(self.file.name)
+        rows = []
+        for r in csv.reader(io.StringIO(text)):
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(r[2]), float(r[3]), float(r[4]), [x.strip() for x in r[5:10]]))
+            except Exception:
+                continue
+        if not rows:
+            return None
+        inside = [x for x in rows if self.t0 - 1 <= x[0] <= self.t1 + 1] or rows
+        reasons = set()
+        names = ("active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for x in inside:
+            for name, val in zip(names[1:], x[4][1:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max(x[2] for x in inside),
+                "power_w_max": max(x[3] for x in inside), "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def gpu_uuid(dev) -> str | None:
+    try:
+        import torch
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ our timing ---
+def make_device_operands(workload, device):
+    from tiled_tensor_core_gemm_gb300.inputs import workload_operands
+    A, B = workload_operands(workload)
+    return A, B, A.to(device), B.to(device)
+
+
+def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=None, on_end=None):
+    """Device-side timing with CUDA events on `stream`: per-launch events for the
+    kernel's average duration, and one pair around all K steps."""
+    import torch
+    _, _, A, B = make_device_operands(workload, device)
+    M, N, K = workload.M, workload.N, workload.K
+    C = torch.empty((M, N), dtype=torch.float32, device=device)
+    code = tg.DTYPES[workload.dtype]
+    s = stream.cuda_stream
+    plan = tg.gemm_plan(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N).as_dict()
+
+    def run():
+        rc = tg.gemm_run(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s)
+        if rc != tg.GEMM_OK:
+            raise RuntimeError(tg.gemm_last_error())
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+        stream.synchronize()
+        st = tg.gemm_get_status(s)
+        if st != tg.GEMM_OK:
+            raise RuntimeError(f"warm-up status {st}: {tg.gemm_last_error()}")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if on_begin:
+            on_begin()
+        e0.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            run()
+            b.record(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if on_end:
+            on_end()
+        if dist is not None:
+            dist.barrier()
+    total_ms = e0.elapsed_time(e1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    st = tg.gemm_get_status(s)
+    if st != tg.GEMM_OK:
+        raise RuntimeError(f"timed-region status {st}: {tg.gemm_last_error()}")
+    launches = 1 + plan["pack_a"] + plan["pack_b"] if plan["path"] == 1 else 1
+    return {"total_ms": total_ms, "launch_ms_mean": statistics.mean(launch_ms),
+            "launch_ms_median": statistics.median(launch_ms), "launch_ms_min": min(launch_ms),
+            "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K}
+
+
+def time_e2e(tg, workload, steps, stream, device):
+    """Same GEMM through gemm_run with the operands in pinned host memory: each
+    step copies A and B host->device, runs, and copies C device->host."""
+    import torch
+    from tiled_tensor_core_gemm_gb300.inputs import workload_operands
+    A_h, B_h = workload_operands(workload)
+    A_h, B_h = A_h.pin_memory(), B_h.pin_memory()
+    M, N, K = workload.M, workload.N, workload.K
+    C_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    A = torch.empty_like(A_h, device=device)
+    B = torch.empty_like(B_h, device=device)
+    C = torch.empty((M, N), dtype=torch.float32, device=device)
+    code = tg.DTYPES[workload.dtype]
+    s = stream.cuda_stream
+
+    def step():
+        A.copy_(A_h, non_blocking=True)
+        B.copy_(B_h, non_blocking=True)
+        rc = tg.gemm_run(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s)
+        if rc != tg.GEMM_OK:
+            raise RuntimeError(tg.gemm_last_error())
+        C_h.copy_(C, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()
+    d2h = C_h.numel() * 4
+    return ms, h2d, d2h
+
+
+def cpu_baseline(workload, target_s):
+    """The oracle, as it stands, on a bounded sample of rows of the same GEMM."""
+    import oracle
+    from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array, workload_operands
+    A, B = workload_operands(workload)
+    a, b = as_oracle_array(A), as_oracle_array(B)
+    bf16 = workload.dtype == "bf16"
+    threads = oracle.num_threads()
+    rows = list(range(threads))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, rows, bf16=bf16, with_scale=False)
+    t_probe = time.perf_counter() - t0
+    n = max(threads, int(threads * max(1.0, (target_s - t_probe) / max(t_probe, 1e-3))))
+    n = min(n, workload.M)
+    rows = list(range(n))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, rows, bf16=bf16, with_scale=False)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n * workload.N * workload.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {workload.M} rows of C (each a full {workload.N}x{workload.K} row-panel product), "
+                      f"fp64 C loops, {dt:.1f} s"}
+
+
+def roofline_tensor(flops, launch_ms, peak, peak_src, nominal, traffic):
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": UNIT,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+            "frac_of_nominal_dense": round(achieved / nominal, 4), "nominal_dense_peak": nominal}
+
+
+def roofline_alu(flops, launch_ms, sm_mhz):
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    peak = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": UNIT,
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": f"derived: {SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {sm_mhz:.0f} MHz"}
+
+
+def run_ours(args):
+    import torch
+    import tiled_tensor_core_gemm_gb300 as tg
+    from tiled_tensor_core_gemm_gb300 import build as tgbuild
+    from tiled_tensor_core_gemm_gb300.inputs import C3_FP32_4096, C3_TF32_4096, C4_BF16_8192
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        tgbuild.build()
+    if dist is not None:
+        dist.barrier()
+    tg.load_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device)
+
+    w = C4_BF16_8192
+    sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    res = None
+    try:
+        res = time_gemm(tg, w, args.steps, args.warmup, stream, device, dist,
+                        on_begin=sampler.mark_begin if sampler else None,
+                        on_end=sampler.mark_end if sampler else None)
+    finally:
+        clocks = sampler.stop() if sampler else None
+
+    total_ms = res["total_ms"]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * res["flops"] * args.steps / (total_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), "
+                               "fp32 accumulate and output, row-major, persistent tcgen05 path",
+                   "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (268 MB of operands, 537 MB with C, vs 129 MB L2); no flush",
+                   "plan": res["plan"]},
+        "roofline": roofline_tensor(res["flops"], res["launch_ms_mean"], peaks["bf16_tflops"],
+                                    f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
+                                    profiled_traffic("bf16_8192")),
+        "kernel_ms": {"mean": round(res["launch_ms_mean"], 5), "median": round(res["launch_ms_median"], 5),
+                      "min": round(res["launch_ms_min"], 5)},
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": clocks,
+    }
+    out["roofline"]["frac_of_sustained"] = round(out["roofline"]["achieved"] / peaks["bf16_tflops_sustained"], 4)
+
+    if not args.no_paths:
+        sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
+        paths = {}
+        n_side = max(3, min(args.steps, 100))
+        for key, wl in (("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)):
+            r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device)
+            tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
+            if wl.dtype == "fp32":
+                rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
+            else:
+                tf32_peak = peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"]
+                rl = roofline_tensor(r["flops"], r["launch_ms_mean"], tf32_peak,
+                                     f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
+                                     NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
+            paths[key] = {"workload": wl.name, "tflops": round(tf, 2), "steps": n_side,
+                          "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
+        out["paths"] = paths
+
+    if not args.no_e2e:
+        ms, h2d, d2h = time_e2e(tg, w, max(3, min(args.steps, 50)), stream, device)
+        out["e2e"] = {"value": round(world * 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+                      "how": "pinned host A,B -> device, gemm_run, C -> pinned host, on one stream, CUDA events"}
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# -------------------------------------------------------- reference arm ---
+def run_reference(args):
+    """The fp64 oracle on the host cores, each step a bounded sample of rows of
+    the same 8192^3 BF16 GEMM."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from tiled_tensor_core_gemm_gb300.inputs import C4_BF16_8192 as w, as_oracle_array, workload_operands
+    oracle.build()
+    A, B = workload_operands(w)
+    a, b = as_oracle_array(A), as_oracle_array(B)
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, list(range(threads)), bf16=True, with_scale=False)
+    t_step = time.perf_counter() - t0
+    budget = 150.0
+    rows = threads
+    if t_step * (args.steps + args.warmup) > budget:
+        rows = max(1, int(threads * budget / (t_step * (args.steps + args.warmup))))
+    sample = list(range(rows))
+    for i in range(args.warmup):
+        oracle.gemm_rows(a, b, [(r + i * rows) % w.M for r in sample], bf16=True, with_scale=False)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm_rows(a, b, [(r + i * rows) % w.M for r in sample], bf16=True, with_scale=False)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    used = min(rows, threads)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), "
+                                  "fp32 accumulate and output, row-major; oracle on bounded row samples",
+                      "M": w.M, "N": w.N, "K": w.K},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                            "sample": f"each step: {rows} rows of C of the 8192^3 GEMM (fp64 loops)"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

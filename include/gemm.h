@@ -1,0 +1,155 @@
+/*
+ * gemm.h -- C ABI of the GB300 dense-GEMM library (libtcgemm.so).
+ *
+ * One operation: C = A . B over row-major operands with an FP32 result,
+ * computed on an NVIDIA GB300 (sm_103a) by hand-written CUDA kernels.
+ *
+ * Where the operation is defined:
+ *   - "Shared memory and tensor cores" (ml-compiler-from-scratch ch. 13),
+ *     section 13.1: C = A @ B, 2*M*N*K flops, traffic of a block tiling;
+ *     sections 13.3-13.7: the shared-memory tiled SIMT kernel with barriers
+ *     and register micro-tiles (the FP32 path here);
+ *     section 13.8: tensor-core precision (exact products, FP32 sums).
+ *   - "Learn CuTeDSL" README, sections 3 (TMA), 4.3 (tcgen05 MMA with the
+ *     accumulator in Tensor Memory, 2-CTA MMA), 5.4 (TMA/MMA pipeline) and
+ *     8.1 (static persistent tile scheduler): the TF32/BF16 tensor-core path.
+ *   - The same README, section 2.2.1: a C entry point taking raw device
+ *     pointers and sizes, called from a thin Python layer.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major.  A is M x K, B is K x N, C is M x N.  Leading
+ *     dimensions are in ELEMENTS: lda >= K, ldb >= N, ldc >= N.
+ *   - A, B and C are DEVICE pointers owned by the caller; the library never
+ *     frees or retains them past the call.  The stream is the caller's
+ *     (NULL = the legacy default stream).  Work is enqueued on it and the call
+ *     returns without synchronising; the result is ready once the stream is.
+ *   - A status code (gemm_status_t) is returned.  On any non-zero status
+ *     nothing was enqueued, except GEMM_ERR_CUDA raised by a launch, in which
+ *     case the stream is in the state CUDA reports.  gemm_last_error() gives
+ *     a human-readable message for the calling thread's last failure.
+ *   - The library is thread-safe for concurrent calls on different streams.
+ */
+#ifndef TCGEMM_GEMM_H
+#define TCGEMM_GEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t is 'struct CUstream_st *'; declaring the tag keeps this header
+ * free of CUDA includes while staying the same type. */
+struct CUstream_st;
+
+typedef enum {
+    GEMM_FP32 = 0, /* A, B float; exact FP32 products and sums on the CUDA cores  */
+    GEMM_TF32 = 1, /* A, B float; tensor cores read them as TF32 (10-bit mantissa)
+                      and accumulate in FP32 in Tensor Memory                      */
+    GEMM_BF16 = 2  /* A, B bfloat16 (raw uint16 storage); exact products,
+                      FP32 accumulation in Tensor Memory                           */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* bad size, leading dimension, pointer or overlap */
+    GEMM_ERR_UNSUPPORTED = 2, /* valid request this build/device cannot serve     */
+    GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                 */
+    GEMM_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (see status)      */
+    GEMM_ERR_NO_MEMORY = 5    /* workspace allocation failed                       */
+} gemm_status_t;
+
+/*
+ * gemm_run -- C = A . B  (C is overwritten; there is no alpha/beta).
+ *
+ *   M, N, K     sizes, each >= 0.  M == 0 or N == 0: no-op.  K == 0: C is
+ *               filled with zeros (the empty sum).
+ *   dtype       gemm_dtype_t.  A and B are 'const float *' for GEMM_FP32 and
+ *               GEMM_TF32 and 'const uint16_t *' (bfloat16 bits) for GEMM_BF16.
+ *   A, lda      device pointer to A[0][0], leading dimension in elements.
+ *   B, ldb      device pointer to B[0][0], leading dimension in elements.
+ *   C, ldc      device pointer to C[0][0] (float), leading dimension in elements.
+ *   stream      the CUDA stream to enqueue on.
+ *
+ * Paths: GEMM_FP32 runs the tiled SIMT kernel; GEMM_TF32 and GEMM_BF16 run the
+ * persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine cannot
+ * address (base not 16-byte aligned, or a row pitch that is not a multiple of
+ * 16 bytes) are first copied into a stream-ordered workspace with a padded
+ * pitch; that workspace is allocated and freed on the stream
+ * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
+ * unavailable.  C with such a layout is written by ordinary stores instead of
+ * TMA stores.
+ *
+ * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
+ * a NULL pointer with a non-empty extent, an unknown dtype, or C overlapping
+ * A or B in memory.  A kernel whose bounded wait expires records
+ * GEMM_ERR_TIMEOUT in a device status word that gemm_get_status() reads.
+ */
+GEMM_API int gemm_run(int64_t M, int64_t N, int64_t K, int dtype,
+             const void *A, int64_t lda, const void *B, int64_t ldb,
+             float *C, int64_t ldc, struct CUstream_st *stream);
+
+/* Message for the calling thread's most recent failed call ("" if none).
+ * The string is owned by the library and valid until the thread's next call. */
+GEMM_API const char *gemm_last_error(void);
+
+/*
+ * gemm_get_status -- synchronise `stream`, then read and clear the device
+ * status word that kernels set when a bounded wait expires.  Returns GEMM_OK,
+ * GEMM_ERR_TIMEOUT (with the role and tile in gemm_last_error()), or
+ * GEMM_ERR_CUDA if the synchronisation itself failed.
+ */
+GEMM_API int gemm_get_status(struct CUstream_st *stream);
+
+/*
+ * gemm_set_option / gemm_get_option -- process-wide tuning overrides, for
+ * sweeps and tests.  Keys (value 0 = automatic unless stated):
+ *   "tc_bn"          force the tensor-core tile width BN (64, 128, 256)
+ *   "tc_cta_group"   force 1- or 2-CTA tiles (1, 2)
+ *   "tc_group_m"     raster group height in tiles (>= 1)
+ *   "tc_max_ctas"    cap on persistent CTAs (>= 1)
+ *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
+ *                    ordinary-store epilogue
+ *   "simt_tile"      force the SIMT tile: 128 (128x128) or 64 (64x64)
+ *   "wait_timeout_ms" bound on every in-kernel wait (default 2000)
+ * Returns GEMM_ERR_INVALID_ARG for an unknown key or an out-of-range value.
+ */
+GEMM_API int gemm_set_option(const char *key, int64_t value);
+GEMM_API int64_t gemm_get_option(const char *key);
+
+/* Plan the library would use for a call, computed on the host only (no GPU
+ * work, no CUDA calls); pointer addresses matter only for alignment.  The
+ * SM count is taken from `num_sms` (pass 0 to query the current device). */
+typedef struct {
+    int32_t path;        /* 0 SIMT FP32, 1 tensor cores                     */
+    int32_t bm, bn, bk;  /* CTA tile (bk in elements)                      */
+    int32_t stages;      /* shared-memory ring depth (tensor-core path)    */
+    int32_t cta_group;   /* 1 or 2 CTAs per MMA tile                       */
+    int32_t group_m;     /* raster group height in tiles                   */
+    int32_t grid;        /* CTAs launched                                  */
+    int32_t tiles;       /* output tiles                                   */
+    int32_t pack_a;      /* A copied to a padded workspace first           */
+    int32_t pack_b;      /* B copied to a padded workspace first           */
+    int32_t tma_store;   /* epilogue writes C with TMA stores              */
+    int32_t vec;         /* SIMT: 16-byte vector loads/stores legal        */
+    int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
+} gemm_plan_t;
+
+GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
+              uint64_t a_addr, int64_t lda, uint64_t b_addr, int64_t ldb,
+              uint64_t c_addr, int64_t ldc, int32_t num_sms, gemm_plan_t *out);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+GEMM_API int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_GEMM_H */

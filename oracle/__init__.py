@@ -112,8 +112,8 @@ def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = Fa
     return (C, D) if with_scale else C
 
 
-def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False):
-    """Rows `rows` of C = A.B and of D = |A|.|B|, each len(rows) x N, fp64."""
+def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale: bool = True):
+    """Rows `rows` of C = A.B and (with_scale) of D = |A|.|B|, each len(rows) x N, fp64."""
     _as_operand(A, bf16), _as_operand(B, bf16)
     M, K = A.shape
     N = B.shape[1]
@@ -121,10 +121,10 @@ def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False):
     if r.size and (r.min() < 0 or r.max() >= M):
         raise IndexError("row index out of range")
     C = np.empty((r.size, N), np.float64)
-    D = np.empty((r.size, N), np.float64)
+    D = np.empty((r.size, N), np.float64) if with_scale else None
     fn = _load().oracle_gemm_rows_bf16 if bf16 else _load().oracle_gemm_rows_f32
     fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), r.ctypes.data, r.size,
-       C.ctypes.data, D.ctypes.data)
+       C.ctypes.data, D.ctypes.data if D is not None else None)
     return C, D
 
 

@@ -1,0 +1,98 @@
+"""Helpers for the GPU parity tests: run the library through its C ABI on
+seeded inputs and compare with the oracle.
+
+Acceptance metric: r = max_ij |C_ij - Cref_ij| / D_ij with D = |A|.|B| (fp64);
+D_ij == 0 requires C_ij == Cref_ij exactly; any NaN/Inf fails.  Bounds: 1e-5
+for FP32 and for BF16 inputs with FP32 accumulation, 2e-3 for TF32.
+Derivation of the TF32 bound: the tensor cores read each FP32 operand with a
+10-bit mantissa; whether they round or truncate, each operand's relative
+error is below 2^-10, so each product's is below (1 + 2^-10)^2 - 1 < 1.96e-3,
+and sum_k |err_k| <= 1.96e-3 * D; FP32 accumulation adds about K * 2^-24 * D
+at worst, which keeps r under 2e-3 for K <= 8192.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import tiled_tensor_core_gemm_gb300 as tg
+from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array
+
+TOL = {"fp32": 1e-5, "bf16": 1e-5, "tf32": 2e-3}
+GUARD = 256   # NaN-filled floats before and after C
+
+
+def to_device(x: torch.Tensor, offset_elems: int = 0):
+    """Copy a (possibly padded) CPU operand to the GPU keeping its leading
+    dimension; optionally start it `offset_elems` elements into its buffer.
+    Returns (keepalive tensor, device address, leading dimension)."""
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 1 else max(cols, 1)
+    if rows == 0 or cols == 0:
+        buf = torch.empty(max(offset_elems, 1) + 1, dtype=x.dtype, device="cuda")
+        return buf, buf.data_ptr() + offset_elems * x.element_size(), ld
+    flat = torch.as_strided(x, (rows, ld), (ld, 1)) if ld != cols else x
+    buf = torch.empty(offset_elems + rows * ld, dtype=x.dtype, device="cuda")
+    buf[offset_elems:].copy_(flat.reshape(-1).contiguous())
+    return buf, buf.data_ptr() + offset_elems * x.element_size(), ld
+
+
+def run_gemm(A: torch.Tensor, B: torch.Tensor, dtype: str, ldc_pad: int = 0, a_offset: int = 0,
+             b_offset: int = 0, stream=None) -> np.ndarray:
+    """C = A.B on the GPU via gemm_run; checks the status word and that nothing
+    outside C (guard bands, ldc padding) was written.  Returns C as float32."""
+    M, K = A.shape
+    N = B.shape[1]
+    a_keep, a_ptr, lda = to_device(A, a_offset)
+    b_keep, b_ptr, ldb = to_device(B, b_offset)
+    ldc = max(N, 1) + ldc_pad
+    cbuf = torch.full((2 * GUARD + M * ldc,), float("nan"), dtype=torch.float32, device="cuda")
+    c_ptr = cbuf.data_ptr() + GUARD * 4
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    rc = tg.gemm_run(M, N, K, tg.DTYPES[dtype], a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream)
+    assert rc == tg.GEMM_OK, tg.gemm_last_error()
+    st = tg.gemm_get_status(stream)
+    assert st == tg.GEMM_OK, tg.gemm_last_error()
+    host = cbuf.cpu().numpy()
+    del a_keep, b_keep
+    assert np.all(np.isnan(host[:GUARD])), "write before C"
+    assert np.all(np.isnan(host[GUARD + M * ldc:])), "write after C"
+    C = host[GUARD:GUARD + M * ldc].reshape(M, ldc)
+    if ldc_pad:
+        assert np.all(np.isnan(C[:, N:])), "write into the ldc padding"
+    return C[:, :N].copy()
+
+
+def error_ratio(C: np.ndarray, Cref: np.ndarray, D: np.ndarray) -> float:
+    C = C.astype(np.float64)
+    if not np.all(np.isfinite(C)):
+        return float("inf")
+    diff = np.abs(C - Cref)
+    zero = D == 0
+    if np.any(diff[zero] != 0):
+        return float("inf")
+    if not np.any(~zero):
+        return 0.0
+    return float(np.max(diff[~zero] / D[~zero]))
+
+
+def oracle_full(A: torch.Tensor, B: torch.Tensor, dtype: str):
+    return oracle.gemm(as_oracle_array(A), as_oracle_array(B), bf16=(dtype == "bf16"), with_scale=True)
+
+
+def oracle_rows(A: torch.Tensor, B: torch.Tensor, dtype: str, rows):
+    return oracle.gemm_rows(as_oracle_array(A), as_oracle_array(B), rows, bf16=(dtype == "bf16"))
+
+
+def sample_rows(M: int, tile: int = 128, extra: int = 8, seed: int = 0):
+    """Rows at every 8th tile boundary (first and last row of the tile), the
+    last rows of the matrix, and a few seeded random rows."""
+    rows = set()
+    for t in range(0, M, tile * 8):
+        rows.update({t, min(t + tile - 1, M - 1)})
+    rows.update({0, M - 1, max(M - 2, 0)})
+    rng = np.random.default_rng(seed)
+    rows.update(int(r) for r in rng.integers(0, M, extra))
+    return sorted(rows)

@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library loads, exports what include/gemm.h
+declares, rejects bad arguments before any CUDA call, and plans on the host."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import tiled_tensor_core_gemm_gb300 as tg
+from tiled_tensor_core_gemm_gb300 import build as tgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tgbuild.build()
+    tg.load_library()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"GEMM_API\s+[\w\s\*]+?\b(gemm_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    declared = _declared_symbols()
+    assert {"gemm_run", "gemm_last_error", "gemm_get_status", "gemm_set_option", "gemm_get_option",
+            "gemm_plan", "gemm_version"} <= declared
+    out = subprocess.run(["nm", "-D", "--defined-only", tg.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (gemm_\w+)", out))
+    assert declared <= exported, declared - exported
+    assert set(tg.EXPORTED) <= exported
+
+
+def test_built_for_sm_103a_only():
+    assert tgbuild.GENCODE == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_version():
+    assert tg.gemm_version() == 10000
+
+
+@pytest.mark.parametrize("args,frag", [
+    ((-1, 4, 4, tg.GEMM_FP32, 16, 4, 16, 4, 64, 4), "negative"),
+    ((4, 4, 4, 7, 16, 4, 16, 4, 64, 4), "dtype"),
+    ((4, 4, 8, tg.GEMM_FP32, 16, 4, 16, 4, 64, 4), "leading dimension"),
+    ((4, 8, 4, tg.GEMM_BF16, 16, 4, 16, 8, 64, 4), "leading dimension"),
+    ((4, 4, 4, tg.GEMM_FP32, 0, 4, 16, 4, 64, 4), "NULL"),
+    ((4, 4, 4, tg.GEMM_FP32, 16, 4, 16, 4, 0, 4), "NULL"),
+    ((1 << 31, 4, 4, tg.GEMM_FP32, 16, 4, 16, 4, 64, 4), "2^31"),
+])
+def test_invalid_arguments_rejected_before_cuda(args, frag):
+    rc = tg.gemm_run(*args, 0)
+    assert rc == tg.GEMM_ERR_INVALID_ARG
+    assert frag in tg.gemm_last_error()
+
+
+def test_overlap_rejected():
+    # C starts inside A's footprint
+    rc = tg.gemm_run(8, 8, 8, tg.GEMM_FP32, 4096, 8, 1 << 20, 8, 4096 + 64, 8, 0)
+    assert rc == tg.GEMM_ERR_INVALID_ARG and "overlap" in tg.gemm_last_error()
+
+
+def test_empty_output_is_noop_without_cuda():
+    assert tg.gemm_run(0, 5, 3, tg.GEMM_BF16, 0, 3, 0, 5, 0, 5, 0) == tg.GEMM_OK
+    assert tg.gemm_run(5, 0, 3, tg.GEMM_FP32, 0, 3, 0, 1, 0, 1, 0) == tg.GEMM_OK
+
+
+def test_options_roundtrip_and_validation():
+    assert tg.gemm_set_option("tc_bn", 128) == tg.GEMM_OK and tg.gemm_get_option("tc_bn") == 128
+    assert tg.gemm_set_option("tc_bn", 0) == tg.GEMM_OK
+    assert tg.gemm_set_option("tc_bn", 96) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_set_option("no_such_key", 1) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_get_option("no_such_key") == -1
+    assert tg.gemm_get_option("wait_timeout_ms") == 2000
+
+
+def _plan(M, N, K, dt, lda=None, ldb=None, ldc=None, a=0, b=0, c=0, sms=152):
+    return tg.gemm_plan(M, N, K, dt, a, lda or K, b, ldb or N, c, ldc or N, sms).as_dict()
+
+
+def test_plan_8192_bf16_uses_cta_pairs_full_machine():
+    p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+    assert p["path"] == 1 and p["cta_group"] == 2 and p["bn"] == 256 and p["bk"] == 64
+    assert p["tiles"] == 32 * 32 and p["grid"] == 152
+    assert not p["pack_a"] and not p["pack_b"] and p["tma_store"]
+    assert p["stages"] >= 4 and p["smem_bytes"] <= 232448
+
+
+def test_plan_tf32_and_fp32_4096():
+    p = _plan(4096, 4096, 4096, tg.GEMM_TF32)
+    assert p["path"] == 1 and p["bk"] == 32
+    s = _plan(4096, 4096, 4096, tg.GEMM_FP32)
+    assert s["path"] == 0 and s["bm"] == 128 and s["vec"] == 1 and s["grid"] == 32 * 32
+
+
+def test_plan_small_fp32_shrinks_tile_to_fill_machine():
+    assert _plan(1024, 1024, 1024, tg.GEMM_FP32)["bm"] == 64
+    assert _plan(256, 256, 256, tg.GEMM_FP32)["bm"] == 64
+
+
+def test_plan_ragged_packs_and_plain_epilogue():
+    p = _plan(4097, 4095, 4099, tg.GEMM_BF16)
+    assert p["pack_a"] and p["pack_b"] and not p["tma_store"]
+    q = _plan(1000, 1000, 1000, tg.GEMM_BF16)   # 2000-byte rows are 16-byte multiples
+    assert not q["pack_a"] and not q["pack_b"] and q["tma_store"]
+
+
+def test_plan_misaligned_base_packs():
+    p = _plan(256, 256, 256, tg.GEMM_BF16, a=2)
+    assert p["pack_a"] and not p["pack_b"]
+    s = _plan(256, 256, 256, tg.GEMM_FP32, a=4)
+    assert s["vec"] == 0
+
+
+def test_plan_low_tile_count_uses_narrow_tiles():
+    p = _plan(128, 8192, 8192, tg.GEMM_BF16)
+    assert p["cta_group"] == 1 and p["bn"] == 64 and p["grid"] == 128
+
+
+def test_plan_forced_options():
+    try:
+        assert tg.gemm_set_option("tc_cta_group", 1) == 0
+        assert tg.gemm_set_option("tc_bn", 128) == 0
+        p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+        assert p["cta_group"] == 1 and p["bn"] == 128
+        assert tg.gemm_set_option("tc_max_ctas", 10) == 0
+        assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["grid"] == 10
+    finally:
+        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas"):
+            tg.gemm_set_option(k, 0)
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(tg, "_lib", None)
+    monkeypatch.setattr(tg, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        tg.gemm_version()

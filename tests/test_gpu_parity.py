@@ -1,0 +1,164 @@
+"""GPU parity of every path against the fp64 oracle, through the C ABI.
+
+* exact: small-integer inputs (every product and partial sum an exact small
+  integer) at tile-edge shapes must give bit-identical C on every path;
+* the published workloads: 256^3 / 1024^3 FP32 and 1024^3 TF32 in full,
+  4096^3 FP32/TF32, 8192^3 BF16 and the ragged BF16 set on sampled rows, in
+  the launch configuration the benchmark uses (automatic plan);
+* structure: identity, permutation, all-ones, K = 0, guard bands and padded
+  leading dimensions, misaligned bases (operand pack), determinism, and every
+  compiled tensor-core variant and epilogue.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tiled_tensor_core_gemm_gb300 as tg
+from tiled_tensor_core_gemm_gb300 import build as tgbuild
+from tiled_tensor_core_gemm_gb300.inputs import (C1_FP32_256, C2_FP32_1024, C2_TF32_1024, C3_FP32_4096,
+                                                 C3_TF32_4096, C4_BF16_8192, C5_BF16_RAGGED, make_operands,
+                                                 workload_operands)
+
+from gemm_check import TOL, error_ratio, oracle_full, oracle_rows, run_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ("fp32", "tf32", "bf16")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    tgbuild.build()
+    tg.load_library()
+    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_tile"):
+        tg.gemm_set_option(k, 0)
+    yield
+
+
+def _exact(A, B, dtype, **kw):
+    C = run_gemm(A, B, dtype, **kw)
+    Cref, _ = oracle_full(A, B, dtype)
+    assert np.array_equal(C.astype(np.float64), Cref), f"max |diff| {np.max(np.abs(C - Cref))}"
+
+
+EDGE = [(1, 1, 1), (15, 17, 16), (16, 16, 16), (17, 15, 17), (63, 65, 64), (127, 129, 63), (128, 128, 128),
+        (129, 257, 65), (255, 256, 257), (257, 513, 129), (300, 700, 1000), (384, 640, 192)]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(map(str, s)))
+def test_small_integers_bit_exact(dtype, shape):
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dtype, "ints", seed=11)
+    _exact(A, B, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_identity_and_permutation(dtype):
+    n, N = 300, 520
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    _, B = make_operands(n, N, n, dtype, "uniform", seed=12)
+    if dtype == "tf32":
+        B = B.to(torch.bfloat16).float()   # values the tensor cores read without loss
+    eye = torch.eye(n, dtype=tdt)
+    C = run_gemm(eye, B, dtype)
+    assert np.array_equal(C, B.float().numpy())
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(3))
+    P = eye[perm]
+    C = run_gemm(P, B, dtype)
+    assert np.array_equal(C, B.float().numpy()[perm.numpy()])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("K", [1, 64, 4099])
+def test_all_ones_gives_K(dtype, K):
+    A, B = make_operands(200, 333, K, dtype, "ones", seed=0)
+    C = run_gemm(A, B, dtype)
+    assert np.all(C == K)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_empty_sum_zero_fills(dtype):
+    A, B = make_operands(37, 45, 0, dtype, "uniform", seed=0)
+    C = run_gemm(A, B, dtype, ldc_pad=3)
+    assert np.all(C == 0)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_padded_leading_dimensions_and_guard_bands(dtype):
+    # NaN in the lda/ldb padding: any read of it would poison C
+    A, B = make_operands(200, 300, 130, dtype, "ints", seed=13, lda_pad=8, ldb_pad=8)
+    _exact(A, B, dtype, ldc_pad=4)
+    A, B = make_operands(199, 301, 129, dtype, "ints", seed=14, lda_pad=3, ldb_pad=5)
+    _exact(A, B, dtype, ldc_pad=1)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_misaligned_bases(dtype):
+    A, B = make_operands(256, 256, 256, dtype, "ints", seed=15)
+    _exact(A, B, dtype, a_offset=1, b_offset=3)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_deterministic(dtype):
+    A, B = make_operands(777, 1024, 1500, dtype, "normal", seed=16)
+    C1 = run_gemm(A, B, dtype)
+    C2 = run_gemm(A, B, dtype)
+    assert np.array_equal(C1, C2)
+
+
+TC_VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 256)]
+
+
+@pytest.mark.parametrize("dtype", ("tf32", "bf16"))
+@pytest.mark.parametrize("variant", TC_VARIANTS, ids=lambda v: f"cg{v[0]}_bn{v[1]}")
+@pytest.mark.parametrize("tma_store", (1, 2), ids=("tma_store", "plain_store"))
+@pytest.mark.parametrize("shape", [(300, 700, 1000), (1024, 768, 333), (2048, 1536, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_every_tensor_core_variant_exact(dtype, variant, tma_store, shape):
+    cg, bn = variant
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dtype, "ints", seed=17)
+    try:
+        tg.gemm_set_option("tc_cta_group", cg)
+        tg.gemm_set_option("tc_bn", bn)
+        tg.gemm_set_option("tc_tma_store", tma_store)
+        _exact(A, B, dtype)
+        # fewer persistent CTAs than tiles: several tiles per CTA, both accumulators
+        tg.gemm_set_option("tc_max_ctas", 2 * cg)
+        _exact(A, B, dtype)
+    finally:
+        for k in ("tc_cta_group", "tc_bn", "tc_tma_store", "tc_max_ctas"):
+            tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("tile", (64, 128))
+def test_simt_tiles_exact(tile):
+    A, B = make_operands(513, 389, 1027, "fp32", "ints", seed=18)
+    try:
+        tg.gemm_set_option("simt_tile", tile)
+        _exact(A, B, "fp32")
+    finally:
+        tg.gemm_set_option("simt_tile", 0)
+
+
+# ------------------------------------------------------- published workloads ---
+@pytest.mark.parametrize("w", [C1_FP32_256, C2_FP32_1024, C2_TF32_1024, C5_BF16_RAGGED[0]], ids=lambda w: w.name)
+def test_workload_full(w):
+    A, B = workload_operands(w)
+    C = run_gemm(A, B, w.dtype)
+    Cref, D = oracle_full(A, B, w.dtype)
+    r = error_ratio(C, Cref, D)
+    assert r <= TOL[w.dtype], r
+
+
+@pytest.mark.parametrize("w", [C3_FP32_4096, C3_TF32_4096, C4_BF16_8192] + list(C5_BF16_RAGGED[1:]),
+                         ids=lambda w: w.name)
+def test_workload_sampled_rows(w):
+    A, B = workload_operands(w)
+    C = run_gemm(A, B, w.dtype)
+    assert np.all(np.isfinite(C))
+    rows = sample_rows(w.M, extra=8, seed=w.seed)
+    Cref, D = oracle_rows(A, B, w.dtype, rows)
+    r = error_ratio(C[rows], Cref, D)
+    assert r <= TOL[w.dtype], r

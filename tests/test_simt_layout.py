@@ -1,0 +1,76 @@
+"""Shared-memory access patterns of the SIMT kernel under the 32-bank model.
+
+The bank model (pinned against the page's printed passes in test_analysis.py)
+is applied to the index expressions of the kernel in
+tiled_tensor_core_gemm_gb300/csrc/simt_fp32.cu: the padded, transposed A tile
+[k][BM+4], the B tile [k][BN], and thread (ty, tx) = (tid / TX, tid % TX) with
+its two 4-wide quads half a tile apart.  No GPU.
+"""
+import pytest
+
+from tiled_tensor_core_gemm_gb300.analysis import bank_passes, vector_bank_passes
+
+BK = 8
+
+
+@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
+def test_transposed_A_stores_conflict_free(BM, BN):
+    threads = (BM // 8) * (BN // 8)
+    lds_a = BM + 4
+    for warp in range(threads // 32):
+        for i in range(BM * BK // 4 // threads):
+            for e in range(4):
+                def addr(t):
+                    f = warp * 32 + t + i * threads
+                    r, kq = f // (BK // 4), f % (BK // 4)
+                    return (4 * kq + e) * lds_a + r
+                assert bank_passes(addr) == 1
+
+
+@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
+def test_unpadded_transpose_would_conflict(BM, BN):
+    # the reason for the +4 pad: with pitch BM the two k-quads share banks
+    threads = (BM // 8) * (BN // 8)
+
+    def addr(t):
+        r, kq = t // (BK // 4), t % (BK // 4)
+        return (4 * kq) * BM + r
+    assert bank_passes(addr) == 2
+    assert threads >= 32
+
+
+@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
+def test_inner_loop_vector_reads_minimal(BM, BN):
+    TX = BN // 8
+    lds_a = BM + 4
+    k = 5
+    for warp in range((BM // 8) * TX // 32):
+        def a_addr(t):
+            ty = (warp * 32 + t) // TX
+            return 4 * (k * lds_a + ty * 4)
+
+        def b_addr(t):
+            tx = (warp * 32 + t) % TX
+            return 4 * (k * BN + tx * 4)
+        # one pass per quarter-warp phase is the floor for 16-byte accesses
+        assert vector_bank_passes(a_addr, 16) == 4
+        assert vector_bank_passes(b_addr, 16) == 4
+
+
+def test_B_tile_vector_stores_minimal():
+    BN, threads = 128, 256
+    for warp in range(threads // 32):
+        def addr(t):
+            f = warp * 32 + t
+            kr, c4 = f // (BN // 4), f % (BN // 4)
+            return 4 * (kr * BN + 4 * c4)
+        assert vector_bank_passes(addr, 16) == 4
+
+
+def test_tc_epilogue_staging_swizzle_conflict_free():
+    # tcgen05 epilogue: lane = row, 16-byte chunk c stored at c ^ (row % 8)
+    for c in range(8):
+        assert vector_bank_passes(lambda t: t * 128 + ((c ^ (t & 7)) * 16), 16) == 4
+    # ordinary-store read-back: lane reads column `lane` of row rr
+    for rr in range(32):
+        assert bank_passes(lambda t: (rr * 128 + (((t >> 2) ^ (rr & 7)) * 16) + (t & 3) * 4) // 4) == 1

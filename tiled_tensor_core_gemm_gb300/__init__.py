@@ -1,1 +1,161 @@
-"""GB300-native dense GEMM: C = A.B over row-major operands, FP32 output."""
+"""GB300-native dense GEMM: C = A.B over row-major operands, FP32 output.
+
+A thin ctypes binding over the C ABI in include/gemm.h (libtcgemm.so, built
+in-tree by ``build.build()``).  The functions below carry the C names and only
+marshal arguments; every step of the computation runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library is missing, every call
+raises.
+
+    gemm_run(M, N, K, dtype, A, lda, B, ldb, C, ldc, stream) -> status
+        A, B, C are device addresses (ints); stream is a cudaStream_t as int.
+    gemm(A, B, C=None, dtype=None, stream=None) -> C
+        torch-tensor convenience: row-major CUDA tensors in, FP32 C out.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libtcgemm.so")
+
+GEMM_FP32, GEMM_TF32, GEMM_BF16 = 0, 1, 2
+DTYPES = {"fp32": GEMM_FP32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_CUDA = 3
+GEMM_ERR_TIMEOUT = 4
+GEMM_ERR_NO_MEMORY = 5
+
+EXPORTED = ("gemm_run", "gemm_last_error", "gemm_get_status", "gemm_set_option",
+            "gemm_get_option", "gemm_plan", "gemm_version")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gemm status {status}: {message}")
+        self.status = status
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "path", "bm", "bn", "bk", "stages", "cta_group", "group_m", "grid", "tiles",
+        "pack_a", "pack_b", "tma_store", "vec", "smem_bytes")]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load libtcgemm.so; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with tiled_tensor_core_gemm_gb300.build.build() "
+                               "(there is no fallback path)")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.gemm_run.argtypes = [i64, i64, i64, ctypes.c_int, p, i64, p, i64, p, i64, p]
+        lib.gemm_run.restype = ctypes.c_int
+        lib.gemm_last_error.argtypes = []
+        lib.gemm_last_error.restype = ctypes.c_char_p
+        lib.gemm_get_status.argtypes = [p]
+        lib.gemm_get_status.restype = ctypes.c_int
+        lib.gemm_set_option.argtypes = [ctypes.c_char_p, i64]
+        lib.gemm_set_option.restype = ctypes.c_int
+        lib.gemm_get_option.argtypes = [ctypes.c_char_p]
+        lib.gemm_get_option.restype = i64
+        lib.gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_uint64, i64, ctypes.c_uint64, i64,
+                                  ctypes.c_uint64, i64, ctypes.c_int32, ctypes.POINTER(GemmPlan)]
+        lib.gemm_plan.restype = ctypes.c_int
+        lib.gemm_version.argtypes = []
+        lib.gemm_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------ C-ABI mirrors ---
+def gemm_run(M, N, K, dtype, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return load_library().gemm_run(M, N, K, dtype, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_last_error() -> str:
+    return load_library().gemm_last_error().decode()
+
+
+def gemm_get_status(stream=0) -> int:
+    return load_library().gemm_get_status(stream)
+
+
+def gemm_set_option(key: str, value: int) -> int:
+    return load_library().gemm_set_option(key.encode(), int(value))
+
+
+def gemm_get_option(key: str) -> int:
+    return int(load_library().gemm_get_option(key.encode()))
+
+
+def gemm_plan(M, N, K, dtype, a_addr, lda, b_addr, ldb, c_addr, ldc, num_sms=0) -> GemmPlan:
+    out = GemmPlan()
+    rc = load_library().gemm_plan(M, N, K, dtype, a_addr, lda, b_addr, ldb, c_addr, ldc, num_sms,
+                                  ctypes.byref(out))
+    if rc != GEMM_OK:
+        raise GemmError(rc, gemm_last_error())
+    return out
+
+
+def gemm_version() -> int:
+    return load_library().gemm_version()
+
+
+# ------------------------------------------------------ tensor convenience ---
+def _ld(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("operands must be row-major (unit stride along columns)")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def gemm(A, B, C=None, dtype=None, stream=None):
+    """C = A.B through gemm_run for CUDA tensors (float32, or bfloat16 for BF16).
+
+    dtype: "fp32" (default for float32 inputs), "tf32" or "bf16" (default for
+    bfloat16 inputs).  C, if given, must be a float32 CUDA tensor of shape
+    (M, N); it is overwritten.
+    """
+    import torch
+
+    if dtype is None:
+        dtype = "bf16" if A.dtype == torch.bfloat16 else "fp32"
+    code = DTYPES[dtype]
+    want = torch.bfloat16 if code == GEMM_BF16 else torch.float32
+    if A.dtype != want or B.dtype != want:
+        raise TypeError(f"{dtype} GEMM takes {want} operands")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    rc = gemm_run(M, N, K, code, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), stream)
+    if rc != GEMM_OK:
+        raise GemmError(rc, gemm_last_error())
+    return C

@@ -1,0 +1,384 @@
+// C ABI of the GEMM library: argument checks, the host-side planner (path,
+// tile shape, ring depth, CTA pairing, raster and grid), operand packing and
+// dispatch.  See include/gemm.h for the contract of every entry point.
+//
+// The planner follows two rules from the pages: fill the machine ("GPU
+// architecture and mapping kernels" ch. 12, exercise 12.8: prefer the largest
+// tile that still gives every SM work, else shrink the tile), and run a
+// persistent grid of one CTA (or CTA pair) per SM ("Learn CuTeDSL" section 8.1).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace tcgemm {
+namespace {
+
+thread_local char t_err[512];
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+std::mutex g_opt_mu;
+Options g_opt;
+
+struct DevInfo {
+    bool valid = false;
+    int sms = 0, cc_major = 0, cc_minor = 0, max_clusters = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+int dev_info(int dev, DevInfo *out) {
+    if (dev < 0 || dev >= 64) return fail(GEMM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.valid) {
+        cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+        d.max_clusters = (d.cc_major == 10 && d.cc_minor == 3) ? tc_max_active_clusters(dev) : 0;
+        cudaGetLastError();
+        d.valid = true;
+    }
+    *out = d;
+    return GEMM_OK;
+}
+
+PFN_cuMemGetAddressRange_v3020 address_range_fn() {
+    static PFN_cuMemGetAddressRange_v3020 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 3020, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(p);
+    });
+    return fn;
+}
+
+// The operand must be device memory of the current device, and its whole
+// footprint [p, p + bytes) must lie inside one allocation.
+int check_device_span(const char *name, const void *p, uint64_t bytes, int dev) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GEMM_ERR_INVALID_ARG, "%s: not a CUDA pointer (%s)", name, cudaGetErrorString(e));
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(GEMM_ERR_INVALID_ARG, "%s: not device memory (memory type %d)", name, (int)attr.type);
+    if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+        return fail(GEMM_ERR_INVALID_ARG, "%s: lives on device %d, current device is %d", name, attr.device, dev);
+    if (auto fn = address_range_fn()) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (fn(&base, &size, (CUdeviceptr)(uintptr_t)p) == CUDA_SUCCESS) {
+            const uint64_t start = (uint64_t)(uintptr_t)p;
+            if (start + bytes > (uint64_t)base + size)
+                return fail(GEMM_ERR_INVALID_ARG,
+                            "%s: footprint of %llu bytes runs past the end of its allocation (%llu bytes left)", name,
+                            (unsigned long long)bytes, (unsigned long long)((uint64_t)base + size - start));
+        }
+    }
+    return GEMM_OK;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int elem_bytes(int dtype) { return dtype == GEMM_BF16 ? 2 : 4; }
+
+}  // namespace
+
+Options options_snapshot() {
+    std::lock_guard<std::mutex> lk(g_opt_mu);
+    return g_opt;
+}
+
+int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64_t lda, uint64_t b_addr, int64_t ldb,
+              uint64_t c_addr, int64_t ldc, int num_sms, int max_clusters_2cta, const Options &opt, Plan *out) {
+    gemm_plan_t &p = out->pub;
+    std::memset(&p, 0, sizeof p);
+    out->lda_eff = lda;
+    out->ldb_eff = ldb;
+    if (num_sms <= 0) num_sms = 1;
+    if (dtype == GEMM_FP32) {
+        int tile = opt.simt_tile;
+        if (tile == 0) tile = cdiv(M, 128) * cdiv(N, 128) >= num_sms ? 128 : 64;
+        p.path = 0;
+        p.bm = p.bn = tile;
+        p.bk = 8;
+        p.stages = 2;
+        p.cta_group = 1;
+        p.group_m = 1;
+        p.tiles = (int32_t)(cdiv(M, tile) * cdiv(N, tile));
+        p.grid = p.tiles;
+        p.vec = (lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && a_addr % 16 == 0 && b_addr % 16 == 0 &&
+                 c_addr % 16 == 0);
+        p.smem_bytes = 2 * 8 * ((tile + 4) + tile) * 4;
+        return GEMM_OK;
+    }
+    const int elem = elem_bytes(dtype);
+    p.path = 1;
+    p.bm = 128;
+    p.bk = 128 / elem;
+    p.pack_a = (a_addr % 16 != 0) || ((lda * elem) % 16 != 0);
+    p.pack_b = (b_addr % 16 != 0) || ((ldb * elem) % 16 != 0);
+    if (p.pack_a) out->lda_eff = round_up(K, 16 / elem);
+    if (p.pack_b) out->ldb_eff = round_up(N, 16 / elem);
+    const bool c_tma_ok = (c_addr % 16 == 0) && ((ldc * 4) % 16 == 0);
+    p.tma_store = (opt.tc_tma_store == 2) ? 0 : (c_tma_ok ? 1 : 0);
+
+    int cg = opt.tc_cta_group, bn = opt.tc_bn;
+    auto tiles_of = [&](int g, int b) { return cdiv(M, 128 * g) * cdiv(N, b); };
+    if (cg == 0 && bn == 0) {
+        if (max_clusters_2cta > 0 && tiles_of(2, 256) >= max_clusters_2cta) {
+            cg = 2;
+            bn = 256;
+        } else if (tiles_of(1, 256) >= num_sms) {
+            cg = 1;
+            bn = 256;
+        } else if (tiles_of(1, 128) >= num_sms) {
+            cg = 1;
+            bn = 128;
+        } else {
+            cg = 1;
+            bn = 64;
+        }
+    } else if (cg == 0) {
+        cg = (bn == 256 && max_clusters_2cta > 0 && tiles_of(2, 256) >= max_clusters_2cta) ? 2 : 1;
+    } else if (bn == 0) {
+        bn = 256;
+    }
+    if (tc_smem_bytes(dtype, cg, bn) == 0)
+        return fail(GEMM_ERR_UNSUPPORTED, "no tensor-core variant with cta_group=%d, BN=%d", cg, bn);
+    if (cg == 2 && max_clusters_2cta <= 0)
+        return fail(GEMM_ERR_UNSUPPORTED, "2-CTA tiles need cluster support on this device");
+    p.cta_group = cg;
+    p.bn = bn;
+    p.stages = tc_stages(dtype, cg, bn);
+    p.smem_bytes = tc_smem_bytes(dtype, cg, bn);
+    p.group_m = opt.tc_group_m > 0 ? opt.tc_group_m : (cg == 2 ? 8 : 16);
+    const int64_t tiles = tiles_of(cg, bn);
+    p.tiles = (int32_t)tiles;
+    int64_t units = cg == 2 ? max_clusters_2cta : num_sms;
+    if (opt.tc_max_ctas > 0) units = std::min<int64_t>(units, std::max(1, opt.tc_max_ctas / cg));
+    units = std::min<int64_t>(units, tiles);
+    p.grid = (int32_t)(units * cg);
+    return GEMM_OK;
+}
+
+}  // namespace tcgemm
+
+using namespace tcgemm;
+
+extern "C" {
+
+int gemm_version(void) { return 10000; }
+
+const char *gemm_last_error(void) { return t_err; }
+
+int gemm_set_option(const char *key, int64_t v) {
+    t_err[0] = 0;
+    if (!key) return fail(GEMM_ERR_INVALID_ARG, "option key is NULL");
+    std::lock_guard<std::mutex> lk(g_opt_mu);
+    if (!std::strcmp(key, "tc_bn")) {
+        if (v != 0 && v != 64 && v != 128 && v != 256) return fail(GEMM_ERR_INVALID_ARG, "tc_bn must be 0/64/128/256");
+        g_opt.tc_bn = (int)v;
+    } else if (!std::strcmp(key, "tc_cta_group")) {
+        if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_cta_group must be 0, 1 or 2");
+        g_opt.tc_cta_group = (int)v;
+    } else if (!std::strcmp(key, "tc_group_m")) {
+        if (v < 0 || v > 4096) return fail(GEMM_ERR_INVALID_ARG, "tc_group_m must be in [0, 4096]");
+        g_opt.tc_group_m = (int)v;
+    } else if (!std::strcmp(key, "tc_max_ctas")) {
+        if (v < 0 || v > (1 << 20)) return fail(GEMM_ERR_INVALID_ARG, "tc_max_ctas out of range");
+        g_opt.tc_max_ctas = (int)v;
+    } else if (!std::strcmp(key, "tc_tma_store")) {
+        if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tma_store must be 0, 1 or 2");
+        g_opt.tc_tma_store = (int)v;
+    } else if (!std::strcmp(key, "simt_tile")) {
+        if (v != 0 && v != 64 && v != 128) return fail(GEMM_ERR_INVALID_ARG, "simt_tile must be 0, 64 or 128");
+        g_opt.simt_tile = (int)v;
+    } else if (!std::strcmp(key, "wait_timeout_ms")) {
+        if (v < 1 || v > 600000) return fail(GEMM_ERR_INVALID_ARG, "wait_timeout_ms must be in [1, 600000]");
+        g_opt.wait_timeout_ms = (int)v;
+    } else {
+        return fail(GEMM_ERR_INVALID_ARG, "unknown option '%s'", key);
+    }
+    return GEMM_OK;
+}
+
+int64_t gemm_get_option(const char *key) {
+    if (!key) return -1;
+    Options o = options_snapshot();
+    if (!std::strcmp(key, "tc_bn")) return o.tc_bn;
+    if (!std::strcmp(key, "tc_cta_group")) return o.tc_cta_group;
+    if (!std::strcmp(key, "tc_group_m")) return o.tc_group_m;
+    if (!std::strcmp(key, "tc_max_ctas")) return o.tc_max_ctas;
+    if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
+    if (!std::strcmp(key, "simt_tile")) return o.simt_tile;
+    if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
+    return -1;
+}
+
+static int validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, const void *C, int64_t ldc) {
+    if (dtype != GEMM_FP32 && dtype != GEMM_TF32 && dtype != GEMM_BF16)
+        return fail(GEMM_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)",
+                                              (long long)M, (long long)N, (long long)K);
+    const int64_t kMax = 0x7fffffffLL;
+    if (M > kMax || N > kMax || K > kMax) return fail(GEMM_ERR_INVALID_ARG, "sizes must be below 2^31");
+    if (lda < (K > 0 ? K : 1) || ldb < (N > 0 ? N : 1) || ldc < (N > 0 ? N : 1))
+        return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (lda=%lld ldb=%lld ldc=%lld)", (long long)lda,
+                    (long long)ldb, (long long)ldc);
+    const int64_t kLdMax = 1LL << 36;
+    if (lda > kLdMax || ldb > kLdMax || ldc > kLdMax)
+        return fail(GEMM_ERR_INVALID_ARG, "leading dimension above 2^36 elements");
+    if (M > 0 && N > 0) {
+        if (!C) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
+        if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+    }
+    return GEMM_OK;
+}
+
+static bool overlaps(uint64_t a0, uint64_t a1, uint64_t b0, uint64_t b1) { return a0 < b1 && b0 < a1; }
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64_t lda, uint64_t b_addr, int64_t ldb,
+              uint64_t c_addr, int64_t ldc, int32_t num_sms, gemm_plan_t *out) {
+    t_err[0] = 0;
+    if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");
+    int rc = validate(M, N, K, dtype, (const void *)1, lda, (const void *)1, ldb, (const void *)1, ldc);
+    if (rc) return rc;
+    int sms = num_sms, clusters = num_sms / 2;
+    if (num_sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        DevInfo d;
+        if ((rc = dev_info(dev, &d))) return rc;
+        sms = d.sms;
+        clusters = d.max_clusters;
+    }
+    Plan plan;
+    rc = make_plan(M, N, K, dtype, a_addr, lda, b_addr, ldb, c_addr, ldc, sms, clusters, options_snapshot(), &plan);
+    if (rc == GEMM_OK) *out = plan.pub;
+    return rc;
+}
+
+int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb,
+             float *C, int64_t ldc, struct CUstream_st *stream_) {
+    t_err[0] = 0;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int rc = validate(M, N, K, dtype, A, lda, B, ldb, C, ldc);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+
+    const int eb = elem_bytes(dtype);
+    const uint64_t c0 = (uint64_t)(uintptr_t)C, c1 = c0 + (uint64_t)((M - 1) * ldc + N) * 4u;
+    if (K > 0) {
+        const uint64_t a0 = (uint64_t)(uintptr_t)A, a1 = a0 + (uint64_t)((M - 1) * lda + K) * eb;
+        const uint64_t b0 = (uint64_t)(uintptr_t)B, b1 = b0 + (uint64_t)((K - 1) * ldb + N) * eb;
+        if (overlaps(a0, a1, c0, c1) || overlaps(b0, b1, c0, c1))
+            return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
+    }
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    DevInfo d;
+    if ((rc = dev_info(dev, &d))) return rc;
+    if (!(d.cc_major == 10 && d.cc_minor == 3))
+        return fail(GEMM_ERR_UNSUPPORTED, "this library is built for sm_103a only (device is sm_%d%d)", d.cc_major,
+                    d.cc_minor);
+    if ((rc = check_device_span("C", C, c1 - c0, dev))) return rc;
+    if (K == 0) {
+        e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, (size_t)M, stream);
+        return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "cudaMemset2DAsync: %s", cudaGetErrorString(e));
+    }
+    if ((rc = check_device_span("A", A, (uint64_t)((M - 1) * lda + K) * eb, dev))) return rc;
+    if ((rc = check_device_span("B", B, (uint64_t)((K - 1) * ldb + N) * eb, dev))) return rc;
+
+    const Options opt = options_snapshot();
+    Plan plan;
+    rc = make_plan(M, N, K, dtype, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, d.sms,
+                   d.max_clusters, opt, &plan);
+    if (rc) return rc;
+    const gemm_plan_t &p = plan.pub;
+
+    if (p.path == 0) {
+        e = simt_fp32_launch(p, (int)M, (int)N, (int)K, static_cast<const float *>(A), lda,
+                             static_cast<const float *>(B), ldb, C, ldc, stream);
+        return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "SIMT kernel launch: %s", cudaGetErrorString(e));
+    }
+
+    // Tensor-core path: pack operands TMA cannot address, then launch.
+    const void *Ause = A, *Buse = B;
+    void *ws = nullptr;
+    const uint64_t a_bytes = p.pack_a ? (uint64_t)M * plan.lda_eff * eb : 0;
+    const uint64_t b_bytes = p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
+    const uint64_t a_off = 0, b_off = (a_bytes + 255) / 256 * 256;
+    if (p.pack_a || p.pack_b) {
+        e = cudaMallocAsync(&ws, (size_t)(b_off + b_bytes), stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(GEMM_ERR_NO_MEMORY, "workspace of %llu bytes: %s", (unsigned long long)(b_off + b_bytes),
+                        cudaGetErrorString(e));
+        }
+        uint8_t *w = static_cast<uint8_t *>(ws);
+        if (p.pack_a) {
+            e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, stream);
+            Ause = w + a_off;
+        }
+        if (e == cudaSuccess && p.pack_b) {
+            e = pack_rows_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
+            Buse = w + b_off;
+        }
+        if (e != cudaSuccess) {
+            cudaFreeAsync(ws, stream);
+            return fail(GEMM_ERR_CUDA, "operand pack: %s", cudaGetErrorString(e));
+        }
+    }
+    char err[256] = {0};
+    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc,
+                   (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
+    if (ws) {
+        e = cudaFreeAsync(ws, stream);
+        if (rc == GEMM_OK && e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
+    }
+    if (rc != GEMM_OK) return fail(rc, "%s", err);
+    return GEMM_OK;
+}
+
+int gemm_get_status(struct CUstream_st *stream_) {
+    t_err[0] = 0;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    uint32_t w[4] = {0, 0, 0, 0};
+    e = tc_read_and_clear_status(w);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (w[0] != 0) {
+        static const char *roles[] = {"?", "producer", "mma", "epilogue", "drain"};
+        return fail((int)w[0], "kernel wait expired: role=%s tile=%d block=%u", roles[w[1] < 5 ? w[1] : 0],
+                    (int)w[2], w[3]);
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

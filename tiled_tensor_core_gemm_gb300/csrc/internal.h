@@ -1,0 +1,69 @@
+// Internal interfaces between the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.h"
+
+namespace tcgemm {
+
+// ---------------------------------------------------------------- options ---
+struct Options {
+    int tc_bn = 0;             // 0 auto, else 64/128/256
+    int tc_cta_group = 0;      // 0 auto, else 1/2
+    int tc_group_m = 0;        // 0 auto
+    int tc_max_ctas = 0;       // 0 auto
+    int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
+    int simt_tile = 0;         // 0 auto, 128 or 64
+    int wait_timeout_ms = 2000;
+};
+Options options_snapshot();
+
+// ------------------------------------------------------------------- plan ---
+struct Plan {
+    gemm_plan_t pub;           // what gemm_plan() reports
+    int64_t lda_eff, ldb_eff;  // leading dimensions the kernel sees (after packing)
+};
+
+// Picks path, tile, ring depth, CTA group and grid for one call.  Host only.
+int make_plan(int64_t M, int64_t N, int64_t K, int dtype,
+              uint64_t a_addr, int64_t lda, uint64_t b_addr, int64_t ldb,
+              uint64_t c_addr, int64_t ldc, int num_sms, int max_clusters_2cta,
+              const Options &opt, Plan *out);
+
+// ------------------------------------------------------------------- SIMT ---
+// C = A.B in exact FP32 with the tile the plan chose.
+cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K,
+                             const float *A, int64_t lda, const float *B, int64_t ldb,
+                             float *C, int64_t ldc, cudaStream_t stream);
+
+// ----------------------------------------------------------- tensor cores ---
+// Fills plan-dependent shared-memory size (bytes) for a tensor-core variant,
+// or returns 0 if the variant is not compiled in.
+int tc_smem_bytes(int dtype, int cta_group, int bn);
+int tc_stages(int dtype, int cta_group, int bn);
+
+// Encodes the tensor maps and launches the persistent kernel.  A/B are the
+// (possibly packed) operands with the leading dimensions the plan reports.
+// Returns a gemm_status_t.
+int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
+              const void *A, int64_t lda, const void *B, int64_t ldb,
+              float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream,
+              char *err, size_t errlen);
+
+// Reads and clears the device status word of the tensor-core kernel.
+// words[0] = error code (0 none), [1] = role, [2] = tile, [3] = block.
+cudaError_t tc_read_and_clear_status(uint32_t words[4]);
+
+// Max co-resident 2-CTA clusters of the widest 2-CTA variant (0 if unknown).
+int tc_max_active_clusters(int device);
+
+// ------------------------------------------------------------------- pack ---
+// dst[r * ld_dst + c] = src[r * ld_src + c] for r < rows, c < cols (elem bytes
+// each); dst columns [cols, ld_dst) are zeroed.
+cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+}  // namespace tcgemm

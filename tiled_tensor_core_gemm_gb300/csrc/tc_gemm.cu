@@ -1,0 +1,529 @@
+// Persistent tensor-core GEMM for TF32 and BF16 inputs with FP32 accumulation
+// in Tensor Memory (tcgen05), fed by TMA, for sm_103a.
+//
+// Structure, after "Learn CuTeDSL":
+//  * section 5.1 / 5.4: warp specialisation around a circular buffer of STAGES
+//    shared-memory slots, each with a "full" mbarrier (TMA bytes landed) and an
+//    "empty" mbarrier (the MMAs that read it have completed); the phase bit of
+//    each barrier flips once per lap of the ring.
+//      warp 0      TMA producer (one thread issues every copy),
+//      warp 1      allocates Tensor Memory; one thread issues every MMA,
+//      warps 2..5  epilogue: Tensor Memory -> registers -> shared -> global.
+//  * section 4.3.1: the accumulator lives in Tensor Memory (128 lanes x 512
+//    columns of 32 bits); it is allocated once by warp 1 for the CTA's life.
+//  * section 4.3.4: every MMA batch follows mbarrier wait -> tcgen05 fence ->
+//    MMA issue -> tcgen05.commit onto an mbarrier; the first MMA of each tile
+//    runs with the accumulate flag off.
+//  * the closing notes of the TFLOPS table: two accumulators (2 x BN columns)
+//    so the epilogue of tile i overlaps the MMAs of tile i+1, and the output
+//    leaves through swizzled shared memory and TMA stores (section 3.3)
+//    instead of strided per-thread stores.
+//  * section 8.1: a static persistent schedule -- one CTA (or CTA pair) per SM,
+//    striding over output tiles, here in grouped raster order so that tiles
+//    that run together share A row-panels and B column-panels in L2.
+//  * section 4.3.5: the 2-CTA variant -- a CTA pair computes a 256-row tile
+//    with one M=256 MMA issued by the even CTA; each CTA loads its own 128 rows
+//    of A and its own half of the B columns with plain (non-multicast) TMA, and
+//    signals the even CTA's "full" barrier.
+//
+// Operand layouts: A is row-major M x K, i.e. K-major; B is row-major K x N,
+// i.e. N-major ("MN-major" for the MMA).  Both are staged with the 128-byte
+// swizzle.  TMA zero-fills everything outside [0,K) x [0,M) and [0,N) x [0,K),
+// so ragged tails add nothing to the sums; TMA stores clip to [0,N) x [0,M).
+//
+// Every wait is bounded (mbarrier try_wait plus a %globaltimer deadline); on
+// expiry the thread records GEMM_ERR_TIMEOUT in a device status word, raises
+// a CTA-wide abort flag that every other wait loop checks, and all roles fall
+// through to the common teardown, which still frees Tensor Memory.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tcgemm {
+
+__device__ uint32_t g_tc_status[4];
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;                       // rows per CTA = Tensor Memory lanes
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufBytes = 32 * 128;         // 32 rows x 32 fp32, 128-byte swizzled
+constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+constexpr int kSmemBudget = 232448;            // 227 KB opt-in dynamic shared memory
+constexpr int kBarBytes = 256;
+
+enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+
+template <bool TF32, int CG, int BN>
+struct TcCfg {
+    static constexpr int ELEM = TF32 ? 4 : 2;
+    static constexpr int BK = 128 / ELEM;           // one 128-byte swizzle row of K
+    static constexpr int UMMA_K = 32 / ELEM;        // K of one MMA: 16 (bf16) / 8 (tf32)
+    static constexpr int KSTEPS = BK / UMMA_K;      // 4 MMAs per stage
+    static constexpr int BN_CTA = BN / CG;          // B columns this CTA loads
+    static constexpr int CHUNK_COLS = 128 / ELEM;   // columns in one 128-byte row of B
+    static constexpr int B_CHUNKS = BN_CTA / CHUNK_COLS;
+    static constexpr int B_CHUNK_BYTES = BK * 128;  // one column chunk: BK rows x 128 B
+    static constexpr int A_BYTES = kBM * 128;
+    static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int B_KSTEP_BYTES = (UMMA_K / 8) * 1024;  // 8 K-rows per 1024-byte swizzle atom
+    static constexpr int STAGES_FIT = (kSmemBudget - 1024 - kEpiBytes - kBarBytes) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + kEpiBytes + kBarBytes;
+    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+    // Instruction descriptor: D f32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12:
+    // bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A K-major (bit 15 = 0),
+    // B MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+    static constexpr uint32_t FMT = TF32 ? 2u : 1u;
+    static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | (1u << 16) |
+                                      ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((kBM * CG) >> 4) << 24);
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N out of range");
+    static_assert(BN_CTA % CHUNK_COLS == 0 && B_CHUNKS >= 1, "B tile must be whole 128-byte chunks");
+    static_assert(STAGES >= 2, "shared memory too small for a ring");
+    static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
+    static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
+};
+
+struct TcParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles;   // tiles of (128*CG) x BN
+    int num_kb;                        // ceil(K / BK)
+    int group_m;                       // raster group height, in tile rows
+    int tma_store;
+    float *C;
+    int64_t ldc;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int &tm, int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first = g * group_m;
+    const int gm = min(tiles_m - first, group_m);
+    const int r = t - g * per_group;
+    tm = first + r % gm;
+    tn = r / gm;
+}
+
+__device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
+    *abort_flag = 1;
+    if (atomicCAS(&g_tc_status[0], 0u, (uint32_t)GEMM_ERR_TIMEOUT) == 0u) {
+        g_tc_status[1] = role;
+        g_tc_status[2] = (uint32_t)tile;
+        g_tc_status[3] = blockIdx.x;
+        __threadfence();
+    }
+}
+
+template <bool CLUSTER>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned long long timeout_ns) {
+    if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+template <bool TF32, int CG, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+    using Cf = TcCfg<TF32, CG, BN>;
+    constexpr bool kPair = CG == 2;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment (in the shared window) for the swizzle atoms.
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *stages = smem;
+    uint8_t *epi = smem + Cf::STAGES * Cf::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + kEpiBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(Cf::STAGES + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 2 + a); };
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+    const int unit = (int)blockIdx.x / CG, nunits = (int)gridDim.x / CG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cf::STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(acce_bar(a), kEpiWarps * CG);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        if (p.tma_store) ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cf::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
+    }
+    ptx::tc_fence_before();
+    if (kPair) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = unit; ok && t < p.num_tiles; t += nunits) {
+                int tm, tn;
+                tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                const int m0 = tm * (kBM * CG) + (int)rank * kBM;
+                const int n0 = tn * BN + (int)rank * Cf::BN_CTA;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+                        record_failure(kRoleProducer, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)(Cf::STAGE_BYTES * CG));
+                    const uint32_t sa = ptx::smem_addr(stages + stage * Cf::STAGE_BYTES);
+                    const uint32_t sb = sa + Cf::A_BYTES;
+                    const int k0 = kb * Cf::BK;
+                    if (!kPair) {
+                        ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
+#pragma unroll
+                        for (int c = 0; c < Cf::B_CHUNKS; ++c)
+                            ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb, n0 + c * Cf::CHUNK_COLS, k0);
+                    } else {
+                        const uint32_t fb_even = ptx::mapa_shared(fb, 0);
+                        ptx::tma_load_2d_pair(sa, &tmA, fb_even, k0, m0);
+#pragma unroll
+                        for (int c = 0; c < Cf::B_CHUNKS; ++c)
+                            ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb_even, n0 + c * Cf::CHUNK_COLS, k0);
+                    }
+                    if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: wait until the MMAs have released every slot, so that no
+            // tensor-core read of this CTA's shared memory and no commit
+            // arrival on its barriers is still outstanding at teardown.
+            for (int i = 0; ok && i < Cf::STAGES; ++i) {
+                if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    record_failure(kRoleDrain, -1, abort_flag);
+                    break;
+                }
+                if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (rank == 0 && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = unit; ok && t < p.num_tiles; t += nunits) {
+                if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    record_failure(kRoleMma, t, abort_flag);
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+                        record_failure(kRoleMma, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(stages + stage * Cf::STAGE_BYTES);
+                    const uint32_t sb = sa + Cf::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
+                        // A: K-major, 8-row groups 1024 B apart; K advances 32 B inside the swizzle row.
+                        const uint64_t adesc = ptx::sdesc_sw128(sa + 32u * kk, 16u, 1024u);
+                        // B: MN-major, 128-byte column chunks B_CHUNK_BYTES apart (leading),
+                        // 8-row K groups 1024 B apart (stride).
+                        const uint64_t bdesc = ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk),
+                                                                (uint32_t)Cf::B_CHUNK_BYTES, 1024u);
+                        ptx::mma<CG, TF32>(d_tmem, adesc, bdesc, Cf::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                    else ptx::mma_commit(empty_bar(stage));
+                    if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (kPair) ptx::mma_commit_pair(accf_bar(acc), 0x3);
+                else ptx::mma_commit(accf_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const uint32_t ew = warp - 2;        // staging-buffer owner index
+        const uint32_t q = warp & 3;         // Tensor Memory lane quarter this warp may read
+        uint8_t *bufs = epi + ew * 2 * kEpiBufBytes;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t nchunk = 0;
+        for (int t = unit; t < p.num_tiles; t += nunits) {
+            int tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int m0 = tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
+            const int n0 = tn * BN;
+            const bool lane_ok = wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+            if (!__all_sync(0xffffffffu, lane_ok)) {
+                if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j, ++nchunk) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(trow + 32u * j, r);
+                ptx::tmem_wait_ld();
+                if (j == BN / 32 - 1) {
+                    // The accumulator is fully in registers/shared: hand it back to the MMA.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kPair) ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0));
+                        else ptx::mbar_arrive(acce_bar(acc));
+                    }
+                }
+                uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
+                const int col0 = n0 + 32 * j;
+                if (p.tma_store) {
+                    // The TMA store that last read this buffer (two chunks ago) must be done.
+                    if (nchunk >= 2) {
+                        if (lane == 0) ptx::bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
+                }
+                // Row `lane`, 16-byte chunk c stored at position c ^ (row % 8): the
+                // 128-byte swizzle the TMA store expects, and conflict-free here.
+                float4 *row = reinterpret_cast<float4 *>(buf + lane * 128u);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    row[c ^ (int)(lane & 7u)] = make_float4(__uint_as_float(r[4 * c + 0]), __uint_as_float(r[4 * c + 1]),
+                                                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                if (p.tma_store) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (m0 < p.M && col0 < p.N) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
+                        ptx::bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    const int col = col0 + (int)lane;
+                    const uint32_t cchunk = lane >> 2, cword = lane & 3u;
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int grow = m0 + rr;
+                        const float v = *reinterpret_cast<const float *>(
+                            buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
+                        if (grow < p.M && col < p.N) p.C[(int64_t)grow * p.ldc + col] = v;
+                    }
+                    __syncwarp();
+                }
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (p.tma_store && lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    if (kPair) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cf::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host ---
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Row-major matrix of `rows` x `cols` elements with a pitch of `ld` elements,
+// tiled in boxes of box_cols x box_rows with the 128-byte swizzle.
+CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base, int64_t cols, int64_t rows,
+                   int64_t ld, int box_cols, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * elem)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <bool TF32, int CG, int BN>
+int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+                   size_t errlen) {
+    using Cf = TcCfg<TF32, CG, BN>;
+    const CUtensorMapDataType dt = TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof tc);
+    CUresult r = encode_2d(&ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
+    if (r == CUDA_SUCCESS) r = encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
+    if (r == CUDA_SUCCESS && plan.tma_store)
+        r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return GEMM_ERR_CUDA;
+    }
+    auto kern = tc_gemm_kernel<TF32, CG, BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
+    if (e != cudaSuccess) {
+        std::snprintf(err, errlen, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return GEMM_ERR_CUDA;
+    }
+    TcParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = (M + kBM * CG - 1) / (kBM * CG);
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.num_kb = (K + Cf::BK - 1) / Cf::BK;
+    p.group_m = plan.group_m > 0 ? plan.group_m : 1;
+    p.tma_store = plan.tma_store;
+    p.C = C;
+    p.ldc = ldc;
+    p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    if (e != cudaSuccess) {
+        std::snprintf(err, errlen, "tensor-core kernel launch: %s", cudaGetErrorString(e));
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+// The variants compiled in: (cta_group, BN) in {(1,64), (1,128), (1,256), (2,256)}.
+#define TC_VARIANTS(X) X(1, 64) X(1, 128) X(1, 256) X(2, 256)
+
+int tc_smem_bytes(int dtype, int cta_group, int bn) {
+#define X(cg, bn_)                                                                               \
+    if (cta_group == cg && bn == bn_)                                                             \
+        return dtype == GEMM_TF32 ? TcCfg<true, cg, bn_>::SMEM_BYTES : TcCfg<false, cg, bn_>::SMEM_BYTES;
+    TC_VARIANTS(X)
+#undef X
+    return 0;
+}
+
+int tc_stages(int dtype, int cta_group, int bn) {
+#define X(cg, bn_)                                                                         \
+    if (cta_group == cg && bn == bn_)                                                       \
+        return dtype == GEMM_TF32 ? TcCfg<true, cg, bn_>::STAGES : TcCfg<false, cg, bn_>::STAGES;
+    TC_VARIANTS(X)
+#undef X
+    return 0;
+}
+
+int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
+              int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+              size_t errlen) {
+#define X(cg, bn_)                                                                                        \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                          \
+        if (dtype == GEMM_TF32)                                                                            \
+            return launch_variant<true, cg, bn_>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream, \
+                                                 err, errlen);                                             \
+        return launch_variant<false, cg, bn_>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream,   \
+                                              err, errlen);                                                \
+    }
+    TC_VARIANTS(X)
+#undef X
+    std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d", plan.cta_group, plan.bn);
+    return GEMM_ERR_UNSUPPORTED;
+}
+
+cudaError_t tc_read_and_clear_status(uint32_t words[4]) {
+    cudaError_t e = cudaMemcpyFromSymbol(words, g_tc_status, sizeof(uint32_t) * 4);
+    if (e != cudaSuccess) return e;
+    static const uint32_t zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_tc_status, zero, sizeof zero);
+}
+
+int tc_max_active_clusters(int device) {
+    (void)device;
+    using Cf = TcCfg<false, 2, 256>;
+    auto kern = tc_gemm_kernel<false, 2, 256>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace tcgemm
