@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("bf16_8192", "tf32_4096", "fp32_4096"), default="bf16_8192",
+                    help="timed workload (default: the headline 8192^3 BF16 GEMM)")
     ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -66,23 +68,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources; profile figures taken from an older build are not reused."""
+def source_digest(files) -> str:
+    """Digest of a kernel's source files; profile figures taken from other sources are not reused."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_tensor_core_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(key: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+    """DRAM bytes per launch from a committed ncu summary (profiles/ncu_traffic.json),
+    or None if the kernel's sources changed since that capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)[key]
-        if d.get("source_digest") == source_digest():
+        if d.get("source_digest") == source_digest(d["source_files"]):
             return float(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -326,7 +329,8 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device)
 
-    w = C4_BF16_8192
+    w = {"bf16_8192": C4_BF16_8192, "tf32_4096": C3_TF32_4096, "fp32_4096": C3_FP32_4096}[args.workload]
+    headline = args.workload == "bf16_8192"
     sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -352,26 +356,40 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    in_bytes = (w.M * w.K + w.K * w.N) * (2 if w.dtype == "bf16" else 4)
+    desc = {"bf16_8192": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), fp32 accumulate "
+                         "and output, row-major, persistent tcgen05 path",
+            "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
+                         "accumulate and output, row-major, persistent tcgen05 path",
+            "fp32_4096": "fp32 GEMM M=N=K=4096, A,B ~ N(0,1) (seed 2), exact fp32 on the CUDA cores (SIMT)"}
+    if w.dtype == "fp32":
+        sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
+        roof = roofline_alu(res["flops"], res["launch_ms_mean"], sm_mhz)
+    elif w.dtype == "tf32":
+        roof = roofline_tensor(res["flops"], res["launch_ms_mean"],
+                               peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"],
+                               f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}", NOMINAL_DENSE_TFLOPS["tf32"],
+                               profiled_traffic(args.workload))
+    else:
+        roof = roofline_tensor(res["flops"], res["launch_ms_mean"], peaks["bf16_tflops"],
+                               f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
+                               profiled_traffic(args.workload))
+        roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), "
-                               "fp32 accumulate and output, row-major, persistent tcgen05 path",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": desc[args.workload],
                    "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (268 MB of operands, 537 MB with C, vs 129 MB L2); no flush",
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of operands vs 129 MB L2); no flush",
                    "plan": res["plan"]},
-        "roofline": roofline_tensor(res["flops"], res["launch_ms_mean"], peaks["bf16_tflops"],
-                                    f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
-                                    profiled_traffic("bf16_8192")),
+        "roofline": roof,
         "kernel_ms": {"mean": round(res["launch_ms_mean"], 5), "median": round(res["launch_ms_median"], 5),
                       "min": round(res["launch_ms_min"], 5)},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": clocks,
     }
-    out["roofline"]["frac_of_sustained"] = round(out["roofline"]["achieved"] / peaks["bf16_tflops_sustained"], 4)
-
-    if not args.no_paths:
+    if not args.no_paths and headline:
         sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
         paths = {}
         n_side = max(3, min(args.steps, 100))

@@ -83,7 +83,9 @@ typedef enum {
  * 16 bytes) are first copied into a stream-ordered workspace with a padded
  * pitch; that workspace is allocated and freed on the stream
  * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
- * unavailable.  C with such a layout is written by ordinary stores instead of
+ * unavailable.  For GEMM_TF32, B is first transposed into the same kind of
+ * workspace, because the TF32 tensor-core instruction reads its B operand
+ * K-major.  C with such a layout is written by ordinary stores instead of
  * TMA stores.
  *
  * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
@@ -117,6 +119,9 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
  *   "simt_tile"      force the SIMT tile: 128 (128x128) or 64 (64x64)
+ *   "tc_b_major"     0 auto (BF16: B read as stored, N-major; TF32: B read
+ *                    from a K-major transposed copy), 1 force the transposed
+ *                    copy, 2 force reading B as stored
  *   "wait_timeout_ms" bound on every in-kernel wait (default 2000)
  * Returns GEMM_ERR_INVALID_ARG for an unknown key or an out-of-range value.
  */
@@ -139,6 +144,7 @@ typedef struct {
     int32_t tma_store;   /* epilogue writes C with TMA stores              */
     int32_t vec;         /* SIMT: 16-byte vector loads/stores legal        */
     int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
+    int32_t b_kmajor;    /* B staged K-major from a transposed copy (TF32)  */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

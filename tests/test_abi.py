@@ -95,7 +95,8 @@ def test_plan_8192_bf16_uses_cta_pairs_full_machine():
 
 def test_plan_tf32_and_fp32_4096():
     p = _plan(4096, 4096, 4096, tg.GEMM_TF32)
-    assert p["path"] == 1 and p["bk"] == 32
+    assert p["path"] == 1 and p["bk"] == 32 and p["b_kmajor"] == 1 and p["pack_b"] == 0
+    assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["b_kmajor"] == 0
     s = _plan(4096, 4096, 4096, tg.GEMM_FP32)
     assert s["path"] == 0 and s["bm"] == 128 and s["vec"] == 1 and s["grid"] == 32 * 32
 
@@ -126,6 +127,11 @@ def test_plan_low_tile_count_uses_narrow_tiles():
 
 def test_plan_forced_options():
     try:
+        assert tg.gemm_set_option("tc_b_major", 1) == 0
+        assert _plan(512, 512, 512, tg.GEMM_BF16)["b_kmajor"] == 1
+        assert tg.gemm_set_option("tc_b_major", 2) == 0
+        assert _plan(512, 512, 512, tg.GEMM_TF32)["b_kmajor"] == 0
+        assert tg.gemm_set_option("tc_b_major", 0) == 0
         assert tg.gemm_set_option("tc_cta_group", 1) == 0
         assert tg.gemm_set_option("tc_bn", 128) == 0
         p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
@@ -133,7 +139,7 @@ def test_plan_forced_options():
         assert tg.gemm_set_option("tc_max_ctas", 10) == 0
         assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["grid"] == 10
     finally:
-        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas"):
+        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas", "tc_b_major"):
             tg.gemm_set_option(k, 0)
 
 

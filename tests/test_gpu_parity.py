@@ -30,7 +30,7 @@ DTYPES = ("fp32", "tf32", "bf16")
 def lib():
     tgbuild.build()
     tg.load_library()
-    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_tile"):
+    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_tile", "tc_b_major"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -110,12 +110,18 @@ def test_deterministic(dtype):
 TC_VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 256)]
 
 
-@pytest.mark.parametrize("dtype", ("tf32", "bf16"))
+# (dtype, B staging): BF16 reads B as stored (N-major) or from the K-major
+# transposed copy; TF32 always uses the K-major copy.
+TC_OPERANDS = [("bf16", 2), ("bf16", 1), ("tf32", 1)]
+
+
+@pytest.mark.parametrize("operands", TC_OPERANDS, ids=lambda o: f"{o[0]}_{'kmajorB' if o[1] == 1 else 'nmajorB'}")
 @pytest.mark.parametrize("variant", TC_VARIANTS, ids=lambda v: f"cg{v[0]}_bn{v[1]}")
 @pytest.mark.parametrize("tma_store", (1, 2), ids=("tma_store", "plain_store"))
 @pytest.mark.parametrize("shape", [(300, 700, 1000), (1024, 768, 333), (2048, 1536, 256)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_every_tensor_core_variant_exact(dtype, variant, tma_store, shape):
+def test_every_tensor_core_variant_exact(operands, variant, tma_store, shape):
+    dtype, b_major = operands
     cg, bn = variant
     M, N, K = shape
     A, B = make_operands(M, N, K, dtype, "ints", seed=17)
@@ -123,12 +129,13 @@ def test_every_tensor_core_variant_exact(dtype, variant, tma_store, shape):
         tg.gemm_set_option("tc_cta_group", cg)
         tg.gemm_set_option("tc_bn", bn)
         tg.gemm_set_option("tc_tma_store", tma_store)
+        tg.gemm_set_option("tc_b_major", b_major)
         _exact(A, B, dtype)
         # fewer persistent CTAs than tiles: several tiles per CTA, both accumulators
         tg.gemm_set_option("tc_max_ctas", 2 * cg)
         _exact(A, B, dtype)
     finally:
-        for k in ("tc_cta_group", "tc_bn", "tc_tma_store", "tc_max_ctas"):
+        for k in ("tc_cta_group", "tc_bn", "tc_tma_store", "tc_max_ctas", "tc_b_major"):
             tg.gemm_set_option(k, 0)
 
 

@@ -137,9 +137,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.bm = 128;
     p.bk = 128 / elem;
     p.pack_a = (a_addr % 16 != 0) || ((lda * elem) % 16 != 0);
-    p.pack_b = (b_addr % 16 != 0) || ((ldb * elem) % 16 != 0);
     if (p.pack_a) out->lda_eff = round_up(K, 16 / elem);
-    if (p.pack_b) out->ldb_eff = round_up(N, 16 / elem);
+    // B is read as stored (N-major) for BF16; TF32 reads a K-major transposed copy.
+    p.b_kmajor = opt.tc_b_major == 1 ? 1 : opt.tc_b_major == 2 ? 0 : (dtype == GEMM_TF32 ? 1 : 0);
+    if (p.b_kmajor) {
+        p.pack_b = 0;
+        out->ldb_eff = round_up(K, 16 / elem);
+    } else {
+        p.pack_b = (b_addr % 16 != 0) || ((ldb * elem) % 16 != 0);
+        if (p.pack_b) out->ldb_eff = round_up(N, 16 / elem);
+    }
     const bool c_tma_ok = (c_addr % 16 == 0) && ((ldc * 4) % 16 == 0);
     p.tma_store = (opt.tc_tma_store == 2) ? 0 : (c_tma_ok ? 1 : 0);
 
@@ -164,14 +171,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     } else if (bn == 0) {
         bn = 256;
     }
-    if (tc_smem_bytes(dtype, cg, bn) == 0)
+    if (tc_smem_bytes(dtype, cg, bn, p.b_kmajor != 0) == 0)
         return fail(GEMM_ERR_UNSUPPORTED, "no tensor-core variant with cta_group=%d, BN=%d", cg, bn);
     if (cg == 2 && max_clusters_2cta <= 0)
         return fail(GEMM_ERR_UNSUPPORTED, "2-CTA tiles need cluster support on this device");
     p.cta_group = cg;
     p.bn = bn;
-    p.stages = tc_stages(dtype, cg, bn);
-    p.smem_bytes = tc_smem_bytes(dtype, cg, bn);
+    p.stages = tc_stages(dtype, cg, bn, p.b_kmajor != 0);
+    p.smem_bytes = tc_smem_bytes(dtype, cg, bn, p.b_kmajor != 0);
     p.group_m = opt.tc_group_m > 0 ? opt.tc_group_m : (cg == 2 ? 8 : 16);
     const int64_t tiles = tiles_of(cg, bn);
     p.tiles = (int32_t)tiles;
@@ -214,6 +221,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "simt_tile")) {
         if (v != 0 && v != 64 && v != 128) return fail(GEMM_ERR_INVALID_ARG, "simt_tile must be 0, 64 or 128");
         g_opt.simt_tile = (int)v;
+    } else if (!std::strcmp(key, "tc_b_major")) {
+        if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_b_major must be 0, 1 or 2");
+        g_opt.tc_b_major = (int)v;
     } else if (!std::strcmp(key, "wait_timeout_ms")) {
         if (v < 1 || v > 600000) return fail(GEMM_ERR_INVALID_ARG, "wait_timeout_ms must be in [1, 600000]");
         g_opt.wait_timeout_ms = (int)v;
@@ -232,6 +242,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_max_ctas")) return o.tc_max_ctas;
     if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
     if (!std::strcmp(key, "simt_tile")) return o.simt_tile;
+    if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;
     if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
     return -1;
 }
@@ -331,9 +342,10 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     const void *Ause = A, *Buse = B;
     void *ws = nullptr;
     const uint64_t a_bytes = p.pack_a ? (uint64_t)M * plan.lda_eff * eb : 0;
-    const uint64_t b_bytes = p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
+    const uint64_t b_bytes = p.b_kmajor ? (uint64_t)N * plan.ldb_eff * eb
+                             : p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
     const uint64_t a_off = 0, b_off = (a_bytes + 255) / 256 * 256;
-    if (p.pack_a || p.pack_b) {
+    if (p.pack_a || p.pack_b || p.b_kmajor) {
         e = cudaMallocAsync(&ws, (size_t)(b_off + b_bytes), stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -345,7 +357,10 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
             e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, stream);
             Ause = w + a_off;
         }
-        if (e == cudaSuccess && p.pack_b) {
+        if (e == cudaSuccess && p.b_kmajor) {
+            e = transpose_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
+            Buse = w + b_off;
+        } else if (e == cudaSuccess && p.pack_b) {
             e = pack_rows_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
             Buse = w + b_off;
         }

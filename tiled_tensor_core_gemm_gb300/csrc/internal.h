@@ -17,6 +17,7 @@ struct Options {
     int tc_max_ctas = 0;       // 0 auto
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_tile = 0;         // 0 auto, 128 or 64
+    int tc_b_major = 0;        // 0 auto (BF16 as stored, TF32 transposed), 1 K-major copy, 2 as stored
     int wait_timeout_ms = 2000;
 };
 Options options_snapshot();
@@ -42,11 +43,12 @@ cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K,
 // ----------------------------------------------------------- tensor cores ---
 // Fills plan-dependent shared-memory size (bytes) for a tensor-core variant,
 // or returns 0 if the variant is not compiled in.
-int tc_smem_bytes(int dtype, int cta_group, int bn);
-int tc_stages(int dtype, int cta_group, int bn);
+int tc_smem_bytes(int dtype, int cta_group, int bn, bool b_kmajor);
+int tc_stages(int dtype, int cta_group, int bn, bool b_kmajor);
 
 // Encodes the tensor maps and launches the persistent kernel.  A/B are the
-// (possibly packed) operands with the leading dimensions the plan reports.
+// (possibly packed) operands with the leading dimensions the plan reports;
+// with plan.b_kmajor, B is the transposed copy (N x K, leading dimension ldb).
 // Returns a gemm_status_t.
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
               const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -64,6 +66,10 @@ int tc_max_active_clusters(int device);
 // dst[r * ld_dst + c] = src[r * ld_src + c] for r < rows, c < cols (elem bytes
 // each); dst columns [cols, ld_dst) are zeroed.
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+// dst[c * ld_dst + r] = src[r * ld_src + c] for r < rows, c < cols.
+cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
 
 }  // namespace tcgemm

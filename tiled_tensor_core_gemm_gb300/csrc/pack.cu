@@ -1,11 +1,16 @@
-// Operand pack: copy a row-major matrix into a buffer whose row pitch the TMA
+// Operand pack and transpose.
+//
+// Pack: copy a row-major matrix into a buffer whose row pitch the TMA
 // engine can address.  "Learn CuTeDSL" section 3.4: every stride of a TMA
 // tensor other than the contiguous one must be a multiple of 16 bytes (and the
 // base 16-byte aligned); a K x N BF16 matrix with N = 4095 has an 8190-byte
 // pitch and cannot be described.  The copy rounds the pitch up to a multiple of
 // 16 bytes and zero-fills the extra columns.
 //
-// HBM-bound: one read and one write of the operand.  The grid is a multiple of
+// Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the TF32
+// path, whose tensor-core instruction reads B K-major.
+//
+// Both are HBM-bound: one read and one write of the operand.  The grid is a multiple of
 // the SM count; each warp walks whole rows so both sides stay coalesced even
 // though the source rows start at arbitrary 2- or 4-byte offsets.
 #include "internal.h"
@@ -26,13 +31,62 @@ __global__ void __launch_bounds__(256) pack_rows(const T *__restrict__ src, int6
     }
 }
 
+// 32 x 32 tiles through shared memory so both the read of `src` rows and the
+// write of `dst` rows are coalesced; the +1 column breaks bank conflicts on the
+// transposed read.
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_tiles(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
+                                                       int64_t ld_dst, int64_t rows, int64_t cols) {
+    __shared__ T tile[32][33];
+    const int64_t tiles_c = (cols + 31) / 32;
+    const int64_t tiles = ((rows + 31) / 32) * tiles_c;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+        for (int i = ty; i < 32; i += 8) {
+            const int64_t r = r0 + i, c = c0 + tx;
+            tile[i][tx] = (r < rows && c < cols) ? src[r * ld_src + c] : T(0);
+        }
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int64_t c = c0 + i, r = r0 + tx;
+            if (c < cols && r < rows) dst[c * ld_dst + r] = tile[tx][i];
+        }
+        __syncthreads();
+    }
+}
+
+int sm_count(cudaError_t *err) {
+    int dev = 0, sms = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err == cudaSuccess) *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
 }  // namespace
+
+cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                             int elem_bytes, cudaStream_t stream) {
+    cudaError_t e;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+    const int blocks = (int)(tiles < (int64_t)sms * 8 ? (tiles > 0 ? tiles : 1) : (int64_t)sms * 8);
+    if (elem_bytes == 2)
+        transpose_tiles<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
+                                                              static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    else if (elem_bytes == 4)
+        transpose_tiles<uint32_t><<<blocks, 256, 0, stream>>>(static_cast<const uint32_t *>(src), ld_src,
+                                                              static_cast<uint32_t *>(dst), ld_dst, rows, cols);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
 
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols,
                              int elem_bytes, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e;
+    const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
     const int64_t want = (rows + 7) / 8;   // 8 warps per block, one row per warp per pass
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);

@@ -60,7 +60,7 @@ constexpr int kBarBytes = 256;
 
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
-template <bool TF32, int CG, int BN>
+template <bool TF32, int CG, int BN, bool BKM>
 struct TcCfg {
     static constexpr int ELEM = TF32 ? 4 : 2;
     static constexpr int BK = 128 / ELEM;           // one 128-byte swizzle row of K
@@ -71,7 +71,9 @@ struct TcCfg {
     static constexpr int B_CHUNKS = BN_CTA / CHUNK_COLS;
     static constexpr int B_CHUNK_BYTES = BK * 128;  // one column chunk: BK rows x 128 B
     static constexpr int A_BYTES = kBM * 128;
-    static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;
+    // B K-major (a transposed copy, N x K): one box of BN_CTA rows x 128 bytes.
+    // B MN-major (as stored, K x N): B_CHUNKS boxes of BK rows x 128 bytes.
+    static constexpr int B_BYTES = BKM ? BN_CTA * 128 : B_CHUNKS * B_CHUNK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int B_KSTEP_BYTES = (UMMA_K / 8) * 1024;  // 8 K-rows per 1024-byte swizzle atom
     static constexpr int STAGES_FIT = (kSmemBudget - 1024 - kEpiBytes - kBarBytes) / STAGE_BYTES;
@@ -80,12 +82,14 @@ struct TcCfg {
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     // Instruction descriptor: D f32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12:
     // bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A K-major (bit 15 = 0),
-    // B MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+    // B MN-major (bit 16 = 1) or K-major (0), N >> 3 in bits 17-22, M >> 4 in
+    // bits 24-28.
     static constexpr uint32_t FMT = TF32 ? 2u : 1u;
-    static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | (1u << 16) |
+    static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((BKM ? 0u : 1u) << 16) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((kBM * CG) >> 4) << 24);
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N out of range");
-    static_assert(BN_CTA % CHUNK_COLS == 0 && B_CHUNKS >= 1, "B tile must be whole 128-byte chunks");
+    static_assert(BKM || (BN_CTA % CHUNK_COLS == 0 && B_CHUNKS >= 1), "B tile must be whole 128-byte chunks");
+    static_assert(BN_CTA <= 256, "TMA box rows");
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
@@ -136,11 +140,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-template <bool TF32, int CG, int BN>
+template <bool TF32, int CG, int BN, bool BKM>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-    using Cf = TcCfg<TF32, CG, BN>;
+    using Cf = TcCfg<TF32, CG, BN, BKM>;
     constexpr bool kPair = CG == 2;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
@@ -212,15 +216,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const int k0 = kb * Cf::BK;
                     if (!kPair) {
                         ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
+                        if (BKM) {
+                            ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                            ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb, n0 + c * Cf::CHUNK_COLS, k0);
+                            for (int c = 0; c < Cf::B_CHUNKS; ++c)
+                                ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb, n0 + c * Cf::CHUNK_COLS, k0);
+                        }
                     } else {
                         const uint32_t fb_even = ptx::mapa_shared(fb, 0);
                         ptx::tma_load_2d_pair(sa, &tmA, fb_even, k0, m0);
+                        if (BKM) {
+                            ptx::tma_load_2d_pair(sb, &tmB, fb_even, k0, n0);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                            ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb_even, n0 + c * Cf::CHUNK_COLS, k0);
+                            for (int c = 0; c < Cf::B_CHUNKS; ++c)
+                                ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb_even, n0 + c * Cf::CHUNK_COLS,
+                                                      k0);
+                        }
                     }
                     if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -265,10 +278,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
                         // A: K-major, 8-row groups 1024 B apart; K advances 32 B inside the swizzle row.
                         const uint64_t adesc = ptx::sdesc_sw128(sa + 32u * kk, 16u, 1024u);
-                        // B: MN-major, 128-byte column chunks B_CHUNK_BYTES apart (leading),
-                        // 8-row K groups 1024 B apart (stride).
-                        const uint64_t bdesc = ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk),
-                                                                (uint32_t)Cf::B_CHUNK_BYTES, 1024u);
+                        // B K-major: laid out like A.  B MN-major: 128-byte column chunks
+                        // B_CHUNK_BYTES apart (leading), 8-row K groups 1024 B apart (stride).
+                        const uint64_t bdesc =
+                            BKM ? ptx::sdesc_sw128(sb + 32u * kk, 16u, 1024u)
+                                : ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
+                                                   1024u);
                         ptx::mma<CG, TF32>(d_tmem, adesc, bdesc, Cf::IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
@@ -397,23 +412,25 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const voi
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool TF32, int CG, int BN>
+template <bool TF32, int CG, int BN, bool BKM>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
                    int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
                    size_t errlen) {
-    using Cf = TcCfg<TF32, CG, BN>;
+    using Cf = TcCfg<TF32, CG, BN, BKM>;
     const CUtensorMapDataType dt = TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb, tc;
     std::memset(&tc, 0, sizeof tc);
     CUresult r = encode_2d(&ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
-    if (r == CUDA_SUCCESS) r = encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
+    if (r == CUDA_SUCCESS)
+        r = BKM ? encode_2d(&tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
+                : encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
     if (r == CUDA_SUCCESS && plan.tma_store)
         r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
     if (r != CUDA_SUCCESS) {
         std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
         return GEMM_ERR_CUDA;
     }
-    auto kern = tc_gemm_kernel<TF32, CG, BN>;
+    auto kern = tc_gemm_kernel<TF32, CG, BN, BKM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -461,19 +478,25 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
 // The variants compiled in: (cta_group, BN) in {(1,64), (1,128), (1,256), (2,256)}.
 #define TC_VARIANTS(X) X(1, 64) X(1, 128) X(1, 256) X(2, 256)
 
-int tc_smem_bytes(int dtype, int cta_group, int bn) {
-#define X(cg, bn_)                                                                               \
-    if (cta_group == cg && bn == bn_)                                                             \
-        return dtype == GEMM_TF32 ? TcCfg<true, cg, bn_>::SMEM_BYTES : TcCfg<false, cg, bn_>::SMEM_BYTES;
+template <bool TF32, int CG, int BN>
+int cfg_value(bool bkm, bool stages) {
+    if (bkm) return stages ? TcCfg<TF32, CG, BN, true>::STAGES : TcCfg<TF32, CG, BN, true>::SMEM_BYTES;
+    return stages ? TcCfg<TF32, CG, BN, false>::STAGES : TcCfg<TF32, CG, BN, false>::SMEM_BYTES;
+}
+
+int tc_smem_bytes(int dtype, int cta_group, int bn, bool b_kmajor) {
+#define X(cg, bn_)                                                                         \
+    if (cta_group == cg && bn == bn_)                                                       \
+        return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, false) : cfg_value<false, cg, bn_>(b_kmajor, false);
     TC_VARIANTS(X)
 #undef X
     return 0;
 }
 
-int tc_stages(int dtype, int cta_group, int bn) {
+int tc_stages(int dtype, int cta_group, int bn, bool b_kmajor) {
 #define X(cg, bn_)                                                                         \
     if (cta_group == cg && bn == bn_)                                                       \
-        return dtype == GEMM_TF32 ? TcCfg<true, cg, bn_>::STAGES : TcCfg<false, cg, bn_>::STAGES;
+        return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, true) : cfg_value<false, cg, bn_>(b_kmajor, true);
     TC_VARIANTS(X)
 #undef X
     return 0;
@@ -482,13 +505,17 @@ int tc_stages(int dtype, int cta_group, int bn) {
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
               int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
               size_t errlen) {
-#define X(cg, bn_)                                                                                        \
-    if (plan.cta_group == cg && plan.bn == bn_) {                                                          \
-        if (dtype == GEMM_TF32)                                                                            \
-            return launch_variant<true, cg, bn_>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream, \
-                                                 err, errlen);                                             \
-        return launch_variant<false, cg, bn_>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream,   \
-                                              err, errlen);                                                \
+#define X(cg, bn_)                                                                                             \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                               \
+        if (dtype == GEMM_TF32)                                                                                 \
+            return plan.b_kmajor ? launch_variant<true, cg, bn_, true>(plan, M, N, K, A, lda, B, ldb, C, ldc,    \
+                                                                       timeout_ms, stream, err, errlen)         \
+                                 : launch_variant<true, cg, bn_, false>(plan, M, N, K, A, lda, B, ldb, C, ldc,   \
+                                                                        timeout_ms, stream, err, errlen);       \
+        return plan.b_kmajor ? launch_variant<false, cg, bn_, true>(plan, M, N, K, A, lda, B, ldb, C, ldc,       \
+                                                                    timeout_ms, stream, err, errlen)            \
+                             : launch_variant<false, cg, bn_, false>(plan, M, N, K, A, lda, B, ldb, C, ldc,      \
+                                                                     timeout_ms, stream, err, errlen);          \
     }
     TC_VARIANTS(X)
 #undef X
@@ -505,8 +532,8 @@ cudaError_t tc_read_and_clear_status(uint32_t words[4]) {
 
 int tc_max_active_clusters(int device) {
     (void)device;
-    using Cf = TcCfg<false, 2, 256>;
-    auto kern = tc_gemm_kernel<false, 2, 256>;
+    using Cf = TcCfg<false, 2, 256, false>;
+    auto kern = tc_gemm_kernel<false, 2, 256, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;
