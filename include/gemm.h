@@ -151,6 +151,38 @@ GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
               uint64_t a_addr, int64_t lda, uint64_t b_addr, int64_t ldb,
               uint64_t c_addr, int64_t ldc, int32_t num_sms, gemm_plan_t *out);
 
+/*
+ * gemm_run_tf32_static -- C = A . B with GEMM_TF32 arithmetic, allocating
+ * nothing.  The pages describe no counterpart; this is a service entry point.
+ *
+ * Who needs it: gemm_run's TF32 path allocates a workspace on the stream for a
+ * transposed copy of B.  Callers that cannot allocate device memory while they
+ * run -- processes that give all free device memory to their own allocator at
+ * start-up, or services that forbid device allocation after start-up because
+ * an allocation can block on the device or fragment memory -- use this entry
+ * point instead.  Its scratch is one fixed array of
+ * GEMM_TF32_STATIC_SCRATCH_BYTES that the library reserves on every GPU it is
+ * loaded on and keeps until the process exits.
+ *
+ * Arguments, layouts, ownership and results are those of gemm_run with
+ * dtype = GEMM_TF32 (A, B, C float device pointers, leading dimensions in
+ * elements, the caller's stream).  Extra limits, each reported as an error
+ * with a message in gemm_last_error():
+ *   - N * roundup(K, 4) must not exceed GEMM_TF32_STATIC_SCRATCH_BYTES / 4
+ *     floats (GEMM_ERR_INVALID_ARG);
+ *   - A must start on a 16-byte boundary with lda a multiple of 4
+ *     (GEMM_ERR_UNSUPPORTED): there is no scratch for a copy of A.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (no call needs it zeroed); calls whose GPU work overlaps -- e.g. on
+ * two unordered streams -- race on it, so order them.
+ */
+#define GEMM_TF32_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
+GEMM_API int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K,
+                                  const float *A, int64_t lda, const float *B, int64_t ldb,
+                                  float *C, int64_t ldc, struct CUstream_st *stream);
+
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 GEMM_API int gemm_version(void);
 

@@ -31,7 +31,8 @@ GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_NO_MEMORY = 5
 
 EXPORTED = ("gemm_run", "gemm_last_error", "gemm_get_status", "gemm_set_option",
-            "gemm_get_option", "gemm_plan", "gemm_version")
+            "gemm_get_option", "gemm_plan", "gemm_version", "gemm_run_tf32_static")
+TF32_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # GEMM_TF32_STATIC_SCRATCH_BYTES in include/gemm.h
 
 
 class GemmError(RuntimeError):
@@ -85,6 +86,8 @@ def load_library():
         lib.gemm_plan.restype = ctypes.c_int
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = ctypes.c_int
+        lib.gemm_run_tf32_static.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, p]
+        lib.gemm_run_tf32_static.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -121,6 +124,11 @@ def gemm_plan(M, N, K, dtype, a_addr, lda, b_addr, ldb, c_addr, ldc, num_sms=0) 
 
 def gemm_version() -> int:
     return load_library().gemm_version()
+
+
+def gemm_run_tf32_static(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """TF32 C = A.B that allocates no device memory (scratch in a fixed library array)."""
+    return load_library().gemm_run_tf32_static(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 # ------------------------------------------------------ tensor convenience ---

@@ -397,3 +397,32 @@ int gemm_get_status(struct CUstream_st *stream_) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ shared with other entry points ---
+namespace tcgemm {
+
+int api_error(int code, const char *message) { return fail(code, "%s", message); }
+
+void api_clear_error() { t_err[0] = 0; }
+
+int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb,
+                 const void *C, int64_t ldc) {
+    return validate(M, N, K, dtype, A, lda, B, ldb, C, ldc);
+}
+
+int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev) {
+    return check_device_span(name, p, bytes, dev);
+}
+
+int api_device_info(int dev, int *sms, int *cc_major, int *cc_minor, int *max_clusters) {
+    DevInfo d;
+    int rc = dev_info(dev, &d);
+    if (rc) return rc;
+    *sms = d.sms;
+    *cc_major = d.cc_major;
+    *cc_minor = d.cc_minor;
+    *max_clusters = d.max_clusters;
+    return GEMM_OK;
+}
+
+}  // namespace tcgemm

@@ -72,4 +72,15 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
 
+// ------------------------------------------- helpers shared by entry points ---
+// Defined in gemm_api.cu.  api_error records a message for gemm_last_error()
+// and returns `code`; the others are the argument, pointer and device checks
+// gemm_run applies.
+int api_error(int code, const char *message);
+void api_clear_error();
+int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
+                 int64_t ldb, const void *C, int64_t ldc);
+int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev);
+int api_device_info(int dev, int *sms, int *cc_major, int *cc_minor, int *max_clusters);
+
 }  // namespace tcgemm
