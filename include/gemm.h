@@ -118,11 +118,18 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_max_ctas"    cap on persistent CTAs (>= 1)
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
- *   "simt_tile"      force the SIMT tile: 128 (128x128) or 64 (64x64)
+ *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8
+ *                    outputs per thread; 2 = same with K step 16; 3 = 128x256,
+ *                    8x16 per thread; 4 = 256x128, 16x8 per thread; 5 = 64x64;
+ *                    6 = 128x256 with K step 16; 7 = 64x64 with K step 16
  *   "tc_b_major"     0 auto (BF16: B read as stored, N-major; TF32: B read
  *                    from a K-major transposed copy), 1 force the transposed
- *                    copy, 2 force reading B as stored
+ *                    copy, 2 force reading B as stored (BF16 only; a TF32
+ *                    call then fails with GEMM_ERR_UNSUPPORTED)
  *   "wait_timeout_ms" bound on every in-kernel wait (default 2000)
+ *   "debug_stall_mma" test hook: 1 makes the tensor-core kernel's MMA thread
+ *                    first wait on a barrier nothing arrives at, so the wait
+ *                    expires and gemm_get_status() reports GEMM_ERR_TIMEOUT
  * Returns GEMM_ERR_INVALID_ARG for an unknown key or an out-of-range value.
  */
 GEMM_API int gemm_set_option(const char *key, int64_t value);

@@ -79,6 +79,8 @@ def test_options_roundtrip_and_validation():
     assert tg.gemm_set_option("no_such_key", 1) == tg.GEMM_ERR_INVALID_ARG
     assert tg.gemm_get_option("no_such_key") == -1
     assert tg.gemm_get_option("wait_timeout_ms") == 2000
+    assert tg.gemm_get_option("debug_stall_mma") == 0
+    assert tg.gemm_set_option("debug_stall_mma", 2) == tg.GEMM_ERR_INVALID_ARG
 
 
 def _plan(M, N, K, dt, lda=None, ldb=None, ldc=None, a=0, b=0, c=0, sms=152):
@@ -98,7 +100,7 @@ def test_plan_tf32_and_fp32_4096():
     assert p["path"] == 1 and p["bk"] == 32 and p["b_kmajor"] == 1 and p["pack_b"] == 0
     assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["b_kmajor"] == 0
     s = _plan(4096, 4096, 4096, tg.GEMM_FP32)
-    assert s["path"] == 0 and s["bm"] == 128 and s["vec"] == 1 and s["grid"] == 32 * 32
+    assert s["path"] == 0 and s["bm"] == 128 and s["bk"] == 16 and s["vec"] == 1 and s["grid"] == 32 * 32
 
 
 def test_plan_small_fp32_shrinks_tile_to_fill_machine():
@@ -130,7 +132,9 @@ def test_plan_forced_options():
         assert tg.gemm_set_option("tc_b_major", 1) == 0
         assert _plan(512, 512, 512, tg.GEMM_BF16)["b_kmajor"] == 1
         assert tg.gemm_set_option("tc_b_major", 2) == 0
-        assert _plan(512, 512, 512, tg.GEMM_TF32)["b_kmajor"] == 0
+        assert _plan(512, 512, 512, tg.GEMM_BF16)["b_kmajor"] == 0
+        with pytest.raises(tg.GemmError, match="K-major copy"):
+            _plan(512, 512, 512, tg.GEMM_TF32)
         assert tg.gemm_set_option("tc_b_major", 0) == 0
         assert tg.gemm_set_option("tc_cta_group", 1) == 0
         assert tg.gemm_set_option("tc_bn", 128) == 0

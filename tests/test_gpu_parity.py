@@ -30,7 +30,8 @@ DTYPES = ("fp32", "tf32", "bf16")
 def lib():
     tgbuild.build()
     tg.load_library()
-    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_tile", "tc_b_major"):
+    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
+              "debug_stall_mma"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -139,14 +140,17 @@ def test_every_tensor_core_variant_exact(operands, variant, tma_store, shape):
             tg.gemm_set_option(k, 0)
 
 
-@pytest.mark.parametrize("tile", (64, 128))
-def test_simt_tiles_exact(tile):
-    A, B = make_operands(513, 389, 1027, "fp32", "ints", seed=18)
+@pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7))
+@pytest.mark.parametrize("shape", [(513, 389, 1027), (300, 520, 64), (1, 1000, 17)], ids=lambda s: "x".join(map(str, s)))
+def test_simt_variants_exact(variant, shape):
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "fp32", "ints", seed=18)
     try:
-        tg.gemm_set_option("simt_tile", tile)
+        tg.gemm_set_option("simt_variant", variant)
         _exact(A, B, "fp32")
+        _exact(A, B, "fp32", a_offset=1, ldc_pad=1)   # scalar (non-vector) loads and stores
     finally:
-        tg.gemm_set_option("simt_tile", 0)
+        tg.gemm_set_option("simt_variant", 0)
 
 
 # ------------------------------------------------------- published workloads ---
@@ -169,3 +173,33 @@ def test_workload_sampled_rows(w):
     Cref, D = oracle_rows(A, B, w.dtype, rows)
     r = error_ratio(C[rows], Cref, D)
     assert r <= TOL[w.dtype], r
+
+
+# ------------------------------------------------------------ bounded waits ---
+@pytest.mark.parametrize("cta_group", (1, 2))
+def test_expired_wait_reports_timeout_and_context_survives(cta_group):
+    """The MMA thread waits on an mbarrier nothing arrives at; the wait expires
+    after wait_timeout_ms, the kernel records GEMM_ERR_TIMEOUT and returns, and
+    the next GEMM on the same context is exact."""
+    A, B = make_operands(512, 768, 320, "bf16", "ints", seed=19)
+    stream = torch.cuda.current_stream().cuda_stream
+    try:
+        tg.gemm_set_option("tc_cta_group", cta_group)
+        tg.gemm_set_option("wait_timeout_ms", 200)
+        tg.gemm_set_option("debug_stall_mma", 1)
+        from gemm_check import to_device
+        a_keep, a_ptr, lda = to_device(A)
+        b_keep, b_ptr, ldb = to_device(B)
+        C = torch.empty((512, 768), dtype=torch.float32, device="cuda")
+        rc = tg.gemm_run(512, 768, 320, tg.GEMM_BF16, a_ptr, lda, b_ptr, ldb, C.data_ptr(), 768, stream)
+        assert rc == tg.GEMM_OK, tg.gemm_last_error()
+        st = tg.gemm_get_status(stream)
+        assert st == tg.GEMM_ERR_TIMEOUT, (st, tg.gemm_last_error())
+        assert "role=mma" in tg.gemm_last_error()
+        assert tg.gemm_get_status(stream) == tg.GEMM_OK   # the status word was cleared
+        tg.gemm_set_option("debug_stall_mma", 0)
+        _exact(A, B, "bf16")
+    finally:
+        tg.gemm_set_option("debug_stall_mma", 0)
+        tg.gemm_set_option("wait_timeout_ms", 2000)
+        tg.gemm_set_option("tc_cta_group", 0)

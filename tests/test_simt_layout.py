@@ -4,27 +4,37 @@ The bank model (pinned against the page's printed passes in test_analysis.py)
 is applied to the index expressions of the kernel in
 tiled_tensor_core_gemm_gb300/csrc/simt_fp32.cu: the padded, transposed A tile
 [k][BM+4], the B tile [k][BN], and thread (ty, tx) = (tid / TX, tid % TX) with
-its two 4-wide quads half a tile apart.  No GPU.
+its RM x RN 4-wide quads BM/RM rows and BN/RN columns apart.  No GPU.
 """
 import pytest
 
 from tiled_tensor_core_gemm_gb300.analysis import bank_passes, vector_bank_passes
 
 BK = 8
+# (BM, BN, BK, RM, RN) of the compiled variants 1..7
+VARIANTS = [(128, 128, 8, 2, 2), (128, 128, 16, 2, 2), (128, 256, 8, 2, 4), (256, 128, 8, 4, 2),
+            (64, 64, 8, 2, 2), (128, 256, 16, 2, 4), (64, 64, 16, 2, 2)]
 
 
-@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
-def test_transposed_A_stores_conflict_free(BM, BN):
-    threads = (BM // 8) * (BN // 8)
+def _threads(BM, BN, RM, RN):
+    return (BM // (4 * RM)) * (BN // (4 * RN))
+
+
+@pytest.mark.parametrize("BM,BN,bk,RM,RN", VARIANTS)
+def test_transposed_A_stores(BM, BN, bk, RM, RN):
+    """K step 8: conflict-free; K step 16: at most 2-way (four k-quads, two bank halves)."""
+    threads = _threads(BM, BN, RM, RN)
     lds_a = BM + 4
+    worst = 0
     for warp in range(threads // 32):
-        for i in range(BM * BK // 4 // threads):
+        for i in range(BM * bk // 4 // threads):
             for e in range(4):
                 def addr(t):
                     f = warp * 32 + t + i * threads
-                    r, kq = f // (BK // 4), f % (BK // 4)
+                    r, kq = f // (bk // 4), f % (bk // 4)
                     return (4 * kq + e) * lds_a + r
-                assert bank_passes(addr) == 1
+                worst = max(worst, bank_passes(addr))
+    assert worst == (1 if bk == 8 else 2)
 
 
 @pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
@@ -39,22 +49,23 @@ def test_unpadded_transpose_would_conflict(BM, BN):
     assert threads >= 32
 
 
-@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 64)])
-def test_inner_loop_vector_reads_minimal(BM, BN):
-    TX = BN // 8
+@pytest.mark.parametrize("BM,BN,bk,RM,RN", VARIANTS)
+def test_inner_loop_vector_reads_minimal(BM, BN, bk, RM, RN):
+    TX = BN // (4 * RN)
     lds_a = BM + 4
     k = 5
-    for warp in range((BM // 8) * TX // 32):
-        def a_addr(t):
-            ty = (warp * 32 + t) // TX
-            return 4 * (k * lds_a + ty * 4)
-
-        def b_addr(t):
-            tx = (warp * 32 + t) % TX
-            return 4 * (k * BN + tx * 4)
-        # one pass per quarter-warp phase is the floor for 16-byte accesses
-        assert vector_bank_passes(a_addr, 16) == 4
-        assert vector_bank_passes(b_addr, 16) == 4
+    for warp in range(_threads(BM, BN, RM, RN) // 32):
+        for qm in range(RM):
+            def a_addr(t):
+                ty = (warp * 32 + t) // TX
+                return 4 * (k * lds_a + qm * (BM // RM) + ty * 4)
+            # one pass per quarter-warp phase is the floor for 16-byte accesses
+            assert vector_bank_passes(a_addr, 16) == 4
+        for qn in range(RN):
+            def b_addr(t):
+                tx = (warp * 32 + t) % TX
+                return 4 * (k * BN + qn * (BN // RN) + tx * 4)
+            assert vector_bank_passes(b_addr, 16) == 4
 
 
 def test_B_tile_vector_stores_minimal():

@@ -102,6 +102,12 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int elem_bytes(int dtype) { return dtype == GEMM_BF16 ? 2 : 4; }
 
+// Measured on GB300 at 4096^3 (profiles/picker.md): the 128 x 128 tile with a
+// K step of 16 beats K step 8 (one barrier per 1024 FMAs per thread instead of
+// 512) and the 8 x 16 register tiles.
+constexpr int kSimtLarge = 2;   // 128 x 128 x 16, 8 x 8 per thread
+constexpr int kSimtSmall = 7;   // 64 x 64 x 16
+
 }  // namespace
 
 Options options_snapshot() {
@@ -117,19 +123,24 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     out->ldb_eff = ldb;
     if (num_sms <= 0) num_sms = 1;
     if (dtype == GEMM_FP32) {
-        int tile = opt.simt_tile;
-        if (tile == 0) tile = cdiv(M, 128) * cdiv(N, 128) >= num_sms ? 128 : 64;
+        // Large problems: the 128 x 128 tile; if that leaves SMs idle, 64 x 64.
+        int id = opt.simt_variant;
+        if (id == 0) id = cdiv(M, 128) * cdiv(N, 128) >= num_sms ? kSimtLarge : kSimtSmall;
+        int bm = 0, bn = 0, bk = 0, smem = 0;
+        if (!simt_variant_tile(id, &bm, &bn, &bk, &smem))
+            return fail(GEMM_ERR_UNSUPPORTED, "no SIMT variant %d", id);
         p.path = 0;
-        p.bm = p.bn = tile;
-        p.bk = 8;
+        p.bm = bm;
+        p.bn = bn;
+        p.bk = bk;
         p.stages = 2;
         p.cta_group = 1;
         p.group_m = 1;
-        p.tiles = (int32_t)(cdiv(M, tile) * cdiv(N, tile));
+        p.tiles = (int32_t)(cdiv(M, bm) * cdiv(N, bn));
         p.grid = p.tiles;
         p.vec = (lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && a_addr % 16 == 0 && b_addr % 16 == 0 &&
                  c_addr % 16 == 0);
-        p.smem_bytes = 2 * 8 * ((tile + 4) + tile) * 4;
+        p.smem_bytes = smem;
         return GEMM_OK;
     }
     const int elem = elem_bytes(dtype);
@@ -138,7 +149,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.bk = 128 / elem;
     p.pack_a = (a_addr % 16 != 0) || ((lda * elem) % 16 != 0);
     if (p.pack_a) out->lda_eff = round_up(K, 16 / elem);
-    // B is read as stored (N-major) for BF16; TF32 reads a K-major transposed copy.
+    // B is read as stored (N-major) for BF16; TF32 always reads a K-major
+    // transposed copy (the N-major TF32 form gave wrong results on GB300).
+    if (dtype == GEMM_TF32 && opt.tc_b_major == 2)
+        return fail(GEMM_ERR_UNSUPPORTED, "TF32 cannot read B as stored; it needs the K-major copy (tc_b_major 0 or 1)");
     p.b_kmajor = opt.tc_b_major == 1 ? 1 : opt.tc_b_major == 2 ? 0 : (dtype == GEMM_TF32 ? 1 : 0);
     if (p.b_kmajor) {
         p.pack_b = 0;
@@ -171,14 +185,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     } else if (bn == 0) {
         bn = 256;
     }
-    if (tc_smem_bytes(dtype, cg, bn, p.b_kmajor != 0) == 0)
+    if (tc_smem_bytes(dtype, cg, bn, p.b_kmajor) == 0)
         return fail(GEMM_ERR_UNSUPPORTED, "no tensor-core variant with cta_group=%d, BN=%d", cg, bn);
     if (cg == 2 && max_clusters_2cta <= 0)
         return fail(GEMM_ERR_UNSUPPORTED, "2-CTA tiles need cluster support on this device");
     p.cta_group = cg;
     p.bn = bn;
-    p.stages = tc_stages(dtype, cg, bn, p.b_kmajor != 0);
-    p.smem_bytes = tc_smem_bytes(dtype, cg, bn, p.b_kmajor != 0);
+    p.stages = tc_stages(dtype, cg, bn, p.b_kmajor);
+    p.smem_bytes = tc_smem_bytes(dtype, cg, bn, p.b_kmajor);
     p.group_m = opt.tc_group_m > 0 ? opt.tc_group_m : (cg == 2 ? 8 : 16);
     const int64_t tiles = tiles_of(cg, bn);
     p.tiles = (int32_t)tiles;
@@ -218,12 +232,17 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_tma_store")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tma_store must be 0, 1 or 2");
         g_opt.tc_tma_store = (int)v;
-    } else if (!std::strcmp(key, "simt_tile")) {
-        if (v != 0 && v != 64 && v != 128) return fail(GEMM_ERR_INVALID_ARG, "simt_tile must be 0, 64 or 128");
-        g_opt.simt_tile = (int)v;
+    } else if (!std::strcmp(key, "simt_variant")) {
+        int bm, bn, bk, smem;
+        if (v != 0 && !simt_variant_tile((int)v, &bm, &bn, &bk, &smem))
+            return fail(GEMM_ERR_INVALID_ARG, "simt_variant must be 0 or a compiled variant id");
+        g_opt.simt_variant = (int)v;
     } else if (!std::strcmp(key, "tc_b_major")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_b_major must be 0, 1 or 2");
         g_opt.tc_b_major = (int)v;
+    } else if (!std::strcmp(key, "debug_stall_mma")) {
+        if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "debug_stall_mma must be 0 or 1");
+        g_opt.debug_stall_mma = (int)v;
     } else if (!std::strcmp(key, "wait_timeout_ms")) {
         if (v < 1 || v > 600000) return fail(GEMM_ERR_INVALID_ARG, "wait_timeout_ms must be in [1, 600000]");
         g_opt.wait_timeout_ms = (int)v;
@@ -241,9 +260,10 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_group_m")) return o.tc_group_m;
     if (!std::strcmp(key, "tc_max_ctas")) return o.tc_max_ctas;
     if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
-    if (!std::strcmp(key, "simt_tile")) return o.simt_tile;
+    if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;
     if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
+    if (!std::strcmp(key, "debug_stall_mma")) return o.debug_stall_mma;
     return -1;
 }
 

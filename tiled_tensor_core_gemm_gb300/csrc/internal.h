@@ -16,9 +16,10 @@ struct Options {
     int tc_group_m = 0;        // 0 auto
     int tc_max_ctas = 0;       // 0 auto
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
-    int simt_tile = 0;         // 0 auto, 128 or 64
+    int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
     int tc_b_major = 0;        // 0 auto (BF16 as stored, TF32 transposed), 1 K-major copy, 2 as stored
     int wait_timeout_ms = 2000;
+    int debug_stall_mma = 0;   // test hook: make the MMA thread's first wait expire
 };
 Options options_snapshot();
 
@@ -40,11 +41,15 @@ cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K,
                              const float *A, int64_t lda, const float *B, int64_t ldb,
                              float *C, int64_t ldc, cudaStream_t stream);
 
+// Tile of SIMT variant `id` (bm, bn, bk, dynamic shared bytes); 0 if unknown.
+int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem);
+
 // ----------------------------------------------------------- tensor cores ---
 // Fills plan-dependent shared-memory size (bytes) for a tensor-core variant,
 // or returns 0 if the variant is not compiled in.
-int tc_smem_bytes(int dtype, int cta_group, int bn, bool b_kmajor);
-int tc_stages(int dtype, int cta_group, int bn, bool b_kmajor);
+// b_kmajor: 1 = B from a K-major transposed copy, 0 = B as stored.
+int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor);
+int tc_stages(int dtype, int cta_group, int bn, int b_kmajor);
 
 // Encodes the tensor maps and launches the persistent kernel.  A/B are the
 // (possibly packed) operands with the leading dimensions the plan reports;

@@ -171,7 +171,7 @@ __device__ __forceinline__ void tc_fence_after() {
 // ------------------------------------------------------------------- MMA ---
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all in 16-byte units), descriptor version 1 in bits
-// 46-47, base offset 0, and the 128-byte swizzle mode (value 2 in bits 61-63).
+// 46-47, base offset 0, and the 128-byte swizzle layout (value 2 in bits 61-63).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);

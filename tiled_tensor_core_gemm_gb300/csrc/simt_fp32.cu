@@ -13,9 +13,9 @@
 //    contiguous rows; its row pitch is padded by 4 floats, which makes the
 //    transposed stores conflict-free under the 32-bank model while keeping
 //    16-byte alignment for vector reads (checked in tests/test_simt_layout.py);
-//  * section 13.7: each thread owns an 8 x 8 micro-tile (two 4 x 4 quads per
-//    axis, half a tile apart, so every shared load is a 16-byte vector and a
-//    warp's B reads are contiguous), i.e. 64 FMAs per 4 vector loads.
+//  * section 13.7: each thread owns a register micro-tile of 4 x 4 quads (8 x 8
+//    or 8 x 16 outputs), i.e. 64 FMAs per 4 vector loads (8 x 8) or 128 per 6
+//    (8 x 16), so shared memory feeds the FMA pipe.
 // From "GPU architecture and mapping kernels" (ch. 12) section 12.5: thread x
 // runs along the contiguous axis of every global access (coalescing).
 //
@@ -27,18 +27,24 @@
 namespace tcgemm {
 namespace {
 
-template <int BM_, int BN_, int BK_>
+// Block tile BM x BN, K step BK; each thread owns RM x RN quads of 4 x 4
+// outputs (TM = 4 RM rows, TN = 4 RN columns), its quads BM/RM rows and BN/RN
+// columns apart so that every shared read is a 16-byte vector and the lanes of
+// a warp read one contiguous run of B.
+template <int BM_, int BN_, int BK_, int RM_, int RN_>
 struct SimtCfg {
-    static constexpr int BM = BM_, BN = BN_, BK = BK_;
-    static constexpr int TM = 8, TN = 8;
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, RM = RM_, RN = RN_;
+    static constexpr int TM = 4 * RM, TN = 4 * RN;
     static constexpr int TY = BM / TM, TX = BN / TN;
     static constexpr int THREADS = TY * TX;
     static constexpr int LDS_A = BM + 4;   // padded pitch of the transposed A tile
     static constexpr int LDS_B = BN;
     static constexpr int A_VEC = BM * BK / 4 / THREADS;  // float4 loads per thread
     static constexpr int B_VEC = BK * BN / 4 / THREADS;
+    static constexpr int SMEM_BYTES = 2 * BK * (LDS_A + LDS_B) * 4;   // double-buffered
     static_assert(A_VEC >= 1 && B_VEC >= 1, "tile too small for the thread count");
     static_assert(BM * BK / 4 % THREADS == 0 && BK * BN / 4 % THREADS == 0, "uneven tile loads");
+    static_assert(TX % 2 == 0 && THREADS % 32 == 0, "warp layout");
 };
 
 template <bool VEC>
@@ -70,13 +76,16 @@ __device__ __forceinline__ void store_row4(float *__restrict__ p, int64_t row, i
     if (col + 3 < cols) q[3] = d;
 }
 
-template <int BM, int BN, int BK, bool VEC>
-__global__ void __launch_bounds__(SimtCfg<BM, BN, BK>::THREADS, (BM == 128 ? 2 : 4))
+template <class Cfg, int MIN_BLOCKS, bool VEC>
+__global__ void __launch_bounds__(Cfg::THREADS, MIN_BLOCKS)
 sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
             const float *__restrict__ B, int64_t ldb, float *__restrict__ C, int64_t ldc) {
-    using Cfg = SimtCfg<BM, BN, BK>;
-    __shared__ __align__(16) float sA[2][BK][Cfg::LDS_A];
-    __shared__ __align__(16) float sB[2][BK][Cfg::LDS_B];
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, RM = Cfg::RM, RN = Cfg::RN;
+    extern __shared__ float4 smem_f4[];
+    float *smem = reinterpret_cast<float *>(smem_f4);
+    // sA[buf][k][m] (transposed, padded pitch), then sB[buf][k][n].
+    auto sA = [&](int buf, int k) { return smem + (buf * BK + k) * Cfg::LDS_A; };
+    auto sB = [&](int buf, int k) { return smem + 2 * BK * Cfg::LDS_A + (buf * BK + k) * Cfg::LDS_B; };
 
     const int tid = threadIdx.x;
     const int tx = tid % Cfg::TX, ty = tid / Cfg::TX;
@@ -106,24 +115,24 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         for (int i = 0; i < Cfg::A_VEC; ++i) {
             const int f = tid + i * Cfg::THREADS;
             const int r = f / (BK / 4), kq = f % (BK / 4);
-            sA[buf][4 * kq + 0][r] = ra[i].x;
-            sA[buf][4 * kq + 1][r] = ra[i].y;
-            sA[buf][4 * kq + 2][r] = ra[i].z;
-            sA[buf][4 * kq + 3][r] = ra[i].w;
+            sA(buf, 4 * kq + 0)[r] = ra[i].x;
+            sA(buf, 4 * kq + 1)[r] = ra[i].y;
+            sA(buf, 4 * kq + 2)[r] = ra[i].z;
+            sA(buf, 4 * kq + 3)[r] = ra[i].w;
         }
 #pragma unroll
         for (int i = 0; i < Cfg::B_VEC; ++i) {
             const int f = tid + i * Cfg::THREADS;
             const int kr = f / (BN / 4), c4 = f % (BN / 4);
-            *reinterpret_cast<float4 *>(&sB[buf][kr][4 * c4]) = rb[i];
+            *reinterpret_cast<float4 *>(sB(buf, kr) + 4 * c4) = rb[i];
         }
     };
 
-    float acc[8][8];
+    float acc[4 * RM][4 * RN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4 * RM; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4 * RN; ++j) acc[i][j] = 0.f;
 
     const int ktiles = (K + BK - 1) / BK;
     fetch(0);
@@ -135,16 +144,21 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         if (more) fetch((kt + 1) * BK);      // in flight while we compute
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&sA[buf][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&sA[buf][k][BM / 2 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&sB[buf][k][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&sB[buf][k][BN / 2 + tx * 4]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float a[4 * RM], b[4 * RN];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int q = 0; q < RM; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(sA(buf, k) + q * (BM / RM) + ty * 4);
+                a[4 * q + 0] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+            }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int q = 0; q < RN; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(sB(buf, k) + q * (BN / RN) + tx * 4);
+                b[4 * q + 0] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4 * RM; ++i)
+#pragma unroll
+                for (int j = 0; j < 4 * RN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
         // The other buffer was last read before the previous barrier, so it can
         // be refilled now; the barrier below publishes it and also keeps this
@@ -154,33 +168,64 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
     }
 
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
-        store_row4<VEC>(C, row, n0 + tx * 4, ldc, M, N, acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        store_row4<VEC>(C, row, n0 + BN / 2 + tx * 4, ldc, M, N, acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    for (int i = 0; i < 4 * RM; ++i) {
+        const int64_t row = m0 + (i / 4) * (BM / RM) + ty * 4 + (i % 4);
+#pragma unroll
+        for (int q = 0; q < RN; ++q)
+            store_row4<VEC>(C, row, n0 + q * (BN / RN) + tx * 4, ldc, M, N, acc[i][4 * q + 0], acc[i][4 * q + 1],
+                            acc[i][4 * q + 2], acc[i][4 * q + 3]);
     }
 }
 
-template <int BM, int BN, int BK>
+template <class Cfg, int MIN_BLOCKS>
 cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t lda, const float *B,
                         int64_t ldb, float *C, int64_t ldc, cudaStream_t s) {
-    using Cfg = SimtCfg<BM, BN, BK>;
-    const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+    const dim3 grid((unsigned)((N + Cfg::BN - 1) / Cfg::BN), (unsigned)((M + Cfg::BM - 1) / Cfg::BM));
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    if (vec)
-        sgemm_tiled<BM, BN, BK, true><<<grid, Cfg::THREADS, 0, s>>>(M, N, K, A, lda, B, ldb, C, ldc);
-    else
-        sgemm_tiled<BM, BN, BK, false><<<grid, Cfg::THREADS, 0, s>>>(M, N, K, A, lda, B, ldb, C, ldc);
+    auto kern = vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true> : sgemm_tiled<Cfg, MIN_BLOCKS, false>;
+    if (Cfg::SMEM_BYTES > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(M, N, K, A, lda, B, ldb, C, ldc);
     return cudaGetLastError();
 }
+
+// The compiled variants: id, tile, K step, quads per thread, min resident blocks.
+#define SIMT_VARIANTS(X)          \
+    X(1, 128, 128, 8, 2, 2, 2)    \
+    X(2, 128, 128, 16, 2, 2, 2)   \
+    X(3, 128, 256, 8, 2, 4, 1)    \
+    X(4, 256, 128, 8, 4, 2, 1)    \
+    X(5, 64, 64, 8, 2, 2, 4)      \
+    X(6, 128, 256, 16, 2, 4, 1)   \
+    X(7, 64, 64, 16, 2, 2, 4)
 
 }  // namespace
 
 cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K, const float *A, int64_t lda,
                              const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
-    if (plan.bm == 128) return launch_tile<128, 128, 8>(plan.vec != 0, M, N, K, A, lda, B, ldb, C, ldc, stream);
-    if (plan.bm == 64) return launch_tile<64, 64, 8>(plan.vec != 0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+#define X(id_, bm_, bn_, bk_, rm_, rn_, minb_)                                                        \
+    if (plan.bm == bm_ && plan.bn == bn_ && plan.bk == bk_)                                             \
+        return launch_tile<SimtCfg<bm_, bn_, bk_, rm_, rn_>, minb_>(plan.vec != 0, M, N, K, A, lda, B, ldb, \
+                                                                    C, ldc, stream);
+    SIMT_VARIANTS(X)
+#undef X
     return cudaErrorInvalidValue;
+}
+
+int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem) {
+#define X(id_, bm_, bn_, bk_, rm, rn, minb)                   \
+    if (id == id_) {                                           \
+        *bm = bm_;                                             \
+        *bn = bn_;                                             \
+        *bk = bk_;                                             \
+        *smem = SimtCfg<bm_, bn_, bk_, rm, rn>::SMEM_BYTES;    \
+        return 1;                                              \
+    }
+    SIMT_VARIANTS(X)
+#undef X
+    return 0;
 }
 
 }  // namespace tcgemm

@@ -60,8 +60,14 @@ constexpr int kBarBytes = 256;
 
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
-template <bool TF32, int CG, int BN, bool BKM>
+// How B is staged: as stored (N-major, "MN-major" for the MMA; BF16 only --
+// with TF32 operands this form gave wrong results on GB300), or from a K-major
+// transposed copy.
+enum BMode : int { kBNMajor = 0, kBKMajor = 1 };
+
+template <bool TF32, int CG, int BN, int BMODE>
 struct TcCfg {
+    static constexpr bool BKM = BMODE == kBKMajor;
     static constexpr int ELEM = TF32 ? 4 : 2;
     static constexpr int BK = 128 / ELEM;           // one 128-byte swizzle row of K
     static constexpr int UMMA_K = 32 / ELEM;        // K of one MMA: 16 (bf16) / 8 (tf32)
@@ -93,6 +99,7 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
+    static_assert(!(TF32 && BMODE == kBNMajor), "TF32 reads B from the K-major copy");
 };
 
 struct TcParams {
@@ -101,6 +108,7 @@ struct TcParams {
     int num_kb;                        // ceil(K / BK)
     int group_m;                       // raster group height, in tile rows
     int tma_store;
+    int debug_stall;                   // test hook: the MMA thread first waits on a barrier nothing arrives at
     float *C;
     int64_t ldc;
     unsigned long long timeout_ns;
@@ -140,12 +148,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-template <bool TF32, int CG, int BN, bool BKM>
+template <bool TF32, int CG, int BN, int BMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-    using Cf = TcCfg<TF32, CG, BN, BKM>;
+    using Cf = TcCfg<TF32, CG, BN, BMODE>;
     constexpr bool kPair = CG == 2;
+    constexpr bool BKM = Cf::BKM;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -153,7 +162,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t *stages = smem;
     uint8_t *epi = smem + Cf::STAGES * Cf::STAGE_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi + kEpiBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -161,6 +170,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(Cf::STAGES + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + a); };
     auto acce_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 2 + a); };
+    const uint32_t never_bar = bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 4);   // never arrived at
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
@@ -175,6 +185,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mbar_init(accf_bar(a), 1);
             ptx::mbar_init(acce_bar(a), kEpiWarps * CG);
         }
+        ptx::mbar_init(never_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -258,6 +269,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            if (p.debug_stall && !wait_bar<kPair>(never_bar, 0u, abort_flag, p.timeout_ns)) {
+                record_failure(kRoleMma, unit, abort_flag);
+                ok = false;
+            }
             for (int t = unit; ok && t < p.num_tiles; t += nunits) {
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleMma, t, abort_flag);
@@ -412,11 +427,12 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const voi
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool TF32, int CG, int BN, bool BKM>
+template <bool TF32, int CG, int BN, int BMODE>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
                    int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
                    size_t errlen) {
-    using Cf = TcCfg<TF32, CG, BN, BKM>;
+    using Cf = TcCfg<TF32, CG, BN, BMODE>;
+    constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb, tc;
     std::memset(&tc, 0, sizeof tc);
@@ -430,7 +446,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
         std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
         return GEMM_ERR_CUDA;
     }
-    auto kern = tc_gemm_kernel<TF32, CG, BN, BKM>;
+    auto kern = tc_gemm_kernel<TF32, CG, BN, BMODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -446,6 +462,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.num_kb = (K + Cf::BK - 1) / Cf::BK;
     p.group_m = plan.group_m > 0 ? plan.group_m : 1;
     p.tma_store = plan.tma_store;
+    p.debug_stall = options_snapshot().debug_stall_mma;
     p.C = C;
     p.ldc = ldc;
     p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
@@ -479,12 +496,13 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
 #define TC_VARIANTS(X) X(1, 64) X(1, 128) X(1, 256) X(2, 256)
 
 template <bool TF32, int CG, int BN>
-int cfg_value(bool bkm, bool stages) {
-    if (bkm) return stages ? TcCfg<TF32, CG, BN, true>::STAGES : TcCfg<TF32, CG, BN, true>::SMEM_BYTES;
-    return stages ? TcCfg<TF32, CG, BN, false>::STAGES : TcCfg<TF32, CG, BN, false>::SMEM_BYTES;
+int cfg_value(int bmode, bool stages) {
+    if (bmode == kBKMajor) return stages ? TcCfg<TF32, CG, BN, kBKMajor>::STAGES : TcCfg<TF32, CG, BN, kBKMajor>::SMEM_BYTES;
+    if (TF32) return 0;   // not compiled: TF32 always reads the K-major copy
+    return stages ? TcCfg<false, CG, BN, kBNMajor>::STAGES : TcCfg<false, CG, BN, kBNMajor>::SMEM_BYTES;
 }
 
-int tc_smem_bytes(int dtype, int cta_group, int bn, bool b_kmajor) {
+int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
 #define X(cg, bn_)                                                                         \
     if (cta_group == cg && bn == bn_)                                                       \
         return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, false) : cfg_value<false, cg, bn_>(b_kmajor, false);
@@ -493,7 +511,7 @@ int tc_smem_bytes(int dtype, int cta_group, int bn, bool b_kmajor) {
     return 0;
 }
 
-int tc_stages(int dtype, int cta_group, int bn, bool b_kmajor) {
+int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) {
 #define X(cg, bn_)                                                                         \
     if (cta_group == cg && bn == bn_)                                                       \
         return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, true) : cfg_value<false, cg, bn_>(b_kmajor, true);
@@ -505,21 +523,25 @@ int tc_stages(int dtype, int cta_group, int bn, bool b_kmajor) {
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
               int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
               size_t errlen) {
-#define X(cg, bn_)                                                                                             \
-    if (plan.cta_group == cg && plan.bn == bn_) {                                                               \
-        if (dtype == GEMM_TF32)                                                                                 \
-            return plan.b_kmajor ? launch_variant<true, cg, bn_, true>(plan, M, N, K, A, lda, B, ldb, C, ldc,    \
-                                                                       timeout_ms, stream, err, errlen)         \
-                                 : launch_variant<true, cg, bn_, false>(plan, M, N, K, A, lda, B, ldb, C, ldc,   \
-                                                                        timeout_ms, stream, err, errlen);       \
-        return plan.b_kmajor ? launch_variant<false, cg, bn_, true>(plan, M, N, K, A, lda, B, ldb, C, ldc,       \
-                                                                    timeout_ms, stream, err, errlen)            \
-                             : launch_variant<false, cg, bn_, false>(plan, M, N, K, A, lda, B, ldb, C, ldc,      \
-                                                                     timeout_ms, stream, err, errlen);          \
+    do {
+#define X(cg, bn_)                                                                                           \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                             \
+        if (dtype == GEMM_TF32) {                                                                             \
+            if (plan.b_kmajor != kBKMajor) break;                                                             \
+            return launch_variant<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
+                                                           stream, err, errlen);                              \
+        }                                                                                                     \
+        return plan.b_kmajor == kBKMajor                                                                      \
+                   ? launch_variant<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, \
+                                                              stream, err, errlen)                            \
+                   : launch_variant<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, \
+                                                              stream, err, errlen);                           \
     }
     TC_VARIANTS(X)
 #undef X
-    std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d", plan.cta_group, plan.bn);
+    } while (0);
+    std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", plan.cta_group, plan.bn,
+                  plan.b_kmajor);
     return GEMM_ERR_UNSUPPORTED;
 }
 
@@ -532,8 +554,8 @@ cudaError_t tc_read_and_clear_status(uint32_t words[4]) {
 
 int tc_max_active_clusters(int device) {
     (void)device;
-    using Cf = TcCfg<false, 2, 256, false>;
-    auto kern = tc_gemm_kernel<false, 2, 256, false>;
+    using Cf = TcCfg<false, 2, 256, kBNMajor>;
+    auto kern = tc_gemm_kernel<false, 2, 256, kBNMajor>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;
