@@ -85,7 +85,9 @@ typedef enum {
  * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
  * unavailable.  For GEMM_TF32, B is first transposed into the same kind of
  * workspace, because the TF32 tensor-core instruction reads its B operand
- * K-major.  C with such a layout is written by ordinary stores instead of
+ * K-major.  When there are too few output tiles to occupy every SM and K is
+ * long, the tensor-core path splits K: partial tiles go to a workspace and a
+ * second kernel sums them into C in a fixed order (results are deterministic).  C with such a layout is written by ordinary stores instead of
  * TMA stores.
  *
  * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
@@ -116,6 +118,9 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_cta_group"   force 1- or 2-CTA tiles (1, 2)
  *   "tc_group_m"     raster group height in tiles (>= 1)
  *   "tc_max_ctas"    cap on persistent CTAs (>= 1)
+ *   "tc_splits"      force split-K: K ranges per output tile (1..32); the
+ *                    partial tiles go to a workspace and are summed into C
+ *                    in a fixed order by a second kernel
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
  *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8
@@ -152,6 +157,7 @@ typedef struct {
     int32_t vec;         /* SIMT: 16-byte vector loads/stores legal        */
     int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
     int32_t b_kmajor;    /* B staged K-major from a transposed copy (TF32)  */
+    int32_t splits;      /* K ranges per output tile (split-K); 1 = none    */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

@@ -122,9 +122,29 @@ def test_plan_misaligned_base_packs():
     assert s["vec"] == 0
 
 
-def test_plan_low_tile_count_uses_narrow_tiles():
+def test_plan_low_tile_count_splits_k():
+    # 32 tiles of 128x256 for 152 SMs and 128 k-blocks: 4 K ranges per tile
     p = _plan(128, 8192, 8192, tg.GEMM_BF16)
-    assert p["cta_group"] == 1 and p["bn"] == 64 and p["grid"] == 128
+    assert p["cta_group"] == 1 and p["bn"] == 256 and p["splits"] == 4 and p["grid"] == 128
+    assert p["tma_store"] == 1
+    # short K: no split, narrow tiles instead
+    q = _plan(128, 8192, 256, tg.GEMM_BF16)
+    assert q["splits"] == 1 and q["bn"] == 64
+    # large problems never split, nor small ones (the reduce would cost more than it saves)
+    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["splits"] == 1
+    assert _plan(1000, 1000, 1000, tg.GEMM_BF16)["splits"] == 1
+
+
+@pytest.mark.parametrize("kb,req,eff", [(9, 4, 3), (10, 4, 4), (16, 3, 3), (5, 8, 5), (128, 32, 32)])
+def test_forced_splits_leave_no_empty_k_range(kb, req, eff):
+    try:
+        assert tg.gemm_set_option("tc_splits", req) == 0
+        p = _plan(256, 256, kb * 64, tg.GEMM_BF16)
+        assert p["splits"] == eff
+        per = -(-kb // eff)
+        assert (eff - 1) * per < kb          # the last K range is not empty
+    finally:
+        tg.gemm_set_option("tc_splits", 0)
 
 
 def test_plan_forced_options():

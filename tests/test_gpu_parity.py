@@ -31,7 +31,7 @@ def lib():
     tgbuild.build()
     tg.load_library()
     for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-              "debug_stall_mma"):
+              "debug_stall_mma", "tc_splits"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -138,6 +138,33 @@ def test_every_tensor_core_variant_exact(operands, variant, tma_store, shape):
     finally:
         for k in ("tc_cta_group", "tc_bn", "tc_tma_store", "tc_max_ctas", "tc_b_major"):
             tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+@pytest.mark.parametrize("variant", TC_VARIANTS, ids=lambda v: f"cg{v[0]}_bn{v[1]}")
+@pytest.mark.parametrize("splits", (2, 3, 7))
+def test_split_k_exact(dtype, variant, splits):
+    """Split-K: partial tiles in the workspace, summed in split order."""
+    cg, bn = variant
+    A, B = make_operands(300, 700, 1100, dtype, "ints", seed=20)
+    try:
+        tg.gemm_set_option("tc_cta_group", cg)
+        tg.gemm_set_option("tc_bn", bn)
+        tg.gemm_set_option("tc_splits", splits)
+        _exact(A, B, dtype)
+        _exact(A, B, dtype, ldc_pad=3)          # C not TMA-addressable: the reduce writes it
+        tg.gemm_set_option("tc_max_ctas", 3 * cg)
+        _exact(A, B, dtype)
+    finally:
+        for k in ("tc_cta_group", "tc_bn", "tc_splits", "tc_max_ctas"):
+            tg.gemm_set_option(k, 0)
+
+
+def test_split_k_deterministic_on_random_data():
+    A, B = make_operands(128, 4096, 8192, "bf16", "normal", seed=24)
+    C1 = run_gemm(A, B, "bf16")
+    C2 = run_gemm(A, B, "bf16")
+    assert np.array_equal(C1, C2)
 
 
 @pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7))

@@ -29,7 +29,8 @@ pytestmark = pytest.mark.gpu
 def lib():
     tgbuild.build()
     lib = tg.load_library()
-    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major"):
+    for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
+              "tc_splits"):
         tg.gemm_set_option(k, 0)
     return lib
 

@@ -107,6 +107,10 @@ int elem_bytes(int dtype) { return dtype == GEMM_BF16 ? 2 : 4; }
 // 512) and the 8 x 16 register tiles.
 constexpr int kSimtLarge = 2;   // 128 x 128 x 16, 8 x 8 per thread
 constexpr int kSimtSmall = 7;   // 64 x 64 x 16
+constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills the ring several times
+// Split-K adds a second kernel and a workspace round trip (a few microseconds):
+// only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
+constexpr int64_t kMinSplitWork = 1LL << 31;
 
 }  // namespace
 
@@ -165,12 +169,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.tma_store = (opt.tc_tma_store == 2) ? 0 : (c_tma_ok ? 1 : 0);
 
     int cg = opt.tc_cta_group, bn = opt.tc_bn;
+    int splits = opt.tc_splits;
     auto tiles_of = [&](int g, int b) { return cdiv(M, 128 * g) * cdiv(N, b); };
+    const int64_t num_kb = cdiv(K, 128 / elem);
     if (cg == 0 && bn == 0) {
         if (max_clusters_2cta > 0 && tiles_of(2, 256) >= max_clusters_2cta) {
             cg = 2;
             bn = 256;
         } else if (tiles_of(1, 256) >= num_sms) {
+            cg = 1;
+            bn = 256;
+        } else if (splits != 1 && M * N * K >= kMinSplitWork &&
+                   std::min<int64_t>(num_sms / tiles_of(1, 256), num_kb / kMinKbPerSplit) >= 2) {
+            // Too few 128x256 tiles for the SMs, but K is long: split K instead of
+            // shrinking the tile (a narrow tile re-reads A once per column tile).
             cg = 1;
             bn = 256;
         } else if (tiles_of(1, 128) >= num_sms) {
@@ -196,9 +208,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.group_m = opt.tc_group_m > 0 ? opt.tc_group_m : (cg == 2 ? 8 : 16);
     const int64_t tiles = tiles_of(cg, bn);
     p.tiles = (int32_t)tiles;
-    int64_t units = cg == 2 ? max_clusters_2cta : num_sms;
+    const int64_t unit_cap = cg == 2 ? max_clusters_2cta : num_sms;
+    if (splits == 0) {
+        splits = 1;
+        if (tiles * 2 <= unit_cap && M * N * K >= kMinSplitWork)
+            splits = (int)std::max<int64_t>(1, std::min<int64_t>({unit_cap / tiles, num_kb / kMinKbPerSplit, 16}));
+    }
+    // Make every K range non-empty: splits = ceil(num_kb / ceil(num_kb / splits)).
+    splits = (int)std::max<int64_t>(1, std::min<int64_t>(splits, num_kb));
+    splits = (int)cdiv(num_kb, cdiv(num_kb, splits));
+    p.splits = splits;
+    if (splits > 1) p.tma_store = 1;   // partial tiles go to the workspace, which TMA can address
+    int64_t units = unit_cap;
     if (opt.tc_max_ctas > 0) units = std::min<int64_t>(units, std::max(1, opt.tc_max_ctas / cg));
-    units = std::min<int64_t>(units, tiles);
+    units = std::min<int64_t>(units, tiles * splits);
     p.grid = (int32_t)(units * cg);
     return GEMM_OK;
 }
@@ -229,6 +252,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_max_ctas")) {
         if (v < 0 || v > (1 << 20)) return fail(GEMM_ERR_INVALID_ARG, "tc_max_ctas out of range");
         g_opt.tc_max_ctas = (int)v;
+    } else if (!std::strcmp(key, "tc_splits")) {
+        if (v < 0 || v > 32) return fail(GEMM_ERR_INVALID_ARG, "tc_splits must be in [0, 32]");
+        g_opt.tc_splits = (int)v;
     } else if (!std::strcmp(key, "tc_tma_store")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tma_store must be 0, 1 or 2");
         g_opt.tc_tma_store = (int)v;
@@ -260,6 +286,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_group_m")) return o.tc_group_m;
     if (!std::strcmp(key, "tc_max_ctas")) return o.tc_max_ctas;
     if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
+    if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;
     if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
@@ -365,11 +392,15 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     const uint64_t b_bytes = p.b_kmajor ? (uint64_t)N * plan.ldb_eff * eb
                              : p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
     const uint64_t a_off = 0, b_off = (a_bytes + 255) / 256 * 256;
-    if (p.pack_a || p.pack_b || p.b_kmajor) {
-        e = cudaMallocAsync(&ws, (size_t)(b_off + b_bytes), stream);
+    // Split-K partial planes: splits x M x ldw floats, ldw = N rounded up to 4 (16-byte rows for TMA).
+    const int64_t ldw = (N + 3) / 4 * 4;
+    const uint64_t w_bytes = p.splits > 1 ? (uint64_t)p.splits * M * ldw * 4 : 0;
+    const uint64_t w_off = (b_off + b_bytes + 255) / 256 * 256;
+    if (p.pack_a || p.pack_b || p.b_kmajor || p.splits > 1) {
+        e = cudaMallocAsync(&ws, (size_t)(w_off + w_bytes), stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
-            return fail(GEMM_ERR_NO_MEMORY, "workspace of %llu bytes: %s", (unsigned long long)(b_off + b_bytes),
+            return fail(GEMM_ERR_NO_MEMORY, "workspace of %llu bytes: %s", (unsigned long long)(w_off + w_bytes),
                         cudaGetErrorString(e));
         }
         uint8_t *w = static_cast<uint8_t *>(ws);
@@ -390,8 +421,16 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
         }
     }
     char err[256] = {0};
-    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc,
-                   (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
+    float *Wp = p.splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
+    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, Wp ? Wp : C,
+                   Wp ? ldw : ldc, (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
+    if (rc == GEMM_OK && Wp) {
+        e = splitk_reduce_launch(Wp, ldw, (int64_t)M * ldw, p.splits, C, ldc, M, N, stream);
+        if (e != cudaSuccess) {
+            std::snprintf(err, sizeof err, "split-K reduce: %s", cudaGetErrorString(e));
+            rc = GEMM_ERR_CUDA;
+        }
+    }
     if (ws) {
         e = cudaFreeAsync(ws, stream);
         if (rc == GEMM_OK && e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));

@@ -15,6 +15,7 @@ struct Options {
     int tc_cta_group = 0;      // 0 auto, else 1/2
     int tc_group_m = 0;        // 0 auto
     int tc_max_ctas = 0;       // 0 auto
+    int tc_splits = 0;         // 0 auto, else K ranges per tile (split-K)
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
     int tc_b_major = 0;        // 0 auto (BF16 as stored, TF32 transposed), 1 K-major copy, 2 as stored
@@ -72,6 +73,10 @@ int tc_max_active_clusters(int device);
 // each); dst columns [cols, ld_dst) are zeroed.
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+// C[m][n] = sum over s < splits of W[s * plane + m * ldw + n], s ascending.
+cudaError_t splitk_reduce_launch(const float *W, int64_t ldw, int64_t plane, int splits, float *C, int64_t ldc,
+                                 int64_t M, int64_t N, cudaStream_t stream);
 
 // dst[c * ld_dst + r] = src[r * ld_src + c] for r < rows, c < cols.
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,

@@ -10,6 +10,8 @@
 // Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the TF32
 // path, whose tensor-core instruction reads B K-major.
 //
+// Split-K reduce: sum the partial-tile planes into C.
+//
 // Both are HBM-bound: one read and one write of the operand.  The grid is a multiple of
 // the SM count; each warp walks whole rows so both sides stay coalesced even
 // though the source rows start at arbitrary 2- or 4-byte offsets.
@@ -56,6 +58,39 @@ __global__ void __launch_bounds__(256) transpose_tiles(const T *__restrict__ src
     }
 }
 
+// Split-K reduction: each thread owns four consecutive columns of one row and
+// adds the partial planes in split order, so the result does not depend on
+// scheduling.  Vector loads/stores when the pitches and C allow them.
+template <bool VEC>
+__global__ void __launch_bounds__(256) splitk_reduce(const float *__restrict__ W, int64_t ldw, int64_t plane,
+                                                     int splits, float *__restrict__ C, int64_t ldc, int64_t M,
+                                                     int64_t N) {
+    const int64_t quads_per_row = (N + 3) / 4;
+    const int64_t total = M * quads_per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / quads_per_row, n = (i - m * quads_per_row) * 4;
+        const float *w = W + m * ldw + n;
+        float *c = C + m * ldc + n;
+        if (VEC && n + 3 < N) {
+            float4 acc = *reinterpret_cast<const float4 *>(w);
+            for (int s = 1; s < splits; ++s) {
+                const float4 v = *reinterpret_cast<const float4 *>(w + s * plane);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<float4 *>(c) = acc;
+        } else {
+            for (int e = 0; e < 4 && n + e < N; ++e) {
+                float acc = w[e];
+                for (int s = 1; s < splits; ++s) acc += w[s * plane + e];
+                c[e] = acc;
+            }
+        }
+    }
+}
+
 int sm_count(cudaError_t *err) {
     int dev = 0, sms = 0;
     *err = cudaGetDevice(&dev);
@@ -80,6 +115,23 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
                                                               static_cast<uint32_t *>(dst), ld_dst, rows, cols);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t splitk_reduce_launch(const float *W, int64_t ldw, int64_t plane, int splits, float *C, int64_t ldc,
+                                 int64_t M, int64_t N, cudaStream_t stream) {
+    cudaError_t e;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    const int64_t quads = M * ((N + 3) / 4);
+    const int64_t want = (quads + 255) / 256;
+    const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    const bool vec = (ldw % 4 == 0) && (plane % 4 == 0) && (ldc % 4 == 0) && ((uintptr_t)W % 16 == 0) &&
+                     ((uintptr_t)C % 16 == 0);
+    if (vec)
+        splitk_reduce<true><<<blocks, 256, 0, stream>>>(W, ldw, plane, splits, C, ldc, M, N);
+    else
+        splitk_reduce<false><<<blocks, 256, 0, stream>>>(W, ldw, plane, splits, C, ldc, M, N);
     return cudaGetLastError();
 }
 

@@ -106,6 +106,10 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, num_tiles;   // tiles of (128*CG) x BN
     int num_kb;                        // ceil(K / BK)
+    int splits;                        // K ranges per tile (split-K); 1 = whole K
+    int kb_per_split;                  // k-blocks per K range
+    int num_units;                     // num_tiles * splits work units
+    int64_t split_stride;              // elements between the partial-sum planes (splits > 1)
     int group_m;                       // raster group height, in tile rows
     int tma_store;
     int debug_stall;                   // test hook: the MMA thread first waits on a barrier nothing arrives at
@@ -122,6 +126,17 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     const int r = t - g * per_group;
     tm = first + r % gm;
     tn = r / gm;
+}
+
+// Work unit u -> output tile (tm, tn), its K range [kb0, kb1) and split index.
+// Units of one K range come first, so units that run together read the same
+// slices of A and B.
+__device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, int &tn, int &kb0, int &kb1,
+                                            int &split) {
+    split = u / p.num_tiles;
+    tile_coords(u - split * p.num_tiles, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    kb0 = split * p.kb_per_split;
+    kb1 = min(p.num_kb, kb0 + p.kb_per_split);
 }
 
 __device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
@@ -209,12 +224,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = unit; ok && t < p.num_tiles; t += nunits) {
-                int tm, tn;
-                tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            for (int t = unit; ok && t < p.num_units; t += nunits) {
+                int tm, tn, kb0, kb1, split;
+                unit_coords(t, p, tm, tn, kb0, kb1, split);
                 const int m0 = tm * (kBM * CG) + (int)rank * kBM;
                 const int n0 = tn * BN + (int)rank * Cf::BN_CTA;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleProducer, t, abort_flag);
                         ok = false;
@@ -273,14 +288,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 record_failure(kRoleMma, unit, abort_flag);
                 ok = false;
             }
-            for (int t = unit; ok && t < p.num_tiles; t += nunits) {
+            for (int t = unit; ok && t < p.num_units; t += nunits) {
+                int tm, tn, kb0, kb1, split;
+                unit_coords(t, p, tm, tn, kb0, kb1, split);
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleMma, t, abort_flag);
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleMma, t, abort_flag);
                         ok = false;
@@ -299,7 +316,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             BKM ? ptx::sdesc_sw128(sb + 32u * kk, 16u, 1024u)
                                 : ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
                                                    1024u);
-                        ptx::mma<CG, TF32>(d_tmem, adesc, bdesc, Cf::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        ptx::mma<CG, TF32>(d_tmem, adesc, bdesc, Cf::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else ptx::mma_commit(empty_bar(stage));
@@ -321,11 +338,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t nchunk = 0;
-        for (int t = unit; t < p.num_tiles; t += nunits) {
-            int tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int t = unit; t < p.num_units; t += nunits) {
+            int tm, tn, kb0, kb1, split;
+            unit_coords(t, p, tm, tn, kb0, kb1, split);
             const int m0 = tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
             const int n0 = tn * BN;
+            // With split-K the partial tile goes to plane `split` of the workspace.
+            float *Cu = p.C + (int64_t)split * p.split_stride;
             const bool lane_ok = wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns);
             if (!__all_sync(0xffffffffu, lane_ok)) {
                 if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
@@ -367,7 +386,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (m0 < p.M && col0 < p.N) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
+                        if (m0 < p.M && col0 < p.N) {
+                            if (p.splits > 1) ptx::tma_store_3d(&tmC, ptx::smem_addr(buf), col0, m0, split);
+                            else ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
+                        }
                         ptx::bulk_commit_group();
                     }
                 } else {
@@ -379,7 +401,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const int grow = m0 + rr;
                         const float v = *reinterpret_cast<const float *>(
                             buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
-                        if (grow < p.M && col < p.N) p.C[(int64_t)grow * p.ldc + col] = v;
+                        if (grow < p.M && col < p.N) Cu[(int64_t)grow * p.ldc + col] = v;
                     }
                     __syncwarp();
                 }
@@ -427,6 +449,21 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const voi
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// FP32 planes [splits][rows][cols] with row pitch `ld` and plane pitch
+// `plane` (elements), stored in 32 x 32 x 1 boxes with the 128-byte swizzle.
+CUresult encode_3d_planes(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t planes, int64_t ld,
+                          int64_t plane) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * 4), (cuuint64_t)(plane * 4)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 template <bool TF32, int CG, int BN, int BMODE>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
                    int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
@@ -441,7 +478,8 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
         r = BKM ? encode_2d(&tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
                 : encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
     if (r == CUDA_SUCCESS && plan.tma_store)
-        r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+        r = plan.splits > 1 ? encode_3d_planes(&tc, C, N, M, plan.splits, ldc, (int64_t)M * ldc)
+                            : encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
     if (r != CUDA_SUCCESS) {
         std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
         return GEMM_ERR_CUDA;
@@ -460,6 +498,10 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.tiles_n = (N + BN - 1) / BN;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = (K + Cf::BK - 1) / Cf::BK;
+    p.splits = plan.splits > 1 ? plan.splits : 1;
+    p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
+    p.num_units = p.num_tiles * p.splits;
+    p.split_stride = (int64_t)M * ldc;
     p.group_m = plan.group_m > 0 ? plan.group_m : 1;
     p.tma_store = plan.tma_store;
     p.debug_stall = options_snapshot().debug_stall_mma;

@@ -101,6 +101,7 @@ extern "C" int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K, const float
 
     Options opt = options_snapshot();
     opt.tc_b_major = 1;   // B always goes through the transposed copy in the scratch
+    opt.tc_splits = 1;    // no workspace for split-K partial sums
     Plan plan;
     rc = make_plan(M, N, K, GEMM_TF32, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, sms,
                    clusters, opt, &plan);
