@@ -39,6 +39,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "sm_max_mhz": 2070.0}
 SMS = 152
 FP32_LANES_PER_SM = 128
+# bench keys of the published workloads (tiled_tensor_core_gemm_gb300/inputs.py)
+WORKLOAD_KEYS = ("bf16_8192", "tf32_4096", "fp32_4096", "fp32_1024", "tf32_1024", "fp32_256",
+                 "bf16_1000", "bf16_4097x4095x4099", "bf16_16384x1024x4096", "bf16_128x8192x8192")
+
+
+def workload_by_key(key):
+    from tiled_tensor_core_gemm_gb300 import inputs as I
+    table = {"bf16_8192": I.C4_BF16_8192, "tf32_4096": I.C3_TF32_4096, "fp32_4096": I.C3_FP32_4096,
+             "fp32_1024": I.C2_FP32_1024, "tf32_1024": I.C2_TF32_1024, "fp32_256": I.C1_FP32_256,
+             "bf16_1000": I.C5_BF16_RAGGED[0], "bf16_4097x4095x4099": I.C5_BF16_RAGGED[1],
+             "bf16_16384x1024x4096": I.C5_BF16_RAGGED[2], "bf16_128x8192x8192": I.C5_BF16_RAGGED[3]}
+    return table[key]
 
 
 def parse_args():
@@ -47,7 +59,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("bf16_8192", "tf32_4096", "fp32_4096"), default="bf16_8192",
+    ap.add_argument("--workload", choices=tuple(WORKLOAD_KEYS), default="bf16_8192",
                     help="timed workload (default: the headline 8192^3 BF16 GEMM)")
     ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -329,7 +341,7 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device)
 
-    w = {"bf16_8192": C4_BF16_8192, "tf32_4096": C3_TF32_4096, "fp32_4096": C3_FP32_4096}[args.workload]
+    w = workload_by_key(args.workload)
     headline = args.workload == "bf16_8192"
     sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
     if sampler:
@@ -362,6 +374,7 @@ def run_ours(args):
             "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
                          "accumulate and output, row-major, persistent tcgen05 path",
             "fp32_4096": "fp32 GEMM M=N=K=4096, A,B ~ N(0,1) (seed 2), exact fp32 on the CUDA cores (SIMT)"}
+    desc.setdefault(args.workload, f"{w.name}, row-major, fp32 output")
     if w.dtype == "fp32":
         sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
         roof = roofline_alu(res["flops"], res["launch_ms_mean"], sm_mhz)
@@ -393,17 +406,34 @@ def run_ours(args):
         sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
         paths = {}
         n_side = max(3, min(args.steps, 100))
-        for key, wl in (("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)):
+        side = [("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)]
+        side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
+                                                    "bf16_4097x4095x4099", "bf16_16384x1024x4096",
+                                                    "bf16_128x8192x8192")]
+        for key, wl in side:
             r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device)
             tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
             if wl.dtype == "fp32":
                 rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
+            elif wl.dtype == "bf16":
+                rl = roofline_tensor(r["flops"], r["launch_ms_mean"], peaks["bf16_tflops"],
+                                     f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
+                                     profiled_traffic(key))
+                # the low-tile-count shape streams B once: bandwidth is its binding roofline
+                if key == "bf16_128x8192x8192":
+                    in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 4
+                    gbs = in_bytes / (r["launch_ms_mean"] * 1e-3) / 1e9
+                    rl = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                          "peak_source": f"hbm_gbs, {peak_src}", "tensor_tflops": rl["achieved"]}
             else:
                 tf32_peak = peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"]
                 rl = roofline_tensor(r["flops"], r["launch_ms_mean"], tf32_peak,
                                      f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
                                      NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
+            in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype == "bf16" else 4)
             paths[key] = {"workload": wl.name, "tflops": round(tf, 2), "steps": n_side,
+                          "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
                           "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
         out["paths"] = paths
 

@@ -114,7 +114,8 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
 /*
  * gemm_set_option / gemm_get_option -- process-wide tuning overrides, for
  * sweeps and tests.  Keys (value 0 = automatic unless stated):
- *   "tc_bn"          force the tensor-core tile width BN (64, 128, 256)
+ *   "tc_bn"          force the tensor-core tile width BN (64, 128, 256; CTA
+ *                    pairs use 256)
  *   "tc_cta_group"   force 1- or 2-CTA tiles (1, 2)
  *   "tc_group_m"     raster group height in tiles (>= 1)
  *   "tc_max_ctas"    cap on persistent CTAs (>= 1)

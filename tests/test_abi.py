@@ -76,6 +76,7 @@ def test_options_roundtrip_and_validation():
     assert tg.gemm_set_option("tc_bn", 128) == tg.GEMM_OK and tg.gemm_get_option("tc_bn") == 128
     assert tg.gemm_set_option("tc_bn", 0) == tg.GEMM_OK
     assert tg.gemm_set_option("tc_bn", 96) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_set_option("tc_bn", 192) == tg.GEMM_ERR_INVALID_ARG
     assert tg.gemm_set_option("no_such_key", 1) == tg.GEMM_ERR_INVALID_ARG
     assert tg.gemm_get_option("no_such_key") == -1
     assert tg.gemm_get_option("wait_timeout_ms") == 2000

@@ -156,7 +156,7 @@ def test_split_k_exact(dtype, variant, splits):
         tg.gemm_set_option("tc_max_ctas", 3 * cg)
         _exact(A, B, dtype)
     finally:
-        for k in ("tc_cta_group", "tc_bn", "tc_splits", "tc_max_ctas"):
+        for k in ("tc_cta_group", "tc_bn", "tc_splits", "tc_max_ctas", "tc_b_major"):
             tg.gemm_set_option(k, 0)
 
 

@@ -532,56 +532,84 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     return GEMM_OK;
 }
 
+// A (dtype, CTA group, BN, B mode) combination is compiled only if it is legal:
+// TF32 always reads the K-major copy of B, and B read as stored needs every
+// CTA's share of the tile width to be whole 128-byte column chunks.
+template <bool TF32, int CG, int BN, int BMODE>
+constexpr bool variant_ok() {
+    return !(TF32 && BMODE == kBNMajor) && (BMODE == kBKMajor || (BN / CG) % (128 / (TF32 ? 4 : 2)) == 0);
+}
+
+template <bool TF32, int CG, int BN, int BMODE>
+int variant_value(bool stages) {
+    if constexpr (variant_ok<TF32, CG, BN, BMODE>()) {
+        using Cf = TcCfg<TF32, CG, BN, BMODE>;
+        return stages ? Cf::STAGES : Cf::SMEM_BYTES;
+    } else {
+        return 0;
+    }
+}
+
+template <bool TF32, int CG, int BN, int BMODE>
+int launch_if_ok(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
+                 int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+                 size_t errlen) {
+    if constexpr (variant_ok<TF32, CG, BN, BMODE>()) {
+        return launch_variant<TF32, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream, err,
+                                                   errlen);
+    } else {
+        std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, BMODE);
+        return GEMM_ERR_UNSUPPORTED;
+    }
+}
+
 }  // namespace
 
-// The variants compiled in: (cta_group, BN) in {(1,64), (1,128), (1,256), (2,256)}.
+// The (cta_group, BN) tiles compiled in.  Narrower pair tiles (256 x 128,
+// 256 x 192) were measured and dropped: the MMA then re-reads A from shared
+// memory twice as often per flop and runs 25-30% slower.
 #define TC_VARIANTS(X) X(1, 64) X(1, 128) X(1, 256) X(2, 256)
 
-template <bool TF32, int CG, int BN>
-int cfg_value(int bmode, bool stages) {
-    if (bmode == kBKMajor) return stages ? TcCfg<TF32, CG, BN, kBKMajor>::STAGES : TcCfg<TF32, CG, BN, kBKMajor>::SMEM_BYTES;
-    if (TF32) return 0;   // not compiled: TF32 always reads the K-major copy
-    return stages ? TcCfg<false, CG, BN, kBNMajor>::STAGES : TcCfg<false, CG, BN, kBNMajor>::SMEM_BYTES;
+static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, bool stages) {
+    const int mode = b_kmajor ? kBKMajor : kBNMajor;
+#define X(cg, bn_)                                                                                   \
+    if (cta_group == cg && bn == bn_) {                                                               \
+        if (dtype == GEMM_TF32)                                                                       \
+            return mode == kBKMajor ? variant_value<true, cg, bn_, kBKMajor>(stages) : 0;             \
+        return mode == kBKMajor ? variant_value<false, cg, bn_, kBKMajor>(stages)                     \
+                                : variant_value<false, cg, bn_, kBNMajor>(stages);                    \
+    }
+    TC_VARIANTS(X)
+#undef X
+    return 0;
 }
 
 int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
-#define X(cg, bn_)                                                                         \
-    if (cta_group == cg && bn == bn_)                                                       \
-        return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, false) : cfg_value<false, cg, bn_>(b_kmajor, false);
-    TC_VARIANTS(X)
-#undef X
-    return 0;
+    return tc_value(dtype, cta_group, bn, b_kmajor, false);
 }
 
-int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) {
-#define X(cg, bn_)                                                                         \
-    if (cta_group == cg && bn == bn_)                                                       \
-        return dtype == GEMM_TF32 ? cfg_value<true, cg, bn_>(b_kmajor, true) : cfg_value<false, cg, bn_>(b_kmajor, true);
-    TC_VARIANTS(X)
-#undef X
-    return 0;
-}
+int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(dtype, cta_group, bn, b_kmajor, true); }
 
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
               int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
               size_t errlen) {
-    do {
-#define X(cg, bn_)                                                                                           \
-    if (plan.cta_group == cg && plan.bn == bn_) {                                                             \
-        if (dtype == GEMM_TF32) {                                                                             \
-            if (plan.b_kmajor != kBKMajor) break;                                                             \
-            return launch_variant<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
-                                                           stream, err, errlen);                              \
-        }                                                                                                     \
-        return plan.b_kmajor == kBKMajor                                                                      \
-                   ? launch_variant<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, \
-                                                              stream, err, errlen)                            \
-                   : launch_variant<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, \
-                                                              stream, err, errlen);                           \
+#define X(cg, bn_)                                                                                              \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                                \
+        if (dtype == GEMM_TF32) {                                                                                \
+            if (plan.b_kmajor != kBKMajor) break;                                                                \
+            return launch_if_ok<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,      \
+                                                         stream, err, errlen);                                   \
+        }                                                                                                        \
+        return plan.b_kmajor == kBKMajor                                                                         \
+                   ? launch_if_ok<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
+                                                            stream, err, errlen)                                 \
+                   : launch_if_ok<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
+                                                            stream, err, errlen);                                \
     }
-    TC_VARIANTS(X)
-#undef X
+    do {
+        TC_VARIANTS(X)
     } while (0);
+#undef X
     std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", plan.cta_group, plan.bn,
                   plan.b_kmajor);
     return GEMM_ERR_UNSUPPORTED;
