@@ -87,7 +87,9 @@ typedef enum {
  * workspace, because the TF32 tensor-core instruction reads its B operand
  * K-major.  When there are too few output tiles to occupy every SM and K is
  * long, the tensor-core path splits K: partial tiles go to a workspace and a
- * second kernel sums them into C in a fixed order (results are deterministic).  C with such a layout is written by ordinary stores instead of
+ * second kernel sums them into C in a fixed order (results are deterministic).
+ * On request ("tc_tail_splits") the tiles of the last, partly idle round of
+ * the persistent schedule are split in K the same way.  C with such a layout is written by ordinary stores instead of
  * TMA stores.
  *
  * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
@@ -119,9 +121,12 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_cta_group"   force 1- or 2-CTA tiles (1, 2)
  *   "tc_group_m"     raster group height in tiles (>= 1)
  *   "tc_max_ctas"    cap on persistent CTAs (>= 1)
- *   "tc_splits"      force split-K: K ranges per output tile (1..32); the
- *                    partial tiles go to a workspace and are summed into C
- *                    in a fixed order by a second kernel
+ *   "tc_splits"      force split-K: K ranges for every output tile (1..32);
+ *                    the partial tiles go to a workspace and are summed into
+ *                    C in a fixed order by a second kernel
+ *   "tc_tail_splits" 0 or 1 off (default), n >= 2: split the tiles of the
+ *                    last, partly idle round of the persistent schedule into
+ *                    n K ranges (same workspace and reduction)
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
  *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8
@@ -158,7 +163,9 @@ typedef struct {
     int32_t vec;         /* SIMT: 16-byte vector loads/stores legal        */
     int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
     int32_t b_kmajor;    /* B staged K-major from a transposed copy (TF32)  */
-    int32_t splits;      /* K ranges per output tile (split-K); 1 = none    */
+    int32_t splits;      /* K ranges per split tile; 1 = no tile split       */
+    int32_t tail_tiles;  /* tiles split into K ranges (the last ones in the
+                            schedule; all tiles under full split-K)       */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

@@ -131,9 +131,29 @@ def test_plan_low_tile_count_splits_k():
     # short K: no split, narrow tiles instead
     q = _plan(128, 8192, 256, tg.GEMM_BF16)
     assert q["splits"] == 1 and q["bn"] == 64
-    # large problems never split, nor small ones (the reduce would cost more than it saves)
-    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["splits"] == 1
+    # small problems never split (the reduce would cost more than it saves)
     assert _plan(1000, 1000, 1000, tg.GEMM_BF16)["splits"] == 1
+    assert p["tail_tiles"] == 32        # every tile is split
+
+
+def test_plan_splits_the_last_round_only_on_request():
+    # off by default (measured: no gain)
+    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["tail_tiles"] == 0
+    try:
+        # 1024 pair tiles over 76 pairs: 13 full rounds and 36 tiles left
+        assert tg.gemm_set_option("tc_tail_splits", 2) == 0
+        p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+        assert p["tail_tiles"] == 36 and p["splits"] == 2 and p["grid"] == 152
+        # TF32 4096^3: 256 pair tiles, 28 left after 3 rounds
+        q = _plan(4096, 4096, 4096, tg.GEMM_TF32)
+        assert q["tail_tiles"] == 28 and q["splits"] == 2
+        assert tg.gemm_set_option("tc_tail_splits", 3) == 0
+        t = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+        assert t["tail_tiles"] == 36 and t["splits"] == 3
+        # no partly idle round: nothing to split
+        assert _plan(256, 256 * 76, 4096, tg.GEMM_BF16)["tail_tiles"] == 0
+    finally:
+        tg.gemm_set_option("tc_tail_splits", 0)
 
 
 @pytest.mark.parametrize("kb,req,eff", [(9, 4, 3), (10, 4, 4), (16, 3, 3), (5, 8, 5), (128, 32, 32)])

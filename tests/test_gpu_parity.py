@@ -31,7 +31,7 @@ def lib():
     tgbuild.build()
     tg.load_library()
     for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-              "debug_stall_mma", "tc_splits"):
+              "debug_stall_mma", "tc_splits", "tc_tail_splits"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -160,10 +160,39 @@ def test_split_k_exact(dtype, variant, splits):
             tg.gemm_set_option(k, 0)
 
 
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+@pytest.mark.parametrize("cg,max_ctas,tail_splits", [(2, 28, 2), (2, 28, 3), (1, 20, 3), (1, 7, 2)])
+def test_split_tail_exact(dtype, cg, max_ctas, tail_splits):
+    """Whole tiles first, then the last round's tiles split in K (slabs + reduce)."""
+    A, B = make_operands(2048, 1536, 1024, dtype, "ints", seed=25)
+    try:
+        tg.gemm_set_option("tc_cta_group", cg)
+        tg.gemm_set_option("tc_bn", 256)
+        tg.gemm_set_option("tc_max_ctas", max_ctas)
+        tg.gemm_set_option("tc_tail_splits", tail_splits)
+        from gemm_check import to_device
+        plan = tg.gemm_plan(2048, 1536, 1024, tg.DTYPES[dtype], 0, 1024, 0, 1536, 0, 1536).as_dict()
+        assert plan["tail_tiles"] > 0 and plan["splits"] > 1, plan
+        _exact(A, B, dtype)
+        _exact(A, B, dtype, ldc_pad=1)
+    finally:
+        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas", "tc_tail_splits"):
+            tg.gemm_set_option(k, 0)
+
+
 def test_split_k_deterministic_on_random_data():
     A, B = make_operands(128, 4096, 8192, "bf16", "normal", seed=24)
     C1 = run_gemm(A, B, "bf16")
     C2 = run_gemm(A, B, "bf16")
+    assert np.array_equal(C1, C2)
+    # the split tail of a many-tile problem as well
+    A, B = make_operands(4096, 4096, 2048, "tf32", "normal", seed=26)
+    try:
+        tg.gemm_set_option("tc_tail_splits", 2)
+        C1 = run_gemm(A, B, "tf32")
+        C2 = run_gemm(A, B, "tf32")
+    finally:
+        tg.gemm_set_option("tc_tail_splits", 0)
     assert np.array_equal(C1, C2)
 
 

@@ -208,20 +208,37 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.group_m = opt.tc_group_m > 0 ? opt.tc_group_m : (cg == 2 ? 8 : 16);
     const int64_t tiles = tiles_of(cg, bn);
     p.tiles = (int32_t)tiles;
-    const int64_t unit_cap = cg == 2 ? max_clusters_2cta : num_sms;
-    if (splits == 0) {
-        splits = 1;
-        if (tiles * 2 <= unit_cap && M * N * K >= kMinSplitWork)
-            splits = (int)std::max<int64_t>(1, std::min<int64_t>({unit_cap / tiles, num_kb / kMinKbPerSplit, 16}));
-    }
-    // Make every K range non-empty: splits = ceil(num_kb / ceil(num_kb / splits)).
-    splits = (int)std::max<int64_t>(1, std::min<int64_t>(splits, num_kb));
-    splits = (int)cdiv(num_kb, cdiv(num_kb, splits));
-    p.splits = splits;
-    if (splits > 1) p.tma_store = 1;   // partial tiles go to the workspace, which TMA can address
-    int64_t units = unit_cap;
+    int64_t units = cg == 2 ? max_clusters_2cta : num_sms;
     if (opt.tc_max_ctas > 0) units = std::min<int64_t>(units, std::max(1, opt.tc_max_ctas / cg));
-    units = std::min<int64_t>(units, tiles * splits);
+    auto exact_splits = [&](int64_t want) {
+        // every K range non-empty: splits = ceil(num_kb / ceil(num_kb / want))
+        want = std::max<int64_t>(1, std::min<int64_t>(want, num_kb));
+        return (int)cdiv(num_kb, cdiv(num_kb, want));
+    };
+    int64_t tail = 0;
+    if (splits == 0 && tiles * 2 <= units && M * N * K >= kMinSplitWork)
+        splits = (int)std::max<int64_t>(1, std::min<int64_t>({units / tiles, num_kb / kMinKbPerSplit, 16}));
+    if (splits > 1) {
+        // split K for every tile
+        splits = exact_splits(splits);
+        if (splits > 1) tail = tiles;
+    } else if (opt.tc_tail_splits >= 2 && tiles > units) {
+        // Split only the tiles of the last, partly idle round of the persistent
+        // schedule, so that round's units each get a share of K.
+        // Off by default: measured on GB300 (profiles/picker.md) it gained nothing
+        // -- units in a partly idle last round already run faster, with less
+        // L2 and power contention -- so it stays an explicit option.
+        const int64_t rem = tiles % units;
+        const int want = opt.tc_tail_splits;
+        if (want >= 2 && rem > 0) {
+            splits = exact_splits(want);
+            if (splits > 1) tail = rem;
+        }
+    }
+    if (tail == 0) splits = 1;
+    p.splits = splits;
+    p.tail_tiles = (int32_t)tail;
+    units = std::min<int64_t>(units, (tiles - tail) + tail * splits);
     p.grid = (int32_t)(units * cg);
     return GEMM_OK;
 }
@@ -255,6 +272,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_splits")) {
         if (v < 0 || v > 32) return fail(GEMM_ERR_INVALID_ARG, "tc_splits must be in [0, 32]");
         g_opt.tc_splits = (int)v;
+    } else if (!std::strcmp(key, "tc_tail_splits")) {
+        if (v < 0 || v > 16) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_splits must be in [0, 16]");
+        g_opt.tc_tail_splits = (int)v;
     } else if (!std::strcmp(key, "tc_tma_store")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tma_store must be 0, 1 or 2");
         g_opt.tc_tma_store = (int)v;
@@ -287,6 +307,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_max_ctas")) return o.tc_max_ctas;
     if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
     if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
+    if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;
     if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
@@ -392,11 +413,10 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     const uint64_t b_bytes = p.b_kmajor ? (uint64_t)N * plan.ldb_eff * eb
                              : p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
     const uint64_t a_off = 0, b_off = (a_bytes + 255) / 256 * 256;
-    // Split-K partial planes: splits x M x ldw floats, ldw = N rounded up to 4 (16-byte rows for TMA).
-    const int64_t ldw = (N + 3) / 4 * 4;
-    const uint64_t w_bytes = p.splits > 1 ? (uint64_t)p.splits * M * ldw * 4 : 0;
+    // Partial tiles of split tiles: tail_tiles x splits slabs of (128 * cta_group) x bn floats.
+    const uint64_t w_bytes = p.tail_tiles > 0 ? (uint64_t)p.tail_tiles * p.splits * 128 * p.cta_group * p.bn * 4 : 0;
     const uint64_t w_off = (b_off + b_bytes + 255) / 256 * 256;
-    if (p.pack_a || p.pack_b || p.b_kmajor || p.splits > 1) {
+    if (p.pack_a || p.pack_b || p.b_kmajor || p.tail_tiles > 0) {
         e = cudaMallocAsync(&ws, (size_t)(w_off + w_bytes), stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -421,13 +441,15 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
         }
     }
     char err[256] = {0};
-    float *Wp = p.splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
-    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, Wp ? Wp : C,
-                   Wp ? ldw : ldc, (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
+    float *Wp = p.tail_tiles > 0 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
+    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc, Wp,
+                   (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
     if (rc == GEMM_OK && Wp) {
-        e = splitk_reduce_launch(Wp, ldw, (int64_t)M * ldw, p.splits, C, ldc, M, N, stream);
+        const int tile_rows = 128 * p.cta_group;
+        e = split_reduce_launch(Wp, p.tail_tiles, p.splits, tile_rows, p.bn, p.tiles - p.tail_tiles,
+                                (int)cdiv(M, tile_rows), (int)cdiv(N, p.bn), p.group_m, C, ldc, M, N, stream);
         if (e != cudaSuccess) {
-            std::snprintf(err, sizeof err, "split-K reduce: %s", cudaGetErrorString(e));
+            std::snprintf(err, sizeof err, "split reduce: %s", cudaGetErrorString(e));
             rc = GEMM_ERR_CUDA;
         }
     }

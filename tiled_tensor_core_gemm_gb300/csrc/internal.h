@@ -15,7 +15,8 @@ struct Options {
     int tc_cta_group = 0;      // 0 auto, else 1/2
     int tc_group_m = 0;        // 0 auto
     int tc_max_ctas = 0;       // 0 auto
-    int tc_splits = 0;         // 0 auto, else K ranges per tile (split-K)
+    int tc_splits = 0;         // 0 auto, else K ranges for every tile (split-K)
+    int tc_tail_splits = 0;    // 0 auto, 1 off, else K ranges for the last round's tiles
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
     int tc_b_major = 0;        // 0 auto (BF16 as stored, TF32 transposed), 1 K-major copy, 2 as stored
@@ -55,10 +56,12 @@ int tc_stages(int dtype, int cta_group, int bn, int b_kmajor);
 // Encodes the tensor maps and launches the persistent kernel.  A/B are the
 // (possibly packed) operands with the leading dimensions the plan reports;
 // with plan.b_kmajor, B is the transposed copy (N x K, leading dimension ldb).
+// W: the slabs for the split tiles' partial sums (plan.tail_tiles * plan.splits
+// tiles of (128 * cta_group) x bn floats), or nullptr if no tile is split.
 // Returns a gemm_status_t.
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
               const void *A, int64_t lda, const void *B, int64_t ldb,
-              float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream,
+              float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream,
               char *err, size_t errlen);
 
 // Reads and clears the device status word of the tensor-core kernel.
@@ -74,9 +77,12 @@ int tc_max_active_clusters(int device);
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
 
-// C[m][n] = sum over s < splits of W[s * plane + m * ldw + n], s ascending.
-cudaError_t splitk_reduce_launch(const float *W, int64_t ldw, int64_t plane, int splits, float *C, int64_t ldc,
-                                 int64_t M, int64_t N, cudaStream_t stream);
+// For each split tile i (tile index full_tiles + i in the raster order), sums
+// its `splits` slabs W[(s * tail_tiles + i) * tile_rows * tile_cols ...] in
+// split order into C (clipped to M x N).
+cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int tile_rows, int tile_cols,
+                                int full_tiles, int tiles_m, int tiles_n, int group_m, float *C, int64_t ldc,
+                                int64_t M, int64_t N, cudaStream_t stream);
 
 // dst[c * ld_dst + r] = src[r * ld_src + c] for r < rows, c < cols.
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,

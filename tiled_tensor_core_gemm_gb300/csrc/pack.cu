@@ -10,12 +10,13 @@
 // Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the TF32
 // path, whose tensor-core instruction reads B K-major.
 //
-// Split-K reduce: sum the partial-tile planes into C.
+// Split reduce: sum the partial tiles of split tiles into C.
 //
 // Both are HBM-bound: one read and one write of the operand.  The grid is a multiple of
 // the SM count; each warp walks whole rows so both sides stay coalesced even
 // though the source rows start at arbitrary 2- or 4-byte offsets.
 #include "internal.h"
+#include "tile_order.cuh"
 
 namespace tcgemm {
 namespace {
@@ -112,35 +113,45 @@ __global__ void __launch_bounds__(256) transpose64_vec(const uint32_t *__restric
     }
 }
 
-// Split-K reduction: each thread owns four consecutive columns of one row and
-// adds the partial planes in split order, so the result does not depend on
-// scheduling.  Vector loads/stores when the pitches and C allow them.
+// Split reduction: each thread owns four consecutive columns of one row of one
+// split tile and adds that tile's slabs in split order, so the result does not
+// depend on scheduling.  Slabs are dense tiles (16-byte aligned rows); C gets
+// vector stores when its pitch and base allow them.
 template <bool VEC>
-__global__ void __launch_bounds__(256) splitk_reduce(const float *__restrict__ W, int64_t ldw, int64_t plane,
-                                                     int splits, float *__restrict__ C, int64_t ldc, int64_t M,
-                                                     int64_t N) {
-    const int64_t quads_per_row = (N + 3) / 4;
-    const int64_t total = M * quads_per_row;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t m = i / quads_per_row, n = (i - m * quads_per_row) * 4;
-        const float *w = W + m * ldw + n;
-        float *c = C + m * ldc + n;
+__global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W, int tail_tiles, int splits,
+                                                    int tile_rows, int tile_cols, int full_tiles, int tiles_m,
+                                                    int tiles_n, int group_m, float *__restrict__ C, int64_t ldc,
+                                                    int64_t M, int64_t N) {
+    const int64_t quads_per_row = tile_cols / 4;
+    const int64_t per_tile = (int64_t)tile_rows * quads_per_row;
+    const int64_t total = (int64_t)tail_tiles * per_tile;
+    const int64_t slab = (int64_t)tile_rows * tile_cols;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(x / per_tile);
+        const int64_t rem = x - (int64_t)i * per_tile;
+        const int r = (int)(rem / quads_per_row);
+        const int c = (int)(rem - (int64_t)r * quads_per_row) * 4;
+        int tm, tn;
+        tile_coords(full_tiles + i, tiles_m, tiles_n, group_m, tm, tn);
+        const int64_t m = (int64_t)tm * tile_rows + r, n = (int64_t)tn * tile_cols + c;
+        if (m >= M || n >= N) continue;
+        const float *w = W + (int64_t)i * slab + (int64_t)r * tile_cols + c;
+        float4 acc = *reinterpret_cast<const float4 *>(w);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(w + (int64_t)s * tail_tiles * slab);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *out = C + m * ldc + n;
         if (VEC && n + 3 < N) {
-            float4 acc = *reinterpret_cast<const float4 *>(w);
-            for (int s = 1; s < splits; ++s) {
-                const float4 v = *reinterpret_cast<const float4 *>(w + s * plane);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            *reinterpret_cast<float4 *>(c) = acc;
+            *reinterpret_cast<float4 *>(out) = acc;
         } else {
-            for (int e = 0; e < 4 && n + e < N; ++e) {
-                float acc = w[e];
-                for (int s = 1; s < splits; ++s) acc += w[s * plane + e];
-                c[e] = acc;
-            }
+            out[0] = acc.x;
+            if (n + 1 < N) out[1] = acc.y;
+            if (n + 2 < N) out[2] = acc.z;
+            if (n + 3 < N) out[3] = acc.w;
         }
     }
 }
@@ -181,20 +192,23 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
     return cudaGetLastError();
 }
 
-cudaError_t splitk_reduce_launch(const float *W, int64_t ldw, int64_t plane, int splits, float *C, int64_t ldc,
-                                 int64_t M, int64_t N, cudaStream_t stream) {
+cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int tile_rows, int tile_cols,
+                                int full_tiles, int tiles_m, int tiles_n, int group_m, float *C, int64_t ldc,
+                                int64_t M, int64_t N, cudaStream_t stream) {
     cudaError_t e;
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
-    const int64_t quads = M * ((N + 3) / 4);
+    if (tile_cols % 4 != 0 || (uintptr_t)W % 16 != 0) return cudaErrorInvalidValue;
+    const int64_t quads = (int64_t)tail_tiles * tile_rows * (tile_cols / 4);
     const int64_t want = (quads + 255) / 256;
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
-    const bool vec = (ldw % 4 == 0) && (plane % 4 == 0) && (ldc % 4 == 0) && ((uintptr_t)W % 16 == 0) &&
-                     ((uintptr_t)C % 16 == 0);
+    const bool vec = (ldc % 4 == 0) && ((uintptr_t)C % 16 == 0);
     if (vec)
-        splitk_reduce<true><<<blocks, 256, 0, stream>>>(W, ldw, plane, splits, C, ldc, M, N);
+        split_reduce<true><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
+                                                        tiles_m, tiles_n, group_m, C, ldc, M, N);
     else
-        splitk_reduce<false><<<blocks, 256, 0, stream>>>(W, ldw, plane, splits, C, ldc, M, N);
+        split_reduce<false><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
+                                                         tiles_m, tiles_n, group_m, C, ldc, M, N);
     return cudaGetLastError();
 }
 

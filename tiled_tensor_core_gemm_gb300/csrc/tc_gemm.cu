@@ -43,6 +43,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tile_order.cuh"
 
 namespace tcgemm {
 
@@ -106,10 +107,11 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, num_tiles;   // tiles of (128*CG) x BN
     int num_kb;                        // ceil(K / BK)
-    int splits;                        // K ranges per tile (split-K); 1 = whole K
+    int full_tiles;                    // tiles [0, full_tiles) run over all of K and store to C
+    int tail_tiles;                    // the remaining tiles run as `splits` K ranges each
+    int splits;                        // K ranges per tail tile
     int kb_per_split;                  // k-blocks per K range
-    int num_units;                     // num_tiles * splits work units
-    int64_t split_stride;              // elements between the partial-sum planes (splits > 1)
+    int num_units;                     // full_tiles + tail_tiles * splits work units
     int group_m;                       // raster group height, in tile rows
     int tma_store;
     int debug_stall;                   // test hook: the MMA thread first waits on a barrier nothing arrives at
@@ -118,25 +120,31 @@ struct TcParams {
     unsigned long long timeout_ns;
 };
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int &tm, int &tn) {
-    const int per_group = group_m * tiles_n;
-    const int g = t / per_group;
-    const int first = g * group_m;
-    const int gm = min(tiles_m - first, group_m);
-    const int r = t - g * per_group;
-    tm = first + r % gm;
-    tn = r / gm;
-}
-
-// Work unit u -> output tile (tm, tn), its K range [kb0, kb1) and split index.
-// Units of one K range come first, so units that run together read the same
-// slices of A and B.
+// Work unit u -> output tile (tm, tn), its K range [kb0, kb1) and the slab its
+// partial sum goes to (-1: the unit covers all of K and stores to C).
+//
+// Units [0, full_tiles) are whole tiles.  The tail tiles -- those that would
+// leave part of the machine idle in the last round of the persistent schedule,
+// or every tile when K is split throughout -- are split into K ranges; the
+// ranges of one split index come together, so units that run at once read the
+// same slices of A and B.  Partial tiles go to slabs (one full tile each) that
+// a second kernel sums in split order.
 __device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, int &tn, int &kb0, int &kb1,
-                                            int &split) {
-    split = u / p.num_tiles;
-    tile_coords(u - split * p.num_tiles, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                                            int &slab) {
+    if (u < p.full_tiles) {
+        tile_coords(u, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        kb0 = 0;
+        kb1 = p.num_kb;
+        slab = -1;
+        return;
+    }
+    const int v = u - p.full_tiles;
+    const int split = v / p.tail_tiles;
+    const int i = v - split * p.tail_tiles;
+    tile_coords(p.full_tiles + i, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+    slab = split * p.tail_tiles + i;
 }
 
 __device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
@@ -166,7 +174,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 template <bool TF32, int CG, int BN, int BMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW, const TcParams p) {
     using Cf = TcCfg<TF32, CG, BN, BMODE>;
     constexpr bool kPair = CG == 2;
     constexpr bool BKM = Cf::BKM;
@@ -208,6 +216,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
         if (p.tma_store) ptx::prefetch_tensormap(&tmC);
+        if (p.tail_tiles) ptx::prefetch_tensormap(&tmW);
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cf::TMEM_COLS);
@@ -225,8 +234,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             bool ok = true;
             for (int t = unit; ok && t < p.num_units; t += nunits) {
-                int tm, tn, kb0, kb1, split;
-                unit_coords(t, p, tm, tn, kb0, kb1, split);
+                int tm, tn, kb0, kb1, slab;
+                unit_coords(t, p, tm, tn, kb0, kb1, slab);
                 const int m0 = tm * (kBM * CG) + (int)rank * kBM;
                 const int n0 = tn * BN + (int)rank * Cf::BN_CTA;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -289,8 +298,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 ok = false;
             }
             for (int t = unit; ok && t < p.num_units; t += nunits) {
-                int tm, tn, kb0, kb1, split;
-                unit_coords(t, p, tm, tn, kb0, kb1, split);
+                int tm, tn, kb0, kb1, slab;
+                unit_coords(t, p, tm, tn, kb0, kb1, slab);
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleMma, t, abort_flag);
                     break;
@@ -339,12 +348,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc_phase = 0;
         uint32_t nchunk = 0;
         for (int t = unit; t < p.num_units; t += nunits) {
-            int tm, tn, kb0, kb1, split;
-            unit_coords(t, p, tm, tn, kb0, kb1, split);
+            int tm, tn, kb0, kb1, slab;
+            unit_coords(t, p, tm, tn, kb0, kb1, slab);
             const int m0 = tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
             const int n0 = tn * BN;
-            // With split-K the partial tile goes to plane `split` of the workspace.
-            float *Cu = p.C + (int64_t)split * p.split_stride;
+            const int srow = (int)rank * kBM + 32 * (int)q;                     // same row inside a slab
+            const bool to_slab = slab >= 0;
+            const bool use_tma = to_slab || p.tma_store;
             const bool lane_ok = wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns);
             if (!__all_sync(0xffffffffu, lane_ok)) {
                 if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
@@ -368,12 +378,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
                 const int col0 = n0 + 32 * j;
-                if (p.tma_store) {
-                    // The TMA store that last read this buffer (two chunks ago) must be done.
-                    if (nchunk >= 2) {
-                        if (lane == 0) ptx::bulk_wait_group_read<1>();
-                        __syncwarp();
-                    }
+                // The TMA store that last read this buffer (two chunks ago) must be done.
+                if (nchunk >= 2) {
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
                 }
                 // Row `lane`, 16-byte chunk c stored at position c ^ (row % 8): the
                 // 128-byte swizzle the TMA store expects, and conflict-free here.
@@ -382,14 +390,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int c = 0; c < 8; ++c)
                     row[c ^ (int)(lane & 7u)] = make_float4(__uint_as_float(r[4 * c + 0]), __uint_as_float(r[4 * c + 1]),
                                                             __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-                if (p.tma_store) {
+                if (use_tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (m0 < p.M && col0 < p.N) {
-                            if (p.splits > 1) ptx::tma_store_3d(&tmC, ptx::smem_addr(buf), col0, m0, split);
-                            else ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
-                        }
+                        if (to_slab) ptx::tma_store_3d(&tmW, ptx::smem_addr(buf), 32 * j, srow, slab);
+                        else if (m0 < p.M && col0 < p.N) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
                         ptx::bulk_commit_group();
                     }
                 } else {
@@ -401,7 +407,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const int grow = m0 + rr;
                         const float v = *reinterpret_cast<const float *>(
                             buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
-                        if (grow < p.M && col < p.N) Cu[(int64_t)grow * p.ldc + col] = v;
+                        if (grow < p.M && col < p.N) p.C[(int64_t)grow * p.ldc + col] = v;
                     }
                     __syncwarp();
                 }
@@ -409,7 +415,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if (p.tma_store && lane == 0) ptx::bulk_wait_group<0>();
+        if (lane == 0) ptx::bulk_wait_group<0>();
         __syncwarp();
     }
 
@@ -449,14 +455,13 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const voi
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// FP32 planes [splits][rows][cols] with row pitch `ld` and plane pitch
-// `plane` (elements), stored in 32 x 32 x 1 boxes with the 128-byte swizzle.
-CUresult encode_3d_planes(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t planes, int64_t ld,
-                          int64_t plane) {
+// FP32 slabs [count][rows][cols], dense, stored in 32 x 32 x 1 boxes with
+// the 128-byte swizzle.
+CUresult encode_3d_slabs(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t count) {
     auto enc = tensor_map_encoder();
     if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
-    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
-    cuuint64_t strides[2] = {(cuuint64_t)(ld * 4), (cuuint64_t)(plane * 4)};
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
+    cuuint64_t strides[2] = {(cuuint64_t)(cols * 4), (cuuint64_t)(rows * cols * 4)};
     cuuint32_t box[3] = {32, 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -466,20 +471,27 @@ CUresult encode_3d_planes(CUtensorMap *map, const void *base, int64_t cols, int6
 
 template <bool TF32, int CG, int BN, int BMODE>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                   int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+                   int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
                    size_t errlen) {
     using Cf = TcCfg<TF32, CG, BN, BMODE>;
     constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tb, tc, tw;
     std::memset(&tc, 0, sizeof tc);
+    std::memset(&tw, 0, sizeof tw);
     CUresult r = encode_2d(&ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
     if (r == CUDA_SUCCESS)
         r = BKM ? encode_2d(&tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
                 : encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
     if (r == CUDA_SUCCESS && plan.tma_store)
-        r = plan.splits > 1 ? encode_3d_planes(&tc, C, N, M, plan.splits, ldc, (int64_t)M * ldc)
-                            : encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+        r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+    if (r == CUDA_SUCCESS && plan.tail_tiles > 0) {
+        if (!W) {
+            std::snprintf(err, errlen, "split tail without a workspace");
+            return GEMM_ERR_INVALID_ARG;
+        }
+        r = encode_3d_slabs(&tw, W, BN, kBM * CG, (int64_t)plan.tail_tiles * plan.splits);
+    }
     if (r != CUDA_SUCCESS) {
         std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
         return GEMM_ERR_CUDA;
@@ -498,10 +510,11 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.tiles_n = (N + BN - 1) / BN;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = (K + Cf::BK - 1) / Cf::BK;
-    p.splits = plan.splits > 1 ? plan.splits : 1;
+    p.tail_tiles = plan.tail_tiles;
+    p.full_tiles = p.num_tiles - p.tail_tiles;
+    p.splits = p.tail_tiles > 0 ? plan.splits : 1;
     p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
-    p.num_units = p.num_tiles * p.splits;
-    p.split_stride = (int64_t)M * ldc;
+    p.num_units = p.full_tiles + p.tail_tiles * p.splits;
     p.group_m = plan.group_m > 0 ? plan.group_m : 1;
     p.tma_store = plan.tma_store;
     p.debug_stall = options_snapshot().debug_stall_mma;
@@ -524,7 +537,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "tensor-core kernel launch: %s", cudaGetErrorString(e));
         return GEMM_ERR_CUDA;
@@ -552,11 +565,11 @@ int variant_value(bool stages) {
 
 template <bool TF32, int CG, int BN, int BMODE>
 int launch_if_ok(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                 int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+                 int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
                  size_t errlen) {
     if constexpr (variant_ok<TF32, CG, BN, BMODE>()) {
-        return launch_variant<TF32, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms, stream, err,
-                                                   errlen);
+        return launch_variant<TF32, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream,
+                                                   err, errlen);
     } else {
         std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, BMODE);
         return GEMM_ERR_UNSUPPORTED;
@@ -591,19 +604,19 @@ int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
 int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(dtype, cta_group, bn, b_kmajor, true); }
 
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
-              int64_t ldb, float *C, int64_t ldc, uint32_t timeout_ms, cudaStream_t stream, char *err,
+              int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
               size_t errlen) {
 #define X(cg, bn_)                                                                                              \
     if (plan.cta_group == cg && plan.bn == bn_) {                                                                \
         if (dtype == GEMM_TF32) {                                                                                \
             if (plan.b_kmajor != kBKMajor) break;                                                                \
-            return launch_if_ok<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,      \
+            return launch_if_ok<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,   \
                                                          stream, err, errlen);                                   \
         }                                                                                                        \
         return plan.b_kmajor == kBKMajor                                                                         \
-                   ? launch_if_ok<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
+                   ? launch_if_ok<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,\
                                                             stream, err, errlen)                                 \
-                   : launch_if_ok<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, timeout_ms,   \
+                   : launch_if_ok<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,\
                                                             stream, err, errlen);                                \
     }
     do {

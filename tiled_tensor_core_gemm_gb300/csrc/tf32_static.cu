@@ -101,7 +101,8 @@ extern "C" int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K, const float
 
     Options opt = options_snapshot();
     opt.tc_b_major = 1;   // B always goes through the transposed copy in the scratch
-    opt.tc_splits = 1;    // no workspace for split-K partial sums
+    opt.tc_splits = 1;    // no workspace for partial sums of split tiles
+    opt.tc_tail_splits = 1;
     Plan plan;
     rc = make_plan(M, N, K, GEMM_TF32, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, sms,
                    clusters, opt, &plan);
@@ -114,7 +115,7 @@ extern "C" int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K, const float
     e = transpose_launch(B, ldb, bt, ldbt, K, N, 4, stream);
     if (e != cudaSuccess) return api_error(GEMM_ERR_CUDA, cudaGetErrorString(e));
     char err[256] = {0};
-    rc = tc_launch(plan.pub, GEMM_TF32, (int)M, (int)N, (int)K, A, lda, bt, ldbt, C, ldc,
+    rc = tc_launch(plan.pub, GEMM_TF32, (int)M, (int)N, (int)K, A, lda, bt, ldbt, C, ldc, nullptr,
                    (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
     if (rc != GEMM_OK) return api_error(rc, err);
     return GEMM_OK;
