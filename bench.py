@@ -424,7 +424,7 @@ def run_ours(args):
                     in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 4
                     gbs = in_bytes / (r["launch_ms_mean"] * 1e-3) / 1e9
                     rl = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(key),
                           "peak_source": f"hbm_gbs, {peak_src}", "tensor_tflops": rl["achieved"]}
             else:
                 tf32_peak = peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"]
