@@ -301,6 +301,22 @@ def cpu_baseline(workload, target_s):
                       f"fp64 C loops, {dt:.1f} s"}
 
 
+def slowest_rank_ms(total_ms: float, dist=None, device="cpu") -> float:
+    """The timed region's length on the slowest rank (every rank gets the max)."""
+    if dist is None:
+        return total_ms
+    import torch
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_tflops(world: int, flops_per_step: float, steps: int, max_total_ms: float) -> float:
+    """Whole-job throughput of `world` independent replicas: all ranks' flops
+    over the slowest rank's time."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def roofline_tensor(flops, launch_ms, peak, peak_src, nominal, traffic):
     achieved = flops / (launch_ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": UNIT,
@@ -354,13 +370,9 @@ def run_ours(args):
     finally:
         clocks = sampler.stop() if sampler else None
 
-    total_ms = res["total_ms"]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(res["total_ms"], dist, device)
     ms_per_step = total_ms / args.steps
-    value = world * res["flops"] * args.steps / (total_ms * 1e-3) / 1e12
+    value = replicas_tflops(world, res["flops"], args.steps, total_ms)
 
     if rank != 0:
         if dist is not None:
