@@ -71,8 +71,12 @@ PFN_cuMemGetAddressRange_v3020 address_range_fn() {
 }
 
 // The operand must be device memory of the current device, and its whole
-// footprint [p, p + bytes) must lie inside one allocation.
-int check_device_span(const char *name, const void *p, uint64_t bytes, int dev) {
+// footprint [p, p + bytes) must lie inside one allocation.  On success,
+// [*lo, *hi) is the allocation (or, if it cannot be queried, the footprint).
+int check_device_span(const char *name, const void *p, uint64_t bytes, int dev, uint64_t *lo = nullptr,
+                      uint64_t *hi = nullptr) {
+    if (lo) *lo = (uint64_t)(uintptr_t)p;
+    if (hi) *hi = (uint64_t)(uintptr_t)p + bytes;
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
     if (e != cudaSuccess) {
@@ -92,6 +96,8 @@ int check_device_span(const char *name, const void *p, uint64_t bytes, int dev) 
                 return fail(GEMM_ERR_INVALID_ARG,
                             "%s: footprint of %llu bytes runs past the end of its allocation (%llu bytes left)", name,
                             (unsigned long long)bytes, (unsigned long long)((uint64_t)base + size - start));
+            if (lo) *lo = (uint64_t)base;
+            if (hi) *hi = (uint64_t)base + size;
         }
     }
     return GEMM_OK;
@@ -390,8 +396,9 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
         e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, (size_t)M, stream);
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "cudaMemset2DAsync: %s", cudaGetErrorString(e));
     }
-    if ((rc = check_device_span("A", A, (uint64_t)((M - 1) * lda + K) * eb, dev))) return rc;
-    if ((rc = check_device_span("B", B, (uint64_t)((K - 1) * ldb + N) * eb, dev))) return rc;
+    uint64_t a_lo = 0, a_hi = 0, b_lo = 0, b_hi = 0;
+    if ((rc = check_device_span("A", A, (uint64_t)((M - 1) * lda + K) * eb, dev, &a_lo, &a_hi))) return rc;
+    if ((rc = check_device_span("B", B, (uint64_t)((K - 1) * ldb + N) * eb, dev, &b_lo, &b_hi))) return rc;
 
     const Options opt = options_snapshot();
     Plan plan;
@@ -425,14 +432,14 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
         }
         uint8_t *w = static_cast<uint8_t *>(ws);
         if (p.pack_a) {
-            e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, stream);
+            e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, a_lo, a_hi, stream);
             Ause = w + a_off;
         }
         if (e == cudaSuccess && p.b_kmajor) {
             e = transpose_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
             Buse = w + b_off;
         } else if (e == cudaSuccess && p.pack_b) {
-            e = pack_rows_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
+            e = pack_rows_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, b_lo, b_hi, stream);
             Buse = w + b_off;
         }
         if (e != cudaSuccess) {

@@ -73,9 +73,11 @@ int tc_max_active_clusters(int device);
 
 // ------------------------------------------------------------------- pack ---
 // dst[r * ld_dst + c] = src[r * ld_src + c] for r < rows, c < cols (elem bytes
-// each); dst columns [cols, ld_dst) are zeroed.
+// each); dst columns [cols, ld_dst) are zeroed.  [src_lo, src_hi) is memory
+// the kernel may read (the source allocation; at least the footprint).
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
-                             int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+                             int64_t rows, int64_t cols, int elem_bytes, uint64_t src_lo, uint64_t src_hi,
+                             cudaStream_t stream);
 
 // For each split tile i (tile index full_tiles + i in the raster order), sums
 // its `splits` slabs W[(s * tail_tiles + i) * tile_rows * tile_cols ...] in
