@@ -34,11 +34,11 @@ __global__ void __launch_bounds__(256) pack_rows(const T *__restrict__ src, int6
     }
 }
 
-// Vector pack: one warp per row, lane j writing destination 16-byte chunk j
-// (then j + 32, ...).  A source row starts at an arbitrary ELEM-aligned
+// Vector pack: one thread per destination 16-byte chunk (consecutive threads
+// along a row, so loads and stores coalesce).  A source row starts at an arbitrary ELEM-aligned
 // address s; chunk j's bytes [s + 16j, s + 16j + 16) straddle the aligned
-// words w0 = (s & ~15) + 16j and w0 + 16, so the lane loads both (coalesced
-// across the warp) and funnel-shifts them by s & 15 bytes.  A word is read
+// words w0 = (s & ~15) + 16j and w0 + 16, so the thread loads both and
+// funnel-shifts them by s & 15 bytes.  A word is read
 // only if it lies inside [lo, hi), the source allocation; otherwise that
 // chunk is copied element by element from inside the row.  Destination bytes
 // past the row's end (the pitch padding) are written as zero.
@@ -60,48 +60,44 @@ template <int ELEM>
 __global__ void __launch_bounds__(256) pack_rows_vec(const uint8_t *__restrict__ src, int64_t ld_src_bytes,
                                                      uint8_t *__restrict__ dst, int64_t ld_dst_bytes, int64_t rows,
                                                      int64_t row_bytes, uintptr_t lo, uintptr_t hi) {
-    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
-    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int lane = threadIdx.x & 31;
+    // one thread per destination 16-byte chunk, consecutive threads along a row
     const int64_t chunks = ld_dst_bytes / 16;
-    for (int64_t r = warp; r < rows; r += warps_total) {
+    const int64_t total = rows * chunks;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = x / chunks, c = x - r * chunks;
         const uintptr_t s = reinterpret_cast<uintptr_t>(src) + (uintptr_t)(r * ld_src_bytes);
         const uintptr_t a = s & ~(uintptr_t)15;
         const int off = (int)(s - a);
         const int ws = off >> 2, hs = (off & 3) * 8;
-        uint4 *d = reinterpret_cast<uint4 *>(dst + r * ld_dst_bytes);
-#pragma unroll 4
-        for (int64_t c = lane; c < chunks; c += 32) {
-            const int64_t b0 = 16 * c;   // first byte of this chunk within the row
-            uint4 out = make_uint4(0u, 0u, 0u, 0u);
-            if (b0 < row_bytes) {
-                const uintptr_t w0 = a + (uintptr_t)b0;
-                const uintptr_t need = off ? 32 : 16;
-                if (w0 >= lo && w0 + need <= hi) {
-                    const uint4 x = *reinterpret_cast<const uint4 *>(w0);
-                    const uint4 y = off ? *reinterpret_cast<const uint4 *>(w0 + 16) : make_uint4(0u, 0u, 0u, 0u);
-                    const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-                    out = shift_words(v, ws, hs);
-                } else {
-                    uint32_t wds[4] = {0u, 0u, 0u, 0u};
-                    for (int e = 0; e < 16 / ELEM && b0 + e * ELEM < row_bytes; ++e) {
-                        const uint32_t val = ELEM == 2 ? (uint32_t)*reinterpret_cast<const uint16_t *>(s + b0 + e * 2)
-                                                       : *reinterpret_cast<const uint32_t *>(s + b0 + e * 4);
-                        const int bit = e * ELEM * 8;
-                        wds[bit / 32] |= val << (bit % 32);
-                    }
-                    out = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        const int64_t b0 = 16 * c;   // first byte of this chunk within the row
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (b0 < row_bytes) {
+            const uintptr_t w0 = a + (uintptr_t)b0;
+            const uintptr_t need = off ? 32 : 16;
+            if (w0 >= lo && w0 + need <= hi) {
+                const uint4 xw = *reinterpret_cast<const uint4 *>(w0);
+                const uint4 yw = off ? *reinterpret_cast<const uint4 *>(w0 + 16) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t v[8] = {xw.x, xw.y, xw.z, xw.w, yw.x, yw.y, yw.z, yw.w};
+                out = shift_words(v, ws, hs);
+            } else {
+                uint32_t wds[4] = {0u, 0u, 0u, 0u};
+                for (int e = 0; e < 16 / ELEM && b0 + e * ELEM < row_bytes; ++e) {
+                    const uint32_t val = ELEM == 2 ? (uint32_t)*reinterpret_cast<const uint16_t *>(s + b0 + e * 2)
+                                                   : *reinterpret_cast<const uint32_t *>(s + b0 + e * 4);
+                    const int bit = e * ELEM * 8;
+                    wds[bit / 32] |= val << (bit % 32);
                 }
-                const int keep = (int)(row_bytes - b0);   // bytes of this chunk inside the row
-                if (keep < 16) {
-                    out.x = keep_bytes(out.x, keep);
-                    out.y = keep_bytes(out.y, keep - 4);
-                    out.z = keep_bytes(out.z, keep - 8);
-                    out.w = keep_bytes(out.w, keep - 12);
-                }
+                out = make_uint4(wds[0], wds[1], wds[2], wds[3]);
             }
-            d[c] = out;
+            const int keep = (int)(row_bytes - b0);   // bytes of this chunk inside the row
+            if (keep < 16) {
+                out.x = keep_bytes(out.x, keep);
+                out.y = keep_bytes(out.y, keep - 4);
+                out.z = keep_bytes(out.z, keep - 8);
+                out.w = keep_bytes(out.w, keep - 12);
+            }
         }
+        *reinterpret_cast<uint4 *>(dst + r * ld_dst_bytes + b0) = out;
     }
 }
 
@@ -292,13 +288,16 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
     // The vector form needs a 16-byte aligned destination with 16-byte rows.
     if ((uintptr_t)dst % 16 == 0 && (ld_dst * elem_bytes) % 16 == 0 && src_hi > src_lo) {
+        const int64_t chunks = rows * (ld_dst * elem_bytes / 16);
+        const int64_t vwant = (chunks + 255) / 256;
+        const int vblocks = (int)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16);
         const uint8_t *s = static_cast<const uint8_t *>(src);
         uint8_t *d = static_cast<uint8_t *>(dst);
         if (elem_bytes == 2)
-            pack_rows_vec<2><<<blocks, 256, 0, stream>>>(s, ld_src * 2, d, ld_dst * 2, rows, cols * 2,
+            pack_rows_vec<2><<<vblocks, 256, 0, stream>>>(s, ld_src * 2, d, ld_dst * 2, rows, cols * 2,
                                                          (uintptr_t)src_lo, (uintptr_t)src_hi);
         else if (elem_bytes == 4)
-            pack_rows_vec<4><<<blocks, 256, 0, stream>>>(s, ld_src * 4, d, ld_dst * 4, rows, cols * 4,
+            pack_rows_vec<4><<<vblocks, 256, 0, stream>>>(s, ld_src * 4, d, ld_dst * 4, rows, cols * 4,
                                                          (uintptr_t)src_lo, (uintptr_t)src_hi);
         else
             return cudaErrorInvalidValue;

@@ -22,6 +22,8 @@
 // Numerics: plain FP32 fmaf with k ascending per output; no fast-math, no
 // TF32.  Every size >= 1 is legal: out-of-range loads read 0 and out-of-range
 // stores are skipped.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace tcgemm {
@@ -135,11 +137,10 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         for (int j = 0; j < 4 * RN; ++j) acc[i][j] = 0.f;
 
     const int ktiles = (K + BK - 1) / BK;
-    fetch(0);
-    deposit(0);
-    __syncthreads();
-    for (int kt = 0; kt < ktiles; ++kt) {
-        const int buf = kt & 1;
+    // One K step on buffer BUF (a compile-time constant, so every shared
+    // address below is a fixed offset from one base register).
+    auto step = [&](auto buf_c, int kt) {
+        constexpr int buf = decltype(buf_c)::value;
         const bool more = kt + 1 < ktiles;   // uniform across the block
         if (more) fetch((kt + 1) * BK);      // in flight while we compute
 #pragma unroll
@@ -165,6 +166,13 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         // buffer intact until every warp has finished reading it.
         if (more) deposit(buf ^ 1);
         __syncthreads();
+    };
+    fetch(0);
+    deposit(0);
+    __syncthreads();
+    for (int kt = 0; kt < ktiles; kt += 2) {
+        step(std::integral_constant<int, 0>{}, kt);
+        if (kt + 1 < ktiles) step(std::integral_constant<int, 1>{}, kt + 1);
     }
 
 #pragma unroll
