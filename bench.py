@@ -41,7 +41,8 @@ SMS = 152
 FP32_LANES_PER_SM = 128
 # bench keys of the published workloads (tiled_tensor_core_gemm_gb300/inputs.py)
 WORKLOAD_KEYS = ("bf16_8192", "tf32_4096", "fp32_4096", "fp32_1024", "tf32_1024", "fp32_256",
-                 "bf16_1000", "bf16_4097x4095x4099", "bf16_16384x1024x4096", "bf16_128x8192x8192")
+                 "bf16_1000", "bf16_4097x4095x4099", "bf16_16384x1024x4096", "bf16_128x8192x8192",
+                 "fp16_4096", "fp16_8192")
 
 
 def workload_by_key(key):
@@ -49,7 +50,8 @@ def workload_by_key(key):
     table = {"bf16_8192": I.C4_BF16_8192, "tf32_4096": I.C3_TF32_4096, "fp32_4096": I.C3_FP32_4096,
              "fp32_1024": I.C2_FP32_1024, "tf32_1024": I.C2_TF32_1024, "fp32_256": I.C1_FP32_256,
              "bf16_1000": I.C5_BF16_RAGGED[0], "bf16_4097x4095x4099": I.C5_BF16_RAGGED[1],
-             "bf16_16384x1024x4096": I.C5_BF16_RAGGED[2], "bf16_128x8192x8192": I.C5_BF16_RAGGED[3]}
+             "bf16_16384x1024x4096": I.C5_BF16_RAGGED[2], "bf16_128x8192x8192": I.C5_BF16_RAGGED[3],
+             "fp16_4096": I.FP16_4096, "fp16_8192": I.FP16_8192}
     return table[key]
 
 
@@ -283,17 +285,17 @@ def cpu_baseline(workload, target_s):
     from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array, workload_operands
     A, B = workload_operands(workload)
     a, b = as_oracle_array(A), as_oracle_array(B)
-    bf16 = workload.dtype == "bf16"
+    bf16, fp16 = workload.dtype == "bf16", workload.dtype == "fp16"
     threads = oracle.num_threads()
     rows = list(range(threads))
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, rows, bf16=bf16, with_scale=False)
+    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, with_scale=False)
     t_probe = time.perf_counter() - t0
     n = max(threads, int(threads * max(1.0, (target_s - t_probe) / max(t_probe, 1e-3))))
     n = min(n, workload.M)
     rows = list(range(n))
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, rows, bf16=bf16, with_scale=False)
+    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, with_scale=False)
     dt = time.perf_counter() - t0
     flops = 2.0 * n * workload.N * workload.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -380,7 +382,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    in_bytes = (w.M * w.K + w.K * w.N) * (2 if w.dtype == "bf16" else 4)
+    in_bytes = (w.M * w.K + w.K * w.N) * (2 if w.dtype in ("bf16", "fp16") else 4)
     desc = {"bf16_8192": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), fp32 accumulate "
                          "and output, row-major, persistent tcgen05 path",
             "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
@@ -421,13 +423,13 @@ def run_ours(args):
         side = [("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)]
         side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
                                                     "bf16_4097x4095x4099", "bf16_16384x1024x4096",
-                                                    "bf16_128x8192x8192")]
+                                                    "bf16_128x8192x8192", "fp16_4096", "fp16_8192")]
         for key, wl in side:
             r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device)
             tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
             if wl.dtype == "fp32":
                 rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
-            elif wl.dtype == "bf16":
+            elif wl.dtype in ("bf16", "fp16"):
                 rl = roofline_tensor(r["flops"], r["launch_ms_mean"], peaks["bf16_tflops"],
                                      f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
                                      profiled_traffic(key))
@@ -443,7 +445,7 @@ def run_ours(args):
                 rl = roofline_tensor(r["flops"], r["launch_ms_mean"], tf32_peak,
                                      f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
                                      NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
-            in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype == "bf16" else 4)
+            in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype in ("bf16", "fp16") else 4)
             paths[key] = {"workload": wl.name, "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
                           "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}

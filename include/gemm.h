@@ -52,7 +52,9 @@ typedef enum {
     GEMM_FP32 = 0, /* A, B float; exact FP32 products and sums on the CUDA cores  */
     GEMM_TF32 = 1, /* A, B float; tensor cores read them as TF32 (10-bit mantissa)
                       and accumulate in FP32 in Tensor Memory                      */
-    GEMM_BF16 = 2  /* A, B bfloat16 (raw uint16 storage); exact products,
+    GEMM_BF16 = 2, /* A, B bfloat16 (raw uint16 storage); exact products,
+                      FP32 accumulation in Tensor Memory                           */
+    GEMM_FP16 = 3  /* A, B IEEE half (raw uint16 storage); exact products,
                       FP32 accumulation in Tensor Memory                           */
 } gemm_dtype_t;
 
@@ -71,14 +73,15 @@ typedef enum {
  *   M, N, K     sizes, each >= 0.  M == 0 or N == 0: no-op.  K == 0: C is
  *               filled with zeros (the empty sum).
  *   dtype       gemm_dtype_t.  A and B are 'const float *' for GEMM_FP32 and
- *               GEMM_TF32 and 'const uint16_t *' (bfloat16 bits) for GEMM_BF16.
+ *               GEMM_TF32, 'const uint16_t *' holding bfloat16 bits for
+ *               GEMM_BF16 and IEEE half bits for GEMM_FP16.
  *   A, lda      device pointer to A[0][0], leading dimension in elements.
  *   B, ldb      device pointer to B[0][0], leading dimension in elements.
  *   C, ldc      device pointer to C[0][0] (float), leading dimension in elements.
  *   stream      the CUDA stream to enqueue on.
  *
- * Paths: GEMM_FP32 runs the tiled SIMT kernel; GEMM_TF32 and GEMM_BF16 run the
- * persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine cannot
+ * Paths: GEMM_FP32 runs the tiled SIMT kernel; GEMM_TF32, GEMM_BF16 and
+ * GEMM_FP16 run the persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine cannot
  * address (base not 16-byte aligned, or a row pitch that is not a multiple of
  * 16 bytes) are first copied into a stream-ordered workspace with a padded
  * pitch; that workspace is allocated and freed on the stream

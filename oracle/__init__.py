@@ -10,8 +10,8 @@ What it computes: "Shared memory and tensor cores" (ml-compiler-from-scratch
 ch. 13) section 13.1 defines the GEMM as C = A @ B with 2*M*N*K flops; section
 13.8 fixes that tensor-core products are exact and sums are FP32.  The oracle
 forms the same exact products and sums them in fp64 (k ascending), so it is at
-least as accurate as any path under test.  BF16 inputs are passed as their raw
-16-bit patterns and widened exactly.
+least as accurate as any path under test.  BF16 and FP16 inputs are passed as
+their raw 16-bit patterns and widened exactly.
 
 Every function also returns D[i, j] = sum_k |A[i, k]| * |B[k, j]| on request,
 the per-entry scale used by the acceptance test max|C - C_ref| / D.
@@ -19,7 +19,7 @@ the per-entry scale used by the acceptance test max|C - C_ref| / D.
 Pins (tests/test_oracle.py): identity and permutation products, all-ones inputs
 (C == K everywhere), small-integer inputs against exact integer arithmetic, a
 second independent loop order at tiny sizes, float64 library matmul, and the
-BF16 widening against the library's own conversion.
+BF16 and FP16 widenings against the library's own conversions.
 """
 from __future__ import annotations
 
@@ -63,10 +63,11 @@ def _load():
         full = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
         rows = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]
         jik = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
-        for name, args in (("oracle_gemm_f32", full), ("oracle_gemm_bf16", full),
+        for name, args in (("oracle_gemm_f32", full), ("oracle_gemm_bf16", full), ("oracle_gemm_f16", full),
                            ("oracle_gemm_rows_f32", rows), ("oracle_gemm_rows_bf16", rows),
-                           ("oracle_gemm_f32_jik", jik), ("oracle_gemm_bf16_jik", jik),
-                           ("oracle_widen_bf16", [_ptr, _ptr, _i64])):
+                           ("oracle_gemm_rows_f16", rows),
+                           ("oracle_gemm_f32_jik", jik), ("oracle_gemm_bf16_jik", jik), ("oracle_gemm_f16_jik", jik),
+                           ("oracle_widen_bf16", [_ptr, _ptr, _i64]), ("oracle_widen_f16", [_ptr, _ptr, _i64])):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = None
@@ -81,8 +82,8 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
-def _as_operand(x: np.ndarray, bf16: bool) -> np.ndarray:
-    want = np.uint16 if bf16 else np.float32
+def _as_operand(x: np.ndarray, half: bool) -> np.ndarray:
+    want = np.uint16 if half else np.float32
     if x.dtype != want:
         raise TypeError(f"oracle operand must be {want.__name__}, got {x.dtype}")
     if x.ndim != 2 or (x.size > 0 and x.shape[1] > 1 and x.strides[1] != x.itemsize):
@@ -94,27 +95,36 @@ def _ld(x: np.ndarray) -> int:
     return x.strides[0] // x.itemsize if (x.shape[0] > 1 and x.size > 0) else max(x.shape[1], 1)
 
 
-def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = False):
+def _kind(bf16: bool, fp16: bool) -> str:
+    if bf16 and fp16:
+        raise ValueError("bf16 and fp16 are exclusive")
+    return "bf16" if bf16 else "f16" if fp16 else "f32"
+
+
+def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = False, fp16: bool = False):
     """C = A.B in fp64 (and D = |A|.|B| if with_scale).
 
-    A: M x K, B: K x N, row-major, float32 or (bf16=True) uint16 BF16 patterns.
+    A: M x K, B: K x N, row-major, float32, or uint16 patterns of BF16
+    (bf16=True) or IEEE half (fp16=True).
     """
-    _as_operand(A, bf16), _as_operand(B, bf16)
+    kind = _kind(bf16, fp16)
+    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
     M, K = A.shape
     K2, N = B.shape
     if K != K2:
         raise ValueError("inner dimensions differ")
     C = np.empty((M, N), np.float64)
     D = np.empty((M, N), np.float64) if with_scale else None
-    fn = _load().oracle_gemm_bf16 if bf16 else _load().oracle_gemm_f32
+    fn = getattr(_load(), f"oracle_gemm_{kind}")
     fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), C.ctypes.data, max(N, 1),
        D.ctypes.data if D is not None else None, max(N, 1))
     return (C, D) if with_scale else C
 
 
-def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale: bool = True):
+def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale: bool = True, fp16: bool = False):
     """Rows `rows` of C = A.B and (with_scale) of D = |A|.|B|, each len(rows) x N, fp64."""
-    _as_operand(A, bf16), _as_operand(B, bf16)
+    kind = _kind(bf16, fp16)
+    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
     M, K = A.shape
     N = B.shape[1]
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
@@ -122,19 +132,20 @@ def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale
         raise IndexError("row index out of range")
     C = np.empty((r.size, N), np.float64)
     D = np.empty((r.size, N), np.float64) if with_scale else None
-    fn = _load().oracle_gemm_rows_bf16 if bf16 else _load().oracle_gemm_rows_f32
+    fn = getattr(_load(), f"oracle_gemm_rows_{kind}")
     fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), r.ctypes.data, r.size,
        C.ctypes.data, D.ctypes.data if D is not None else None)
     return C, D
 
 
-def gemm_jik(A: np.ndarray, B: np.ndarray, bf16: bool = False) -> np.ndarray:
+def gemm_jik(A: np.ndarray, B: np.ndarray, bf16: bool = False, fp16: bool = False) -> np.ndarray:
     """The same product with the j-i-k loop order (tiny sizes only)."""
-    _as_operand(A, bf16), _as_operand(B, bf16)
+    kind = _kind(bf16, fp16)
+    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
     M, K = A.shape
     N = B.shape[1]
     C = np.empty((M, N), np.float64)
-    fn = _load().oracle_gemm_bf16_jik if bf16 else _load().oracle_gemm_f32_jik
+    fn = getattr(_load(), f"oracle_gemm_{kind}_jik")
     fn(M, N, K, A.ctypes.data, _ld(A), B.ctypes.data, _ld(B), C.ctypes.data, max(N, 1))
     return C
 
@@ -144,4 +155,12 @@ def widen_bf16(bits: np.ndarray) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(b.shape, np.float64)
     _load().oracle_widen_bf16(b.ctypes.data, out.ctypes.data, b.size)
+    return out
+
+
+def widen_f16(bits: np.ndarray) -> np.ndarray:
+    """Exact value of each IEEE half pattern, as fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_widen_f16(b.ctypes.data, out.ctypes.data, b.size)
     return out

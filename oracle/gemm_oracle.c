@@ -10,15 +10,16 @@
  * operations, one multiply and one add per (i, j, k) triple, and nothing else.
  * Section 13.8 of the same page fixes the precision contract of the tensor-core
  * paths: products of the narrow inputs are formed exactly and summed in FP32.
- * This oracle is stricter: every product of two FP32 or BF16 values is exact in
- * IEEE double (24 + 24 significand bits < 53), and the sums are done in double,
+ * This oracle is stricter: every product of two FP32, BF16 or FP16 values is
+ * exact in IEEE double (at most 24 + 24 significand bits < 53), and the sums are done in double,
  * so the only rounding is that of a double-precision running sum.
  *
  * Layout: every matrix is row-major with a leading dimension in ELEMENTS
  * (A is M x K with lda >= K, B is K x N with ldb >= N, C is M x N with ldc >= N).
- * BF16 operands arrive as their raw 16-bit patterns and are widened exactly
- * (a BF16 value is the top half of the FP32 with the same sign, exponent and
- * first 7 mantissa bits).
+ * BF16 and FP16 operands arrive as their raw 16-bit patterns and are widened
+ * exactly (a BF16 value is the top half of the FP32 with the same sign,
+ * exponent and first 7 mantissa bits; an IEEE half is sign, 5-bit exponent
+ * with bias 15, 10-bit mantissa, with subnormals at exponent 0).
  *
  * Besides C, every entry point can also return D[i][j] = sum_k |A[i][k]|*|B[k][j]|,
  * the scale against which an error in C[i][j] is judged (max |dC| / D).
@@ -45,6 +46,24 @@ static double widen_bf16(uint16_t bits)
     memcpy(&f, &u, sizeof f);
     return (double)f;
 }
+
+static double widen_f16(uint16_t bits)
+{
+    const int sign = bits >> 15, e = (bits >> 10) & 31, m = bits & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* 16-bit operand formats */
+enum { FMT_BF16 = 0, FMT_F16 = 1 };
+
+static double widen16(uint16_t bits, int fmt) { return fmt == FMT_F16 ? widen_f16(bits) : widen_bf16(bits); }
 
 int oracle_num_threads(void)
 {
@@ -73,15 +92,18 @@ static void row_f32(int64_t i, int64_t N, int64_t K, const float *A, int64_t lda
     }
 }
 
-static void row_bf16(int64_t i, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
-                     const uint16_t *B, int64_t ldb, double *c, double *d, double *bw)
+static void row_h16(int fmt, int64_t i, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                    const uint16_t *B, int64_t ldb, double *c, double *d, double *bw)
 {
     for (int64_t j = 0; j < N; ++j) c[j] = 0.0;
     if (d) for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        const double a = widen_bf16(A[i * lda + k]);
+        const double a = widen16(A[i * lda + k], fmt);
         const uint16_t *b = B + k * ldb;
-        for (int64_t j = 0; j < N; ++j) bw[j] = widen_bf16(b[j]);
+        if (fmt == FMT_F16)
+            for (int64_t j = 0; j < N; ++j) bw[j] = widen_f16(b[j]);
+        else
+            for (int64_t j = 0; j < N; ++j) bw[j] = widen_bf16(b[j]);
         for (int64_t j = 0; j < N; ++j) c[j] += a * bw[j];
         if (d) {
             const double aa = fabs(a);
@@ -100,18 +122,32 @@ void oracle_gemm_f32(int64_t M, int64_t N, int64_t K,
         row_f32(i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL);
 }
 
-void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
-                      const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-                      double *C, int64_t ldc, double *D, int64_t ldd)
+static void gemm_h16(int fmt, int64_t M, int64_t N, int64_t K,
+                     const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                     double *C, int64_t ldc, double *D, int64_t ldd)
 {
     #pragma omp parallel
     {
         double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
         #pragma omp for schedule(dynamic, 1)
         for (int64_t i = 0; i < M; ++i)
-            row_bf16(i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL, bw);
+            row_h16(fmt, i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL, bw);
         free(bw);
     }
+}
+
+void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                      const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                      double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    gemm_h16(FMT_BF16, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+}
+
+void oracle_gemm_f16(int64_t M, int64_t N, int64_t K,
+                     const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                     double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    gemm_h16(FMT_F16, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
 }
 
 /* Only the rows listed in rows[0..nrows): C and D are dense nrows x N outputs.
@@ -126,19 +162,33 @@ void oracle_gemm_rows_f32(int64_t M, int64_t N, int64_t K,
         row_f32(rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL);
 }
 
-void oracle_gemm_rows_bf16(int64_t M, int64_t N, int64_t K,
-                           const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-                           const int64_t *rows, int64_t nrows, double *C, double *D)
+static void rows_h16(int fmt, int64_t N, int64_t K, const uint16_t *A, int64_t lda, const uint16_t *B,
+                     int64_t ldb, const int64_t *rows, int64_t nrows, double *C, double *D)
 {
-    (void)M;
     #pragma omp parallel
     {
         double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
         #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < nrows; ++r)
-            row_bf16(rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL, bw);
+            row_h16(fmt, rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL, bw);
         free(bw);
     }
+}
+
+void oracle_gemm_rows_bf16(int64_t M, int64_t N, int64_t K,
+                           const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                           const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    rows_h16(FMT_BF16, N, K, A, lda, B, ldb, rows, nrows, C, D);
+}
+
+void oracle_gemm_rows_f16(int64_t M, int64_t N, int64_t K,
+                          const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                          const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    rows_h16(FMT_F16, N, K, A, lda, B, ldb, rows, nrows, C, D);
 }
 
 /* Second loop order (j outer, then i, then k), single-threaded, for brute-force
@@ -156,21 +206,39 @@ void oracle_gemm_f32_jik(int64_t M, int64_t N, int64_t K,
         }
 }
 
-void oracle_gemm_bf16_jik(int64_t M, int64_t N, int64_t K,
-                          const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-                          double *C, int64_t ldc)
+static void jik_h16(int fmt, int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda, const uint16_t *B,
+                    int64_t ldb, double *C, int64_t ldc)
 {
     for (int64_t j = 0; j < N; ++j)
         for (int64_t i = 0; i < M; ++i) {
             double s = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                s += widen_bf16(A[i * lda + k]) * widen_bf16(B[k * ldb + j]);
+                s += widen16(A[i * lda + k], fmt) * widen16(B[k * ldb + j], fmt);
             C[i * ldc + j] = s;
         }
 }
 
-/* Exact widening of n BF16 patterns, exposed so the tests can pin it. */
+void oracle_gemm_bf16_jik(int64_t M, int64_t N, int64_t K,
+                          const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                          double *C, int64_t ldc)
+{
+    jik_h16(FMT_BF16, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
+void oracle_gemm_f16_jik(int64_t M, int64_t N, int64_t K,
+                         const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                         double *C, int64_t ldc)
+{
+    jik_h16(FMT_F16, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
+/* Exact widening of n BF16 / FP16 patterns, exposed so the tests can pin it. */
 void oracle_widen_bf16(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) dst[i] = widen_bf16(src[i]);
+}
+
+void oracle_widen_f16(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = widen_f16(src[i]);
 }

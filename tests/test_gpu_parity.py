@@ -16,14 +16,14 @@ import torch
 import tiled_tensor_core_gemm_gb300 as tg
 from tiled_tensor_core_gemm_gb300 import build as tgbuild
 from tiled_tensor_core_gemm_gb300.inputs import (C1_FP32_256, C2_FP32_1024, C2_TF32_1024, C3_FP32_4096,
-                                                 C3_TF32_4096, C4_BF16_8192, C5_BF16_RAGGED, make_operands,
-                                                 workload_operands)
+                                                 C3_TF32_4096, C4_BF16_8192, C5_BF16_RAGGED, FP16_4096, FP16_8192,
+                                                 make_operands, workload_operands)
 
 from gemm_check import TOL, error_ratio, oracle_full, oracle_rows, run_gemm, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ("fp32", "tf32", "bf16")
+DTYPES = ("fp32", "tf32", "bf16", "fp16")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,7 +57,7 @@ def test_small_integers_bit_exact(dtype, shape):
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_identity_and_permutation(dtype):
     n, N = 300, 520
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(dtype, torch.float32)
     _, B = make_operands(n, N, n, dtype, "uniform", seed=12)
     if dtype == "tf32":
         B = B.to(torch.bfloat16).float()   # values the tensor cores read without loss
@@ -113,7 +113,7 @@ TC_VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 256)]
 
 # (dtype, B staging): BF16 reads B as stored (N-major) or from the K-major
 # transposed copy; TF32 always uses the K-major copy.
-TC_OPERANDS = [("bf16", 2), ("bf16", 1), ("tf32", 1)]
+TC_OPERANDS = [("bf16", 2), ("bf16", 1), ("tf32", 1), ("fp16", 2), ("fp16", 1)]
 
 
 @pytest.mark.parametrize("operands", TC_OPERANDS, ids=lambda o: f"{o[0]}_{'kmajorB' if o[1] == 1 else 'nmajorB'}")
@@ -140,7 +140,7 @@ def test_every_tensor_core_variant_exact(operands, variant, tma_store, shape):
             tg.gemm_set_option(k, 0)
 
 
-@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16"))
 @pytest.mark.parametrize("variant", TC_VARIANTS, ids=lambda v: f"cg{v[0]}_bn{v[1]}")
 @pytest.mark.parametrize("splits", (2, 3, 7))
 def test_split_k_exact(dtype, variant, splits):
@@ -219,8 +219,8 @@ def test_workload_full(w):
     assert r <= TOL[w.dtype], r
 
 
-@pytest.mark.parametrize("w", [C3_FP32_4096, C3_TF32_4096, C4_BF16_8192] + list(C5_BF16_RAGGED[1:]),
-                         ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [C3_FP32_4096, C3_TF32_4096, C4_BF16_8192] + list(C5_BF16_RAGGED[1:]) +
+                         [FP16_4096, FP16_8192], ids=lambda w: w.name)
 def test_workload_sampled_rows(w):
     A, B = workload_operands(w)
     C = run_gemm(A, B, w.dtype)

@@ -4,7 +4,7 @@ No GPU.  Every check here is fixed by the mathematics of C = A.B ("Shared
 memory and tensor cores", ml-compiler-from-scratch ch. 13, section 13.1) or by
 an independent library routine: identity and permutation products, all-ones
 inputs, exact integer arithmetic, a second loop order, float64 matmul, and the
-library's own BF16 conversion.
+libraries' own BF16 and FP16 conversions.
 """
 import numpy as np
 import pytest
@@ -21,6 +21,10 @@ def _f32(x):
 def _bf16_bits(x_float):
     t = torch.as_tensor(np.asarray(x_float, dtype=np.float32)).to(torch.bfloat16)
     return as_oracle_array(t).copy()
+
+
+def _f16_bits(x_float):
+    return np.asarray(x_float, dtype=np.float32).astype(np.float16).view(np.uint16).copy()
 
 
 @pytest.mark.parametrize("M,N", [(1, 1), (7, 13), (64, 33)])
@@ -134,3 +138,38 @@ def test_empty_sum_and_empty_shapes():
 
 def test_threads_reported():
     assert oracle.num_threads() >= 1
+
+
+def test_f16_widening_matches_library_conversion():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen_f16(bits)
+    lib = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], lib[~nan])
+    # 1.0, -2.0, the largest finite value, the smallest subnormal, +inf
+    assert list(oracle.widen_f16(np.array([0x3C00, 0xC000, 0x7BFF, 0x0001, 0x7C00], np.uint16))) == [
+        1.0, -2.0, 65504.0, 2.0 ** -24, float("inf")]
+
+
+def test_small_integers_exact_f16():
+    rng = np.random.default_rng(9)
+    M, N, K = 29, 43, 300
+    Ai = rng.integers(-8, 9, (M, K))
+    Bi = rng.integers(-8, 9, (K, N))
+    C, D = oracle.gemm(_f16_bits(Ai), _f16_bits(Bi), fp16=True, with_scale=True)
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(D, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (17, 16, 15)])
+def test_f16_second_loop_order_and_library(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = _f16_bits(rng.standard_normal((M, K)))
+    B = _f16_bits(rng.standard_normal((K, N)))
+    C = oracle.gemm(A, B, fp16=True)
+    assert np.array_equal(C, oracle.gemm_jik(A, B, fp16=True))
+    ref = A.view(np.float16).astype(np.float64) @ B.view(np.float16).astype(np.float64)
+    assert np.allclose(C, ref, rtol=1e-13, atol=1e-13)
+    r, _ = oracle.gemm_rows(A, B, [M - 1], fp16=True)
+    assert np.array_equal(r[0], C[M - 1])

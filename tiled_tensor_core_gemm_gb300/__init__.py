@@ -20,8 +20,8 @@ import threading
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libtcgemm.so")
 
-GEMM_FP32, GEMM_TF32, GEMM_BF16 = 0, 1, 2
-DTYPES = {"fp32": GEMM_FP32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
+GEMM_FP32, GEMM_TF32, GEMM_BF16, GEMM_FP16 = 0, 1, 2, 3
+DTYPES = {"fp32": GEMM_FP32, "tf32": GEMM_TF32, "bf16": GEMM_BF16, "fp16": GEMM_FP16}
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = 1
@@ -141,18 +141,18 @@ def _ld(t) -> int:
 
 
 def gemm(A, B, C=None, dtype=None, stream=None):
-    """C = A.B through gemm_run for CUDA tensors (float32, or bfloat16 for BF16).
+    """C = A.B through gemm_run for CUDA tensors (float32, bfloat16 or float16).
 
-    dtype: "fp32" (default for float32 inputs), "tf32" or "bf16" (default for
-    bfloat16 inputs).  C, if given, must be a float32 CUDA tensor of shape
-    (M, N); it is overwritten.
+    dtype: "fp32" (default for float32 inputs), "tf32", "bf16" (default for
+    bfloat16 inputs) or "fp16" (default for float16 inputs).  C, if given, must
+    be a float32 CUDA tensor of shape (M, N); it is overwritten.
     """
     import torch
 
     if dtype is None:
-        dtype = "bf16" if A.dtype == torch.bfloat16 else "fp32"
+        dtype = {torch.bfloat16: "bf16", torch.float16: "fp16"}.get(A.dtype, "fp32")
     code = DTYPES[dtype]
-    want = torch.bfloat16 if code == GEMM_BF16 else torch.float32
+    want = {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16}.get(code, torch.float32)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"{dtype} GEMM takes {want} operands")
     M, K = A.shape

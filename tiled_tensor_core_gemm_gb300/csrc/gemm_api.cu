@@ -106,7 +106,7 @@ int check_device_span(const char *name, const void *p, uint64_t bytes, int dev, 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int elem_bytes(int dtype) { return dtype == GEMM_BF16 ? 2 : 4; }
+int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 2 : 4; }
 
 // Measured on GB300 (profiles/picker.md): at 4096^3 the 128 x 128 tile with a
 // K step of 16 beats K step 8 and the 8 x 16 register tiles; when 128 x 128
@@ -323,7 +323,7 @@ int64_t gemm_get_option(const char *key) {
 
 static int validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
                     int64_t ldb, const void *C, int64_t ldc) {
-    if (dtype != GEMM_FP32 && dtype != GEMM_TF32 && dtype != GEMM_BF16)
+    if (dtype != GEMM_FP32 && dtype != GEMM_TF32 && dtype != GEMM_BF16 && dtype != GEMM_FP16)
         return fail(GEMM_ERR_INVALID_ARG, "unknown dtype %d", dtype);
     if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)",
                                               (long long)M, (long long)N, (long long)K);

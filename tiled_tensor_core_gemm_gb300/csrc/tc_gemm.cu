@@ -1,4 +1,4 @@
-// Persistent tensor-core GEMM for TF32 and BF16 inputs with FP32 accumulation
+// Persistent tensor-core GEMM for BF16, FP16 and TF32 inputs with FP32 accumulation
 // in Tensor Memory (tcgen05), fed by TMA, for sm_103a.
 //
 // Structure, after "Learn CuTeDSL":
@@ -66,8 +66,12 @@ enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRole
 // transposed copy.
 enum BMode : int { kBNMajor = 0, kBKMajor = 1 };
 
-template <bool TF32, int CG, int BN, int BMODE>
+// Operand element type of a variant.
+enum Dt : int { kDtBF16 = 0, kDtTF32 = 1, kDtFP16 = 2 };
+
+template <int DT, int CG, int BN, int BMODE>
 struct TcCfg {
+    static constexpr bool TF32 = DT == kDtTF32;
     static constexpr bool BKM = BMODE == kBKMajor;
     static constexpr int ELEM = TF32 ? 4 : 2;
     static constexpr int BK = 128 / ELEM;           // one 128-byte swizzle row of K
@@ -88,10 +92,10 @@ struct TcCfg {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + kEpiBytes + kBarBytes;
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     // Instruction descriptor: D f32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12:
-    // bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A K-major (bit 15 = 0),
+    // f16 = 0 and bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A K-major (bit 15 = 0),
     // B MN-major (bit 16 = 1) or K-major (0), N >> 3 in bits 17-22, M >> 4 in
     // bits 24-28.
-    static constexpr uint32_t FMT = TF32 ? 2u : 1u;
+    static constexpr uint32_t FMT = DT == kDtTF32 ? 2u : DT == kDtFP16 ? 0u : 1u;   // f16 = 0 for kind::f16
     static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((BKM ? 0u : 1u) << 16) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((kBM * CG) >> 4) << 24);
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N out of range");
@@ -171,13 +175,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-template <bool TF32, int CG, int BN, int BMODE>
+template <int DT, int CG, int BN, int BMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW, const TcParams p) {
-    using Cf = TcCfg<TF32, CG, BN, BMODE>;
+    using Cf = TcCfg<DT, CG, BN, BMODE>;
     constexpr bool kPair = CG == 2;
     constexpr bool BKM = Cf::BKM;
+    constexpr bool TF32 = Cf::TF32;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -469,13 +474,15 @@ CUresult encode_3d_slabs(CUtensorMap *map, const void *base, int64_t cols, int64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool TF32, int CG, int BN, int BMODE>
+template <int DT, int CG, int BN, int BMODE>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
                    int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
                    size_t errlen) {
-    using Cf = TcCfg<TF32, CG, BN, BMODE>;
+    using Cf = TcCfg<DT, CG, BN, BMODE>;
     constexpr bool BKM = Cf::BKM;
-    const CUtensorMapDataType dt = TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = DT == kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : DT == kDtFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb, tc, tw;
     std::memset(&tc, 0, sizeof tc);
     std::memset(&tw, 0, sizeof tw);
@@ -496,7 +503,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
         std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
         return GEMM_ERR_CUDA;
     }
-    auto kern = tc_gemm_kernel<TF32, CG, BN, BMODE>;
+    auto kern = tc_gemm_kernel<DT, CG, BN, BMODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -548,27 +555,28 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
 // A (dtype, CTA group, BN, B mode) combination is compiled only if it is legal:
 // TF32 always reads the K-major copy of B, and B read as stored needs every
 // CTA's share of the tile width to be whole 128-byte column chunks.
-template <bool TF32, int CG, int BN, int BMODE>
+template <int DT, int CG, int BN, int BMODE>
 constexpr bool variant_ok() {
-    return !(TF32 && BMODE == kBNMajor) && (BMODE == kBKMajor || (BN / CG) % (128 / (TF32 ? 4 : 2)) == 0);
+    return !(DT == kDtTF32 && BMODE == kBNMajor) &&
+           (BMODE == kBKMajor || (BN / CG) % (128 / (DT == kDtTF32 ? 4 : 2)) == 0);
 }
 
-template <bool TF32, int CG, int BN, int BMODE>
+template <int DT, int CG, int BN, int BMODE>
 int variant_value(bool stages) {
-    if constexpr (variant_ok<TF32, CG, BN, BMODE>()) {
-        using Cf = TcCfg<TF32, CG, BN, BMODE>;
+    if constexpr (variant_ok<DT, CG, BN, BMODE>()) {
+        using Cf = TcCfg<DT, CG, BN, BMODE>;
         return stages ? Cf::STAGES : Cf::SMEM_BYTES;
     } else {
         return 0;
     }
 }
 
-template <bool TF32, int CG, int BN, int BMODE>
+template <int DT, int CG, int BN, int BMODE>
 int launch_if_ok(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
                  int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
                  size_t errlen) {
-    if constexpr (variant_ok<TF32, CG, BN, BMODE>()) {
-        return launch_variant<TF32, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream,
+    if constexpr (variant_ok<DT, CG, BN, BMODE>()) {
+        return launch_variant<DT, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream,
                                                    err, errlen);
     } else {
         std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, BMODE);
@@ -588,9 +596,12 @@ static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, bool stages)
 #define X(cg, bn_)                                                                                   \
     if (cta_group == cg && bn == bn_) {                                                               \
         if (dtype == GEMM_TF32)                                                                       \
-            return mode == kBKMajor ? variant_value<true, cg, bn_, kBKMajor>(stages) : 0;             \
-        return mode == kBKMajor ? variant_value<false, cg, bn_, kBKMajor>(stages)                     \
-                                : variant_value<false, cg, bn_, kBNMajor>(stages);                    \
+            return mode == kBKMajor ? variant_value<kDtTF32, cg, bn_, kBKMajor>(stages) : 0;          \
+        if (dtype == GEMM_FP16)                                                                       \
+            return mode == kBKMajor ? variant_value<kDtFP16, cg, bn_, kBKMajor>(stages)               \
+                                    : variant_value<kDtFP16, cg, bn_, kBNMajor>(stages);              \
+        return mode == kBKMajor ? variant_value<kDtBF16, cg, bn_, kBKMajor>(stages)                   \
+                                : variant_value<kDtBF16, cg, bn_, kBNMajor>(stages);                  \
     }
     TC_VARIANTS(X)
 #undef X
@@ -606,23 +617,25 @@ int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
               int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
               size_t errlen) {
-#define X(cg, bn_)                                                                                              \
-    if (plan.cta_group == cg && plan.bn == bn_) {                                                                \
-        if (dtype == GEMM_TF32) {                                                                                \
-            if (plan.b_kmajor != kBKMajor) break;                                                                \
-            return launch_if_ok<true, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,   \
-                                                         stream, err, errlen);                                   \
-        }                                                                                                        \
-        return plan.b_kmajor == kBKMajor                                                                         \
-                   ? launch_if_ok<false, cg, bn_, kBKMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,\
-                                                            stream, err, errlen)                                 \
-                   : launch_if_ok<false, cg, bn_, kBNMajor>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms,\
-                                                            stream, err, errlen);                                \
+#define TC_LAUNCH(DT_, MODE_, CG_, BN_) \
+    launch_if_ok<DT_, CG_, BN_, MODE_>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream, err, errlen)
+#define X(cg, bn_)                                                                                      \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                        \
+        if (dtype == GEMM_TF32) {                                                                        \
+            if (plan.b_kmajor != kBKMajor) break;                                                        \
+            return TC_LAUNCH(kDtTF32, kBKMajor, cg, bn_);                                                \
+        }                                                                                                \
+        if (dtype == GEMM_FP16)                                                                          \
+            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtFP16, kBKMajor, cg, bn_)                     \
+                                             : TC_LAUNCH(kDtFP16, kBNMajor, cg, bn_);                    \
+        return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtBF16, kBKMajor, cg, bn_)                         \
+                                         : TC_LAUNCH(kDtBF16, kBNMajor, cg, bn_);                        \
     }
     do {
         TC_VARIANTS(X)
     } while (0);
 #undef X
+#undef TC_LAUNCH
     std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", plan.cta_group, plan.bn,
                   plan.b_kmajor);
     return GEMM_ERR_UNSUPPORTED;
@@ -637,8 +650,8 @@ cudaError_t tc_read_and_clear_status(uint32_t words[4]) {
 
 int tc_max_active_clusters(int device) {
     (void)device;
-    using Cf = TcCfg<false, 2, 256, kBNMajor>;
-    auto kern = tc_gemm_kernel<false, 2, 256, kBNMajor>;
+    using Cf = TcCfg<kDtBF16, 2, 256, kBNMajor>;
+    auto kern = tc_gemm_kernel<kDtBF16, 2, 256, kBNMajor>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;

@@ -9,8 +9,8 @@ Recipe (the workloads are synthetic square and ragged GEMMs, as in the
 * one CPU ``torch.Generator`` seeded with the workload's seed; A (M x K) is
   drawn first, then B (K x N), from the same generator;
 * ``uniform`` is U[-1, 1) = 2*rand - 1, ``normal`` is N(0, 1) via randn;
-* for BF16 operands the FP32 draw is rounded once to BF16 (round to nearest
-  even, the library's own ``.to(torch.bfloat16)``); those BF16 values are the
+* for BF16 (FP16) operands the FP32 draw is rounded once to BF16 (FP16) by
+  round to nearest even, the library's own ``.to(...)``; those values are the
   ground truth for every check;
 * ``ints`` draws integers uniformly from [-lo_hi, lo_hi], for the exactness
   tests (every product and partial sum is then an exact small integer).
@@ -45,6 +45,10 @@ C2_TF32_1024 = Workload("tf32 1024^3 U[-1,1] seed 1", 1024, 1024, 1024, "tf32", 
 C3_FP32_4096 = Workload("fp32 4096^3 N(0,1) seed 2", 4096, 4096, 4096, "fp32", "normal", 2)
 C3_TF32_4096 = Workload("tf32 4096^3 N(0,1) seed 2", 4096, 4096, 4096, "tf32", "normal", 2)
 C4_BF16_8192 = Workload("bf16 8192^3 N(0,1) seed 3", 8192, 8192, 8192, "bf16", "normal", 3)
+# FP16 inputs at the pages' own benchmark sizes (their TFLOPS table is FP16 at
+# 4096^3, their Nsight comparison FP16 at 8192^3), N(0,1) rounded to FP16.
+FP16_4096 = Workload("fp16 4096^3 N(0,1) seed 5", 4096, 4096, 4096, "fp16", "normal", 5)
+FP16_8192 = Workload("fp16 8192^3 N(0,1) seed 6", 8192, 8192, 8192, "fp16", "normal", 6)
 C5_BF16_RAGGED = tuple(
     Workload(f"bf16 {m}x{n}x{k} U[-1,1] seed 4", m, n, k, "bf16", "uniform", 4)
     for (m, n, k) in ((1000, 1000, 1000), (4097, 4095, 4099), (16384, 1024, 4096), (128, 8192, 8192))
@@ -74,7 +78,7 @@ def _pad(x: torch.Tensor, ld_pad: int) -> torch.Tensor:
 
 def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
                   lda_pad: int = 0, ldb_pad: int = 0, lo_hi: int = 8):
-    """(A, B) as CPU torch tensors: float32 for fp32/tf32, bfloat16 for bf16.
+    """(A, B) as CPU torch tensors: float32 for fp32/tf32, bfloat16 for bf16, float16 for fp16.
 
     The tensors may be views with a leading dimension larger than their width
     (``*_pad``); use ``.stride(0)`` for the leading dimension.
@@ -86,6 +90,9 @@ def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
     if dtype == "bf16":
         a = a.to(torch.bfloat16)
         b = b.to(torch.bfloat16)
+    elif dtype == "fp16":
+        a = a.to(torch.float16)
+        b = b.to(torch.float16)
     elif dtype not in ("fp32", "tf32"):
         raise ValueError(f"unknown dtype {dtype!r}")
     return _pad(a, lda_pad), _pad(b, ldb_pad)
@@ -96,9 +103,9 @@ def workload_operands(w: Workload):
 
 
 def as_oracle_array(t: torch.Tensor) -> np.ndarray:
-    """A CPU tensor as the numpy array the oracle takes (float32, or uint16 BF16 bits)."""
+    """A CPU tensor as the numpy array the oracle takes (float32, or uint16 BF16/FP16 bits)."""
     t = t.detach().cpu()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.float32:
         return t.numpy()
