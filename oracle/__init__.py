@@ -13,13 +13,19 @@ forms the same exact products and sums them in fp64 (k ascending), so it is at
 least as accurate as any path under test.  BF16 and FP16 inputs are passed as
 their raw 16-bit patterns and widened exactly.
 
-Every function also returns D[i, j] = sum_k |A[i, k]| * |B[k, j]| on request,
+``epilogue`` applies the fused epilogue of section 13.10 (bias, activation,
+residual add, output type) to an fp64 product: y = act(alpha * acc + beta *
+c_old + bias[j]), returned unrounded.
+
+Every GEMM function also returns D[i, j] = sum_k |A[i, k]| * |B[k, j]| on request,
 the per-entry scale used by the acceptance test max|C - C_ref| / D.
 
 Pins (tests/test_oracle.py): identity and permutation products, all-ones inputs
 (C == K everywhere), small-integer inputs against exact integer arithmetic, a
 second independent loop order at tiny sizes, float64 library matmul, and the
-BF16 and FP16 widenings against the library's own conversions.
+BF16 and FP16 widenings against the library's own conversions; the epilogue
+against the library's addmm, ReLU and GELU, printed values of the normal CDF,
+GELU's odd-part identity, and per-column bias broadcasting.
 """
 from __future__ import annotations
 
@@ -71,6 +77,9 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = None
+        lib.oracle_epilogue.argtypes = [_i64, _i64, _ptr, _i64, ctypes.c_double, ctypes.c_double, _ptr,
+                                        ctypes.c_int, _i64, _ptr, ctypes.c_int, _ptr, _i64]
+        lib.oracle_epilogue.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -164,3 +173,40 @@ def widen_f16(bits: np.ndarray) -> np.ndarray:
     out = np.empty(b.shape, np.float64)
     _load().oracle_widen_f16(b.ctypes.data, out.ctypes.data, b.size)
     return out
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+OUT_TYPES = {"f32": 0, "bf16": 1, "f16": 2}
+
+
+def epilogue(acc: np.ndarray, alpha: float = 1.0, beta: float = 0.0, c_old=None, out: str = "f32",
+             bias=None, act: str = "none") -> np.ndarray:
+    """y = act(alpha * acc + beta * c_old + bias[j]) in fp64, unrounded.
+
+    acc: M x N fp64 product.  c_old: M x N C already in memory, float32 for
+    out="f32" or the uint16 patterns of BF16 / IEEE half; read only when
+    beta != 0.  bias: N float32 values or None.  act: "none", "relu", "gelu".
+    """
+    a = np.ascontiguousarray(acc, dtype=np.float64)
+    if a.ndim != 2:
+        raise ValueError("acc must be 2-D")
+    M, N = a.shape
+    if out not in OUT_TYPES or act not in ACTIVATIONS:
+        raise ValueError(f"unknown output type {out!r} or activation {act!r}")
+    old = None
+    if beta != 0.0:
+        if c_old is None:
+            raise ValueError("beta != 0 needs c_old")
+        old = np.ascontiguousarray(c_old, dtype=np.float32 if out == "f32" else np.uint16)
+        if old.shape != (M, N):
+            raise ValueError("c_old must match acc")
+    b = None
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float32)
+        if b.shape != (N,):
+            raise ValueError("bias must hold N values")
+    Y = np.empty((M, N), np.float64)
+    _load().oracle_epilogue(M, N, a.ctypes.data, max(N, 1), float(alpha), float(beta),
+                            old.ctypes.data if old is not None else None, OUT_TYPES[out], max(N, 1),
+                            b.ctypes.data if b is not None else None, ACTIVATIONS[act], Y.ctypes.data, max(N, 1))
+    return Y

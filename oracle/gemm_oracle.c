@@ -28,6 +28,16 @@
  * OpenMP loop over rows.  A second, independent j-i-k routine exists only so the
  * tests can brute-force one loop order against the other at tiny sizes.
  *
+ * Fused epilogue (oracle_epilogue): section 13.10 of the same page names epilogue
+ * fusion -- bias, activation, residual add or a type cast applied to the
+ * accumulator before it is stored.  The reading taken here, written out in
+ * fp64 on the exact product: y = act(alpha * acc + beta * c_old + bias[j]),
+ * where c_old is the C already in memory (the residual, in the output type),
+ * bias is one FP32 value per column, and act is none, ReLU (max(x, 0)) or
+ * GELU (x times the standard normal CDF, Phi(x) = (1 + erf(x / sqrt 2)) / 2).
+ * The result is returned unrounded; the cast to the output type is left to
+ * the comparison, which allows for it.
+ *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no -march flags, so
  * x86 and Arm hosts give the same bits).
  */
@@ -241,4 +251,35 @@ void oracle_widen_bf16(const uint16_t *src, double *dst, int64_t n)
 void oracle_widen_f16(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) dst[i] = widen_f16(src[i]);
+}
+
+/* ------------------------------------------------------------ epilogue --- */
+enum { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
+enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
+
+static double read_old(const void *c_old, int out, int64_t idx)
+{
+    if (out == OUT_BF16) return widen_bf16(((const uint16_t *)c_old)[idx]);
+    if (out == OUT_F16) return widen_f16(((const uint16_t *)c_old)[idx]);
+    return (double)((const float *)c_old)[idx];
+}
+
+/* Y[i][j] = act(alpha * acc[i][j] + beta * c_old[i][j] + bias[j]) for an M x N
+ * block.  c_old (element type `out`) is read only when beta != 0; bias may be
+ * NULL.  acc, c_old and Y have their own leading dimensions. */
+void oracle_epilogue(int64_t M, int64_t N, const double *acc, int64_t ld_acc, double alpha, double beta,
+                     const void *c_old, int out, int64_t ld_old, const float *bias, int act,
+                     double *Y, int64_t ldy)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double x = alpha * acc[i * ld_acc + j];
+            if (beta != 0.0) x += beta * read_old(c_old, out, i * ld_old + j);
+            if (bias) x += (double)bias[j];
+            if (act == ACT_RELU)
+                x = x > 0.0 ? x : 0.0;
+            else if (act == ACT_GELU)
+                x = x * 0.5 * (1.0 + erf(x / sqrt(2.0)));
+            Y[i * ldy + j] = x;
+        }
 }

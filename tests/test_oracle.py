@@ -173,3 +173,80 @@ def test_f16_second_loop_order_and_library(M, N, K):
     assert np.allclose(C, ref, rtol=1e-13, atol=1e-13)
     r, _ = oracle.gemm_rows(A, B, [M - 1], fp16=True)
     assert np.array_equal(r[0], C[M - 1])
+
+
+# ---------------------------------------------------------------- epilogue --
+# Pins for the fused epilogue ("Shared memory and tensor cores" section 13.10:
+# bias, activation, residual add, type cast on the accumulator), each against
+# a library routine, printed values of the normal CDF, or an identity.
+
+def test_epilogue_default_is_the_product():
+    acc = np.random.default_rng(20).standard_normal((9, 14))
+    assert np.array_equal(oracle.epilogue(acc), acc)
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu"])
+def test_epilogue_against_library_addmm_and_activation(act):
+    rng = np.random.default_rng(21)
+    M, N, K = 23, 17, 40
+    Ai = rng.integers(-6, 7, (M, K))
+    Bi = rng.integers(-6, 7, (K, N))
+    c_old = _f32(rng.standard_normal((M, N)))
+    bias = _f32(rng.standard_normal(N))
+    alpha, beta = 0.37, -1.25
+    acc = oracle.gemm(_f32(Ai), _f32(Bi))
+    y = oracle.epilogue(acc, alpha, beta, c_old, "f32", bias, act)
+    t = torch.addmm(torch.from_numpy(c_old).double(), torch.from_numpy(Ai).double(), torch.from_numpy(Bi).double(),
+                    beta=beta, alpha=alpha) + torch.from_numpy(bias).double()
+    if act == "relu":
+        t = torch.relu(t)
+    elif act == "gelu":
+        t = torch.nn.functional.gelu(t)            # the erf form
+    assert np.allclose(y, t.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_epilogue_gelu_printed_normal_cdf_values():
+    # Phi(1), Phi(-1), Phi(2), Phi(3) as printed in standard normal tables.
+    x = np.array([[0.0, 1.0, -1.0, 2.0, 3.0]])
+    y = oracle.epilogue(x, act="gelu")
+    ref = [0.0, 0.8413447460685429, -0.15865525393145707, 2 * 0.9772498680518208, 3 * 0.9986501019683699]
+    assert np.allclose(y[0], ref, rtol=1e-14, atol=0)
+
+
+def test_epilogue_gelu_odd_part_is_half_identity():
+    # Phi(-x) = 1 - Phi(x), so GELU(x) - GELU(-x) = x for every x.
+    x = np.random.default_rng(22).uniform(-6, 6, (4, 50))
+    d = oracle.epilogue(x, act="gelu") - oracle.epilogue(-x, act="gelu")
+    assert np.allclose(d, x, rtol=1e-14, atol=1e-14)
+
+
+def test_epilogue_relu_signs():
+    pos = np.abs(np.random.default_rng(23).standard_normal((6, 7))) + 0.1
+    assert np.array_equal(oracle.epilogue(pos, act="relu"), pos)
+    assert np.array_equal(oracle.epilogue(-pos, act="relu"), np.zeros_like(pos))
+
+
+def test_epilogue_bias_is_per_column():
+    M, N = 5, 11                          # M != N: a row-indexed bias would differ
+    bias = np.arange(N, dtype=np.float32) - 3.5
+    y = oracle.epilogue(np.zeros((M, N)), bias=bias)
+    assert np.array_equal(y, np.broadcast_to(bias.astype(np.float64), (M, N)))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_epilogue_reads_old_c_in_the_output_type(out):
+    vals = np.random.default_rng(24).standard_normal((7, 9)).astype(np.float32)
+    if out == "bf16":
+        t = torch.from_numpy(vals).to(torch.bfloat16)
+        bits = as_oracle_array(t).copy()
+        lib = t.double().numpy()
+    else:
+        bits = _f16_bits(vals)
+        lib = bits.view(np.float16).astype(np.float64)
+    y = oracle.epilogue(np.zeros((7, 9)), alpha=1.0, beta=-2.0, c_old=bits, out=out)
+    assert np.array_equal(y, -2.0 * lib)
+
+
+def test_epilogue_beta_zero_never_reads_old_c():
+    acc = np.ones((3, 4))
+    assert np.array_equal(oracle.epilogue(acc, alpha=3.0, beta=0.0, c_old=None), 3.0 * acc)
