@@ -188,21 +188,39 @@ def make_device_operands(workload, device):
     return A, B, A.to(device), B.to(device)
 
 
-def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=None, on_end=None):
+def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=None, on_end=None, epi=None):
     """Device-side timing with CUDA events on `stream`: per-launch events for the
-    kernel's average duration, and one pair around all K steps."""
+    kernel's average duration, and one pair around all K steps.
+
+    epi: None (gemm_run, FP32 C) or a fused epilogue for gemm_run_ex, as a dict
+    with keys act, out, bias (bool), alpha, beta (seeded old C and bias)."""
     import torch
     _, _, A, B = make_device_operands(workload, device)
     M, N, K = workload.M, workload.N, workload.K
-    C = torch.empty((M, N), dtype=torch.float32, device=device)
     code = tg.DTYPES[workload.dtype]
     s = stream.cuda_stream
-    plan = tg.gemm_plan(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N).as_dict()
+    if epi is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=device)
+        plan = tg.gemm_plan(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N).as_dict()
 
-    def run():
-        rc = tg.gemm_run(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s)
-        if rc != tg.GEMM_OK:
-            raise RuntimeError(tg.gemm_last_error())
+        def run():
+            rc = tg.gemm_run(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s)
+            if rc != tg.GEMM_OK:
+                raise RuntimeError(tg.gemm_last_error())
+    else:
+        from tiled_tensor_core_gemm_gb300.inputs import make_epilogue_inputs
+        c_old, bias = make_epilogue_inputs(M, N, epi["out"], workload.seed)
+        C = c_old.to(device)
+        bias_d = bias.to(device) if epi.get("bias") else None
+        ep = tg.make_epilogue(epi.get("alpha", 1.0), epi.get("beta", 0.0),
+                              bias_d.data_ptr() if bias_d is not None else 0, epi.get("act", "none"), epi["out"])
+        plan = tg.gemm_plan(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N).as_dict()
+        plan["tma_store"] = 0      # the fused epilogue stores C with plain coalesced stores
+
+        def run():
+            rc = tg.gemm_run_ex(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, ep, s)
+            if rc != tg.GEMM_OK:
+                raise RuntimeError(tg.gemm_last_error())
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -424,8 +442,13 @@ def run_ours(args):
         side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
                                                     "bf16_4097x4095x4099", "bf16_16384x1024x4096",
                                                     "bf16_128x8192x8192", "fp16_4096", "fp16_8192")]
+        # the fused epilogue on the headline shape: bias + GELU with a BF16 C, and
+        # a residual add (beta = 1, the old BF16 C read back) with a BF16 C
+        fused = {"bf16_8192_bias_gelu_bf16out": {"act": "gelu", "out": "bf16", "bias": True},
+                 "bf16_8192_residual_bf16out": {"beta": 1.0, "out": "bf16"}}
+        side += [(k, workload_by_key("bf16_8192")) for k in fused]
         for key, wl in side:
-            r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device)
+            r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device, epi=fused.get(key))
             tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
             if wl.dtype == "fp32":
                 rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
@@ -446,7 +469,10 @@ def run_ours(args):
                                      f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
                                      NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
             in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype in ("bf16", "fp16") else 4)
-            paths[key] = {"workload": wl.name, "tflops": round(tf, 2), "steps": n_side,
+            if key in fused:
+                rl["traffic"] = None     # no capture of the fused-epilogue launch
+            paths[key] = {"workload": wl.name + (f", fused epilogue {fused[key]}" if key in fused else ""),
+                          "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
                           "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
         out["paths"] = paths

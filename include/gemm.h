@@ -104,6 +104,47 @@ GEMM_API int gemm_run(int64_t M, int64_t N, int64_t K, int dtype,
              const void *A, int64_t lda, const void *B, int64_t ldb,
              float *C, int64_t ldc, struct CUstream_st *stream);
 
+/*
+ * gemm_run_ex -- C = act(alpha * (A . B) + beta * C + bias), stored as
+ * out_dtype: the GEMM with its epilogue fused into the kernel that writes C.
+ * "Shared memory and tensor cores" (ml-compiler-from-scratch ch. 13) section
+ * 13.10 lists epilogue fusion among what production kernels add; "Learn
+ * CuTeDSL" (section 6) fuses work on the accumulator before C is written.
+ *
+ *   M..ldb      as gemm_run.
+ *   C, ldc      device pointer to C[0][0] of element type epi->out_dtype
+ *               (float, or bfloat16 / IEEE half bits), leading dimension in
+ *               elements.  Read first when epi->beta != 0.
+ *   epi         NULL means alpha = 1, beta = 0, no bias, no activation, FP32
+ *               output (exactly gemm_run).  Otherwise:
+ *     alpha     scale of A . B
+ *     beta      scale of the C already in memory (0: C is not read)
+ *     bias      device pointer to N floats added to every row, or NULL
+ *     activation  GEMM_ACT_NONE, GEMM_ACT_RELU (max(x, 0)) or GEMM_ACT_GELU
+ *               (x * Phi(x) with the normal CDF written through erf)
+ *     out_dtype GEMM_OUT_F32, GEMM_OUT_BF16 or GEMM_OUT_F16; the value is
+ *               computed in FP32 and rounded to nearest even once
+ * The epilogue is applied after all of K is summed (with split-K, by the
+ * kernel that sums the K ranges).  Errors as gemm_run, plus
+ * GEMM_ERR_INVALID_ARG for an unknown activation or output type, or a bias
+ * pointer that is not device memory covering N floats.
+ */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
+typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1, GEMM_OUT_F16 = 2 } gemm_out_t;
+
+typedef struct {
+    float alpha;
+    float beta;
+    const float *bias;
+    int32_t activation;
+    int32_t out_dtype;
+} gemm_epilogue_t;
+
+GEMM_API int gemm_run_ex(int64_t M, int64_t N, int64_t K, int dtype,
+                         const void *A, int64_t lda, const void *B, int64_t ldb,
+                         void *C, int64_t ldc, const gemm_epilogue_t *epi,
+                         struct CUstream_st *stream);
+
 /* Message for the calling thread's most recent failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 GEMM_API const char *gemm_last_error(void);

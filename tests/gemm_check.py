@@ -100,3 +100,82 @@ def sample_rows(M: int, tile: int = 128, extra: int = 8, seed: int = 0):
     rng = np.random.default_rng(seed)
     rows.update(int(r) for r in rng.integers(0, M, extra))
     return sorted(rows)
+
+
+# ----------------------------------------------------------- fused epilogue --
+# Acceptance for C = act(alpha * A.B + beta * C_old + bias) stored as `out`:
+#   |out_ij - y_ij| <= (1 + u) * b_ij + u * |y_ij| + s
+# where y is the oracle's fp64 value, S = |alpha| D + |beta C_old| + |bias| is
+# the scale of the pre-activation sum, b = (1.13 * tol + 1e-6) * S bounds the
+# FP32 result before the cast (the GEMM's own bound on alpha * A.B, a few FP32
+# roundings of the three-term sum and of the activation; 1.13 bounds the slope
+# of GELU, ReLU's is 1), u is the unit roundoff of the output type (2^-24, 2^-8,
+# 2^-11) and s half the smallest subnormal spacing of FP16 (2^-25; 0 otherwise).
+OUT_U = {"f32": 2.0 ** -24, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+OUT_SUB = {"f32": 0.0, "bf16": 0.0, "f16": 2.0 ** -25}
+OUT_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def run_gemm_ex(A: torch.Tensor, B: torch.Tensor, dtype: str, out: str = "f32", alpha: float = 1.0,
+                beta: float = 0.0, c_old: torch.Tensor | None = None, bias: torch.Tensor | None = None,
+                act: str = "none", ldc_pad: int = 0, epilogue: bool = True) -> np.ndarray:
+    """C through gemm_run_ex on the GPU (C starts as c_old when given); checks the
+    status word and that nothing outside C (guard bands, ldc padding) was
+    written.  Returns C as float64.  epilogue=False passes a NULL epilogue."""
+    M, K = A.shape
+    N = B.shape[1]
+    a_keep, a_ptr, lda = to_device(A)
+    b_keep, b_ptr, ldb = to_device(B)
+    ldc = max(N, 1) + ldc_pad
+    cdt = OUT_TORCH[out]
+    cbuf = torch.full((2 * GUARD + M * ldc,), float("nan"), dtype=cdt, device="cuda")
+    body = cbuf[GUARD:GUARD + M * ldc].view(M, ldc) if M * ldc else None
+    if c_old is not None and M and N:
+        body[:, :N].copy_(c_old.to(cdt))
+    c_ptr = cbuf.data_ptr() + GUARD * cbuf.element_size()
+    bias_d = bias.to(torch.float32).contiguous().cuda() if bias is not None else None
+    stream = torch.cuda.current_stream().cuda_stream
+    ep = tg.make_epilogue(alpha, beta, bias_d.data_ptr() if bias_d is not None else 0, act, out) if epilogue else None
+    rc = tg.gemm_run_ex(M, N, K, tg.DTYPES[dtype], a_ptr, lda, b_ptr, ldb, c_ptr, ldc, ep, stream)
+    assert rc == tg.GEMM_OK, tg.gemm_last_error()
+    st = tg.gemm_get_status(stream)
+    assert st == tg.GEMM_OK, tg.gemm_last_error()
+    host = cbuf.cpu().to(torch.float64).numpy()
+    del a_keep, b_keep
+    assert np.all(np.isnan(host[:GUARD])), "write before C"
+    assert np.all(np.isnan(host[GUARD + M * ldc:])), "write after C"
+    C = host[GUARD:GUARD + M * ldc].reshape(M, ldc)
+    if ldc_pad:
+        assert np.all(np.isnan(C[:, N:])), "write into the ldc padding"
+    return C[:, :N].copy()
+
+
+def oracle_c_old(c_old: torch.Tensor | None, out: str):
+    """The old C as the oracle takes it (float32 or 16-bit patterns)."""
+    if c_old is None:
+        return None
+    return as_oracle_array(c_old.to(OUT_TORCH[out])).copy()
+
+
+def epilogue_check(C: np.ndarray, acc: np.ndarray, D: np.ndarray, dtype: str, out: str, alpha: float, beta: float,
+                   c_old, bias, act: str):
+    """Worst (|out - y| / bound) over C; <= 1 passes.  Also returns y."""
+    old = oracle_c_old(c_old, out)
+    b = bias.numpy() if bias is not None else None
+    y = oracle.epilogue(acc, alpha, beta, old, out, b, act)
+    S = abs(alpha) * D
+    if beta != 0.0:
+        S = S + abs(beta) * np.abs(oracle.epilogue(np.zeros_like(acc), 0.0, 1.0, old, out))
+    if b is not None:
+        S = S + np.abs(b.astype(np.float64))[None, :]
+    u = OUT_U[out]
+    bound = (1.0 + u) * (1.13 * TOL[dtype] + 1e-6) * S + u * np.abs(y) + OUT_SUB[out]
+    if not np.all(np.isfinite(C)):
+        return float("inf"), y
+    diff = np.abs(C - y)
+    zero = bound == 0
+    if np.any(diff[zero] != 0):
+        return float("inf"), y
+    if not np.any(~zero):
+        return 0.0, y
+    return float(np.max(diff[~zero] / bound[~zero])), y

@@ -1,5 +1,6 @@
 """The C ABI without a GPU: the library loads, exports what include/gemm.h
 declares, rejects bad arguments before any CUDA call, and plans on the host."""
+import ctypes
 import os
 import re
 import subprocess
@@ -193,3 +194,62 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(tg, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         tg.gemm_version()
+
+
+# ------------------------------------------------------------ gemm_run_ex ---
+def _ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, **epi):
+    return tg.gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, tg.make_epilogue(**epi), 0)
+
+
+def test_epilogue_struct_layout_matches_the_header(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(gemm_epilogue_t),'
+                   ' offsetof(gemm_epilogue_t, alpha), offsetof(gemm_epilogue_t, beta),'
+                   ' offsetof(gemm_epilogue_t, bias), offsetof(gemm_epilogue_t, activation),'
+                   ' offsetof(gemm_epilogue_t, out_dtype)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    E = tg.GemmEpilogue
+    assert got == [ctypes.sizeof(E), E.alpha.offset, E.beta.offset, E.bias.offset, E.activation.offset,
+                   E.out_dtype.offset]
+
+
+def test_epilogue_enumerations_match_the_header():
+    src = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    for name, value in (("GEMM_ACT_NONE", 0), ("GEMM_ACT_RELU", 1), ("GEMM_ACT_GELU", 2), ("GEMM_OUT_F32", 0),
+                        ("GEMM_OUT_BF16", 1), ("GEMM_OUT_F16", 2)):
+        assert re.search(rf"\b{name}\s*=\s*{value}\b", src), name
+        assert getattr(tg, name) == value
+
+
+def test_epilogue_rejects_unknown_activation_and_output_type():
+    ep = tg.GemmEpilogue(1.0, 0.0, None, 7, 0)
+    assert tg.gemm_run_ex(8, 8, 8, tg.GEMM_BF16, 1 << 20, 8, 1 << 21, 8, 1 << 22, 8, ep, 0) == tg.GEMM_ERR_INVALID_ARG
+    assert "activation" in tg.gemm_last_error()
+    ep = tg.GemmEpilogue(1.0, 0.0, None, 0, 9)
+    assert tg.gemm_run_ex(8, 8, 8, tg.GEMM_BF16, 1 << 20, 8, 1 << 21, 8, 1 << 22, 8, ep, 0) == tg.GEMM_ERR_INVALID_ARG
+    assert "output type" in tg.gemm_last_error()
+
+
+def test_epilogue_argument_checks_before_cuda():
+    A, B = 1 << 20, 1 << 21
+    # bias inside C's footprint
+    rc = _ex(8, 8, 8, tg.GEMM_BF16, A, 8, B, 8, 1 << 22, 8, bias=(1 << 22) + 16, act="relu", out="bf16")
+    assert rc == tg.GEMM_ERR_INVALID_ARG and "bias overlaps C" in tg.gemm_last_error()
+    # a BF16 C at an odd address, a bias that is not 4-byte aligned
+    rc = _ex(8, 8, 8, tg.GEMM_BF16, A, 8, B, 8, (1 << 22) + 1, 8, out="bf16")
+    assert rc == tg.GEMM_ERR_INVALID_ARG and "aligned" in tg.gemm_last_error()
+    rc = _ex(8, 8, 8, tg.GEMM_BF16, A, 8, B, 8, 1 << 22, 8, bias=(1 << 23) + 2, out="bf16")
+    assert rc == tg.GEMM_ERR_INVALID_ARG and "bias is not 4-byte aligned" in tg.gemm_last_error()
+    # a BF16 C half the size of an FP32 one: C right after A's footprint is fine
+    # for the overlap check, C one element earlier overlaps
+    a_end = A + (7 * 8 + 8) * 2
+    rc = _ex(8, 8, 8, tg.GEMM_BF16, A, 8, B, 8, a_end - 2, 8, out="bf16")
+    assert rc == tg.GEMM_ERR_INVALID_ARG and "overlap" in tg.gemm_last_error()
+
+
+def test_null_epilogue_behaves_as_gemm_run():
+    assert tg.gemm_run_ex(0, 5, 3, tg.GEMM_BF16, 0, 3, 0, 5, 0, 5, None, 0) == tg.GEMM_OK
+    assert tg.gemm_run_ex(4, 4, 4, 7, 16, 4, 16, 4, 64, 4, None, 0) == tg.GEMM_ERR_INVALID_ARG

@@ -1,4 +1,6 @@
-"""GB300-native dense GEMM: C = A.B over row-major operands, FP32 output.
+"""GB300-native dense GEMM: C = A.B over row-major operands, FP32 output, with
+an optional fused epilogue C = act(alpha * A.B + beta * C + bias) stored as
+FP32, BF16 or FP16.
 
 A thin ctypes binding over the C ABI in include/gemm.h (libtcgemm.so, built
 in-tree by ``build.build()``).  The functions below carry the C names and only
@@ -8,8 +10,12 @@ raises.
 
     gemm_run(M, N, K, dtype, A, lda, B, ldb, C, ldc, stream) -> status
         A, B, C are device addresses (ints); stream is a cudaStream_t as int.
+    gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, epilogue, stream) -> status
+        epilogue: a GemmEpilogue (or None for plain gemm_run behaviour).
     gemm(A, B, C=None, dtype=None, stream=None) -> C
         torch-tensor convenience: row-major CUDA tensors in, FP32 C out.
+    gemm_ex(A, B, C=None, alpha=1, beta=0, bias=None, act="none", out="f32", ...) -> C
+        the same with the fused epilogue.
 """
 from __future__ import annotations
 
@@ -30,8 +36,13 @@ GEMM_ERR_CUDA = 3
 GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_NO_MEMORY = 5
 
+GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
+ACTIVATIONS = {"none": GEMM_ACT_NONE, "relu": GEMM_ACT_RELU, "gelu": GEMM_ACT_GELU}
+GEMM_OUT_F32, GEMM_OUT_BF16, GEMM_OUT_F16 = 0, 1, 2
+OUT_TYPES = {"f32": GEMM_OUT_F32, "bf16": GEMM_OUT_BF16, "f16": GEMM_OUT_F16}
+
 EXPORTED = ("gemm_run", "gemm_last_error", "gemm_get_status", "gemm_set_option",
-            "gemm_get_option", "gemm_plan", "gemm_version", "gemm_run_tf32_static")
+            "gemm_get_option", "gemm_plan", "gemm_version", "gemm_run_tf32_static", "gemm_run_ex")
 TF32_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # GEMM_TF32_STATIC_SCRATCH_BYTES in include/gemm.h
 
 
@@ -48,6 +59,17 @@ class GemmPlan(ctypes.Structure):
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemmEpilogue(ctypes.Structure):
+    """gemm_epilogue_t: y = act(alpha * acc + beta * C_old + bias[col]) stored as out_dtype."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+
+
+def make_epilogue(alpha=1.0, beta=0.0, bias=0, act="none", out="f32") -> GemmEpilogue:
+    """A GemmEpilogue from names; bias is a device address (0 for none)."""
+    return GemmEpilogue(float(alpha), float(beta), int(bias) or None, ACTIVATIONS[act], OUT_TYPES[out])
 
 
 _lock = threading.Lock()
@@ -88,6 +110,9 @@ def load_library():
         lib.gemm_version.restype = ctypes.c_int
         lib.gemm_run_tf32_static.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, p]
         lib.gemm_run_tf32_static.restype = ctypes.c_int
+        lib.gemm_run_ex.argtypes = [i64, i64, i64, ctypes.c_int, p, i64, p, i64, p, i64, ctypes.POINTER(GemmEpilogue),
+                                    p]
+        lib.gemm_run_ex.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -131,6 +156,12 @@ def gemm_run_tf32_static(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return load_library().gemm_run_tf32_static(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
+def gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, epilogue=None, stream=0) -> int:
+    """C = act(alpha * A.B + beta * C + bias) stored as the epilogue's output type."""
+    ep = ctypes.byref(epilogue) if epilogue is not None else None
+    return load_library().gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, ep, stream)
+
+
 # ------------------------------------------------------ tensor convenience ---
 def _ld(t) -> int:
     if t.dim() != 2:
@@ -164,6 +195,42 @@ def gemm(A, B, C=None, dtype=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
     rc = gemm_run(M, N, K, code, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), stream)
+    if rc != GEMM_OK:
+        raise GemmError(rc, gemm_last_error())
+    return C
+
+
+def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act="none", out="f32", dtype=None, stream=None):
+    """C = act(alpha * A.B + beta * C + bias) through gemm_run_ex for CUDA tensors.
+
+    out: "f32", "bf16" or "f16", the element type of C (allocated if None;
+    beta must then be 0).  bias: a float32 CUDA tensor of N values or None.
+    """
+    import torch
+
+    if dtype is None:
+        dtype = {torch.bfloat16: "bf16", torch.float16: "fp16"}.get(A.dtype, "fp32")
+    code = DTYPES[dtype]
+    want = {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16}.get(code, torch.float32)
+    if A.dtype != want or B.dtype != want:
+        raise TypeError(f"{dtype} GEMM takes {want} operands")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    cdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out]
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=cdt, device=A.device)
+    elif C.dtype != cdt or tuple(C.shape) != (M, N):
+        raise TypeError(f"C must be a ({M}, {N}) {cdt} tensor")
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous()):
+        raise TypeError(f"bias must be {N} contiguous float32 values")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    ep = make_epilogue(alpha, beta, bias.data_ptr() if bias is not None else 0, act, out)
+    rc = gemm_run_ex(M, N, K, code, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), ep, stream)
     if rc != GEMM_OK:
         raise GemmError(rc, gemm_last_error())
     return C

@@ -366,21 +366,36 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     return rc;
 }
 
-int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb,
-             float *C, int64_t ldc, struct CUstream_st *stream_) {
-    t_err[0] = 0;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+}  // extern "C"
+
+namespace tcgemm {
+namespace {
+
+// One GEMM call: checks, plan, packs, kernels.  C's element type is epi.out
+// when the epilogue is active, else FP32.
+int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+        int64_t ldc, const EpiParams &epi, cudaStream_t stream) {
     int rc = validate(M, N, K, dtype, A, lda, B, ldb, C, ldc);
     if (rc) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
 
     const int eb = elem_bytes(dtype);
-    const uint64_t c0 = (uint64_t)(uintptr_t)C, c1 = c0 + (uint64_t)((M - 1) * ldc + N) * 4u;
+    const int ob = (epi.active && epi.out != GEMM_OUT_F32) ? 2 : 4;
+    const uint64_t c0 = (uint64_t)(uintptr_t)C, c1 = c0 + (uint64_t)((M - 1) * ldc + N) * ob;
+    if (c0 % ob != 0) return fail(GEMM_ERR_INVALID_ARG, "C is not aligned to its %d-byte element", ob);
     if (K > 0) {
         const uint64_t a0 = (uint64_t)(uintptr_t)A, a1 = a0 + (uint64_t)((M - 1) * lda + K) * eb;
         const uint64_t b0 = (uint64_t)(uintptr_t)B, b1 = b0 + (uint64_t)((K - 1) * ldb + N) * eb;
+        if (a0 % eb != 0 || b0 % eb != 0)
+            return fail(GEMM_ERR_INVALID_ARG, "A or B is not aligned to its %d-byte element", eb);
         if (overlaps(a0, a1, c0, c1) || overlaps(b0, b1, c0, c1))
             return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
+    }
+    const bool has_bias = epi.active && epi.bias;
+    if (has_bias) {
+        const uint64_t s0 = (uint64_t)(uintptr_t)epi.bias, s1 = s0 + (uint64_t)N * 4;
+        if (s0 % 4 != 0) return fail(GEMM_ERR_INVALID_ARG, "bias is not 4-byte aligned");
+        if (overlaps(s0, s1, c0, c1)) return fail(GEMM_ERR_INVALID_ARG, "bias overlaps C");
     }
 
     int dev = 0;
@@ -392,7 +407,12 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
         return fail(GEMM_ERR_UNSUPPORTED, "this library is built for sm_103a only (device is sm_%d%d)", d.cc_major,
                     d.cc_minor);
     if ((rc = check_device_span("C", C, c1 - c0, dev))) return rc;
+    if (has_bias && (rc = check_device_span("bias", epi.bias, (uint64_t)N * 4, dev))) return rc;
     if (K == 0) {
+        if (epi.active) {
+            e = epilogue_fill_launch(C, ldc, M, N, epi, stream);
+            return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "epilogue fill: %s", cudaGetErrorString(e));
+        }
         e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, (size_t)M, stream);
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "cudaMemset2DAsync: %s", cudaGetErrorString(e));
     }
@@ -405,14 +425,16 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     rc = make_plan(M, N, K, dtype, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, d.sms,
                    d.max_clusters, opt, &plan);
     if (rc) return rc;
+    // The fused epilogue is applied on the plain-store path (lane = column,
+    // one coalesced row per store), which also reads the old C there.
+    if (epi.active) plan.pub.tma_store = 0;
     const gemm_plan_t &p = plan.pub;
 
     if (p.path == 0) {
         e = simt_fp32_launch(p, (int)M, (int)N, (int)K, static_cast<const float *>(A), lda,
-                             static_cast<const float *>(B), ldb, C, ldc, stream);
+                             static_cast<const float *>(B), ldb, C, ldc, epi, stream);
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "SIMT kernel launch: %s", cudaGetErrorString(e));
     }
-
     // Tensor-core path: pack operands TMA cannot address, then launch.
     const void *Ause = A, *Buse = B;
     void *ws = nullptr;
@@ -449,12 +471,13 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     }
     char err[256] = {0};
     float *Wp = p.tail_tiles > 0 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
-    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc, Wp,
+    rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc, Wp, epi,
                    (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
     if (rc == GEMM_OK && Wp) {
         const int tile_rows = 128 * p.cta_group;
         e = split_reduce_launch(Wp, p.tail_tiles, p.splits, tile_rows, p.bn, p.tiles - p.tail_tiles,
-                                (int)cdiv(M, tile_rows), (int)cdiv(N, p.bn), p.group_m, C, ldc, M, N, stream);
+                                (int)cdiv(M, tile_rows), (int)cdiv(N, p.bn), p.group_m, C, ldc, M, N, epi,
+                                stream);
         if (e != cudaSuccess) {
             std::snprintf(err, sizeof err, "split reduce: %s", cudaGetErrorString(e));
             rc = GEMM_ERR_CUDA;
@@ -466,6 +489,36 @@ int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t 
     }
     if (rc != GEMM_OK) return fail(rc, "%s", err);
     return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace tcgemm
+
+extern "C" {
+
+int gemm_run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb,
+             float *C, int64_t ldc, struct CUstream_st *stream_) {
+    t_err[0] = 0;
+    return run(M, N, K, dtype, A, lda, B, ldb, C, ldc, EpiParams(), reinterpret_cast<cudaStream_t>(stream_));
+}
+
+int gemm_run_ex(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B, int64_t ldb,
+                void *C, int64_t ldc, const gemm_epilogue_t *epi, struct CUstream_st *stream_) {
+    t_err[0] = 0;
+    EpiParams e;
+    if (epi) {
+        if (epi->activation != GEMM_ACT_NONE && epi->activation != GEMM_ACT_RELU && epi->activation != GEMM_ACT_GELU)
+            return fail(GEMM_ERR_INVALID_ARG, "unknown activation %d", (int)epi->activation);
+        if (epi->out_dtype != GEMM_OUT_F32 && epi->out_dtype != GEMM_OUT_BF16 && epi->out_dtype != GEMM_OUT_F16)
+            return fail(GEMM_ERR_INVALID_ARG, "unknown output type %d", (int)epi->out_dtype);
+        e.alpha = epi->alpha;
+        e.beta = epi->beta;
+        e.bias = epi->bias;
+        e.act = epi->activation;
+        e.out = epi->out_dtype;
+        e.active = !(e.alpha == 1.f && e.beta == 0.f && !e.bias && e.act == GEMM_ACT_NONE && e.out == GEMM_OUT_F32);
+    }
+    return run(M, N, K, dtype, A, lda, B, ldb, C, ldc, e, reinterpret_cast<cudaStream_t>(stream_));
 }
 
 int gemm_get_status(struct CUstream_st *stream_) {

@@ -25,6 +25,18 @@ struct Options {
 };
 Options options_snapshot();
 
+// --------------------------------------------------------------- epilogue ---
+// Fused epilogue of one call (gemm_run_ex).  active == 0: C is FP32 and gets
+// the accumulator as is (gemm_run); the other fields are then ignored.
+struct EpiParams {
+    float alpha = 1.f;
+    float beta = 0.f;
+    const float *bias = nullptr;   // N floats or nullptr
+    int act = GEMM_ACT_NONE;
+    int out = GEMM_OUT_F32;
+    int active = 0;
+};
+
 // ------------------------------------------------------------------- plan ---
 struct Plan {
     gemm_plan_t pub;           // what gemm_plan() reports
@@ -38,10 +50,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype,
               const Options &opt, Plan *out);
 
 // ------------------------------------------------------------------- SIMT ---
-// C = A.B in exact FP32 with the tile the plan chose.
+// C = A.B in exact FP32 with the tile the plan chose, written through `epi`
+// (C's element type is epi.out when epi.active, else FP32).
 cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K,
                              const float *A, int64_t lda, const float *B, int64_t ldb,
-                             float *C, int64_t ldc, cudaStream_t stream);
+                             void *C, int64_t ldc, const EpiParams &epi, cudaStream_t stream);
 
 // Tile of SIMT variant `id` (bm, bn, bk, dynamic shared bytes); 0 if unknown.
 int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem);
@@ -58,10 +71,11 @@ int tc_stages(int dtype, int cta_group, int bn, int b_kmajor);
 // with plan.b_kmajor, B is the transposed copy (N x K, leading dimension ldb).
 // W: the slabs for the split tiles' partial sums (plan.tail_tiles * plan.splits
 // tiles of (128 * cta_group) x bn floats), or nullptr if no tile is split.
-// Returns a gemm_status_t.
+// Whole tiles are written through `epi`; with epi.active the plan must not ask
+// for TMA stores.  Returns a gemm_status_t.
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
               const void *A, int64_t lda, const void *B, int64_t ldb,
-              float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream,
+              void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream,
               char *err, size_t errlen);
 
 // Reads and clears the device status word of the tensor-core kernel.
@@ -81,10 +95,14 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
 
 // For each split tile i (tile index full_tiles + i in the raster order), sums
 // its `splits` slabs W[(s * tail_tiles + i) * tile_rows * tile_cols ...] in
-// split order into C (clipped to M x N).
+// split order into C (clipped to M x N), through `epi`.
 cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int tile_rows, int tile_cols,
-                                int full_tiles, int tiles_m, int tiles_n, int group_m, float *C, int64_t ldc,
-                                int64_t M, int64_t N, cudaStream_t stream);
+                                int full_tiles, int tiles_m, int tiles_n, int group_m, void *C, int64_t ldc,
+                                int64_t M, int64_t N, const EpiParams &epi, cudaStream_t stream);
+
+// C = epilogue of a zero accumulator (the K = 0 product) over M x N.
+cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, const EpiParams &epi,
+                                 cudaStream_t stream);
 
 // dst[c * ld_dst + r] = src[r * ld_src + c] for r < rows, c < cols.
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,

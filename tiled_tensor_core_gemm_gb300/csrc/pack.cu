@@ -10,11 +10,13 @@
 // Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the TF32
 // path, whose tensor-core instruction reads B K-major.
 //
-// Split reduce: sum the partial tiles of split tiles into C.
+// Split reduce: sum the partial tiles of split tiles into C, through the
+// fused epilogue.  Epilogue fill: the epilogue of a zero product (K = 0).
 //
 // Both are HBM-bound: one read and one write of the operand.  The grid is a multiple of
 // the SM count; each warp walks whole rows so both sides stay coalesced even
 // though the source rows start at arbitrary 2- or 4-byte offsets.
+#include "epilogue.cuh"
 #include "internal.h"
 #include "tile_order.cuh"
 
@@ -187,8 +189,8 @@ __global__ void __launch_bounds__(256) transpose64_vec(const uint32_t *__restric
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W, int tail_tiles, int splits,
                                                     int tile_rows, int tile_cols, int full_tiles, int tiles_m,
-                                                    int tiles_n, int group_m, float *__restrict__ C, int64_t ldc,
-                                                    int64_t M, int64_t N) {
+                                                    int tiles_n, int group_m, void *__restrict__ Cv, int64_t ldc,
+                                                    int64_t M, int64_t N, const EpiParams epi) {
     const int64_t quads_per_row = tile_cols / 4;
     const int64_t per_tile = (int64_t)tile_rows * quads_per_row;
     const int64_t total = (int64_t)tail_tiles * per_tile;
@@ -211,7 +213,14 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
             acc.z += v.z;
             acc.w += v.w;
         }
-        float *out = C + m * ldc + n;
+        if (epi.active) {
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n + q < N) epi_write(epi, Cv, m * ldc + n + q, v[q], epi_bias(epi, n + q, N));
+            continue;
+        }
+        float *out = static_cast<float *>(Cv) + m * ldc + n;
         if (VEC && n + 3 < N) {
             *reinterpret_cast<float4 *>(out) = acc;
         } else {
@@ -220,6 +229,15 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
             if (n + 2 < N) out[2] = acc.z;
             if (n + 3 < N) out[3] = acc.w;
         }
+    }
+}
+
+__global__ void __launch_bounds__(256) epilogue_fill(void *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                                     const EpiParams epi) {
+    const int64_t total = M * N;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = x / N, c = x - r * N;
+        epi_write(epi, C, r * ldc + c, 0.f, epi_bias(epi, c, N));
     }
 }
 
@@ -260,8 +278,8 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
 }
 
 cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int tile_rows, int tile_cols,
-                                int full_tiles, int tiles_m, int tiles_n, int group_m, float *C, int64_t ldc,
-                                int64_t M, int64_t N, cudaStream_t stream) {
+                                int full_tiles, int tiles_m, int tiles_n, int group_m, void *C, int64_t ldc,
+                                int64_t M, int64_t N, const EpiParams &epi, cudaStream_t stream) {
     cudaError_t e;
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
@@ -272,10 +290,21 @@ cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int 
     const bool vec = (ldc % 4 == 0) && ((uintptr_t)C % 16 == 0);
     if (vec)
         split_reduce<true><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                                                        tiles_m, tiles_n, group_m, C, ldc, M, N);
+                                                        tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
     else
         split_reduce<false><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                                                         tiles_m, tiles_n, group_m, C, ldc, M, N);
+                                                         tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
+    return cudaGetLastError();
+}
+
+cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, const EpiParams &epi,
+                                 cudaStream_t stream) {
+    cudaError_t e;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (M * N + 255) / 256;
+    const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    epilogue_fill<<<blocks, 256, 0, stream>>>(C, ldc, M, N, epi);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@
 // stores are skipped.
 #include <type_traits>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace tcgemm {
@@ -81,7 +82,7 @@ __device__ __forceinline__ void store_row4(float *__restrict__ p, int64_t row, i
 template <class Cfg, int MIN_BLOCKS, bool VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, MIN_BLOCKS)
 sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
-            const float *__restrict__ B, int64_t ldb, float *__restrict__ C, int64_t ldc) {
+            const float *__restrict__ B, int64_t ldb, void *__restrict__ Cv, int64_t ldc, const EpiParams epi) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, RM = Cfg::RM, RN = Cfg::RN;
     extern __shared__ float4 smem_f4[];
     float *smem = reinterpret_cast<float *>(smem_f4);
@@ -175,6 +176,24 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         if (kt + 1 < ktiles) step(std::integral_constant<int, 1>{}, kt + 1);
     }
 
+    if (epi.active) {
+        // Fused epilogue: element by element, each column's bias read once.
+        float bias[4 * RN];
+#pragma unroll
+        for (int j = 0; j < 4 * RN; ++j) bias[j] = epi_bias(epi, n0 + (j / 4) * (BN / RN) + tx * 4 + (j % 4), N);
+#pragma unroll
+        for (int i = 0; i < 4 * RM; ++i) {
+            const int64_t row = m0 + (i / 4) * (BM / RM) + ty * 4 + (i % 4);
+            if (row >= M) continue;
+#pragma unroll
+            for (int j = 0; j < 4 * RN; ++j) {
+                const int64_t col = n0 + (j / 4) * (BN / RN) + tx * 4 + (j % 4);
+                if (col < N) epi_write(epi, Cv, row * ldc + col, acc[i][j], bias[j]);
+            }
+        }
+        return;
+    }
+    float *C = static_cast<float *>(Cv);
 #pragma unroll
     for (int i = 0; i < 4 * RM; ++i) {
         const int64_t row = m0 + (i / 4) * (BM / RM) + ty * 4 + (i % 4);
@@ -187,7 +206,7 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
 
 template <class Cfg, int MIN_BLOCKS>
 cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, float *C, int64_t ldc, cudaStream_t s) {
+                        int64_t ldb, void *C, int64_t ldc, const EpiParams &epi, cudaStream_t s) {
     const dim3 grid((unsigned)((N + Cfg::BN - 1) / Cfg::BN), (unsigned)((M + Cfg::BM - 1) / Cfg::BM));
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     auto kern = vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true> : sgemm_tiled<Cfg, MIN_BLOCKS, false>;
@@ -195,7 +214,7 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
     }
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(M, N, K, A, lda, B, ldb, C, ldc);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(M, N, K, A, lda, B, ldb, C, ldc, epi);
     return cudaGetLastError();
 }
 
@@ -212,11 +231,12 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
 }  // namespace
 
 cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K, const float *A, int64_t lda,
-                             const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+                             const float *B, int64_t ldb, void *C, int64_t ldc, const EpiParams &epi,
+                             cudaStream_t stream) {
 #define X(id_, bm_, bn_, bk_, rm_, rn_, minb_)                                                        \
     if (plan.bm == bm_ && plan.bn == bn_ && plan.bk == bk_)                                             \
         return launch_tile<SimtCfg<bm_, bn_, bk_, rm_, rn_>, minb_>(plan.vec != 0, M, N, K, A, lda, B, ldb, \
-                                                                    C, ldc, stream);
+                                                                    C, ldc, epi, stream);
     SIMT_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;

@@ -41,6 +41,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tile_order.cuh"
@@ -119,8 +120,9 @@ struct TcParams {
     int group_m;                       // raster group height, in tile rows
     int tma_store;
     int debug_stall;                   // test hook: the MMA thread first waits on a barrier nothing arrives at
-    float *C;
+    void *C;                           // FP32, or epi.out when the epilogue is active
     int64_t ldc;
+    EpiParams epi;                     // fused epilogue (plain-store path only)
     unsigned long long timeout_ns;
 };
 
@@ -404,15 +406,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ptx::bulk_commit_group();
                     }
                 } else {
+                    // Lane = column: each row of the chunk leaves as one coalesced
+                    // store (and the old C, for beta != 0, arrives as one load).
                     __syncwarp();
                     const int col = col0 + (int)lane;
                     const uint32_t cchunk = lane >> 2, cword = lane & 3u;
+                    const float bias = epi_bias(p.epi, col, p.N);
 #pragma unroll 4
                     for (int rr = 0; rr < 32; ++rr) {
                         const int grow = m0 + rr;
                         const float v = *reinterpret_cast<const float *>(
                             buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
-                        if (grow < p.M && col < p.N) p.C[(int64_t)grow * p.ldc + col] = v;
+                        if (grow < p.M && col < p.N) epi_write(p.epi, p.C, (int64_t)grow * p.ldc + col, v, bias);
                     }
                     __syncwarp();
                 }
@@ -476,9 +481,13 @@ CUresult encode_3d_slabs(CUtensorMap *map, const void *base, int64_t cols, int64
 
 template <int DT, int CG, int BN, int BMODE>
 int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                   int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
-                   size_t errlen) {
+                   int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
+                   cudaStream_t stream, char *err, size_t errlen) {
     using Cf = TcCfg<DT, CG, BN, BMODE>;
+    if (epi.active && plan.tma_store) {
+        std::snprintf(err, errlen, "the fused epilogue writes C with plain stores (plan asks for TMA stores)");
+        return GEMM_ERR_INVALID_ARG;
+    }
     constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = DT == kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : DT == kDtFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -527,6 +536,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.debug_stall = options_snapshot().debug_stall_mma;
     p.C = C;
     p.ldc = ldc;
+    p.epi = epi;
     p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
 
     cudaLaunchConfig_t cfg;
@@ -573,10 +583,10 @@ int variant_value(bool stages) {
 
 template <int DT, int CG, int BN, int BMODE>
 int launch_if_ok(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                 int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
-                 size_t errlen) {
+                 int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
+                 cudaStream_t stream, char *err, size_t errlen) {
     if constexpr (variant_ok<DT, CG, BN, BMODE>()) {
-        return launch_variant<DT, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream,
+        return launch_variant<DT, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, epi, timeout_ms, stream,
                                                    err, errlen);
     } else {
         std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, BMODE);
@@ -615,10 +625,10 @@ int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
 int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(dtype, cta_group, bn, b_kmajor, true); }
 
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
-              int64_t ldb, float *C, int64_t ldc, float *W, uint32_t timeout_ms, cudaStream_t stream, char *err,
-              size_t errlen) {
+              int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
+              cudaStream_t stream, char *err, size_t errlen) {
 #define TC_LAUNCH(DT_, MODE_, CG_, BN_) \
-    launch_if_ok<DT_, CG_, BN_, MODE_>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, timeout_ms, stream, err, errlen)
+    launch_if_ok<DT_, CG_, BN_, MODE_>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, epi, timeout_ms, stream, err, errlen)
 #define X(cg, bn_)                                                                                      \
     if (plan.cta_group == cg && plan.bn == bn_) {                                                        \
         if (dtype == GEMM_TF32) {                                                                        \

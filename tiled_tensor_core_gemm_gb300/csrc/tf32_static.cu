@@ -115,7 +115,7 @@ extern "C" int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K, const float
     e = transpose_launch(B, ldb, bt, ldbt, K, N, 4, stream);
     if (e != cudaSuccess) return api_error(GEMM_ERR_CUDA, cudaGetErrorString(e));
     char err[256] = {0};
-    rc = tc_launch(plan.pub, GEMM_TF32, (int)M, (int)N, (int)K, A, lda, bt, ldbt, C, ldc, nullptr,
+    rc = tc_launch(plan.pub, GEMM_TF32, (int)M, (int)N, (int)K, A, lda, bt, ldbt, C, ldc, nullptr, EpiParams(),
                    (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
     if (rc != GEMM_OK) return api_error(rc, err);
     return GEMM_OK;

@@ -15,6 +15,10 @@ Recipe (the workloads are synthetic square and ragged GEMMs, as in the
 * ``ints`` draws integers uniformly from [-lo_hi, lo_hi], for the exactness
   tests (every product and partial sum is then an exact small integer).
 
+For the fused epilogue, ``make_epilogue_inputs`` draws the old C (N(0,1),
+rounded once to the output type) and the bias (N(0,1) FP32) from a generator
+of their own, seeded separately from A and B.
+
 Every array is row-major; ``ld_pad`` adds unused trailing columns so the
 leading dimension exceeds the logical width (the padding is filled with NaN so
 any read of it shows up in the result).
@@ -96,6 +100,19 @@ def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
     elif dtype not in ("fp32", "tf32"):
         raise ValueError(f"unknown dtype {dtype!r}")
     return _pad(a, lda_pad), _pad(b, ldb_pad)
+
+
+OUT_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def make_epilogue_inputs(M: int, N: int, out: str, seed: int, scale: float = 1.0):
+    """(c_old, bias): an M x N old C in the output type and N FP32 bias values,
+    both N(0, scale^2), from their own seeded CPU generator."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed) + 7919)
+    c_old = (torch.randn((M, N), generator=gen, dtype=torch.float32) * scale).to(OUT_TORCH[out])
+    bias = torch.randn((N,), generator=gen, dtype=torch.float32) * scale
+    return c_old, bias
 
 
 def workload_operands(w: Workload):
