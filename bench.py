@@ -45,6 +45,12 @@ WORKLOAD_KEYS = ("bf16_8192", "tf32_4096", "fp32_4096", "fp32_1024", "tf32_1024"
                  "fp16_4096", "fp16_8192")
 
 
+# fused epilogues timed beside the plain GEMM (gemm_run_ex): bias + GELU with a
+# BF16 C, and a residual add (beta = 1, the old BF16 C read back) with a BF16 C
+FUSED_EPILOGUES = {"bias_gelu_bf16out": {"act": "gelu", "out": "bf16", "bias": True},
+                   "residual_bf16out": {"beta": 1.0, "out": "bf16"}}
+
+
 def workload_by_key(key):
     from tiled_tensor_core_gemm_gb300 import inputs as I
     table = {"bf16_8192": I.C4_BF16_8192, "tf32_4096": I.C3_TF32_4096, "fp32_4096": I.C3_FP32_4096,
@@ -63,6 +69,8 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_KEYS), default="bf16_8192",
                     help="timed workload (default: the headline 8192^3 BF16 GEMM)")
+    ap.add_argument("--epilogue", choices=tuple(FUSED_EPILOGUES), default=None,
+                    help="time the workload through gemm_run_ex with this fused epilogue")
     ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -215,7 +223,6 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
         ep = tg.make_epilogue(epi.get("alpha", 1.0), epi.get("beta", 0.0),
                               bias_d.data_ptr() if bias_d is not None else 0, epi.get("act", "none"), epi["out"])
         plan = tg.gemm_plan(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N).as_dict()
-        plan["tma_store"] = 0      # the fused epilogue stores C with plain coalesced stores
 
         def run():
             rc = tg.gemm_run_ex(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, ep, s)
@@ -378,7 +385,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
 
     w = workload_by_key(args.workload)
-    headline = args.workload == "bf16_8192"
+    headline = args.workload == "bf16_8192" and not args.epilogue
     sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -386,7 +393,8 @@ def run_ours(args):
     try:
         res = time_gemm(tg, w, args.steps, args.warmup, stream, device, dist,
                         on_begin=sampler.mark_begin if sampler else None,
-                        on_end=sampler.mark_end if sampler else None)
+                        on_end=sampler.mark_end if sampler else None,
+                        epi=FUSED_EPILOGUES[args.epilogue] if args.epilogue else None)
     finally:
         clocks = sampler.stop() if sampler else None
 
@@ -418,13 +426,14 @@ def run_ours(args):
     else:
         roof = roofline_tensor(res["flops"], res["launch_ms_mean"], peaks["bf16_tflops"],
                                f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
-                               profiled_traffic(args.workload))
+                               profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else "")))
         roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": desc[args.workload],
+        "config": {"workload": desc[args.workload] + (f"; fused epilogue {FUSED_EPILOGUES[args.epilogue]} "
+                                                        "through gemm_run_ex" if args.epilogue else ""),
                    "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of operands vs 129 MB L2); no flush",
                    "plan": res["plan"]},
@@ -442,10 +451,8 @@ def run_ours(args):
         side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
                                                     "bf16_4097x4095x4099", "bf16_16384x1024x4096",
                                                     "bf16_128x8192x8192", "fp16_4096", "fp16_8192")]
-        # the fused epilogue on the headline shape: bias + GELU with a BF16 C, and
-        # a residual add (beta = 1, the old BF16 C read back) with a BF16 C
-        fused = {"bf16_8192_bias_gelu_bf16out": {"act": "gelu", "out": "bf16", "bias": True},
-                 "bf16_8192_residual_bf16out": {"beta": 1.0, "out": "bf16"}}
+        # the fused epilogues on the headline shape
+        fused = {f"bf16_8192_{k}": v for k, v in FUSED_EPILOGUES.items()}
         side += [(k, workload_by_key("bf16_8192")) for k in fused]
         for key, wl in side:
             r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device, epi=fused.get(key))
@@ -469,8 +476,6 @@ def run_ours(args):
                                      f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
                                      NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
             in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype in ("bf16", "fp16") else 4)
-            if key in fused:
-                rl["traffic"] = None     # no capture of the fused-epilogue launch
             paths[key] = {"workload": wl.name + (f", fused epilogue {fused[key]}" if key in fused else ""),
                           "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",

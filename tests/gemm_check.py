@@ -104,15 +104,28 @@ def sample_rows(M: int, tile: int = 128, extra: int = 8, seed: int = 0):
 
 # ----------------------------------------------------------- fused epilogue --
 # Acceptance for C = act(alpha * A.B + beta * C_old + bias) stored as `out`:
-#   |out_ij - y_ij| <= (1 + u) * b_ij + u * |y_ij| + s
-# where y is the oracle's fp64 value, S = |alpha| D + |beta C_old| + |bias| is
-# the scale of the pre-activation sum, b = (1.13 * tol + 1e-6) * S bounds the
-# FP32 result before the cast (the GEMM's own bound on alpha * A.B, a few FP32
-# roundings of the three-term sum and of the activation; 1.13 bounds the slope
-# of GELU, ReLU's is 1), u is the unit roundoff of the output type (2^-24, 2^-8,
-# 2^-11) and s half the smallest subnormal spacing of FP16 (2^-25; 0 otherwise).
-OUT_U = {"f32": 2.0 ** -24, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
-OUT_SUB = {"f32": 0.0, "bf16": 0.0, "f16": 2.0 ** -25}
+# the stored value must lie between the output type's grid points at or
+# beyond y - b and y + b (rounded down and up), where y is the oracle's fp64
+# value and b bounds the error of the FP32 result before the cast:
+#   b = (1.13 * tol + 1e-6) * S,  S = |alpha| D + |beta C_old| + |bias|,
+# i.e. the GEMM's own bound on alpha * A.B, times the largest slope of the
+# activation (GELU's is below 1.13, ReLU's is 1), plus a few FP32 roundings of
+# the three-term sum and of the activation.  Any correctly rounded cast of a
+# value within b of y passes; an off-by-one-ulp cast of a value outside fails.
+OUT_P = {"f32": 24, "bf16": 8, "f16": 11}          # significand bits
+OUT_EMIN = {"f32": -126, "bf16": -126, "f16": -14}  # smallest normal exponent
+
+
+def grid_round(x: np.ndarray, out: str, up: bool) -> np.ndarray:
+    """x rounded down (up=False) or up to the output type's representable grid."""
+    x = np.asarray(x, np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e - 1, OUT_EMIN[out])
+    ulp = np.ldexp(1.0, e - (OUT_P[out] - 1))
+    q = x / ulp
+    return (np.ceil(q) if up else np.floor(q)) * ulp
+
+
 OUT_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
@@ -159,7 +172,8 @@ def oracle_c_old(c_old: torch.Tensor | None, out: str):
 
 def epilogue_check(C: np.ndarray, acc: np.ndarray, D: np.ndarray, dtype: str, out: str, alpha: float, beta: float,
                    c_old, bias, act: str):
-    """Worst (|out - y| / bound) over C; <= 1 passes.  Also returns y."""
+    """Worst |out - y| / (distance from y to the allowed edge on that side);
+    <= 1 passes.  Also returns y."""
     old = oracle_c_old(c_old, out)
     b = bias.numpy() if bias is not None else None
     y = oracle.epilogue(acc, alpha, beta, old, out, b, act)
@@ -168,14 +182,14 @@ def epilogue_check(C: np.ndarray, acc: np.ndarray, D: np.ndarray, dtype: str, ou
         S = S + abs(beta) * np.abs(oracle.epilogue(np.zeros_like(acc), 0.0, 1.0, old, out))
     if b is not None:
         S = S + np.abs(b.astype(np.float64))[None, :]
-    u = OUT_U[out]
-    bound = (1.0 + u) * (1.13 * TOL[dtype] + 1e-6) * S + u * np.abs(y) + OUT_SUB[out]
+    slack = (1.13 * TOL[dtype] + 1e-6) * S
+    lo = grid_round(y - slack, out, up=False)
+    hi = grid_round(y + slack, out, up=True)
     if not np.all(np.isfinite(C)):
         return float("inf"), y
+    room = np.where(C >= y, hi - y, y - lo)
     diff = np.abs(C - y)
-    zero = bound == 0
-    if np.any(diff[zero] != 0):
+    if np.any(diff[room == 0] != 0):
         return float("inf"), y
-    if not np.any(~zero):
-        return 0.0, y
-    return float(np.max(diff[~zero] / bound[~zero])), y
+    live = room > 0
+    return (float(np.max(diff[live] / room[live])) if np.any(live) else 0.0), y

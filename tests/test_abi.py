@@ -117,6 +117,14 @@ def test_plan_ragged_packs_and_plain_epilogue():
     assert not q["pack_a"] and not q["pack_b"] and q["tma_store"]
 
 
+def test_plan_tma_store_needs_whole_16_byte_rows():
+    # A TMA store at a ragged right edge writes the whole 16-byte chunk holding
+    # column N - 1, so a padded ldc with N * 4 not a multiple of 16 stores plainly.
+    assert not _plan(200, 257, 128, tg.GEMM_BF16, ldc=260)["tma_store"]
+    assert not _plan(200, 258, 128, tg.GEMM_BF16, ldc=260)["tma_store"]
+    assert _plan(200, 260, 128, tg.GEMM_BF16, ldc=264)["tma_store"]
+
+
 def test_plan_misaligned_base_packs():
     p = _plan(256, 256, 256, tg.GEMM_BF16, a=2)
     assert p["pack_a"] and not p["pack_b"]

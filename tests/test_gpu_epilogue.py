@@ -94,13 +94,18 @@ def test_small_integers_bit_exact_through_epilogue(dtype, out):
         assert np.array_equal(C, y)
 
 
+@pytest.mark.parametrize("store", ("tma", "plain"))
+@pytest.mark.parametrize("out", ("f32", "bf16", "f16"))
 @pytest.mark.parametrize("cg,bn", [(1, 64), (1, 128), (1, 256), (2, 256)])
 @pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16"))
-def test_epilogue_every_tensor_core_variant(dtype, cg, bn):
+def test_epilogue_every_tensor_core_variant(dtype, cg, bn, out, store):
+    """Every compiled tile with the epilogue in registers ahead of a TMA store
+    (old C loaded by TMA) and on the lane = column plain-store path."""
     tg.gemm_set_option("tc_cta_group", cg)
     tg.gemm_set_option("tc_bn", bn)
+    tg.gemm_set_option("tc_tma_store", 2 if store == "plain" else 0)
     A, B = make_operands(520, 600, 320, dtype, "normal", seed=36)
-    _check(A, B, dtype, "bf16", 1.5, 0.25, "gelu", seed=37)
+    _check(A, B, dtype, out, 1.5, 0.25, "gelu", seed=37)
 
 
 @pytest.mark.parametrize("splits,tail", [(3, 0), (0, 2)])

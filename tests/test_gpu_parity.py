@@ -86,6 +86,19 @@ def test_empty_sum_zero_fills(dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape,pads", [((200, 257, 128), (0, 7, 3)), ((200, 258, 128), (0, 6, 2)),
+                                        ((200, 256, 130), (6, 0, 0)), ((200, 260, 132), (4, 4, 4))],
+                         ids=["raggedN-ldc260", "raggedN-ldc260b", "raggedK-lda136", "ldc264"])
+def test_ragged_edges_with_16_byte_pitches(dtype, shape, pads):
+    """Pitches TMA can address (no pack) around ragged edges: NaN in the lda/ldb
+    padding must not be read, and nothing may be stored into the ldc padding
+    (a TMA store at a ragged right edge would write the whole 16-byte chunk)."""
+    (M, N, K), (pa, pb, pc) = shape, pads
+    A, B = make_operands(M, N, K, dtype, "ints", seed=15, lda_pad=pa, ldb_pad=pb)
+    _exact(A, B, dtype, ldc_pad=pc)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_padded_leading_dimensions_and_guard_bands(dtype):
     # NaN in the lda/ldb padding: any read of it would poison C
     A, B = make_operands(200, 300, 130, dtype, "ints", seed=13, lda_pad=8, ldb_pad=8)

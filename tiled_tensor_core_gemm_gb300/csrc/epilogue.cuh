@@ -27,6 +27,52 @@ __device__ __forceinline__ float epi_bias(const EpiParams &e, int64_t col, int64
     return (e.active && e.bias && col < N) ? __ldg(e.bias + col) : 0.f;
 }
 
+// y = act(alpha * acc + beta * old + bias) in FP32 (old is ignored when beta == 0).
+__device__ __forceinline__ float epi_value(const EpiParams &e, float acc, float old, float bias) {
+    float y = e.alpha * acc;
+    if (e.beta != 0.f) y = fmaf(e.beta, old, y);
+    y += bias;
+    if (e.act == GEMM_ACT_RELU)
+        y = fmaxf(y, 0.f);
+    else if (e.act == GEMM_ACT_GELU)
+        y = 0.5f * y * (1.f + erff(y * 0.70710678118654752f));   // x * Phi(x), Phi through erf
+    return y;
+}
+
+// y rounded once (to nearest even) to the output type and stored at C[idx].
+__device__ __forceinline__ void epi_store(void *C, int64_t idx, int out, float y) {
+    if (out == GEMM_OUT_BF16)
+        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(y);
+    else if (out == GEMM_OUT_F16)
+        static_cast<__half *>(C)[idx] = __float2half_rn(y);
+    else
+        static_cast<float *>(C)[idx] = y;
+}
+
+// Two values rounded to the output type (16-bit outputs) and packed low-first
+// into one 32-bit word, as they sit in memory.
+__device__ __forceinline__ uint32_t epi_pack2(int out, float lo, float hi) {
+    if (out == GEMM_OUT_F16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// The two 16-bit values of a packed word, widened (low half first).
+__device__ __forceinline__ void epi_unpack2(int out, uint32_t w, float &lo, float &hi) {
+    if (out == GEMM_OUT_F16) {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+        lo = __low2float(h);
+        hi = __high2float(h);
+    } else {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+        lo = __low2float(b);
+        hi = __high2float(b);
+    }
+}
+
 // Writes acc (the full sum over K) for C[idx] through the epilogue; bias is
 // epi_bias() of the element's column.
 __device__ __forceinline__ void epi_write(const EpiParams &e, void *C, int64_t idx, float acc, float bias) {
@@ -34,19 +80,8 @@ __device__ __forceinline__ void epi_write(const EpiParams &e, void *C, int64_t i
         static_cast<float *>(C)[idx] = acc;
         return;
     }
-    float y = e.alpha * acc;
-    if (e.beta != 0.f) y = fmaf(e.beta, epi_load_old(C, idx, e.out), y);
-    y += bias;
-    if (e.act == GEMM_ACT_RELU)
-        y = fmaxf(y, 0.f);
-    else if (e.act == GEMM_ACT_GELU)
-        y = 0.5f * y * (1.f + erff(y * 0.70710678118654752f));   // x * Phi(x), Phi through erf
-    if (e.out == GEMM_OUT_BF16)
-        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(y);
-    else if (e.out == GEMM_OUT_F16)
-        static_cast<__half *>(C)[idx] = __float2half_rn(y);
-    else
-        static_cast<float *>(C)[idx] = y;
+    const float old = e.beta != 0.f ? epi_load_old(C, idx, e.out) : 0.f;
+    epi_store(C, idx, e.out, epi_value(e, acc, old, bias));
 }
 
 }  // namespace tcgemm

@@ -171,7 +171,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         p.pack_b = (b_addr % 16 != 0) || ((ldb * elem) % 16 != 0);
         if (p.pack_b) out->ldb_eff = round_up(N, 16 / elem);
     }
-    const bool c_tma_ok = (c_addr % 16 == 0) && ((ldc * 4) % 16 == 0);
+    // TMA stores need a 16-byte aligned base and pitch, and a row length of
+    // whole 16-byte chunks: at a ragged right edge the store writes the whole
+    // 16-byte chunk holding column N - 1 (measured on GB300), which would reach
+    // into the ldc padding.
+    const bool c_tma_ok = (c_addr % 16 == 0) && ((ldc * 4) % 16 == 0) && ((N * 4) % 16 == 0);
     p.tma_store = (opt.tc_tma_store == 2) ? 0 : (c_tma_ok ? 1 : 0);
 
     int cg = opt.tc_cta_group, bn = opt.tc_bn;
@@ -425,9 +429,13 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
     rc = make_plan(M, N, K, dtype, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, d.sms,
                    d.max_clusters, opt, &plan);
     if (rc) return rc;
-    // The fused epilogue is applied on the plain-store path (lane = column,
-    // one coalesced row per store), which also reads the old C there.
-    if (epi.active) plan.pub.tma_store = 0;
+    // With the fused epilogue, C's element may be 2 bytes: the TMA store rules
+    // of make_plan (aligned base, pitch and row length) in that element size.
+    if (epi.active)
+        plan.pub.tma_store = (opt.tc_tma_store != 2 && c0 % 16 == 0 && ((uint64_t)ldc * ob) % 16 == 0 &&
+                              ((uint64_t)N * ob) % 16 == 0)
+                                 ? 1
+                                 : 0;
     const gemm_plan_t &p = plan.pub;
 
     if (p.path == 0) {

@@ -71,8 +71,9 @@ int tc_stages(int dtype, int cta_group, int bn, int b_kmajor);
 // with plan.b_kmajor, B is the transposed copy (N x K, leading dimension ldb).
 // W: the slabs for the split tiles' partial sums (plan.tail_tiles * plan.splits
 // tiles of (128 * cta_group) x bn floats), or nullptr if no tile is split.
-// Whole tiles are written through `epi`; with epi.active the plan must not ask
-// for TMA stores.  Returns a gemm_status_t.
+// Whole tiles are written through `epi` (C's element type is epi.out when the
+// epilogue is active; plan.tma_store then refers to that type).  Returns a
+// gemm_status_t.
 int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
               const void *A, int64_t lda, const void *B, int64_t ldb,
               void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream,

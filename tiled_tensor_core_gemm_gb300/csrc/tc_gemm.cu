@@ -105,6 +105,7 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
+    static_assert((2 * STAGES + 5 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
     static_assert(!(TF32 && BMODE == kBNMajor), "TF32 reads B from the K-major copy");
 };
 
@@ -192,7 +193,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t *stages = smem;
     uint8_t *epi = smem + Cf::STAGES * Cf::STAGE_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi + kEpiBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 5 + 2 * kEpiWarps);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -201,6 +202,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto accf_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + a); };
     auto acce_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 2 + a); };
     const uint32_t never_bar = bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 4);   // never arrived at
+    // old-C loads of the residual epilogue: one barrier per staging buffer
+    auto oldc_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 5 + i); };
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
@@ -216,6 +219,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mbar_init(acce_bar(a), kEpiWarps * CG);
         }
         ptx::mbar_init(never_bar, 1);
+        for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(oldc_bar(i), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -348,13 +352,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
+        // Each warp owns 32 accumulator rows (its Tensor Memory lane quarter)
+        // and stages boxes of 32 rows x 128 bytes -- 32 FP32 columns, or 64
+        // columns of a 16-bit output -- in two buffers, so one box is filled
+        // while the TMA store of the previous one drains.
         const uint32_t ew = warp - 2;        // staging-buffer owner index
         const uint32_t q = warp & 3;         // Tensor Memory lane quarter this warp may read
         uint8_t *bufs = epi + ew * 2 * kEpiBufBytes;
+        const bool fused = p.epi.active != 0;
+        const bool need_old = fused && p.epi.beta != 0.f;
+        const int out = p.epi.out;
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t nchunk = 0;
-        for (int t = unit; t < p.num_units; t += nunits) {
+        uint32_t nchunk = 0;                 // boxes staged so far (buffer nchunk & 1)
+        uint32_t old_phase = 0;              // parity of each buffer's old-C barrier
+        bool ok = true;
+        for (int t = unit; ok && t < p.num_units; t += nunits) {
             int tm, tn, kb0, kb1, slab;
             unit_coords(t, p, tm, tn, kb0, kb1, slab);
             const int m0 = tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
@@ -362,6 +375,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int srow = (int)rank * kBM + 32 * (int)q;                     // same row inside a slab
             const bool to_slab = slab >= 0;
             const bool use_tma = to_slab || p.tma_store;
+            // The epilogue runs in registers (thread = row) when the box leaves
+            // through TMA; partial sums of a split tile go to their slab raw.
+            const bool reg_epi = fused && p.tma_store && !to_slab;
+            const bool pack16 = reg_epi && out != GEMM_OUT_F32;
+            const int box_cols = pack16 ? 64 : 32;
             const bool lane_ok = wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns);
             if (!__all_sync(0xffffffffu, lane_ok)) {
                 if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
@@ -370,54 +388,145 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tc_fence_after();
             const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j, ++nchunk) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(trow + 32u * j, r);
-                ptx::tmem_wait_ld();
-                if (j == BN / 32 - 1) {
-                    // The accumulator is fully in registers/shared: hand it back to the MMA.
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (kPair) ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0));
-                        else ptx::mbar_arrive(acce_bar(acc));
-                    }
-                }
+            for (int jb = 0; jb < BN / box_cols; ++jb, ++nchunk) {
                 uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
-                const int col0 = n0 + 32 * j;
-                // The TMA store that last read this buffer (two chunks ago) must be done.
+                const int col0 = n0 + box_cols * jb;
+                const bool box_live = m0 < p.M && col0 < p.N;
+                // The TMA store that last read this buffer (two boxes ago) must be done.
                 if (nchunk >= 2) {
                     if (lane == 0) ptx::bulk_wait_group_read<1>();
                     __syncwarp();
                 }
-                // Row `lane`, 16-byte chunk c stored at position c ^ (row % 8): the
-                // 128-byte swizzle the TMA store expects, and conflict-free here.
-                float4 *row = reinterpret_cast<float4 *>(buf + lane * 128u);
+                // Residual (beta != 0): the old C box arrives by TMA in this buffer
+                // and each thread rewrites its own row in place.
+                if (reg_epi && need_old && box_live) {
+                    const uint32_t bi = nchunk & 1u;
+                    const uint32_t ob = oldc_bar(2 * (int)ew + (int)bi);
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(ob, (uint32_t)kEpiBufBytes);
+                        ptx::tma_load_2d(ptx::smem_addr(buf), &tmC, ob, col0, m0);
+                    }
+                    const bool got = wait_bar<false>(ob, (old_phase >> bi) & 1u, abort_flag, p.timeout_ns);
+                    old_phase ^= 1u << bi;
+                    if (!__all_sync(0xffffffffu, got)) {
+                        if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                }
+                uint8_t *row_base = buf + lane * 128u;
+#pragma unroll 1
+                for (int h = 0; h < box_cols / 32; ++h) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(box_cols * jb + 32 * h), r);
+                    ptx::tmem_wait_ld();
+                    if (jb == BN / box_cols - 1 && h == box_cols / 32 - 1) {
+                        // The accumulator is fully in registers/shared: hand it back to the MMA.
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (kPair) ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0));
+                            else ptx::mbar_arrive(acce_bar(acc));
+                        }
+                    }
+                    if (reg_epi) {
+                        // Row m0 + lane, columns cb .. cb + 31: lane c holds bias[cb + c].
+                        const int cb = col0 + 32 * h;
+                        const float bias_lane = epi_bias(p.epi, cb + (int)lane, p.N);
+                        // The old C of these 32 columns, read in 16-byte chunks (one
+                        // chunk per lane per quarter-warp phase: conflict-free).
+                        float old[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    row[c ^ (int)(lane & 7u)] = make_float4(__uint_as_float(r[4 * c + 0]), __uint_as_float(r[4 * c + 1]),
-                                                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                        for (int c = 0; c < 32; ++c) old[c] = 0.f;
+                        if (need_old) {
+                            if (pack16) {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                                        row_base + (((uint32_t)(4 * h + k) ^ (lane & 7u)) * 16u));
+                                    epi_unpack2(out, v.x, old[8 * k + 0], old[8 * k + 1]);
+                                    epi_unpack2(out, v.y, old[8 * k + 2], old[8 * k + 3]);
+                                    epi_unpack2(out, v.z, old[8 * k + 4], old[8 * k + 5]);
+                                    epi_unpack2(out, v.w, old[8 * k + 6], old[8 * k + 7]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    const float4 v = *reinterpret_cast<const float4 *>(
+                                        row_base + (((uint32_t)k ^ (lane & 7u)) * 16u));
+                                    old[4 * k + 0] = v.x;
+                                    old[4 * k + 1] = v.y;
+                                    old[4 * k + 2] = v.z;
+                                    old[4 * k + 3] = v.w;
+                                }
+                            }
+                        }
+                        float y[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            y[c] = epi_value(p.epi, __uint_as_float(r[c]), old[c],
+                                             __shfl_sync(0xffffffffu, bias_lane, c));
+                        if (pack16) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                uint4 v;
+                                v.x = epi_pack2(out, y[8 * k + 0], y[8 * k + 1]);
+                                v.y = epi_pack2(out, y[8 * k + 2], y[8 * k + 3]);
+                                v.z = epi_pack2(out, y[8 * k + 4], y[8 * k + 5]);
+                                v.w = epi_pack2(out, y[8 * k + 6], y[8 * k + 7]);
+                                *reinterpret_cast<uint4 *>(row_base + (((uint32_t)(4 * h + k) ^ (lane & 7u)) * 16u)) = v;
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<float4 *>(row_base + (((uint32_t)c ^ (lane & 7u)) * 16u)) =
+                                    make_float4(y[4 * c + 0], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
+                        }
+                    } else {
+                        // Row `lane`, 16-byte chunk c stored at position c ^ (row % 8): the
+                        // 128-byte swizzle the TMA store expects, and conflict-free here.
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<float4 *>(row_base + (((uint32_t)c ^ (lane & 7u)) * 16u)) =
+                                make_float4(__uint_as_float(r[4 * c + 0]), __uint_as_float(r[4 * c + 1]),
+                                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                    }
+                }
                 if (use_tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (to_slab) ptx::tma_store_3d(&tmW, ptx::smem_addr(buf), 32 * j, srow, slab);
-                        else if (m0 < p.M && col0 < p.N) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
+                        if (to_slab) ptx::tma_store_3d(&tmW, ptx::smem_addr(buf), 32 * jb, srow, slab);
+                        else if (box_live) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
                         ptx::bulk_commit_group();
                     }
                 } else {
-                    // Lane = column: each row of the chunk leaves as one coalesced
-                    // store (and the old C, for beta != 0, arrives as one load).
+                    // C not addressable by TMA: lane = column, each row of the box
+                    // leaves as one coalesced store; the old C (beta != 0) is
+                    // loaded eight rows at a time ahead of their stores.
                     __syncwarp();
                     const int col = col0 + (int)lane;
                     const uint32_t cchunk = lane >> 2, cword = lane & 3u;
                     const float bias = epi_bias(p.epi, col, p.N);
-#pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int grow = m0 + rr;
-                        const float v = *reinterpret_cast<const float *>(
-                            buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
-                        if (grow < p.M && col < p.N) epi_write(p.epi, p.C, (int64_t)grow * p.ldc + col, v, bias);
+#pragma unroll 1
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        float old[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            old[i] = (need_old && m0 + r0 + i < p.M && col < p.N)
+                                         ? epi_load_old(p.C, (int64_t)(m0 + r0 + i) * p.ldc + col, out)
+                                         : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = r0 + i, grow = m0 + rr;
+                            const float v = *reinterpret_cast<const float *>(
+                                buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
+                            if (grow < p.M && col < p.N) {
+                                const int64_t idx = (int64_t)grow * p.ldc + col;
+                                if (fused) epi_store(p.C, idx, out, epi_value(p.epi, v, old[i], bias));
+                                else static_cast<float *>(p.C)[idx] = v;
+                            }
+                        }
                     }
                     __syncwarp();
                 }
@@ -484,10 +593,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
                    int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
                    cudaStream_t stream, char *err, size_t errlen) {
     using Cf = TcCfg<DT, CG, BN, BMODE>;
-    if (epi.active && plan.tma_store) {
-        std::snprintf(err, errlen, "the fused epilogue writes C with plain stores (plan asks for TMA stores)");
-        return GEMM_ERR_INVALID_ARG;
-    }
+
     constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = DT == kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : DT == kDtFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -499,8 +605,15 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     if (r == CUDA_SUCCESS)
         r = BKM ? encode_2d(&tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
                 : encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
-    if (r == CUDA_SUCCESS && plan.tma_store)
-        r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+    if (r == CUDA_SUCCESS && plan.tma_store) {
+        // C in boxes of 32 rows x 128 bytes: 32 FP32 columns, or 64 of a 16-bit output.
+        const int out = epi.active ? epi.out : GEMM_OUT_F32;
+        if (out == GEMM_OUT_F32)
+            r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+        else
+            r = encode_2d(&tc, out == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, C, N, M, ldc, 64, 32);
+    }
     if (r == CUDA_SUCCESS && plan.tail_tiles > 0) {
         if (!W) {
             std::snprintf(err, errlen, "split tail without a workspace");
