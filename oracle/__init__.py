@@ -11,7 +11,8 @@ ch. 13) section 13.1 defines the GEMM as C = A @ B with 2*M*N*K flops; section
 13.8 fixes that tensor-core products are exact and sums are FP32.  The oracle
 forms the same exact products and sums them in fp64 (k ascending), so it is at
 least as accurate as any path under test.  BF16 and FP16 inputs are passed as
-their raw 16-bit patterns and widened exactly.
+their raw 16-bit patterns, FP8 (E4M3, E5M2) inputs as bytes; all are widened
+exactly.
 
 ``epilogue`` applies the fused epilogue of section 13.10 (bias, activation,
 residual add, output type) to an fp64 product: y = act(alpha * acc + beta *
@@ -23,7 +24,7 @@ the per-entry scale used by the acceptance test max|C - C_ref| / D.
 Pins (tests/test_oracle.py): identity and permutation products, all-ones inputs
 (C == K everywhere), small-integer inputs against exact integer arithmetic, a
 second independent loop order at tiny sizes, float64 library matmul, and the
-BF16 and FP16 widenings against the library's own conversions; the epilogue
+BF16, FP16 and FP8 widenings against the library's own conversions; the epilogue
 against the library's addmm, ReLU and GELU, printed values of the normal CDF,
 GELU's odd-part identity, and per-column bias broadcasting.
 """
@@ -69,11 +70,11 @@ def _load():
         full = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
         rows = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]
         jik = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
-        for name, args in (("oracle_gemm_f32", full), ("oracle_gemm_bf16", full), ("oracle_gemm_f16", full),
-                           ("oracle_gemm_rows_f32", rows), ("oracle_gemm_rows_bf16", rows),
-                           ("oracle_gemm_rows_f16", rows),
-                           ("oracle_gemm_f32_jik", jik), ("oracle_gemm_bf16_jik", jik), ("oracle_gemm_f16_jik", jik),
-                           ("oracle_widen_bf16", [_ptr, _ptr, _i64]), ("oracle_widen_f16", [_ptr, _ptr, _i64])):
+        kinds = ("f32", "bf16", "f16", "e4m3", "e5m2")
+        table = [(f"oracle_gemm_{k}", full) for k in kinds] + [(f"oracle_gemm_rows_{k}", rows) for k in kinds]
+        table += [(f"oracle_gemm_{k}_jik", jik) for k in kinds]
+        table += [(f"oracle_widen_{k}", [_ptr, _ptr, _i64]) for k in ("bf16", "f16", "e4m3", "e5m2")]
+        for name, args in table:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = None
@@ -91,8 +92,11 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
-def _as_operand(x: np.ndarray, half: bool) -> np.ndarray:
-    want = np.uint16 if half else np.float32
+_STORAGE = {"f32": np.float32, "bf16": np.uint16, "f16": np.uint16, "e4m3": np.uint8, "e5m2": np.uint8}
+
+
+def _as_operand(x: np.ndarray, kind: str) -> np.ndarray:
+    want = _STORAGE[kind]
     if x.dtype != want:
         raise TypeError(f"oracle operand must be {want.__name__}, got {x.dtype}")
     if x.ndim != 2 or (x.size > 0 and x.shape[1] > 1 and x.strides[1] != x.itemsize):
@@ -104,20 +108,26 @@ def _ld(x: np.ndarray) -> int:
     return x.strides[0] // x.itemsize if (x.shape[0] > 1 and x.size > 0) else max(x.shape[1], 1)
 
 
-def _kind(bf16: bool, fp16: bool) -> str:
-    if bf16 and fp16:
-        raise ValueError("bf16 and fp16 are exclusive")
+def _kind(bf16: bool, fp16: bool, fp8=None) -> str:
+    if (bf16, fp16, fp8 is not None).count(True) > 1:
+        raise ValueError("bf16, fp16 and fp8 are exclusive")
+    if fp8 is not None:
+        if fp8 not in ("e4m3", "e5m2"):
+            raise ValueError(f"unknown FP8 format {fp8!r}")
+        return fp8
     return "bf16" if bf16 else "f16" if fp16 else "f32"
 
 
-def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = False, fp16: bool = False):
+def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = False, fp16: bool = False,
+         fp8=None):
     """C = A.B in fp64 (and D = |A|.|B| if with_scale).
 
     A: M x K, B: K x N, row-major, float32, or uint16 patterns of BF16
-    (bf16=True) or IEEE half (fp16=True).
+    (bf16=True) or IEEE half (fp16=True), or uint8 patterns of an FP8 format
+    (fp8="e4m3" or "e5m2").
     """
-    kind = _kind(bf16, fp16)
-    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
+    kind = _kind(bf16, fp16, fp8)
+    _as_operand(A, kind), _as_operand(B, kind)
     M, K = A.shape
     K2, N = B.shape
     if K != K2:
@@ -130,10 +140,11 @@ def gemm(A: np.ndarray, B: np.ndarray, bf16: bool = False, with_scale: bool = Fa
     return (C, D) if with_scale else C
 
 
-def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale: bool = True, fp16: bool = False):
+def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale: bool = True, fp16: bool = False,
+              fp8=None):
     """Rows `rows` of C = A.B and (with_scale) of D = |A|.|B|, each len(rows) x N, fp64."""
-    kind = _kind(bf16, fp16)
-    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
+    kind = _kind(bf16, fp16, fp8)
+    _as_operand(A, kind), _as_operand(B, kind)
     M, K = A.shape
     N = B.shape[1]
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
@@ -147,10 +158,10 @@ def gemm_rows(A: np.ndarray, B: np.ndarray, rows, bf16: bool = False, with_scale
     return C, D
 
 
-def gemm_jik(A: np.ndarray, B: np.ndarray, bf16: bool = False, fp16: bool = False) -> np.ndarray:
+def gemm_jik(A: np.ndarray, B: np.ndarray, bf16: bool = False, fp16: bool = False, fp8=None) -> np.ndarray:
     """The same product with the j-i-k loop order (tiny sizes only)."""
-    kind = _kind(bf16, fp16)
-    _as_operand(A, kind != "f32"), _as_operand(B, kind != "f32")
+    kind = _kind(bf16, fp16, fp8)
+    _as_operand(A, kind), _as_operand(B, kind)
     M, K = A.shape
     N = B.shape[1]
     C = np.empty((M, N), np.float64)
@@ -172,6 +183,14 @@ def widen_f16(bits: np.ndarray) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(b.shape, np.float64)
     _load().oracle_widen_f16(b.ctypes.data, out.ctypes.data, b.size)
+    return out
+
+
+def widen_fp8(bits: np.ndarray, fmt: str) -> np.ndarray:
+    """Exact value of each FP8 byte (fmt "e4m3" or "e5m2"), as fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(b.shape, np.float64)
+    getattr(_load(), f"oracle_widen_{_kind(False, False, fmt)}")(b.ctypes.data, out.ctypes.data, b.size)
     return out
 
 

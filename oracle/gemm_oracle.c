@@ -19,7 +19,12 @@
  * BF16 and FP16 operands arrive as their raw 16-bit patterns and are widened
  * exactly (a BF16 value is the top half of the FP32 with the same sign,
  * exponent and first 7 mantissa bits; an IEEE half is sign, 5-bit exponent
- * with bias 15, 10-bit mantissa, with subnormals at exponent 0).
+ * with bias 15, 10-bit mantissa, with subnormals at exponent 0).  FP8
+ * operands (the OCP 8-bit formats) arrive as bytes: E4M3 is sign, 4-bit
+ * exponent with bias 7, 3-bit mantissa, no infinities, S.1111.111 the only
+ * NaN (largest finite 448); E5M2 is sign, 5-bit exponent with bias 15, 2-bit
+ * mantissa, IEEE-style infinities and NaNs; both have subnormals at exponent
+ * 0.  Every product of two such values is exact in double as well.
  *
  * Besides C, every entry point can also return D[i][j] = sum_k |A[i][k]|*|B[k][j]|,
  * the scale against which an error in C[i][j] is judged (max |dC| / D).
@@ -70,6 +75,41 @@ static double widen_f16(uint16_t bits)
     return sign ? -v : v;
 }
 
+static double widen_e4m3(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                  /* subnormal: (m/8) * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+static double widen_e5m2(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 2) & 31, m = bits & 3;
+    double v;
+    if (e == 31)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -16);                 /* subnormal: (m/4) * 2^-14 */
+    else
+        v = ldexp((double)(4 + m), e - 17);        /* (1 + m/4) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* The 256 values of an 8-bit format. */
+enum { FMT8_E4M3 = 0, FMT8_E5M2 = 1 };
+
+static void fill_table8(int fmt, double *tab)
+{
+    for (int b = 0; b < 256; ++b)
+        tab[b] = fmt == FMT8_E5M2 ? widen_e5m2((uint8_t)b) : widen_e4m3((uint8_t)b);
+}
+
 /* 16-bit operand formats */
 enum { FMT_BF16 = 0, FMT_F16 = 1 };
 
@@ -114,6 +154,23 @@ static void row_h16(int fmt, int64_t i, int64_t N, int64_t K, const uint16_t *A,
             for (int64_t j = 0; j < N; ++j) bw[j] = widen_f16(b[j]);
         else
             for (int64_t j = 0; j < N; ++j) bw[j] = widen_bf16(b[j]);
+        for (int64_t j = 0; j < N; ++j) c[j] += a * bw[j];
+        if (d) {
+            const double aa = fabs(a);
+            for (int64_t j = 0; j < N; ++j) d[j] += aa * fabs(bw[j]);
+        }
+    }
+}
+
+static void row_u8(const double *tab, int64_t i, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                   const uint8_t *B, int64_t ldb, double *c, double *d, double *bw)
+{
+    for (int64_t j = 0; j < N; ++j) c[j] = 0.0;
+    if (d) for (int64_t j = 0; j < N; ++j) d[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = tab[A[i * lda + k]];
+        const uint8_t *b = B + k * ldb;
+        for (int64_t j = 0; j < N; ++j) bw[j] = tab[b[j]];
         for (int64_t j = 0; j < N; ++j) c[j] += a * bw[j];
         if (d) {
             const double aa = fabs(a);
@@ -201,6 +258,62 @@ void oracle_gemm_rows_f16(int64_t M, int64_t N, int64_t K,
     rows_h16(FMT_F16, N, K, A, lda, B, ldb, rows, nrows, C, D);
 }
 
+static void gemm_u8(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                    int64_t ldb, double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    double tab[256];
+    fill_table8(fmt, tab);
+    #pragma omp parallel
+    {
+        double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i)
+            row_u8(tab, i, N, K, A, lda, B, ldb, C + i * ldc, D ? D + i * ldd : NULL, bw);
+        free(bw);
+    }
+}
+
+void oracle_gemm_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                      double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    gemm_u8(FMT8_E4M3, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+}
+
+void oracle_gemm_e5m2(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                      double *C, int64_t ldc, double *D, int64_t ldd)
+{
+    gemm_u8(FMT8_E5M2, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+}
+
+static void rows_u8(int fmt, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                    const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    double tab[256];
+    fill_table8(fmt, tab);
+    #pragma omp parallel
+    {
+        double *bw = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r)
+            row_u8(tab, rows[r], N, K, A, lda, B, ldb, C + r * N, D ? D + r * N : NULL, bw);
+        free(bw);
+    }
+}
+
+void oracle_gemm_rows_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                           int64_t ldb, const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    rows_u8(FMT8_E4M3, N, K, A, lda, B, ldb, rows, nrows, C, D);
+}
+
+void oracle_gemm_rows_e5m2(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                           int64_t ldb, const int64_t *rows, int64_t nrows, double *C, double *D)
+{
+    (void)M;
+    rows_u8(FMT8_E5M2, N, K, A, lda, B, ldb, rows, nrows, C, D);
+}
+
 /* Second loop order (j outer, then i, then k), single-threaded, for brute-force
  * self-checks of the routine above on tiny sizes. */
 void oracle_gemm_f32_jik(int64_t M, int64_t N, int64_t K,
@@ -242,6 +355,32 @@ void oracle_gemm_f16_jik(int64_t M, int64_t N, int64_t K,
     jik_h16(FMT_F16, M, N, K, A, lda, B, ldb, C, ldc);
 }
 
+static void jik_u8(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                   int64_t ldb, double *C, int64_t ldc)
+{
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t i = 0; i < M; ++i) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint8_t a = A[i * lda + k], b = B[k * ldb + j];
+                s += fmt == FMT8_E5M2 ? widen_e5m2(a) * widen_e5m2(b) : widen_e4m3(a) * widen_e4m3(b);
+            }
+            C[i * ldc + j] = s;
+        }
+}
+
+void oracle_gemm_e4m3_jik(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                          int64_t ldb, double *C, int64_t ldc)
+{
+    jik_u8(FMT8_E4M3, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
+void oracle_gemm_e5m2_jik(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                          int64_t ldb, double *C, int64_t ldc)
+{
+    jik_u8(FMT8_E5M2, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
 /* Exact widening of n BF16 / FP16 patterns, exposed so the tests can pin it. */
 void oracle_widen_bf16(const uint16_t *src, double *dst, int64_t n)
 {
@@ -251,6 +390,17 @@ void oracle_widen_bf16(const uint16_t *src, double *dst, int64_t n)
 void oracle_widen_f16(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) dst[i] = widen_f16(src[i]);
+}
+
+/* ... and of n FP8 bytes (the j-i-k routines call these directly, not the table). */
+void oracle_widen_e4m3(const uint8_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = widen_e4m3(src[i]);
+}
+
+void oracle_widen_e5m2(const uint8_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = widen_e5m2(src[i]);
 }
 
 /* ------------------------------------------------------------ epilogue --- */

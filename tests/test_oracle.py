@@ -250,3 +250,60 @@ def test_epilogue_reads_old_c_in_the_output_type(out):
 def test_epilogue_beta_zero_never_reads_old_c():
     acc = np.ones((3, 4))
     assert np.array_equal(oracle.epilogue(acc, alpha=3.0, beta=0.0, c_old=None), 3.0 * acc)
+
+
+# -------------------------------------------------------------------- FP8 --
+# Pins for the FP8 (OCP E4M3 and E5M2) widening and products: every byte
+# against the library's own FP8 types, printed format constants, exact
+# integer products, and the second loop order.
+FP8_LIB = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+def _fp8_bytes(x_float, fmt):
+    t = torch.as_tensor(np.asarray(x_float, dtype=np.float32)).to(FP8_LIB[fmt])
+    return as_oracle_array(t).copy()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_widening_matches_library_conversion(fmt):
+    bits = np.arange(256, dtype=np.uint8)
+    ours = oracle.widen_fp8(bits, fmt)
+    lib = torch.from_numpy(bits).view(FP8_LIB[fmt]).to(torch.float64).numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], lib[~nan])
+
+
+def test_fp8_format_constants():
+    # E4M3: 1.0, the largest finite value 448, the smallest subnormal 2^-9, the only NaN pattern
+    e4 = oracle.widen_fp8(np.array([0x38, 0x7E, 0x01, 0xB8, 0x7F], np.uint8), "e4m3")
+    assert list(e4[:4]) == [1.0, 448.0, 2.0 ** -9, -1.0] and np.isnan(e4[4])
+    # E5M2: 1.0, the largest finite value 57344, the smallest subnormal 2^-16, +inf
+    e5 = oracle.widen_fp8(np.array([0x3C, 0x7B, 0x01, 0x7C], np.uint8), "e5m2")
+    assert list(e5) == [1.0, 57344.0, 2.0 ** -16, float("inf")]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_small_integers_exact_fp8(fmt):
+    # integers up to 8 are exact in both formats
+    rng = np.random.default_rng(10)
+    M, N, K = 27, 41, 333
+    Ai = rng.integers(-8, 9, (M, K))
+    Bi = rng.integers(-8, 9, (K, N))
+    C, D = oracle.gemm(_fp8_bytes(Ai, fmt), _fp8_bytes(Bi, fmt), fp8=fmt, with_scale=True)
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(D, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (17, 16, 15)])
+def test_fp8_second_loop_order_library_and_rows(fmt, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = _fp8_bytes(rng.standard_normal((M, K)), fmt)
+    B = _fp8_bytes(rng.standard_normal((K, N)), fmt)
+    C = oracle.gemm(A, B, fp8=fmt)
+    assert np.array_equal(C, oracle.gemm_jik(A, B, fp8=fmt))
+    lib = (torch.from_numpy(A).view(FP8_LIB[fmt]).double() @ torch.from_numpy(B).view(FP8_LIB[fmt]).double()).numpy()
+    assert np.allclose(C, lib, rtol=1e-13, atol=1e-13)
+    r, _ = oracle.gemm_rows(A, B, [M - 1, 0], fp8=fmt)
+    assert np.array_equal(r, C[[M - 1, 0]])

@@ -9,9 +9,9 @@ Recipe (the workloads are synthetic square and ragged GEMMs, as in the
 * one CPU ``torch.Generator`` seeded with the workload's seed; A (M x K) is
   drawn first, then B (K x N), from the same generator;
 * ``uniform`` is U[-1, 1) = 2*rand - 1, ``normal`` is N(0, 1) via randn;
-* for BF16 (FP16) operands the FP32 draw is rounded once to BF16 (FP16) by
-  round to nearest even, the library's own ``.to(...)``; those values are the
-  ground truth for every check;
+* for BF16 (FP16, FP8 E4M3 / E5M2) operands the FP32 draw is rounded once to
+  that format by round to nearest even, the library's own ``.to(...)``; those
+  values are the ground truth for every check;
 * ``ints`` draws integers uniformly from [-lo_hi, lo_hi], for the exactness
   tests (every product and partial sum is then an exact small integer).
 
@@ -71,6 +71,10 @@ def _draw(gen: torch.Generator, shape, dist: str, lo_hi: int = 8) -> torch.Tenso
     raise ValueError(f"unknown distribution {dist!r}")
 
 
+# The OCP FP8 formats, as the library's own types (E4M3 without infinities).
+FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
 def _pad(x: torch.Tensor, ld_pad: int) -> torch.Tensor:
     if ld_pad == 0:
         return x
@@ -82,7 +86,8 @@ def _pad(x: torch.Tensor, ld_pad: int) -> torch.Tensor:
 
 def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
                   lda_pad: int = 0, ldb_pad: int = 0, lo_hi: int = 8):
-    """(A, B) as CPU torch tensors: float32 for fp32/tf32, bfloat16 for bf16, float16 for fp16.
+    """(A, B) as CPU torch tensors: float32 for fp32/tf32, bfloat16 for bf16, float16 for
+    fp16, float8 for e4m3 / e5m2.
 
     The tensors may be views with a leading dimension larger than their width
     (``*_pad``); use ``.stride(0)`` for the leading dimension.
@@ -97,6 +102,9 @@ def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int,
     elif dtype == "fp16":
         a = a.to(torch.float16)
         b = b.to(torch.float16)
+    elif dtype in FP8_TORCH:
+        a = a.to(FP8_TORCH[dtype])
+        b = b.to(FP8_TORCH[dtype])
     elif dtype not in ("fp32", "tf32"):
         raise ValueError(f"unknown dtype {dtype!r}")
     return _pad(a, lda_pad), _pad(b, ldb_pad)
@@ -120,10 +128,13 @@ def workload_operands(w: Workload):
 
 
 def as_oracle_array(t: torch.Tensor) -> np.ndarray:
-    """A CPU tensor as the numpy array the oracle takes (float32, or uint16 BF16/FP16 bits)."""
+    """A CPU tensor as the numpy array the oracle takes (float32, uint16 BF16/FP16
+    bits, or uint8 FP8 bytes)."""
     t = t.detach().cpu()
     if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype in FP8_TORCH.values():
+        return t.view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(f"unsupported operand dtype {t.dtype}")
