@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GEMM TFLOP/s at 4096³/8192³ (FP32, TF32, BF16) and % of GB300 dense peak"
 UNIT = "TFLOP/s"
 L2_BYTES = 129e6
-NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0}   # GB300 per-GPU dense, nominal
+NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0, "fp8": 4500.0}   # GB300 per-GPU dense, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 SMS = 152
@@ -42,7 +42,7 @@ FP32_LANES_PER_SM = 128
 # bench keys of the published workloads (tiled_tensor_core_gemm_gb300/inputs.py)
 WORKLOAD_KEYS = ("bf16_8192", "tf32_4096", "fp32_4096", "fp32_1024", "tf32_1024", "fp32_256",
                  "bf16_1000", "bf16_4097x4095x4099", "bf16_16384x1024x4096", "bf16_128x8192x8192",
-                 "fp16_4096", "fp16_8192")
+                 "fp16_4096", "fp16_8192", "e4m3_4096", "e4m3_8192", "e5m2_8192")
 
 
 # fused epilogues timed beside the plain GEMM (gemm_run_ex): bias + GELU with a
@@ -57,7 +57,8 @@ def workload_by_key(key):
              "fp32_1024": I.C2_FP32_1024, "tf32_1024": I.C2_TF32_1024, "fp32_256": I.C1_FP32_256,
              "bf16_1000": I.C5_BF16_RAGGED[0], "bf16_4097x4095x4099": I.C5_BF16_RAGGED[1],
              "bf16_16384x1024x4096": I.C5_BF16_RAGGED[2], "bf16_128x8192x8192": I.C5_BF16_RAGGED[3],
-             "fp16_4096": I.FP16_4096, "fp16_8192": I.FP16_8192}
+             "fp16_4096": I.FP16_4096, "fp16_8192": I.FP16_8192, "e4m3_4096": I.E4M3_4096,
+             "e4m3_8192": I.E4M3_8192, "e5m2_8192": I.E5M2_8192}
     return table[key]
 
 
@@ -311,16 +312,17 @@ def cpu_baseline(workload, target_s):
     A, B = workload_operands(workload)
     a, b = as_oracle_array(A), as_oracle_array(B)
     bf16, fp16 = workload.dtype == "bf16", workload.dtype == "fp16"
+    fp8 = workload.dtype if workload.dtype in ("e4m3", "e5m2") else None
     threads = oracle.num_threads()
     rows = list(range(threads))
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, with_scale=False)
+    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, fp8=fp8, with_scale=False)
     t_probe = time.perf_counter() - t0
     n = max(threads, int(threads * max(1.0, (target_s - t_probe) / max(t_probe, 1e-3))))
     n = min(n, workload.M)
     rows = list(range(n))
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, with_scale=False)
+    oracle.gemm_rows(a, b, rows, bf16=bf16, fp16=fp16, fp8=fp8, with_scale=False)
     dt = time.perf_counter() - t0
     flops = 2.0 * n * workload.N * workload.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -349,6 +351,18 @@ def roofline_tensor(flops, launch_ms, peak, peak_src, nominal, traffic):
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": UNIT,
             "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
             "frac_of_nominal_dense": round(achieved / nominal, 4), "nominal_dense_peak": nominal}
+
+
+ELEM_BYTES = {"fp32": 4, "tf32": 4, "bf16": 2, "fp16": 2, "e4m3": 1, "e5m2": 1}
+
+
+def roofline_for_dtype(dtype, flops, launch_ms, peaks, peak_src, traffic):
+    """Tensor roofline against the measured BF16 burst peak, scaled by the
+    nominal dense ratio for TF32 (1100/2250) and FP8 (4500/2250)."""
+    fam = {"tf32": "tf32", "e4m3": "fp8", "e5m2": "fp8"}.get(dtype, "bf16")
+    ratio = NOMINAL_DENSE_TFLOPS[fam] / NOMINAL_DENSE_TFLOPS["bf16"]
+    src = f"bf16_tflops burst, {peak_src}" if fam == "bf16" else f"bf16 burst x nominal {fam}/bf16 ratio, {peak_src}"
+    return roofline_tensor(flops, launch_ms, peaks["bf16_tflops"] * ratio, src, NOMINAL_DENSE_TFLOPS[fam], traffic)
 
 
 def roofline_alu(flops, launch_ms, sm_mhz):
@@ -408,7 +422,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    in_bytes = (w.M * w.K + w.K * w.N) * (2 if w.dtype in ("bf16", "fp16") else 4)
+    in_bytes = (w.M * w.K + w.K * w.N) * ELEM_BYTES[w.dtype]
     desc = {"bf16_8192": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), fp32 accumulate "
                          "and output, row-major, persistent tcgen05 path",
             "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
@@ -418,16 +432,11 @@ def run_ours(args):
     if w.dtype == "fp32":
         sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
         roof = roofline_alu(res["flops"], res["launch_ms_mean"], sm_mhz)
-    elif w.dtype == "tf32":
-        roof = roofline_tensor(res["flops"], res["launch_ms_mean"],
-                               peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"],
-                               f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}", NOMINAL_DENSE_TFLOPS["tf32"],
-                               profiled_traffic(args.workload))
     else:
-        roof = roofline_tensor(res["flops"], res["launch_ms_mean"], peaks["bf16_tflops"],
-                               f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
-                               profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else "")))
-        roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
+        roof = roofline_for_dtype(w.dtype, res["flops"], res["launch_ms_mean"], peaks, peak_src,
+                                  profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else "")))
+        if w.dtype in ("bf16", "fp16"):
+            roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -450,7 +459,8 @@ def run_ours(args):
         side = [("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)]
         side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
                                                     "bf16_4097x4095x4099", "bf16_16384x1024x4096",
-                                                    "bf16_128x8192x8192", "fp16_4096", "fp16_8192")]
+                                                    "bf16_128x8192x8192", "fp16_4096", "fp16_8192",
+                                                    "e4m3_4096", "e4m3_8192", "e5m2_8192")]
         # the fused epilogues on the headline shape
         fused = {f"bf16_8192_{k}": v for k, v in FUSED_EPILOGUES.items()}
         side += [(k, workload_by_key("bf16_8192")) for k in fused]
@@ -459,10 +469,9 @@ def run_ours(args):
             tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
             if wl.dtype == "fp32":
                 rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
-            elif wl.dtype in ("bf16", "fp16"):
-                rl = roofline_tensor(r["flops"], r["launch_ms_mean"], peaks["bf16_tflops"],
-                                     f"bf16_tflops burst, {peak_src}", NOMINAL_DENSE_TFLOPS["bf16"],
-                                     profiled_traffic(key))
+            else:
+                rl = roofline_for_dtype(wl.dtype, r["flops"], r["launch_ms_mean"], peaks, peak_src,
+                                        profiled_traffic(key))
                 # the low-tile-count shape streams B once: bandwidth is its binding roofline
                 if key == "bf16_128x8192x8192":
                     in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 4
@@ -470,12 +479,7 @@ def run_ours(args):
                     rl = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(key),
                           "peak_source": f"hbm_gbs, {peak_src}", "tensor_tflops": rl["achieved"]}
-            else:
-                tf32_peak = peaks["bf16_tflops"] * NOMINAL_DENSE_TFLOPS["tf32"] / NOMINAL_DENSE_TFLOPS["bf16"]
-                rl = roofline_tensor(r["flops"], r["launch_ms_mean"], tf32_peak,
-                                     f"bf16 burst x nominal tf32/bf16 ratio, {peak_src}",
-                                     NOMINAL_DENSE_TFLOPS["tf32"], profiled_traffic(key))
-            in_b = (wl.M * wl.K + wl.K * wl.N) * (2 if wl.dtype in ("bf16", "fp16") else 4)
+            in_b = (wl.M * wl.K + wl.K * wl.N) * ELEM_BYTES[wl.dtype]
             paths[key] = {"workload": wl.name + (f", fused epilogue {fused[key]}" if key in fused else ""),
                           "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",

@@ -54,8 +54,12 @@ typedef enum {
                       and accumulate in FP32 in Tensor Memory                      */
     GEMM_BF16 = 2, /* A, B bfloat16 (raw uint16 storage); exact products,
                       FP32 accumulation in Tensor Memory                           */
-    GEMM_FP16 = 3  /* A, B IEEE half (raw uint16 storage); exact products,
+    GEMM_FP16 = 3, /* A, B IEEE half (raw uint16 storage); exact products,
                       FP32 accumulation in Tensor Memory                           */
+    GEMM_E4M3 = 4, /* A, B OCP FP8 E4M3 bytes (bias 7, no infinities); exact
+                      products, FP32 accumulation in Tensor Memory                 */
+    GEMM_E5M2 = 5  /* A, B OCP FP8 E5M2 bytes (bias 15); exact products, FP32
+                      accumulation in Tensor Memory                                */
 } gemm_dtype_t;
 
 typedef enum {
@@ -68,36 +72,41 @@ typedef enum {
 } gemm_status_t;
 
 /*
- * gemm_run -- C = A . B  (C is overwritten; there is no alpha/beta).
+ * gemm_run -- C = A . B  (C is overwritten; gemm_run_ex adds alpha, beta, a
+ * bias, an activation and a 16-bit output).
  *
  *   M, N, K     sizes, each >= 0.  M == 0 or N == 0: no-op.  K == 0: C is
  *               filled with zeros (the empty sum).
  *   dtype       gemm_dtype_t.  A and B are 'const float *' for GEMM_FP32 and
  *               GEMM_TF32, 'const uint16_t *' holding bfloat16 bits for
- *               GEMM_BF16 and IEEE half bits for GEMM_FP16.
+ *               GEMM_BF16 and IEEE half bits for GEMM_FP16, 'const uint8_t *'
+ *               holding FP8 bytes for GEMM_E4M3 and GEMM_E5M2 ("Learn
+ *               CuTeDSL" section 4: the tcgen05 MMA reads 8-bit inputs with
+ *               twice the K per instruction of 16-bit ones).
  *   A, lda      device pointer to A[0][0], leading dimension in elements.
  *   B, ldb      device pointer to B[0][0], leading dimension in elements.
  *   C, ldc      device pointer to C[0][0] (float), leading dimension in elements.
  *   stream      the CUDA stream to enqueue on.
  *
- * Paths: GEMM_FP32 runs the tiled SIMT kernel; GEMM_TF32, GEMM_BF16 and
- * GEMM_FP16 run the persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine cannot
- * address (base not 16-byte aligned, or a row pitch that is not a multiple of
- * 16 bytes) are first copied into a stream-ordered workspace with a padded
- * pitch; that workspace is allocated and freed on the stream
+ * Paths: GEMM_FP32 runs the tiled SIMT kernel; every other dtype runs the
+ * persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine
+ * cannot address (base not 16-byte aligned, or a row pitch that is not a
+ * multiple of 16 bytes) are first copied into a stream-ordered workspace with
+ * a padded pitch; that workspace is allocated and freed on the stream
  * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
- * unavailable.  For GEMM_TF32, B is first transposed into the same kind of
- * workspace, because the TF32 tensor-core instruction reads its B operand
- * K-major.  When there are too few output tiles to occupy every SM and K is
- * long, the tensor-core path splits K: partial tiles go to a workspace and a
- * second kernel sums them into C in a fixed order (results are deterministic).
- * On request ("tc_tail_splits") the tiles of the last, partly idle round of
- * the persistent schedule are split in K the same way.  C with such a layout is written by ordinary stores instead of
- * TMA stores.
+ * unavailable.  For GEMM_TF32 (and FP8 tiles narrower than 128 columns), B is
+ * first transposed into the same kind of workspace, because the MMA then
+ * reads its B operand K-major.  When there are too few output tiles to occupy
+ * every SM and K is long, the tensor-core path splits K: partial tiles go to
+ * a workspace and a second kernel sums them into C in a fixed order (results
+ * are deterministic).  On request ("tc_tail_splits") the tiles of the last,
+ * partly idle round of the persistent schedule are split in K the same way.
+ * C leaves through TMA stores when its base, pitch and row length (N
+ * elements) are all multiples of 16 bytes, else through ordinary stores.
  *
  * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
- * a NULL pointer with a non-empty extent, an unknown dtype, or C overlapping
- * A or B in memory.  A kernel whose bounded wait expires records
+ * a NULL pointer with a non-empty extent, an unknown dtype, a pointer not
+ * aligned to its element, or C overlapping A or B in memory.  A kernel whose bounded wait expires records
  * GEMM_ERR_TIMEOUT in a device status word that gemm_get_status() reads.
  */
 GEMM_API int gemm_run(int64_t M, int64_t N, int64_t K, int dtype,

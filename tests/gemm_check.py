@@ -3,9 +3,9 @@ seeded inputs and compare with the oracle.
 
 Acceptance metric: r = max_ij |C_ij - Cref_ij| / D_ij with D = |A|.|B| (fp64);
 D_ij == 0 requires C_ij == Cref_ij exactly; any NaN/Inf fails.  Bounds: 1e-5
-for FP32 and for BF16 or FP16 inputs with FP32 accumulation (the oracle uses
-the rounded 16-bit inputs, so only the accumulation error counts), 2e-3 for
-TF32.
+for FP32 and for BF16, FP16 or FP8 inputs with FP32 accumulation (the oracle
+uses the rounded narrow inputs, whose products are exact in FP32, so only the
+accumulation error counts), 2e-3 for TF32.
 Derivation of the TF32 bound: the tensor cores read each FP32 operand with a
 10-bit mantissa; whether they round or truncate, each operand's relative
 error is below 2^-10, so each product's is below (1 + 2^-10)^2 - 1 < 1.96e-3,
@@ -21,7 +21,8 @@ import oracle
 import tiled_tensor_core_gemm_gb300 as tg
 from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array
 
-TOL = {"fp32": 1e-5, "bf16": 1e-5, "fp16": 1e-5, "tf32": 2e-3}
+TOL = {"fp32": 1e-5, "bf16": 1e-5, "fp16": 1e-5, "tf32": 2e-3, "e4m3": 1e-5, "e5m2": 1e-5}
+FP8 = ("e4m3", "e5m2")
 GUARD = 256   # NaN-filled floats before and after C
 
 
@@ -82,12 +83,12 @@ def error_ratio(C: np.ndarray, Cref: np.ndarray, D: np.ndarray) -> float:
 
 def oracle_full(A: torch.Tensor, B: torch.Tensor, dtype: str):
     return oracle.gemm(as_oracle_array(A), as_oracle_array(B), bf16=(dtype == "bf16"), fp16=(dtype == "fp16"),
-                       with_scale=True)
+                       fp8=dtype if dtype in FP8 else None, with_scale=True)
 
 
 def oracle_rows(A: torch.Tensor, B: torch.Tensor, dtype: str, rows):
     return oracle.gemm_rows(as_oracle_array(A), as_oracle_array(B), rows, bf16=(dtype == "bf16"),
-                            fp16=(dtype == "fp16"))
+                            fp16=(dtype == "fp16"), fp8=dtype if dtype in FP8 else None)
 
 
 def sample_rows(M: int, tile: int = 128, extra: int = 8, seed: int = 0):

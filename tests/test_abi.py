@@ -125,6 +125,27 @@ def test_plan_tma_store_needs_whole_16_byte_rows():
     assert _plan(200, 260, 128, tg.GEMM_BF16, ldc=264)["tma_store"]
 
 
+def test_plan_fp8():
+    p = _plan(8192, 8192, 8192, tg.GEMM_E4M3)
+    assert p["path"] == 1 and p["cta_group"] == 2 and p["bn"] == 256 and p["bk"] == 128
+    assert not p["b_kmajor"] and not p["pack_a"] and not p["pack_b"]     # B read as stored
+    # a narrow tile (64 columns per CTA) reads B from the K-major copy instead
+    q = _plan(128, 8192, 256, tg.GEMM_E5M2)
+    assert q["bn"] == 64 and q["b_kmajor"] == 1
+    # 8-bit rows need a pitch that is a multiple of 16 elements for TMA (B here
+    # goes through the K-major copy, whose pitch is rounded up anyway)
+    r = _plan(1000, 1000, 1000, tg.GEMM_E4M3)
+    assert r["pack_a"] and r["b_kmajor"] and not r["pack_b"]
+    s = _plan(2000, 3000, 1000, tg.GEMM_E4M3)
+    assert s["bn"] == 256 and s["pack_a"] and s["pack_b"] and not s["b_kmajor"]
+    try:
+        tg.gemm_set_option("tc_b_major", 2)
+        with pytest.raises(tg.GemmError):
+            _plan(128, 8192, 256, tg.GEMM_E5M2)
+    finally:
+        tg.gemm_set_option("tc_b_major", 0)
+
+
 def test_plan_misaligned_base_packs():
     p = _plan(256, 256, 256, tg.GEMM_BF16, a=2)
     assert p["pack_a"] and not p["pack_b"]

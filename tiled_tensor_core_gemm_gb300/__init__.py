@@ -26,8 +26,9 @@ import threading
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libtcgemm.so")
 
-GEMM_FP32, GEMM_TF32, GEMM_BF16, GEMM_FP16 = 0, 1, 2, 3
-DTYPES = {"fp32": GEMM_FP32, "tf32": GEMM_TF32, "bf16": GEMM_BF16, "fp16": GEMM_FP16}
+GEMM_FP32, GEMM_TF32, GEMM_BF16, GEMM_FP16, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4, 5
+DTYPES = {"fp32": GEMM_FP32, "tf32": GEMM_TF32, "bf16": GEMM_BF16, "fp16": GEMM_FP16, "e4m3": GEMM_E4M3,
+          "e5m2": GEMM_E5M2}
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = 1
@@ -171,19 +172,31 @@ def _ld(t) -> int:
     return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
 
-def gemm(A, B, C=None, dtype=None, stream=None):
-    """C = A.B through gemm_run for CUDA tensors (float32, bfloat16 or float16).
+def _operand_types(torch):
+    """dtype code -> torch element type of A and B."""
+    return {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16, GEMM_E4M3: torch.float8_e4m3fn,
+            GEMM_E5M2: torch.float8_e5m2}
 
-    dtype: "fp32" (default for float32 inputs), "tf32", "bf16" (default for
-    bfloat16 inputs) or "fp16" (default for float16 inputs).  C, if given, must
-    be a float32 CUDA tensor of shape (M, N); it is overwritten.
+
+def _default_dtype(torch, t) -> str:
+    return {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float8_e4m3fn: "e4m3",
+            torch.float8_e5m2: "e5m2"}.get(t.dtype, "fp32")
+
+
+def gemm(A, B, C=None, dtype=None, stream=None):
+    """C = A.B through gemm_run for CUDA tensors (float32, bfloat16, float16 or float8).
+
+    dtype: "fp32" (default for float32 inputs), "tf32", "bf16", "fp16", "e4m3"
+    or "e5m2" (the defaults for bfloat16, float16, float8_e4m3fn and
+    float8_e5m2 inputs).  C, if given, must be a float32 CUDA tensor of shape
+    (M, N); it is overwritten.
     """
     import torch
 
     if dtype is None:
-        dtype = {torch.bfloat16: "bf16", torch.float16: "fp16"}.get(A.dtype, "fp32")
+        dtype = _default_dtype(torch, A)
     code = DTYPES[dtype]
-    want = {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16}.get(code, torch.float32)
+    want = _operand_types(torch).get(code, torch.float32)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"{dtype} GEMM takes {want} operands")
     M, K = A.shape
@@ -209,9 +222,9 @@ def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act="none", out="f32",
     import torch
 
     if dtype is None:
-        dtype = {torch.bfloat16: "bf16", torch.float16: "fp16"}.get(A.dtype, "fp32")
+        dtype = _default_dtype(torch, A)
     code = DTYPES[dtype]
-    want = {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16}.get(code, torch.float32)
+    want = _operand_types(torch).get(code, torch.float32)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"{dtype} GEMM takes {want} operands")
     M, K = A.shape

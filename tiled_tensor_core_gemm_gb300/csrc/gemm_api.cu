@@ -106,7 +106,9 @@ int check_device_span(const char *name, const void *p, uint64_t bytes, int dev, 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 2 : 4; }
+bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
+
+int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 2 : is_fp8(dtype) ? 1 : 4; }
 
 // Measured on GB300 (profiles/picker.md): at 4096^3 the 128 x 128 tile with a
 // K step of 16 beats K step 8 and the 8 x 16 register tiles; when 128 x 128
@@ -206,6 +208,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         cg = (bn == 256 && max_clusters_2cta > 0 && tiles_of(2, 256) >= max_clusters_2cta) ? 2 : 1;
     } else if (bn == 0) {
         bn = 256;
+    }
+    // FP8 B read as stored comes in 128-column chunks (128 bytes): a CTA's
+    // share of a narrower tile reads the K-major copy instead.
+    if (is_fp8(dtype) && !p.b_kmajor && (bn / cg) % 128 != 0) {
+        if (opt.tc_b_major == 2)
+            return fail(GEMM_ERR_UNSUPPORTED, "FP8 B as stored needs 128 columns per CTA (BN=%d, cta_group=%d)", bn,
+                        cg);
+        p.b_kmajor = 1;
+        p.pack_b = 0;
+        out->ldb_eff = round_up(K, 16 / elem);
     }
     if (tc_smem_bytes(dtype, cg, bn, p.b_kmajor) == 0)
         return fail(GEMM_ERR_UNSUPPORTED, "no tensor-core variant with cta_group=%d, BN=%d", cg, bn);
@@ -327,7 +339,8 @@ int64_t gemm_get_option(const char *key) {
 
 static int validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
                     int64_t ldb, const void *C, int64_t ldc) {
-    if (dtype != GEMM_FP32 && dtype != GEMM_TF32 && dtype != GEMM_BF16 && dtype != GEMM_FP16)
+    if (dtype != GEMM_FP32 && dtype != GEMM_TF32 && dtype != GEMM_BF16 && dtype != GEMM_FP16 && dtype != GEMM_E4M3 &&
+        dtype != GEMM_E5M2)
         return fail(GEMM_ERR_INVALID_ARG, "unknown dtype %d", dtype);
     if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)",
                                               (long long)M, (long long)N, (long long)K);

@@ -7,8 +7,8 @@
 // pitch and cannot be described.  The copy rounds the pitch up to a multiple of
 // 16 bytes and zero-fills the extra columns.
 //
-// Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the TF32
-// path, whose tensor-core instruction reads B K-major.
+// Transpose: B (K x N, N contiguous) -> B^T (N x K, K contiguous) for the
+// paths whose MMA reads B K-major (TF32; FP8 tiles narrower than 128 columns).
 //
 // Split reduce: sum the partial tiles of split tiles into C, through the
 // fused epilogue.  Epilogue fill: the epilogue of a zero product (K = 0).
@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(256) pack_rows_vec(const uint8_t *__restrict__
             } else {
                 uint32_t wds[4] = {0u, 0u, 0u, 0u};
                 for (int e = 0; e < 16 / ELEM && b0 + e * ELEM < row_bytes; ++e) {
-                    const uint32_t val = ELEM == 2 ? (uint32_t)*reinterpret_cast<const uint16_t *>(s + b0 + e * 2)
-                                                   : *reinterpret_cast<const uint32_t *>(s + b0 + e * 4);
+                    const uint32_t val = ELEM == 1   ? (uint32_t)*reinterpret_cast<const uint8_t *>(s + b0 + e)
+                                         : ELEM == 2 ? (uint32_t)*reinterpret_cast<const uint16_t *>(s + b0 + e * 2)
+                                                     : *reinterpret_cast<const uint32_t *>(s + b0 + e * 4);
                     const int bit = e * ELEM * 8;
                     wds[bit / 32] |= val << (bit % 32);
                 }
@@ -266,7 +267,10 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
     }
     const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
     const int blocks = (int)(tiles < (int64_t)sms * 8 ? (tiles > 0 ? tiles : 1) : (int64_t)sms * 8);
-    if (elem_bytes == 2)
+    if (elem_bytes == 1)
+        transpose_tiles<uint8_t><<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(src), ld_src,
+                                                             static_cast<uint8_t *>(dst), ld_dst, rows, cols);
+    else if (elem_bytes == 2)
         transpose_tiles<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
                                                               static_cast<uint16_t *>(dst), ld_dst, rows, cols);
     else if (elem_bytes == 4)
@@ -322,7 +326,10 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
         const int vblocks = (int)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16);
         const uint8_t *s = static_cast<const uint8_t *>(src);
         uint8_t *d = static_cast<uint8_t *>(dst);
-        if (elem_bytes == 2)
+        if (elem_bytes == 1)
+            pack_rows_vec<1><<<vblocks, 256, 0, stream>>>(s, ld_src, d, ld_dst, rows, cols, (uintptr_t)src_lo,
+                                                         (uintptr_t)src_hi);
+        else if (elem_bytes == 2)
             pack_rows_vec<2><<<vblocks, 256, 0, stream>>>(s, ld_src * 2, d, ld_dst * 2, rows, cols * 2,
                                                          (uintptr_t)src_lo, (uintptr_t)src_hi);
         else if (elem_bytes == 4)
@@ -332,7 +339,10 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
             return cudaErrorInvalidValue;
         return cudaGetLastError();
     }
-    if (elem_bytes == 2)
+    if (elem_bytes == 1)
+        pack_rows<uint8_t><<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(src), ld_src,
+                                                       static_cast<uint8_t *>(dst), ld_dst, rows, cols);
+    else if (elem_bytes == 2)
         pack_rows<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
                                                         static_cast<uint16_t *>(dst), ld_dst, rows, cols);
     else if (elem_bytes == 4)

@@ -189,25 +189,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; accumulate when `acc` is non-zero.
-template <int CG, bool TF32>
+// MMA kinds: 16-bit inputs, TF32 inputs, 8-bit (FP8) inputs.
+enum MmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
+
+#define TCGEMM_MMA_ASM(cg, kind)                                                                 \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                            \
+                 "tcgen05.mma.cta_group::" #cg ".kind::" #kind " [%0], %1, %2, %3, p;\n\t}"      \
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory")
+
+// D (Tensor Memory) += A (shared, adesc) x B (shared, bdesc); acc == 0 overwrites D.
+template <int CG, int KIND>
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if (CG == 1 && !TF32)
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                     ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-    else if (CG == 1 && TF32)
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-                     ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-    else if (CG == 2 && !TF32)
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                     ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-    else
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-                     ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+    if constexpr (CG == 1 && KIND == kKindF16) TCGEMM_MMA_ASM(1, f16);
+    else if constexpr (CG == 1 && KIND == kKindTF32) TCGEMM_MMA_ASM(1, tf32);
+    else if constexpr (CG == 1 && KIND == kKindF8) TCGEMM_MMA_ASM(1, f8f6f4);
+    else if constexpr (CG == 2 && KIND == kKindF16) TCGEMM_MMA_ASM(2, f16);
+    else if constexpr (CG == 2 && KIND == kKindTF32) TCGEMM_MMA_ASM(2, tf32);
+    else TCGEMM_MMA_ASM(2, f8f6f4);
 }
+#undef TCGEMM_MMA_ASM
 
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

@@ -1,4 +1,4 @@
-// Persistent tensor-core GEMM for BF16, FP16 and TF32 inputs with FP32 accumulation
+// Persistent tensor-core GEMM for BF16, FP16, TF32 and FP8 inputs with FP32 accumulation
 // in Tensor Memory (tcgen05), fed by TMA, for sm_103a.
 //
 // Structure, after "Learn CuTeDSL":
@@ -68,15 +68,19 @@ enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRole
 enum BMode : int { kBNMajor = 0, kBKMajor = 1 };
 
 // Operand element type of a variant.
-enum Dt : int { kDtBF16 = 0, kDtTF32 = 1, kDtFP16 = 2 };
+enum Dt : int { kDtBF16 = 0, kDtTF32 = 1, kDtFP16 = 2, kDtE4M3 = 3, kDtE5M2 = 4 };
+
+constexpr int dt_elem(int dt) { return dt == kDtTF32 ? 4 : (dt == kDtE4M3 || dt == kDtE5M2) ? 1 : 2; }
 
 template <int DT, int CG, int BN, int BMODE>
 struct TcCfg {
     static constexpr bool TF32 = DT == kDtTF32;
+    static constexpr bool F8 = DT == kDtE4M3 || DT == kDtE5M2;
+    static constexpr int KIND = TF32 ? ptx::kKindTF32 : F8 ? ptx::kKindF8 : ptx::kKindF16;
     static constexpr bool BKM = BMODE == kBKMajor;
-    static constexpr int ELEM = TF32 ? 4 : 2;
+    static constexpr int ELEM = dt_elem(DT);
     static constexpr int BK = 128 / ELEM;           // one 128-byte swizzle row of K
-    static constexpr int UMMA_K = 32 / ELEM;        // K of one MMA: 16 (bf16) / 8 (tf32)
+    static constexpr int UMMA_K = 32 / ELEM;        // K of one MMA: 16 (16-bit) / 8 (tf32) / 32 (fp8)
     static constexpr int KSTEPS = BK / UMMA_K;      // 4 MMAs per stage
     static constexpr int BN_CTA = BN / CG;          // B columns this CTA loads
     static constexpr int CHUNK_COLS = 128 / ELEM;   // columns in one 128-byte row of B
@@ -93,10 +97,10 @@ struct TcCfg {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + kEpiBytes + kBarBytes;
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     // Instruction descriptor: D f32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12:
-    // f16 = 0 and bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A K-major (bit 15 = 0),
-    // B MN-major (bit 16 = 1) or K-major (0), N >> 3 in bits 17-22, M >> 4 in
-    // bits 24-28.
-    static constexpr uint32_t FMT = DT == kDtTF32 ? 2u : DT == kDtFP16 ? 0u : 1u;   // f16 = 0 for kind::f16
+    // f16 = 0 and bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32, e4m3 = 0 and
+    // e5m2 = 1 for kind::f8f6f4), A K-major (bit 15 = 0), B MN-major (bit 16 = 1)
+    // or K-major (0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+    static constexpr uint32_t FMT = DT == kDtTF32 ? 2u : (DT == kDtFP16 || DT == kDtE4M3) ? 0u : 1u;
     static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((BKM ? 0u : 1u) << 16) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((kBM * CG) >> 4) << 24);
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N out of range");
@@ -185,7 +189,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     using Cf = TcCfg<DT, CG, BN, BMODE>;
     constexpr bool kPair = CG == 2;
     constexpr bool BKM = Cf::BKM;
-    constexpr bool TF32 = Cf::TF32;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -336,7 +339,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             BKM ? ptx::sdesc_sw128(sb + 32u * kk, 16u, 1024u)
                                 : ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
                                                    1024u);
-                        ptx::mma<CG, TF32>(d_tmem, adesc, bdesc, Cf::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        ptx::mma<CG, Cf::KIND>(d_tmem, adesc, bdesc, Cf::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else ptx::mma_commit(empty_bar(stage));
@@ -597,6 +600,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = DT == kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : DT == kDtFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : Cf::F8        ? CU_TENSOR_MAP_DATA_TYPE_UINT8     // bytes, moved as is
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb, tc, tw;
     std::memset(&tc, 0, sizeof tc);
@@ -680,8 +684,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
 // CTA's share of the tile width to be whole 128-byte column chunks.
 template <int DT, int CG, int BN, int BMODE>
 constexpr bool variant_ok() {
-    return !(DT == kDtTF32 && BMODE == kBNMajor) &&
-           (BMODE == kBKMajor || (BN / CG) % (128 / (DT == kDtTF32 ? 4 : 2)) == 0);
+    return !(DT == kDtTF32 && BMODE == kBNMajor) && (BMODE == kBKMajor || (BN / CG) % (128 / dt_elem(DT)) == 0);
 }
 
 template <int DT, int CG, int BN, int BMODE>
@@ -723,6 +726,12 @@ static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, bool stages)
         if (dtype == GEMM_FP16)                                                                       \
             return mode == kBKMajor ? variant_value<kDtFP16, cg, bn_, kBKMajor>(stages)               \
                                     : variant_value<kDtFP16, cg, bn_, kBNMajor>(stages);              \
+        if (dtype == GEMM_E4M3)                                                                       \
+            return mode == kBKMajor ? variant_value<kDtE4M3, cg, bn_, kBKMajor>(stages)               \
+                                    : variant_value<kDtE4M3, cg, bn_, kBNMajor>(stages);              \
+        if (dtype == GEMM_E5M2)                                                                       \
+            return mode == kBKMajor ? variant_value<kDtE5M2, cg, bn_, kBKMajor>(stages)               \
+                                    : variant_value<kDtE5M2, cg, bn_, kBNMajor>(stages);              \
         return mode == kBKMajor ? variant_value<kDtBF16, cg, bn_, kBKMajor>(stages)                   \
                                 : variant_value<kDtBF16, cg, bn_, kBNMajor>(stages);                  \
     }
@@ -751,6 +760,12 @@ int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const voi
         if (dtype == GEMM_FP16)                                                                          \
             return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtFP16, kBKMajor, cg, bn_)                     \
                                              : TC_LAUNCH(kDtFP16, kBNMajor, cg, bn_);                    \
+        if (dtype == GEMM_E4M3)                                                                          \
+            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtE4M3, kBKMajor, cg, bn_)                     \
+                                             : TC_LAUNCH(kDtE4M3, kBNMajor, cg, bn_);                    \
+        if (dtype == GEMM_E5M2)                                                                          \
+            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtE5M2, kBKMajor, cg, bn_)                     \
+                                             : TC_LAUNCH(kDtE5M2, kBNMajor, cg, bn_);                    \
         return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtBF16, kBKMajor, cg, bn_)                         \
                                          : TC_LAUNCH(kDtBF16, kBNMajor, cg, bn_);                        \
     }

@@ -37,7 +37,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype: str          # "fp32" | "tf32" | "bf16"  (the arithmetic path)
+    dtype: str          # "fp32" | "tf32" | "bf16" | "fp16" | "e4m3" | "e5m2"  (the arithmetic path)
     dist: str           # "uniform" | "normal"
     seed: int
 
@@ -53,6 +53,10 @@ C4_BF16_8192 = Workload("bf16 8192^3 N(0,1) seed 3", 8192, 8192, 8192, "bf16", "
 # 4096^3, their Nsight comparison FP16 at 8192^3), N(0,1) rounded to FP16.
 FP16_4096 = Workload("fp16 4096^3 N(0,1) seed 5", 4096, 4096, 4096, "fp16", "normal", 5)
 FP16_8192 = Workload("fp16 8192^3 N(0,1) seed 6", 8192, 8192, 8192, "fp16", "normal", 6)
+# FP8 inputs (OCP E4M3 and E5M2) at the same two sizes, N(0,1) rounded to FP8.
+E4M3_4096 = Workload("e4m3 4096^3 N(0,1) seed 7", 4096, 4096, 4096, "e4m3", "normal", 7)
+E4M3_8192 = Workload("e4m3 8192^3 N(0,1) seed 8", 8192, 8192, 8192, "e4m3", "normal", 8)
+E5M2_8192 = Workload("e5m2 8192^3 N(0,1) seed 9", 8192, 8192, 8192, "e5m2", "normal", 9)
 C5_BF16_RAGGED = tuple(
     Workload(f"bf16 {m}x{n}x{k} U[-1,1] seed 4", m, n, k, "bf16", "uniform", 4)
     for (m, n, k) in ((1000, 1000, 1000), (4097, 4095, 4099), (16384, 1024, 4096), (128, 8192, 8192))
