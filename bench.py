@@ -266,6 +266,49 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
             "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K}
 
 
+def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False):
+    """A grouped workload through gemm_run_grouped (one launch per step), or the
+    same GEMMs through one gemm_run each; CUDA events around all steps."""
+    import torch
+    from tiled_tensor_core_gemm_gb300.inputs import grouped_operands
+    pairs = [(A.to(device), B.to(device)) for A, B in grouped_operands(workload)]
+    Cs = [torch.empty((A.shape[0], B.shape[1]), dtype=torch.float32, device=device) for A, B in pairs]
+    code = tg.DTYPES[workload.dtype]
+    s = stream.cuda_stream
+    groups = [tg.GemmGroup(A.shape[0], B.shape[1], A.shape[1], A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1],
+                           C.data_ptr(), C.shape[1], None) for (A, B), C in zip(pairs, Cs)]
+
+    def run():
+        if one_by_one:
+            for (A, B), C in zip(pairs, Cs):
+                rc = tg.gemm_run(A.shape[0], B.shape[1], A.shape[1], code, A.data_ptr(), A.shape[1], B.data_ptr(),
+                                 B.shape[1], C.data_ptr(), C.shape[1], s)
+                if rc != tg.GEMM_OK:
+                    raise RuntimeError(tg.gemm_last_error())
+        else:
+            rc = tg.gemm_run_grouped(code, groups, None, s)
+            if rc != tg.GEMM_OK:
+                raise RuntimeError(tg.gemm_last_error())
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    st = tg.gemm_get_status(s)
+    if st != tg.GEMM_OK:
+        raise RuntimeError(f"grouped status {st}: {tg.gemm_last_error()}")
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms": ms, "tflops": workload.flops / (ms * 1e-3) / 1e12,
+            "launches_per_step": len(pairs) if one_by_one else 1}
+
+
 def time_e2e(tg, workload, steps, stream, device):
     """Same GEMM through gemm_run with the operands in pinned host memory: each
     step copies A and B host->device, runs, and copies C device->host."""
@@ -484,6 +527,16 @@ def run_ours(args):
                           "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
                           "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
+        # the skewed 16-group workload: one grouped launch, and the same GEMMs one by one
+        from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16
+        for key, obo in (("grouped_bf16_16", False), ("grouped_bf16_16_one_by_one", True)):
+            r = time_grouped(tg, GROUPED_BF16, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
+            rl = roofline_for_dtype("bf16", GROUPED_BF16.flops, r["ms"], peaks, peak_src, None)
+            paths[key] = {"workload": GROUPED_BF16.name + (", as 16 gemm_run calls" if obo else
+                                                           ", one gemm_run_grouped launch"),
+                          "group_rows": list(GROUPED_BF16.Ms), "tflops": round(r["tflops"], 2), "steps": n_side,
+                          "ms_per_step": round(r["ms"], 4), "launches_per_step": r["launches_per_step"],
+                          "l2": "inputs larger than L2", "roofline": rl}
         out["paths"] = paths
 
     if not args.no_e2e:

@@ -154,6 +154,45 @@ GEMM_API int gemm_run_ex(int64_t M, int64_t N, int64_t K, int dtype,
                          void *C, int64_t ldc, const gemm_epilogue_t *epi,
                          struct CUstream_st *stream);
 
+/*
+ * gemm_run_grouped -- a batch of independent GEMMs in one persistent launch,
+ * C_g = act(alpha * A_g . B_g + beta * C_g + bias_g) for g < group_count
+ * ("Learn CuTeDSL" section 8.4, grouped tile scheduler: the tiles of every
+ * group flattened into one list of work units that the persistent CTAs share).
+ *
+ *   dtype        one gemm_dtype_t for every group.  Tensor-core dtypes run as
+ *                one launch; GEMM_FP32 runs one SIMT launch per group.
+ *   group_count  number of groups, 0 .. 2^20 (0: no-op).
+ *   groups       HOST array of group_count gemm_group_t, read during the call
+ *                only.  Each group's M..ldc follow gemm_run_ex (C in the
+ *                epilogue's output type); bias is the group's own N floats
+ *                (device memory) or NULL.
+ *   epi          shared alpha, beta, activation and output type, or NULL (as
+ *                gemm_run); its bias must be NULL.
+ *   stream       the CUDA stream to enqueue on.
+ * Groups with M == 0 or N == 0 are skipped; groups with K == 0 get the
+ * epilogue of an empty sum.  All groups share one tile shape and CTA pairing,
+ * chosen from their total tile count; there is no split-K.  Operands TMA cannot
+ * address are packed (and TF32 B transposed) into a stream-ordered workspace,
+ * which also holds the groups' descriptors.
+ * Errors: as gemm_run_ex for any group's arguments, plus GEMM_ERR_INVALID_ARG
+ * for group_count out of range, a NULL groups array, a non-NULL epi->bias, or
+ * a group's C overlapping another group's A, B, C or bias.
+ */
+typedef struct {
+    int64_t M, N, K;
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    void *C;
+    int64_t ldc;
+    const float *bias;
+} gemm_group_t;
+
+GEMM_API int gemm_run_grouped(int dtype, int64_t group_count, const gemm_group_t *groups,
+                              const gemm_epilogue_t *epi, struct CUstream_st *stream);
+
 /* Message for the calling thread's most recent failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 GEMM_API const char *gemm_last_error(void);

@@ -282,3 +282,49 @@ def test_epilogue_argument_checks_before_cuda():
 def test_null_epilogue_behaves_as_gemm_run():
     assert tg.gemm_run_ex(0, 5, 3, tg.GEMM_BF16, 0, 3, 0, 5, 0, 5, None, 0) == tg.GEMM_OK
     assert tg.gemm_run_ex(4, 4, 4, 7, 16, 4, 16, 4, 64, 4, None, 0) == tg.GEMM_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------- gemm_run_grouped ---
+def _grp(M, N, K, A, lda, B, ldb, C, ldc, bias=0):
+    return tg.GemmGroup(M, N, K, A, lda, B, ldb, C, ldc, bias or None)
+
+
+def test_group_struct_layout_matches_the_header(tmp_path):
+    src = tmp_path / "glayout.c"
+    fields = ("M", "N", "K", "A", "lda", "B", "ldb", "C", "ldc", "bias")
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\n'
+                   'int main(void) { printf("%zu' + ' %zu' * len(fields) + '\\n", sizeof(gemm_group_t)'
+                   + "".join(f", offsetof(gemm_group_t, {f})" for f in fields) + '); return 0; }\n')
+    exe = tmp_path / "glayout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got == [ctypes.sizeof(tg.GemmGroup)] + [getattr(tg.GemmGroup, f).offset for f in fields]
+
+
+def test_grouped_argument_checks_before_cuda():
+    BF = tg.GEMM_BF16
+    ok = _grp(8, 8, 8, 1 << 20, 8, 1 << 21, 8, 1 << 22, 8)
+    assert tg.gemm_run_grouped(BF, []) == tg.GEMM_OK                                  # nothing to do
+    assert tg.gemm_run_grouped(BF, [_grp(0, 8, 8, 0, 8, 0, 8, 0, 8)]) == tg.GEMM_OK   # only empty groups
+    lib = tg.load_library()
+    assert lib.gemm_run_grouped(BF, -1, None, None, None) == tg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_grouped(BF, 3, None, None, None) == tg.GEMM_ERR_INVALID_ARG
+    assert "NULL" in tg.gemm_last_error()
+    # the shared epilogue may not carry a bias
+    ep = tg.make_epilogue(1.0, 0.0, 1 << 23, "none", "f32")
+    assert tg.gemm_run_grouped(BF, [ok], ep) == tg.GEMM_ERR_INVALID_ARG and "bias" in tg.gemm_last_error()
+    # a bad group anywhere in the list
+    assert tg.gemm_run_grouped(BF, [ok, _grp(8, 8, 8, 1 << 24, 4, 1 << 25, 8, 1 << 26, 8)]) == tg.GEMM_ERR_INVALID_ARG
+    assert "leading dimension" in tg.gemm_last_error()
+    # two groups writing overlapping C
+    two = [ok, _grp(8, 8, 8, 1 << 24, 8, 1 << 25, 8, (1 << 22) + 64, 8)]
+    assert tg.gemm_run_grouped(BF, two) == tg.GEMM_ERR_INVALID_ARG and "C overlap" in tg.gemm_last_error()
+    # one group's C over another group's A
+    cross = [ok, _grp(8, 8, 8, 1 << 24, 8, 1 << 25, 8, (1 << 20) + 16, 8)]
+    assert tg.gemm_run_grouped(BF, cross) == tg.GEMM_ERR_INVALID_ARG and "overlaps" in tg.gemm_last_error()
+    # a bias inside some C, a misaligned bias
+    bad_bias = [ok, _grp(8, 8, 8, 1 << 24, 8, 1 << 25, 8, 1 << 26, 8, bias=(1 << 22) + 8)]
+    assert tg.gemm_run_grouped(BF, bad_bias) == tg.GEMM_ERR_INVALID_ARG and "bias" in tg.gemm_last_error()
+    mis = [_grp(8, 8, 8, 1 << 24, 8, 1 << 25, 8, 1 << 26, 8, bias=(1 << 27) + 2)]
+    assert tg.gemm_run_grouped(BF, mis) == tg.GEMM_ERR_INVALID_ARG and "aligned" in tg.gemm_last_error()
+    assert tg.gemm_run_grouped(9, [ok]) == tg.GEMM_ERR_INVALID_ARG and "dtype" in tg.gemm_last_error()

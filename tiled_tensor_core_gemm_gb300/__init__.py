@@ -43,7 +43,8 @@ GEMM_OUT_F32, GEMM_OUT_BF16, GEMM_OUT_F16 = 0, 1, 2
 OUT_TYPES = {"f32": GEMM_OUT_F32, "bf16": GEMM_OUT_BF16, "f16": GEMM_OUT_F16}
 
 EXPORTED = ("gemm_run", "gemm_last_error", "gemm_get_status", "gemm_set_option",
-            "gemm_get_option", "gemm_plan", "gemm_version", "gemm_run_tf32_static", "gemm_run_ex")
+            "gemm_get_option", "gemm_plan", "gemm_version", "gemm_run_tf32_static", "gemm_run_ex",
+            "gemm_run_grouped")
 TF32_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # GEMM_TF32_STATIC_SCRATCH_BYTES in include/gemm.h
 
 
@@ -66,6 +67,13 @@ class GemmEpilogue(ctypes.Structure):
     """gemm_epilogue_t: y = act(alpha * acc + beta * C_old + bias[col]) stored as out_dtype."""
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
                 ("activation", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+
+
+class GemmGroup(ctypes.Structure):
+    """gemm_group_t: one GEMM of a grouped launch (device addresses as ints)."""
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("A", ctypes.c_void_p),
+                ("lda", ctypes.c_int64), ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("C", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64), ("bias", ctypes.c_void_p)]
 
 
 def make_epilogue(alpha=1.0, beta=0.0, bias=0, act="none", out="f32") -> GemmEpilogue:
@@ -114,6 +122,8 @@ def load_library():
         lib.gemm_run_ex.argtypes = [i64, i64, i64, ctypes.c_int, p, i64, p, i64, p, i64, ctypes.POINTER(GemmEpilogue),
                                     p]
         lib.gemm_run_ex.restype = ctypes.c_int
+        lib.gemm_run_grouped.argtypes = [ctypes.c_int, i64, ctypes.POINTER(GemmGroup), ctypes.POINTER(GemmEpilogue), p]
+        lib.gemm_run_grouped.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -161,6 +171,13 @@ def gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, epilogue=None, stream=0)
     """C = act(alpha * A.B + beta * C + bias) stored as the epilogue's output type."""
     ep = ctypes.byref(epilogue) if epilogue is not None else None
     return load_library().gemm_run_ex(M, N, K, dtype, A, lda, B, ldb, C, ldc, ep, stream)
+
+
+def gemm_run_grouped(dtype, groups, epilogue=None, stream=0) -> int:
+    """A batch of independent GEMMs in one launch; groups: a sequence of GemmGroup."""
+    arr = (GemmGroup * len(groups))(*groups) if len(groups) else None
+    ep = ctypes.byref(epilogue) if epilogue is not None else None
+    return load_library().gemm_run_grouped(dtype, len(groups), arr, ep, stream)
 
 
 # ------------------------------------------------------ tensor convenience ---
@@ -247,3 +264,43 @@ def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act="none", out="f32",
     if rc != GEMM_OK:
         raise GemmError(rc, gemm_last_error())
     return C
+
+
+def gemm_grouped(As, Bs, Cs=None, biases=None, alpha=1.0, beta=0.0, act="none", out="f32", dtype=None, stream=None):
+    """C_g = act(alpha * A_g.B_g + beta * C_g + bias_g) for every g, in one grouped launch.
+
+    As, Bs: sequences of row-major CUDA tensors of one type; Cs (allocated if
+    None, beta must then be 0) in the output type; biases: None or a sequence
+    of float32 tensors of N_g values (or None entries).  Returns the Cs.
+    """
+    import torch
+
+    if len(As) != len(Bs):
+        raise ValueError("As and Bs differ in length")
+    if not As:
+        return []
+    if dtype is None:
+        dtype = _default_dtype(torch, As[0])
+    code = DTYPES[dtype]
+    want = _operand_types(torch).get(code, torch.float32)
+    cdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out]
+    if Cs is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs Cs")
+        Cs = [torch.empty((a.shape[0], b.shape[1]), dtype=cdt, device=a.device) for a, b in zip(As, Bs)]
+    groups = []
+    for i, (a, b, c) in enumerate(zip(As, Bs, Cs)):
+        if a.dtype != want or b.dtype != want:
+            raise TypeError(f"{dtype} GEMM takes {want} operands")
+        if a.shape[1] != b.shape[0] or tuple(c.shape) != (a.shape[0], b.shape[1]) or c.dtype != cdt:
+            raise ValueError(f"group {i}: shapes or C type do not match")
+        bias = biases[i] if biases is not None else None
+        groups.append(GemmGroup(a.shape[0], b.shape[1], a.shape[1], a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                                c.data_ptr(), _ld(c), bias.data_ptr() if bias is not None else None))
+    if stream is None:
+        stream = torch.cuda.current_stream(As[0].device).cuda_stream
+    ep = make_epilogue(alpha, beta, 0, act, out)
+    rc = gemm_run_grouped(code, groups, ep, stream)
+    if rc != GEMM_OK:
+        raise GemmError(rc, gemm_last_error())
+    return Cs

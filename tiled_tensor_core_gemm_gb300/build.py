@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtcgemm.so")
-SOURCES = ("gemm_api.cu", "simt_fp32.cu", "tc_gemm.cu", "pack.cu", "tf32_static.cu")
+SOURCES = ("gemm_api.cu", "simt_fp32.cu", "tc_gemm.cu", "pack.cu", "tf32_static.cu", "grouped.cu")
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC] + GENCODE

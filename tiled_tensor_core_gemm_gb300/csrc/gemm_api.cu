@@ -527,18 +527,8 @@ int gemm_run_ex(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64
                 void *C, int64_t ldc, const gemm_epilogue_t *epi, struct CUstream_st *stream_) {
     t_err[0] = 0;
     EpiParams e;
-    if (epi) {
-        if (epi->activation != GEMM_ACT_NONE && epi->activation != GEMM_ACT_RELU && epi->activation != GEMM_ACT_GELU)
-            return fail(GEMM_ERR_INVALID_ARG, "unknown activation %d", (int)epi->activation);
-        if (epi->out_dtype != GEMM_OUT_F32 && epi->out_dtype != GEMM_OUT_BF16 && epi->out_dtype != GEMM_OUT_F16)
-            return fail(GEMM_ERR_INVALID_ARG, "unknown output type %d", (int)epi->out_dtype);
-        e.alpha = epi->alpha;
-        e.beta = epi->beta;
-        e.bias = epi->bias;
-        e.act = epi->activation;
-        e.out = epi->out_dtype;
-        e.active = !(e.alpha == 1.f && e.beta == 0.f && !e.bias && e.act == GEMM_ACT_NONE && e.out == GEMM_OUT_F32);
-    }
+    const int rc = api_epilogue(epi, &e);
+    if (rc) return rc;
     return run(M, N, K, dtype, A, lda, B, ldb, C, ldc, e, reinterpret_cast<cudaStream_t>(stream_));
 }
 
@@ -575,6 +565,30 @@ int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int6
 int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev) {
     return check_device_span(name, p, bytes, dev);
 }
+
+int api_check_device_span_range(const char *name, const void *p, uint64_t bytes, int dev, uint64_t *lo,
+                                uint64_t *hi) {
+    return check_device_span(name, p, bytes, dev, lo, hi);
+}
+
+int api_epilogue(const gemm_epilogue_t *in, EpiParams *out) {
+    *out = EpiParams();
+    if (!in) return GEMM_OK;
+    if (in->activation != GEMM_ACT_NONE && in->activation != GEMM_ACT_RELU && in->activation != GEMM_ACT_GELU)
+        return fail(GEMM_ERR_INVALID_ARG, "unknown activation %d", (int)in->activation);
+    if (in->out_dtype != GEMM_OUT_F32 && in->out_dtype != GEMM_OUT_BF16 && in->out_dtype != GEMM_OUT_F16)
+        return fail(GEMM_ERR_INVALID_ARG, "unknown output type %d", (int)in->out_dtype);
+    out->alpha = in->alpha;
+    out->beta = in->beta;
+    out->bias = in->bias;
+    out->act = in->activation;
+    out->out = in->out_dtype;
+    out->active =
+        !(out->alpha == 1.f && out->beta == 0.f && !out->bias && out->act == GEMM_ACT_NONE && out->out == GEMM_OUT_F32);
+    return GEMM_OK;
+}
+
+int api_elem_bytes(int dtype) { return elem_bytes(dtype); }
 
 int api_device_info(int dev, int *sms, int *cc_major, int *cc_minor, int *max_clusters) {
     DevInfo d;

@@ -37,6 +37,19 @@ struct EpiParams {
     int active = 0;
 };
 
+// ------------------------------------------------------------ grouped GEMM ---
+// One GEMM of a grouped launch as the tensor-core kernel reads it from device
+// memory ("Learn CuTeDSL" section 8.4: the tiles of every group flattened into
+// one list of work units, unit_start being the group's first).  The TMA
+// descriptors come first: they must be 64-byte aligned.
+struct alignas(128) GroupDesc {
+    CUtensorMap tmA, tmB, tmC;
+    int32_t M, N, num_kb, tiles_m, tiles_n, unit_start, tma_store, reserved;
+    void *C;
+    int64_t ldc;
+    const float *bias;
+};
+
 // ------------------------------------------------------------------- plan ---
 struct Plan {
     gemm_plan_t pub;           // what gemm_plan() reports
@@ -79,6 +92,18 @@ int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K,
               void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream,
               char *err, size_t errlen);
 
+// Grouped launch: encodes one group's tensor maps into `d` (A and B as the
+// plan stages them, C in the output type when d->tma_store); returns a
+// gemm_status_t.
+int tc_encode_group(const gemm_plan_t &plan, int dtype, GroupDesc *d, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, void *C, int64_t ldc, int out, int M, int N, int K, char *err, size_t errlen);
+
+// Launches the persistent kernel over `group_count` groups whose descriptors
+// are in device memory (unit_start ascending, every group non-empty with
+// K > 0) and `num_units` units in all.
+int tc_launch_grouped(const gemm_plan_t &plan, int dtype, const GroupDesc *groups, int group_count, int num_units,
+                      const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream, char *err, size_t errlen);
+
 // Reads and clears the device status word of the tensor-core kernel.
 // words[0] = error code (0 none), [1] = role, [2] = tile, [3] = block.
 cudaError_t tc_read_and_clear_status(uint32_t words[4]);
@@ -118,6 +143,13 @@ void api_clear_error();
 int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
                  int64_t ldb, const void *C, int64_t ldc);
 int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev);
+// The same, also reporting the allocation [*lo, *hi) that holds the span.
+int api_check_device_span_range(const char *name, const void *p, uint64_t bytes, int dev, uint64_t *lo,
+                                uint64_t *hi);
+// gemm_epilogue_t -> EpiParams (NULL: inactive); checks the enumerations.
+int api_epilogue(const gemm_epilogue_t *in, EpiParams *out);
+// Element size in bytes of a gemm_dtype_t's operands.
+int api_elem_bytes(int dtype);
 int api_device_info(int dev, int *sms, int *cc_major, int *cc_minor, int *max_clusters);
 
 }  // namespace tcgemm

@@ -189,6 +189,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; accumulate when `acc` is non-zero.
+// Makes a tensor map written through ordinary memory (here: copied in before
+// the launch) visible to the TMA unit before this thread first uses it.
+__device__ __forceinline__ void fence_tensormap_acquire(const void *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
 // MMA kinds: 16-bit inputs, TF32 inputs, 8-bit (FP8) inputs.
 enum MmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 

@@ -40,6 +40,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -127,7 +128,9 @@ struct TcParams {
     int debug_stall;                   // test hook: the MMA thread first waits on a barrier nothing arrives at
     void *C;                           // FP32, or epi.out when the epilogue is active
     int64_t ldc;
-    EpiParams epi;                     // fused epilogue (plain-store path only)
+    EpiParams epi;                     // fused epilogue
+    const GroupDesc *groups;           // grouped launch: per-group sizes, maps and C (nullptr: one GEMM)
+    int group_count;
     unsigned long long timeout_ns;
 };
 
@@ -156,6 +159,62 @@ __device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, i
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
     slab = split * p.tail_tiles + i;
+}
+
+// Everything a role needs about one work unit: its tile, K range and slab
+// (unit_coords), and the GEMM it belongs to -- the kernel's own parameters, or
+// in a grouped launch the descriptor of the group whose units contain u (a
+// binary search over the groups' first units).
+struct Unit {
+    int tm, tn, kb0, kb1, slab;
+    int M, N;
+    const CUtensorMap *mA, *mB, *mC;
+    void *C;
+    int64_t ldc;
+    const float *bias;
+    int tma_store;
+    int group;                         // -1 outside a grouped launch
+};
+
+__device__ __forceinline__ Unit unit_info(int u, const TcParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                          const CUtensorMap *tmC) {
+    Unit U;
+    if (p.groups == nullptr) {
+        unit_coords(u, p, U.tm, U.tn, U.kb0, U.kb1, U.slab);
+        U.M = p.M;
+        U.N = p.N;
+        U.mA = tmA;
+        U.mB = tmB;
+        U.mC = tmC;
+        U.C = p.C;
+        U.ldc = p.ldc;
+        U.bias = p.epi.bias;
+        U.tma_store = p.tma_store;
+        U.group = -1;
+        return U;
+    }
+    int lo = 0, hi = p.group_count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.groups[mid].unit_start <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const GroupDesc *g = p.groups + lo;
+    tile_coords(u - g->unit_start, g->tiles_m, g->tiles_n, p.group_m, U.tm, U.tn);
+    U.kb0 = 0;
+    U.kb1 = g->num_kb;
+    U.slab = -1;
+    U.M = g->M;
+    U.N = g->N;
+    U.mA = &g->tmA;
+    U.mB = &g->tmB;
+    U.mC = &g->tmC;
+    U.C = g->C;
+    U.ldc = g->ldc;
+    U.bias = g->bias;
+    U.tma_store = g->tma_store;
+    U.group = lo;
+    return U;
 }
 
 __device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
@@ -226,7 +285,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && p.groups == nullptr) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
         if (p.tma_store) ptx::prefetch_tensormap(&tmC);
@@ -247,12 +306,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            int last_group = -1;
             for (int t = unit; ok && t < p.num_units; t += nunits) {
-                int tm, tn, kb0, kb1, slab;
-                unit_coords(t, p, tm, tn, kb0, kb1, slab);
-                const int m0 = tm * (kBM * CG) + (int)rank * kBM;
-                const int n0 = tn * BN + (int)rank * Cf::BN_CTA;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
+                if (U.group != last_group) {
+                    // a group's maps were copied in before the launch: acquire them for TMA
+                    ptx::fence_tensormap_acquire(U.mA);
+                    ptx::fence_tensormap_acquire(U.mB);
+                    ptx::prefetch_tensormap(U.mA);
+                    ptx::prefetch_tensormap(U.mB);
+                    last_group = U.group;
+                }
+                const int m0 = U.tm * (kBM * CG) + (int)rank * kBM;
+                const int n0 = U.tn * BN + (int)rank * Cf::BN_CTA;
+                for (int kb = U.kb0; kb < U.kb1; ++kb) {
                     if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleProducer, t, abort_flag);
                         ok = false;
@@ -264,23 +331,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t sb = sa + Cf::A_BYTES;
                     const int k0 = kb * Cf::BK;
                     if (!kPair) {
-                        ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
+                        ptx::tma_load_2d(sa, U.mA, fb, k0, m0);
                         if (BKM) {
-                            ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
+                            ptx::tma_load_2d(sb, U.mB, fb, k0, n0);
                         } else {
 #pragma unroll
                             for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                                ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb, n0 + c * Cf::CHUNK_COLS, k0);
+                                ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb, n0 + c * Cf::CHUNK_COLS, k0);
                         }
                     } else {
                         const uint32_t fb_even = ptx::mapa_shared(fb, 0);
-                        ptx::tma_load_2d_pair(sa, &tmA, fb_even, k0, m0);
+                        ptx::tma_load_2d_pair(sa, U.mA, fb_even, k0, m0);
                         if (BKM) {
-                            ptx::tma_load_2d_pair(sb, &tmB, fb_even, k0, n0);
+                            ptx::tma_load_2d_pair(sb, U.mB, fb_even, k0, n0);
                         } else {
 #pragma unroll
                             for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                                ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, &tmB, fb_even, n0 + c * Cf::CHUNK_COLS,
+                                ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb_even, n0 + c * Cf::CHUNK_COLS,
                                                       k0);
                         }
                     }
@@ -312,8 +379,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 ok = false;
             }
             for (int t = unit; ok && t < p.num_units; t += nunits) {
-                int tm, tn, kb0, kb1, slab;
-                unit_coords(t, p, tm, tn, kb0, kb1, slab);
+                const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
+                const int kb0 = U.kb0, kb1 = U.kb1;
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleMma, t, abort_flag);
                     break;
@@ -370,17 +437,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t nchunk = 0;                 // boxes staged so far (buffer nchunk & 1)
         uint32_t old_phase = 0;              // parity of each buffer's old-C barrier
         bool ok = true;
+        int last_group = -1;
         for (int t = unit; ok && t < p.num_units; t += nunits) {
-            int tm, tn, kb0, kb1, slab;
-            unit_coords(t, p, tm, tn, kb0, kb1, slab);
-            const int m0 = tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
-            const int n0 = tn * BN;
-            const int srow = (int)rank * kBM + 32 * (int)q;                     // same row inside a slab
+            const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
+            const int slab = U.slab;
+            const int m0 = U.tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
+            const int n0 = U.tn * BN;
+            const int srow = (int)rank * kBM + 32 * (int)q;                       // same row inside a slab
             const bool to_slab = slab >= 0;
-            const bool use_tma = to_slab || p.tma_store;
+            const bool use_tma = to_slab || U.tma_store;
+            if (U.group != last_group) {
+                if (lane == 0 && U.tma_store) {
+                    ptx::fence_tensormap_acquire(U.mC);
+                    ptx::prefetch_tensormap(U.mC);
+                }
+                last_group = U.group;
+            }
+            EpiParams e = p.epi;             // the group's own bias in a grouped launch
+            e.bias = U.bias;
             // The epilogue runs in registers (thread = row) when the box leaves
             // through TMA; partial sums of a split tile go to their slab raw.
-            const bool reg_epi = fused && p.tma_store && !to_slab;
+            const bool reg_epi = fused && U.tma_store && !to_slab;
             const bool pack16 = reg_epi && out != GEMM_OUT_F32;
             const int box_cols = pack16 ? 64 : 32;
             const bool lane_ok = wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns);
@@ -394,7 +471,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int jb = 0; jb < BN / box_cols; ++jb, ++nchunk) {
                 uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
                 const int col0 = n0 + box_cols * jb;
-                const bool box_live = m0 < p.M && col0 < p.N;
+                const bool box_live = m0 < U.M && col0 < U.N;
                 // The TMA store that last read this buffer (two boxes ago) must be done.
                 if (nchunk >= 2) {
                     if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -407,7 +484,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t ob = oldc_bar(2 * (int)ew + (int)bi);
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(ob, (uint32_t)kEpiBufBytes);
-                        ptx::tma_load_2d(ptx::smem_addr(buf), &tmC, ob, col0, m0);
+                        ptx::tma_load_2d(ptx::smem_addr(buf), U.mC, ob, col0, m0);
                     }
                     const bool got = wait_bar<false>(ob, (old_phase >> bi) & 1u, abort_flag, p.timeout_ns);
                     old_phase ^= 1u << bi;
@@ -435,7 +512,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (reg_epi) {
                         // Row m0 + lane, columns cb .. cb + 31: lane c holds bias[cb + c].
                         const int cb = col0 + 32 * h;
-                        const float bias_lane = epi_bias(p.epi, cb + (int)lane, p.N);
+                        const float bias_lane = epi_bias(e, cb + (int)lane, U.N);
                         // The old C of these 32 columns, read in 16-byte chunks (one
                         // chunk per lane per quarter-warp phase: conflict-free).
                         float old[32];
@@ -467,7 +544,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         float y[32];
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            y[c] = epi_value(p.epi, __uint_as_float(r[c]), old[c],
+                            y[c] = epi_value(e, __uint_as_float(r[c]), old[c],
                                              __shfl_sync(0xffffffffu, bias_lane, c));
                         if (pack16) {
 #pragma unroll
@@ -500,7 +577,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                     if (lane == 0) {
                         if (to_slab) ptx::tma_store_3d(&tmW, ptx::smem_addr(buf), 32 * jb, srow, slab);
-                        else if (box_live) ptx::tma_store_2d(&tmC, ptx::smem_addr(buf), col0, m0);
+                        else if (box_live) ptx::tma_store_2d(U.mC, ptx::smem_addr(buf), col0, m0);
                         ptx::bulk_commit_group();
                     }
                 } else {
@@ -510,24 +587,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                     const int col = col0 + (int)lane;
                     const uint32_t cchunk = lane >> 2, cword = lane & 3u;
-                    const float bias = epi_bias(p.epi, col, p.N);
+                    const float bias = epi_bias(e, col, U.N);
 #pragma unroll 1
                     for (int r0 = 0; r0 < 32; r0 += 8) {
                         float old[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            old[i] = (need_old && m0 + r0 + i < p.M && col < p.N)
-                                         ? epi_load_old(p.C, (int64_t)(m0 + r0 + i) * p.ldc + col, out)
+                            old[i] = (need_old && m0 + r0 + i < U.M && col < U.N)
+                                         ? epi_load_old(U.C, (int64_t)(m0 + r0 + i) * U.ldc + col, out)
                                          : 0.f;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int rr = r0 + i, grow = m0 + rr;
                             const float v = *reinterpret_cast<const float *>(
                                 buf + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u) + cword * 4u);
-                            if (grow < p.M && col < p.N) {
-                                const int64_t idx = (int64_t)grow * p.ldc + col;
-                                if (fused) epi_store(p.C, idx, out, epi_value(p.epi, v, old[i], bias));
-                                else static_cast<float *>(p.C)[idx] = v;
+                            if (grow < U.M && col < U.N) {
+                                const int64_t idx = (int64_t)grow * U.ldc + col;
+                                if (fused) epi_store(U.C, idx, out, epi_value(e, v, old[i], bias));
+                                else static_cast<float *>(U.C)[idx] = v;
                             }
                         }
                     }
@@ -591,71 +668,44 @@ CUresult encode_3d_slabs(CUtensorMap *map, const void *base, int64_t cols, int64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Tensor maps of one GEMM's operands as variant <DT, CG, BN, BMODE> stages
+// them: A in BK x 128-row boxes, B as stored (128-byte column chunks) or as the
+// K-major copy, C (when it leaves through TMA) in 32-row boxes of 128 bytes:
+// 32 FP32 columns, or 64 of a 16-bit output.
 template <int DT, int CG, int BN, int BMODE>
-int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                   int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
-                   cudaStream_t stream, char *err, size_t errlen) {
+CUresult encode_operands(int M, int N, int K, const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                         int64_t ldc, int out, bool tma_store, CUtensorMap *ta, CUtensorMap *tb, CUtensorMap *tc) {
     using Cf = TcCfg<DT, CG, BN, BMODE>;
-
-    constexpr bool BKM = Cf::BKM;
     const CUtensorMapDataType dt = DT == kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : DT == kDtFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                    : Cf::F8        ? CU_TENSOR_MAP_DATA_TYPE_UINT8     // bytes, moved as is
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap ta, tb, tc, tw;
-    std::memset(&tc, 0, sizeof tc);
-    std::memset(&tw, 0, sizeof tw);
-    CUresult r = encode_2d(&ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
+    std::memset(tc, 0, sizeof *tc);
+    CUresult r = encode_2d(ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
     if (r == CUDA_SUCCESS)
-        r = BKM ? encode_2d(&tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
-                : encode_2d(&tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
-    if (r == CUDA_SUCCESS && plan.tma_store) {
-        // C in boxes of 32 rows x 128 bytes: 32 FP32 columns, or 64 of a 16-bit output.
-        const int out = epi.active ? epi.out : GEMM_OUT_F32;
+        r = Cf::BKM ? encode_2d(tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
+                    : encode_2d(tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
+    if (r == CUDA_SUCCESS && tma_store) {
         if (out == GEMM_OUT_F32)
-            r = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
+            r = encode_2d(tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
         else
-            r = encode_2d(&tc, out == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            r = encode_2d(tc, out == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                           2, C, N, M, ldc, 64, 32);
     }
-    if (r == CUDA_SUCCESS && plan.tail_tiles > 0) {
-        if (!W) {
-            std::snprintf(err, errlen, "split tail without a workspace");
-            return GEMM_ERR_INVALID_ARG;
-        }
-        r = encode_3d_slabs(&tw, W, BN, kBM * CG, (int64_t)plan.tail_tiles * plan.splits);
-    }
-    if (r != CUDA_SUCCESS) {
-        std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-        return GEMM_ERR_CUDA;
-    }
+    return r;
+}
+
+// Launches the kernel with the plan's grid (CTA pairs as clusters of two).
+template <int DT, int CG, int BN, int BMODE>
+int launch_kernel(const gemm_plan_t &plan, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                  const CUtensorMap &tw, const TcParams &p, cudaStream_t stream, char *err, size_t errlen) {
+    using Cf = TcCfg<DT, CG, BN, BMODE>;
     auto kern = tc_gemm_kernel<DT, CG, BN, BMODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return GEMM_ERR_CUDA;
     }
-    TcParams p;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.tiles_m = (M + kBM * CG - 1) / (kBM * CG);
-    p.tiles_n = (N + BN - 1) / BN;
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.num_kb = (K + Cf::BK - 1) / Cf::BK;
-    p.tail_tiles = plan.tail_tiles;
-    p.full_tiles = p.num_tiles - p.tail_tiles;
-    p.splits = p.tail_tiles > 0 ? plan.splits : 1;
-    p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
-    p.num_units = p.full_tiles + p.tail_tiles * p.splits;
-    p.group_m = plan.group_m > 0 ? plan.group_m : 1;
-    p.tma_store = plan.tma_store;
-    p.debug_stall = options_snapshot().debug_stall_mma;
-    p.C = C;
-    p.ldc = ldc;
-    p.epi = epi;
-    p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
-
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
@@ -679,6 +729,90 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     return GEMM_OK;
 }
 
+TcParams base_params(const gemm_plan_t &plan, const EpiParams &epi, uint32_t timeout_ms) {
+    TcParams p;
+    std::memset(&p, 0, sizeof p);
+    p.splits = 1;
+    p.group_m = plan.group_m > 0 ? plan.group_m : 1;
+    p.tma_store = plan.tma_store;
+    p.debug_stall = options_snapshot().debug_stall_mma;
+    p.epi = epi;
+    p.groups = nullptr;
+    p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+    return p;
+}
+
+template <int DT, int CG, int BN, int BMODE>
+int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
+                   cudaStream_t stream, char *err, size_t errlen) {
+    using Cf = TcCfg<DT, CG, BN, BMODE>;
+    CUtensorMap ta, tb, tc, tw;
+    std::memset(&tw, 0, sizeof tw);
+    CUresult r = encode_operands<DT, CG, BN, BMODE>(M, N, K, A, lda, B, ldb, C, ldc,
+                                                    epi.active ? epi.out : GEMM_OUT_F32, plan.tma_store != 0, &ta,
+                                                    &tb, &tc);
+    if (r == CUDA_SUCCESS && plan.tail_tiles > 0) {
+        if (!W) {
+            std::snprintf(err, errlen, "split tail without a workspace");
+            return GEMM_ERR_INVALID_ARG;
+        }
+        r = encode_3d_slabs(&tw, W, BN, kBM * CG, (int64_t)plan.tail_tiles * plan.splits);
+    }
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return GEMM_ERR_CUDA;
+    }
+    TcParams p = base_params(plan, epi, timeout_ms);
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = (M + kBM * CG - 1) / (kBM * CG);
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.num_kb = (K + Cf::BK - 1) / Cf::BK;
+    p.tail_tiles = plan.tail_tiles;
+    p.full_tiles = p.num_tiles - p.tail_tiles;
+    p.splits = p.tail_tiles > 0 ? plan.splits : 1;
+    p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
+    p.num_units = p.full_tiles + p.tail_tiles * p.splits;
+    p.C = C;
+    p.ldc = ldc;
+    return launch_kernel<DT, CG, BN, BMODE>(plan, ta, tb, tc, tw, p, stream, err, errlen);
+}
+
+// One group's descriptor fields that depend on the variant (maps, tile counts).
+template <int DT, int CG, int BN, int BMODE>
+int encode_group_variant(GroupDesc *d, const void *A, int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
+                         int out, int M, int N, int K, char *err, size_t errlen) {
+    using Cf = TcCfg<DT, CG, BN, BMODE>;
+    const CUresult r = encode_operands<DT, CG, BN, BMODE>(M, N, K, A, lda, B, ldb, C, ldc, out, d->tma_store != 0,
+                                                          &d->tmA, &d->tmB, &d->tmC);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(err, errlen, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return GEMM_ERR_CUDA;
+    }
+    d->M = M;
+    d->N = N;
+    d->num_kb = (K + Cf::BK - 1) / Cf::BK;
+    d->tiles_m = (M + kBM * CG - 1) / (kBM * CG);
+    d->tiles_n = (N + BN - 1) / BN;
+    return GEMM_OK;
+}
+
+template <int DT, int CG, int BN, int BMODE>
+int launch_grouped_variant(const gemm_plan_t &plan, const GroupDesc *groups, int group_count, int num_units,
+                           const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream, char *err, size_t errlen) {
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof unused);
+    TcParams p = base_params(plan, epi, timeout_ms);
+    p.num_units = num_units;
+    p.full_tiles = num_units;
+    p.groups = groups;
+    p.group_count = group_count;
+    return launch_kernel<DT, CG, BN, BMODE>(plan, unused, unused, unused, unused, p, stream, err, errlen);
+}
+
 // A (dtype, CTA group, BN, B mode) combination is compiled only if it is legal:
 // TF32 always reads the K-major copy of B, and B read as stored needs every
 // CTA's share of the tile width to be whole 128-byte column chunks.
@@ -697,18 +831,6 @@ int variant_value(bool stages) {
     }
 }
 
-template <int DT, int CG, int BN, int BMODE>
-int launch_if_ok(const gemm_plan_t &plan, int M, int N, int K, const void *A, int64_t lda, const void *B,
-                 int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
-                 cudaStream_t stream, char *err, size_t errlen) {
-    if constexpr (variant_ok<DT, CG, BN, BMODE>()) {
-        return launch_variant<DT, CG, BN, BMODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, epi, timeout_ms, stream,
-                                                   err, errlen);
-    } else {
-        std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, BMODE);
-        return GEMM_ERR_UNSUPPORTED;
-    }
-}
 
 }  // namespace
 
@@ -746,38 +868,86 @@ int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
 
 int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(dtype, cta_group, bn, b_kmajor, true); }
 
-int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
-              int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
-              cudaStream_t stream, char *err, size_t errlen) {
-#define TC_LAUNCH(DT_, MODE_, CG_, BN_) \
-    launch_if_ok<DT_, CG_, BN_, MODE_>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, epi, timeout_ms, stream, err, errlen)
-#define X(cg, bn_)                                                                                      \
-    if (plan.cta_group == cg && plan.bn == bn_) {                                                        \
-        if (dtype == GEMM_TF32) {                                                                        \
-            if (plan.b_kmajor != kBKMajor) break;                                                        \
-            return TC_LAUNCH(kDtTF32, kBKMajor, cg, bn_);                                                \
-        }                                                                                                \
-        if (dtype == GEMM_FP16)                                                                          \
-            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtFP16, kBKMajor, cg, bn_)                     \
-                                             : TC_LAUNCH(kDtFP16, kBNMajor, cg, bn_);                    \
-        if (dtype == GEMM_E4M3)                                                                          \
-            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtE4M3, kBKMajor, cg, bn_)                     \
-                                             : TC_LAUNCH(kDtE4M3, kBNMajor, cg, bn_);                    \
-        if (dtype == GEMM_E5M2)                                                                          \
-            return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtE5M2, kBKMajor, cg, bn_)                     \
-                                             : TC_LAUNCH(kDtE5M2, kBNMajor, cg, bn_);                    \
-        return plan.b_kmajor == kBKMajor ? TC_LAUNCH(kDtBF16, kBKMajor, cg, bn_)                         \
-                                         : TC_LAUNCH(kDtBF16, kBNMajor, cg, bn_);                        \
+// Calls f(dt, cg, bn, mode) -- each an std::integral_constant -- for the
+// variant the plan names; f returns a gemm_status_t.
+template <class F>
+static int dispatch_variant(const gemm_plan_t &plan, int dtype, F &&f, char *err, size_t errlen) {
+    using std::integral_constant;
+#define TC_CALL(DT_, MODE_, CG_, BN_) \
+    f(integral_constant<int, DT_>{}, integral_constant<int, CG_>{}, integral_constant<int, BN_>{}, \
+      integral_constant<int, MODE_>{})
+#define X(cg, bn_)                                                                                       \
+    if (plan.cta_group == cg && plan.bn == bn_) {                                                         \
+        if (dtype == GEMM_TF32) {                                                                         \
+            if (plan.b_kmajor != kBKMajor) break;                                                         \
+            return TC_CALL(kDtTF32, kBKMajor, cg, bn_);                                                   \
+        }                                                                                                 \
+        if (dtype == GEMM_FP16)                                                                           \
+            return plan.b_kmajor == kBKMajor ? TC_CALL(kDtFP16, kBKMajor, cg, bn_)                        \
+                                             : TC_CALL(kDtFP16, kBNMajor, cg, bn_);                       \
+        if (dtype == GEMM_E4M3)                                                                           \
+            return plan.b_kmajor == kBKMajor ? TC_CALL(kDtE4M3, kBKMajor, cg, bn_)                        \
+                                             : TC_CALL(kDtE4M3, kBNMajor, cg, bn_);                       \
+        if (dtype == GEMM_E5M2)                                                                           \
+            return plan.b_kmajor == kBKMajor ? TC_CALL(kDtE5M2, kBKMajor, cg, bn_)                        \
+                                             : TC_CALL(kDtE5M2, kBNMajor, cg, bn_);                       \
+        return plan.b_kmajor == kBKMajor ? TC_CALL(kDtBF16, kBKMajor, cg, bn_)                            \
+                                         : TC_CALL(kDtBF16, kBNMajor, cg, bn_);                           \
     }
     do {
         TC_VARIANTS(X)
     } while (0);
 #undef X
-#undef TC_LAUNCH
+#undef TC_CALL
     std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", plan.cta_group, plan.bn,
                   plan.b_kmajor);
     return GEMM_ERR_UNSUPPORTED;
 }
+
+#define TC_IF_COMPILED(...)                                                                               \
+    constexpr int DT = decltype(dt)::value, CG = decltype(cg)::value, BN = decltype(bn)::value,         \
+                  MODE = decltype(mode)::value;                                                           \
+    if constexpr (variant_ok<DT, CG, BN, MODE>()) {                                                       \
+        __VA_ARGS__;                                                                                      \
+    } else {                                                                                              \
+        std::snprintf(err, errlen, "no tensor-core variant for cta_group=%d bn=%d b_kmajor=%d", CG, BN, MODE); \
+        return GEMM_ERR_UNSUPPORTED;                                                                      \
+    }
+
+int tc_launch(const gemm_plan_t &plan, int dtype, int M, int N, int K, const void *A, int64_t lda, const void *B,
+              int64_t ldb, void *C, int64_t ldc, float *W, const EpiParams &epi, uint32_t timeout_ms,
+              cudaStream_t stream, char *err, size_t errlen) {
+    return dispatch_variant(
+        plan, dtype,
+        [&](auto dt, auto cg, auto bn, auto mode) -> int {
+            TC_IF_COMPILED(return launch_variant<DT, CG, BN, MODE>(plan, M, N, K, A, lda, B, ldb, C, ldc, W, epi,
+                                                                   timeout_ms, stream, err, errlen))
+        },
+        err, errlen);
+}
+
+int tc_encode_group(const gemm_plan_t &plan, int dtype, GroupDesc *d, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, void *C, int64_t ldc, int out, int M, int N, int K, char *err, size_t errlen) {
+    return dispatch_variant(
+        plan, dtype,
+        [&](auto dt, auto cg, auto bn, auto mode) -> int {
+            TC_IF_COMPILED(return encode_group_variant<DT, CG, BN, MODE>(d, A, lda, B, ldb, C, ldc, out, M, N, K,
+                                                                         err, errlen))
+        },
+        err, errlen);
+}
+
+int tc_launch_grouped(const gemm_plan_t &plan, int dtype, const GroupDesc *groups, int group_count, int num_units,
+                      const EpiParams &epi, uint32_t timeout_ms, cudaStream_t stream, char *err, size_t errlen) {
+    return dispatch_variant(
+        plan, dtype,
+        [&](auto dt, auto cg, auto bn, auto mode) -> int {
+            TC_IF_COMPILED(return launch_grouped_variant<DT, CG, BN, MODE>(plan, groups, group_count, num_units, epi,
+                                                                           timeout_ms, stream, err, errlen))
+        },
+        err, errlen);
+}
+#undef TC_IF_COMPILED
 
 cudaError_t tc_read_and_clear_status(uint32_t words[4]) {
     cudaError_t e = cudaMemcpyFromSymbol(words, g_tc_status, sizeof(uint32_t) * 4);

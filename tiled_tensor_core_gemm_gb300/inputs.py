@@ -63,6 +63,45 @@ C5_BF16_RAGGED = tuple(
 )
 
 
+@dataclass(frozen=True)
+class GroupedWorkload:
+    """A batch of independent GEMMs C_g = A_g . B_g (M_g x K times K x N)."""
+    name: str
+    Ms: tuple
+    N: int
+    K: int
+    dtype: str
+    dist: str
+    seed: int
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * sum(self.Ms) * self.N * self.K
+
+
+def skewed_group_rows(total: int, groups: int, seed: int, sigma: float = 0.75) -> tuple:
+    """Row counts of `groups` GEMMs summing to `total`: shares proportional to
+    seeded lognormal(0, sigma) weights (the uneven token counts a batch of
+    experts sees), floored, the remainder added to the largest."""
+    rng = np.random.default_rng(seed)
+    w = rng.lognormal(0.0, sigma, groups)
+    Ms = np.floor(total * w / w.sum()).astype(np.int64)
+    Ms[int(np.argmax(Ms))] += total - int(Ms.sum())
+    return tuple(int(m) for m in Ms)
+
+
+# 16 GEMMs of skewed row counts (32768 rows in all) against their own
+# 4096 x 4096 B: the same 1.1 TFLOP as the 8192^3 GEMM, as one grouped launch.
+GROUPED_BF16 = GroupedWorkload("grouped bf16 16 groups, sum M = 32768, N = K = 4096, lognormal(0, 0.75) row "
+                               "shares, N(0,1), seed 10", skewed_group_rows(32768, 16, 10), 4096, 4096, "bf16",
+                               "normal", 10)
+
+
+def grouped_operands(w: GroupedWorkload):
+    """[(A_g, B_g)]: group g drawn by make_operands with seed w.seed + g."""
+    return [make_operands(m, w.N, w.K, w.dtype, w.dist, w.seed + g) for g, m in enumerate(w.Ms)]
+
+
 def _draw(gen: torch.Generator, shape, dist: str, lo_hi: int = 8) -> torch.Tensor:
     if dist == "uniform":
         return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
