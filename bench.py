@@ -266,6 +266,21 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
             "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K}
 
 
+class with_option:
+    """Sets a library option for the duration of a block, then restores it."""
+
+    def __init__(self, tg, key, value):
+        self.tg, self.key, self.value = tg, key, value
+
+    def __enter__(self):
+        self.old = self.tg.gemm_get_option(self.key)
+        if self.tg.gemm_set_option(self.key, self.value) != self.tg.GEMM_OK:
+            raise RuntimeError(self.tg.gemm_last_error())
+
+    def __exit__(self, *exc):
+        self.tg.gemm_set_option(self.key, self.old)
+
+
 def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False):
     """A grouped workload through gemm_run_grouped (one launch per step), or the
     same GEMMs through one gemm_run each; CUDA events around all steps."""
@@ -527,14 +542,32 @@ def run_ours(args):
                           "tflops": round(tf, 2), "steps": n_side,
                           "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
                           "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
-        # the skewed 16-group workload: one grouped launch, and the same GEMMs one by one
-        from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16
-        for key, obo in (("grouped_bf16_16", False), ("grouped_bf16_16_one_by_one", True)):
-            r = time_grouped(tg, GROUPED_BF16, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
-            rl = roofline_for_dtype("bf16", GROUPED_BF16.flops, r["ms"], peaks, peak_src, None)
-            paths[key] = {"workload": GROUPED_BF16.name + (", as 16 gemm_run calls" if obo else
-                                                           ", one gemm_run_grouped launch"),
-                          "group_rows": list(GROUPED_BF16.Ms), "tflops": round(r["tflops"], 2), "steps": n_side,
+        # the headline shape under the dynamic schedule (Cluster Launch Control)
+        with with_option(tg, "tc_sched", 2):
+            r = time_gemm(tg, w, n_side, max(3, min(args.warmup, 10)), stream, device)
+        paths["bf16_8192_dynamic_schedule"] = {
+            "workload": w.name + ", Cluster Launch Control schedule", "steps": n_side,
+            "tflops": round(r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12, 2),
+            "kernel_ms_mean": round(r["launch_ms_mean"], 4), "plan": r["plan"],
+            "roofline": roofline_for_dtype("bf16", r["flops"], r["launch_ms_mean"], peaks, peak_src, None)}
+        # the skewed 16-group workload: one grouped launch (static and dynamic
+        # schedule), and the same GEMMs one by one
+        from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16, GROUPED_BF16_SKEWK
+        # (tc_sched: 1 static, 2 dynamic)
+        for key, gw, obo, sched in (("grouped_bf16_16", GROUPED_BF16, False, 1),
+                                    ("grouped_bf16_16_dynamic_schedule", GROUPED_BF16, False, 2),
+                                    ("grouped_bf16_16_one_by_one", GROUPED_BF16, True, 1),
+                                    ("grouped_bf16_16_skewed_k_static_schedule", GROUPED_BF16_SKEWK, False, 1),
+                                    ("grouped_bf16_16_skewed_k", GROUPED_BF16_SKEWK, False, 0)):
+            with with_option(tg, "tc_sched", sched):
+                r = time_grouped(tg, gw, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
+            rl = roofline_for_dtype("bf16", gw.flops, r["ms"], peaks, peak_src, None)
+            paths[key] = {"workload": gw.name + (", as 16 gemm_run calls" if obo else
+                                                 ", one gemm_run_grouped launch") +
+                                      {0: ", automatic schedule (dynamic: K differs by 2x or more)", 1: "",
+                                       2: ", Cluster Launch Control schedule"}[sched],
+                          "group_rows": list(gw.Ms), "group_k": [gw.k_of(g) for g in range(len(gw.Ms))],
+                          "tflops": round(r["tflops"], 2), "steps": n_side,
                           "ms_per_step": round(r["ms"], 4), "launches_per_step": r["launches_per_step"],
                           "l2": "inputs larger than L2", "roofline": rl}
         out["paths"] = paths

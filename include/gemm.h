@@ -212,7 +212,14 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    pairs use 256)
  *   "tc_cta_group"   force 1- or 2-CTA tiles (1, 2)
  *   "tc_group_m"     raster group height in tiles (>= 1)
- *   "tc_max_ctas"    cap on persistent CTAs (>= 1)
+ *   "tc_max_ctas"    cap on persistent CTAs (>= 1; static schedule only)
+ *   "tc_sched"       tensor-core work schedule: 1 static persistent (each
+ *                    CTA or pair strides over the work units), 2 dynamic
+ *                    ("Learn CuTeDSL" section 8.2, Cluster Launch Control:
+ *                    one cluster per unit is launched and the running ones
+ *                    steal the units of clusters that have not started);
+ *                    0 auto: static, except grouped launches whose groups'
+ *                    K differ by 2x or more (units of unequal cost)
  *   "tc_splits"      force split-K: K ranges for every output tile (1..32);
  *                    the partial tiles go to a workspace and are summed into
  *                    C in a fixed order by a second kernel
@@ -225,10 +232,12 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    outputs per thread; 2 = same with K step 16; 3 = 128x256,
  *                    8x16 per thread; 4 = 256x128, 16x8 per thread; 5 = 64x64;
  *                    6 = 128x256 with K step 16; 7 = 64x64 with K step 16
- *   "tc_b_major"     0 auto (BF16: B read as stored, N-major; TF32: B read
- *                    from a K-major transposed copy), 1 force the transposed
- *                    copy, 2 force reading B as stored (BF16 only; a TF32
- *                    call then fails with GEMM_ERR_UNSUPPORTED)
+ *   "tc_b_major"     0 auto (BF16, FP16, FP8: B read as stored, N-major, except
+ *                    FP8 tiles of 64 columns per CTA; TF32: B read from a
+ *                    K-major transposed copy), 1 force the transposed copy,
+ *                    2 force reading B as stored (a TF32 call, or an FP8 call
+ *                    with 64 columns per CTA, then fails with
+ *                    GEMM_ERR_UNSUPPORTED)
  *   "wait_timeout_ms" bound on every in-kernel wait (default 2000)
  *   "debug_stall_mma" test hook: 1 makes the tensor-core kernel's MMA thread
  *                    first wait on a barrier nothing arrives at, so the wait
@@ -258,6 +267,9 @@ typedef struct {
     int32_t splits;      /* K ranges per split tile; 1 = no tile split       */
     int32_t tail_tiles;  /* tiles split into K ranges (the last ones in the
                             schedule; all tiles under full split-K)       */
+    int32_t sched;       /* 0: static persistent stride over work units;
+                            1: Cluster Launch Control (one cluster per unit
+                            launched, running CTAs steal the rest)         */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

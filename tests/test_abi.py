@@ -83,6 +83,20 @@ def test_options_roundtrip_and_validation():
     assert tg.gemm_get_option("wait_timeout_ms") == 2000
     assert tg.gemm_get_option("debug_stall_mma") == 0
     assert tg.gemm_set_option("debug_stall_mma", 2) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_get_option("tc_sched") == 0
+    assert tg.gemm_set_option("tc_sched", 3) == tg.GEMM_ERR_INVALID_ARG
+
+
+def test_plan_dynamic_schedule_launches_one_cluster_per_unit():
+    try:
+        assert tg.gemm_set_option("tc_sched", 2) == tg.GEMM_OK
+        p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+        assert p["sched"] == 1 and p["cta_group"] == 2 and p["grid"] == 2 * p["tiles"] == 2048
+        q = _plan(128, 8192, 8192, tg.GEMM_BF16)          # split-K units count too
+        assert q["grid"] == q["tiles"] * q["splits"]
+    finally:
+        tg.gemm_set_option("tc_sched", 0)
+    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["sched"] == 0
 
 
 def _plan(M, N, K, dt, lda=None, ldb=None, ldc=None, a=0, b=0, c=0, sms=152):

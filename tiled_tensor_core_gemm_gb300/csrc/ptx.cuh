@@ -195,6 +195,37 @@ __device__ __forceinline__ void fence_tensormap_acquire(const void *map) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 
+// Cluster Launch Control ("Learn CuTeDSL" section 8.2): ask the hardware to
+// cancel a cluster of this grid that has not started yet; the 16-byte
+// response lands at `resp` and completes 16 transaction bytes on `bar` (in
+// every CTA of the cluster with the multicast form).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+                 ::"r"(resp), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                 ".multicast::cluster::all.b128 [%0], [%1];"
+                 ::"r"(resp), "r"(bar) : "memory");
+}
+
+// Decodes a response: 1 and the x index of the cancelled cluster's first CTA,
+// or 0 when no cluster was left to cancel.
+__device__ __forceinline__ uint32_t clc_query(uint32_t resp, uint32_t &first_x) {
+    uint32_t ok = 0, x = 0;
+    asm volatile("{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+                 "ld.shared.b128 r, [%2];\n\t"
+                 "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t"
+                 "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+                 : "=r"(ok), "+r"(x)
+                 : "r"(resp)
+                 : "memory");
+    first_x = x;
+    return ok;
+}
+
 // MMA kinds: 16-bit inputs, TF32 inputs, 8-bit (FP8) inputs.
 enum MmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 

@@ -59,7 +59,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;         // 32 rows x 32 fp32, 128-byte swizzled
 constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
 constexpr int kSmemBudget = 232448;            // 227 KB opt-in dynamic shared memory
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
+constexpr int kUQ = 4;                         // unit-queue slots (dynamic schedule)
 
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
@@ -110,7 +111,7 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
-    static_assert((2 * STAGES + 5 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
+    static_assert((2 * STAGES + 29) * 8 <= kBarBytes, "barrier area too small");
     static_assert(!(TF32 && BMODE == kBNMajor), "TF32 reads B from the K-major copy");
 };
 
@@ -131,6 +132,7 @@ struct TcParams {
     EpiParams epi;                     // fused epilogue
     const GroupDesc *groups;           // grouped launch: per-group sizes, maps and C (nullptr: one GEMM)
     int group_count;
+    int sched;                         // 0: static stride over units; 1: Cluster Launch Control
     unsigned long long timeout_ns;
 };
 
@@ -254,8 +256,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *stages = smem;
     uint8_t *epi = smem + Cf::STAGES * Cf::STAGE_BYTES;
+    // Barrier area, in 8-byte words: full[S], empty[S], acc_full[2], acc_empty[2],
+    // never, old_c[8], unit queue full[4] / empty[4], clc_full, clc_used, pad,
+    // CLC response (2 words), unit queue (2 words), TMEM slot + abort flag.
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi + kEpiBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cf::STAGES + 5 + 2 * kEpiWarps);
+    constexpr int kW = 2 * Cf::STAGES;
+    uint8_t *clc_resp = reinterpret_cast<uint8_t *>(bars + kW + 24);          // 16-byte aligned
+    volatile int *unit_q = reinterpret_cast<volatile int *>(bars + kW + 26);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kW + 28);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -265,7 +273,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto acce_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 2 + a); };
     const uint32_t never_bar = bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 4);   // never arrived at
     // old-C loads of the residual epilogue: one barrier per staging buffer
-    auto oldc_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * Cf::STAGES + 5 + i); };
+    auto oldc_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kW + 5 + i); };
+    // dynamic schedule: unit queue slots (producer -> MMA, epilogue) and the CLC response
+    auto uq_full = [&](int i) { return bar0 + 8u * (uint32_t)(kW + 13 + i); };
+    auto uq_empty = [&](int i) { return bar0 + 8u * (uint32_t)(kW + 17 + i); };
+    const uint32_t clc_full = bar0 + 8u * (uint32_t)(kW + 21);
+    const uint32_t clc_used = bar0 + 8u * (uint32_t)(kW + 22);   // leader: both CTAs read the response
+    const bool dyn = p.sched != 0;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
@@ -282,6 +296,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         ptx::mbar_init(never_bar, 1);
         for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(oldc_bar(i), 1);
+        for (int i = 0; i < kUQ; ++i) {
+            ptx::mbar_init(uq_full(i), 1);
+            // consumers: the MMA thread (leader CTA only) and each epilogue warp
+            ptx::mbar_init(uq_empty(i), (rank == 0 ? 1 : 0) + kEpiWarps);
+        }
+        ptx::mbar_init(clc_full, 1);
+        ptx::mbar_init(clc_used, CG);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -307,7 +328,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             bool ok = true;
             int last_group = -1;
-            for (int t = unit; ok && t < p.num_units; t += nunits) {
+            // All k-blocks of unit t into the ring; false once a wait expired.
+            auto load_unit = [&](int t) -> bool {
                 const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
                 if (U.group != last_group) {
                     // a group's maps were copied in before the launch: acquire them for TMA
@@ -322,8 +344,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kb = U.kb0; kb < U.kb1; ++kb) {
                     if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleProducer, t, abort_flag);
-                        ok = false;
-                        break;
+                        return false;
                     }
                     const uint32_t fb = full_bar(stage);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)(Cf::STAGE_BYTES * CG));
@@ -353,6 +374,73 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
                 }
+                return true;
+            };
+            if (!dyn) {
+                // static persistent schedule: every unit'th unit, striding by the grid
+                for (int t = unit; ok && t < p.num_units; t += nunits) ok = load_unit(t);
+            } else {
+                // Cluster Launch Control: start on this cluster's own unit, then
+                // steal the units of clusters that have not started yet.  Each
+                // unit (and finally -1) is published to the MMA thread and the
+                // epilogue warps through the unit queue.  In a CTA pair the
+                // leader asks, the response reaches both CTAs, and the leader
+                // asks again only once both have read the previous one.
+                int t = unit;
+                int qslot = 0;
+                uint32_t qphase = 0, clc_phase = 0, used_phase = 0;
+                bool more = true, asked_before = false;
+                const uint32_t resp = ptx::smem_addr(clc_resp);
+                while (ok) {
+                    if (!wait_bar<false>(uq_empty(qslot), qphase ^ 1u, abort_flag, p.timeout_ns)) {
+                        record_failure(kRoleProducer, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    unit_q[qslot] = t;
+                    ptx::mbar_arrive(uq_full(qslot));
+                    if (++qslot == kUQ) { qslot = 0; qphase ^= 1u; }
+                    if (t < 0) break;
+                    if (more) {
+                        // ask for the next unit while this one loads
+                        ptx::mbar_arrive_expect_tx(clc_full, 16u);
+                        if (rank == 0) {
+                            if (kPair && asked_before) {
+                                if (!wait_bar<kPair>(clc_used, used_phase, abort_flag, p.timeout_ns)) {
+                                    record_failure(kRoleProducer, t, abort_flag);
+                                    ok = false;
+                                    break;
+                                }
+                                used_phase ^= 1u;
+                            }
+                            ptx::fence_proxy_async_smem();   // our read of the last response before the next write
+                            if (kPair) ptx::clc_try_cancel_multicast(resp, clc_full);
+                            else ptx::clc_try_cancel(resp, clc_full);
+                        }
+                        asked_before = true;
+                    }
+                    ok = load_unit(t);
+                    if (!ok) break;
+                    if (!more) {
+                        t = -1;
+                        continue;
+                    }
+                    if (!wait_bar<kPair>(clc_full, clc_phase, abort_flag, p.timeout_ns)) {
+                        record_failure(kRoleProducer, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    clc_phase ^= 1u;
+                    uint32_t first_x = 0;
+                    const bool got = ptx::clc_query(resp, first_x) != 0;
+                    if (kPair) ptx::mbar_arrive_cluster(ptx::mapa_shared(clc_used, 0));
+                    if (got && (int)(first_x / CG) < p.num_units) {
+                        t = (int)(first_x / CG);
+                    } else {
+                        t = -1;                  // nothing left to steal: every unit has its cluster
+                        more = false;
+                    }
+                }
             }
             // Drain: wait until the MMAs have released every slot, so that no
             // tensor-core read of this CTA's shared memory and no commit
@@ -378,7 +466,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 record_failure(kRoleMma, unit, abort_flag);
                 ok = false;
             }
-            for (int t = unit; ok && t < p.num_units; t += nunits) {
+            // The unit sequence: the static stride, or the producer's unit queue.
+            int qslot = 0;
+            uint32_t qphase = 0;
+            auto next_unit = [&](int t, int &out) -> bool {
+                if (!dyn) {
+                    out = (t < 0 ? unit : t + nunits);
+                    if (out >= p.num_units) out = -1;
+                    return true;
+                }
+                if (!wait_bar<false>(uq_full(qslot), qphase, abort_flag, p.timeout_ns)) return false;
+                out = unit_q[qslot];
+                ptx::mbar_arrive(uq_empty(qslot));
+                if (++qslot == kUQ) { qslot = 0; qphase ^= 1u; }
+                return true;
+            };
+            int t = -1;
+            if (ok && !next_unit(-1, t)) {
+                record_failure(kRoleMma, unit, abort_flag);
+                ok = false;
+            }
+            while (ok && t >= 0) {
                 const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
                 const int kb0 = U.kb0, kb1 = U.kb1;
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -417,6 +525,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 else ptx::mma_commit(accf_bar(acc));
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
+                if (!next_unit(t, t)) {
+                    record_failure(kRoleMma, t, abort_flag);
+                    break;
+                }
             }
         }
         __syncwarp();
@@ -438,7 +550,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t old_phase = 0;              // parity of each buffer's old-C barrier
         bool ok = true;
         int last_group = -1;
-        for (int t = unit; ok && t < p.num_units; t += nunits) {
+        // The unit sequence: the static stride, or the producer's unit queue
+        // (every lane waits, lane 0 frees the slot).
+        int qslot = 0;
+        uint32_t qphase = 0;
+        auto next_unit = [&](int t, int &out) -> bool {
+            if (!dyn) {
+                out = (t < 0 ? unit : t + nunits);
+                if (out >= p.num_units) out = -1;
+                return true;
+            }
+            const bool got = wait_bar<false>(uq_full(qslot), qphase, abort_flag, p.timeout_ns);
+            if (!__all_sync(0xffffffffu, got)) return false;
+            out = unit_q[qslot];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(uq_empty(qslot));
+            if (++qslot == kUQ) { qslot = 0; qphase ^= 1u; }
+            return true;
+        };
+        int t = -1;
+        if (!next_unit(-1, t)) {
+            if (lane == 0) record_failure(kRoleEpilogue, unit, abort_flag);
+            ok = false;
+        }
+        while (ok && t >= 0) {
             const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
             const int slab = U.slab;
             const int m0 = U.tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
@@ -613,6 +748,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
+            if (ok && !next_unit(t, t)) {
+                if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                break;
+            }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
         __syncwarp();
@@ -738,6 +877,7 @@ TcParams base_params(const gemm_plan_t &plan, const EpiParams &epi, uint32_t tim
     p.debug_stall = options_snapshot().debug_stall_mma;
     p.epi = epi;
     p.groups = nullptr;
+    p.sched = plan.sched;
     p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
     return p;
 }

@@ -65,7 +65,8 @@ C5_BF16_RAGGED = tuple(
 
 @dataclass(frozen=True)
 class GroupedWorkload:
-    """A batch of independent GEMMs C_g = A_g . B_g (M_g x K times K x N)."""
+    """A batch of independent GEMMs C_g = A_g . B_g (M_g x K_g times K_g x N);
+    K_g = K unless Ks gives one per group."""
     name: str
     Ms: tuple
     N: int
@@ -73,10 +74,14 @@ class GroupedWorkload:
     dtype: str
     dist: str
     seed: int
+    Ks: tuple = ()
+
+    def k_of(self, g: int) -> int:
+        return self.Ks[g] if self.Ks else self.K
 
     @property
     def flops(self) -> float:
-        return 2.0 * sum(self.Ms) * self.N * self.K
+        return 2.0 * sum(m * self.k_of(g) for g, m in enumerate(self.Ms)) * self.N
 
 
 def skewed_group_rows(total: int, groups: int, seed: int, sigma: float = 0.75) -> tuple:
@@ -97,9 +102,23 @@ GROUPED_BF16 = GroupedWorkload("grouped bf16 16 groups, sum M = 32768, N = K = 4
                                "normal", 10)
 
 
+def skewed_group_depths(groups: int, seed: int, lo: int = 512, hi: int = 8192) -> tuple:
+    """K of each group: log-uniform between lo and hi, rounded to a multiple of 64."""
+    rng = np.random.default_rng(seed)
+    ks = np.exp(rng.uniform(np.log(lo), np.log(hi), groups))
+    return tuple(int(max(64, round(k / 64) * 64)) for k in ks)
+
+
+# The same 16 GEMMs with K differing per group (log-uniform in [512, 8192]):
+# work units of unequal cost, where a dynamic schedule can balance the load.
+GROUPED_BF16_SKEWK = GroupedWorkload("grouped bf16 16 groups, M = 2048, N = 4096, K log-uniform in [512, 8192], "
+                                     "N(0,1), seed 11", (2048,) * 16, 4096, 0, "bf16", "normal", 11,
+                                     skewed_group_depths(16, 11))
+
+
 def grouped_operands(w: GroupedWorkload):
     """[(A_g, B_g)]: group g drawn by make_operands with seed w.seed + g."""
-    return [make_operands(m, w.N, w.K, w.dtype, w.dist, w.seed + g) for g, m in enumerate(w.Ms)]
+    return [make_operands(m, w.N, w.k_of(g), w.dtype, w.dist, w.seed + g) for g, m in enumerate(w.Ms)]
 
 
 def _draw(gen: torch.Generator, shape, dist: str, lo_hi: int = 8) -> torch.Tensor:
