@@ -72,6 +72,10 @@ def parse_args():
                     help="timed workload (default: the headline 8192^3 BF16 GEMM)")
     ap.add_argument("--epilogue", choices=tuple(FUSED_EPILOGUES), default=None,
                     help="time the workload through gemm_run_ex with this fused epilogue")
+    ap.add_argument("--grouped", choices=("equal_k", "skewed_k"), default=None,
+                    help="time a 16-group BF16 grouped launch instead (equal K = 4096, or K log-uniform 512..8192)")
+    ap.add_argument("--option", action="append", default=[], metavar="KEY=VALUE",
+                    help="set a library option (gemm_set_option) for the whole run, e.g. tc_sched=2")
     ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -281,7 +285,8 @@ class with_option:
         self.tg.gemm_set_option(self.key, self.old)
 
 
-def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False):
+def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False, dist=None, on_begin=None,
+                 on_end=None):
     """A grouped workload through gemm_run_grouped (one launch per step), or the
     same GEMMs through one gemm_run each; CUDA events around all steps."""
     import torch
@@ -310,17 +315,27 @@ def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False):
             run()
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
         torch.cuda.synchronize()
+        if on_begin:
+            on_begin()
         e0.record(stream)
         for _ in range(steps):
             run()
         e1.record(stream)
         torch.cuda.synchronize()
+        if on_end:
+            on_end()
+        if dist is not None:
+            dist.barrier()
     st = tg.gemm_get_status(s)
     if st != tg.GEMM_OK:
         raise RuntimeError(f"grouped status {st}: {tg.gemm_last_error()}")
-    ms = e0.elapsed_time(e1) / steps
-    return {"ms": ms, "tflops": workload.flops / (ms * 1e-3) / 1e12,
+    total = e0.elapsed_time(e1)
+    ms = total / steps
+    return {"ms": ms, "tflops": workload.flops / (ms * 1e-3) / 1e12, "total_ms": total, "launch_ms_mean": ms,
+            "launch_ms_median": ms, "launch_ms_min": ms, "flops": workload.flops, "plan": None,
             "launches_per_step": len(pairs) if one_by_one else 1}
 
 
@@ -453,20 +468,28 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     tg.load_library()
+    for kv in args.option:
+        key, _, val = kv.partition("=")
+        if tg.gemm_set_option(key, int(val)) != tg.GEMM_OK:
+            raise SystemExit(f"--option {kv}: {tg.gemm_last_error()}")
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device)
 
-    w = workload_by_key(args.workload)
-    headline = args.workload == "bf16_8192" and not args.epilogue
+    from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16, GROUPED_BF16_SKEWK
+    gw = {"equal_k": GROUPED_BF16, "skewed_k": GROUPED_BF16_SKEWK}.get(args.grouped)
+    w = gw if gw is not None else workload_by_key(args.workload)
+    headline = args.workload == "bf16_8192" and not args.epilogue and gw is None
     sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
     if sampler:
         sampler.start()
     res = None
     try:
-        res = time_gemm(tg, w, args.steps, args.warmup, stream, device, dist,
-                        on_begin=sampler.mark_begin if sampler else None,
-                        on_end=sampler.mark_end if sampler else None,
-                        epi=FUSED_EPILOGUES[args.epilogue] if args.epilogue else None)
+        hooks = dict(on_begin=sampler.mark_begin if sampler else None, on_end=sampler.mark_end if sampler else None)
+        if gw is not None:
+            res = time_grouped(tg, gw, args.steps, args.warmup, stream, device, dist=dist, **hooks)
+        else:
+            res = time_gemm(tg, w, args.steps, args.warmup, stream, device, dist, **hooks,
+                            epi=FUSED_EPILOGUES[args.epilogue] if args.epilogue else None)
     finally:
         clocks = sampler.stop() if sampler else None
 
@@ -480,18 +503,26 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    in_bytes = (w.M * w.K + w.K * w.N) * ELEM_BYTES[w.dtype]
+    if gw is not None:
+        in_bytes = sum((m * gw.k_of(g) + gw.k_of(g) * gw.N) * ELEM_BYTES[gw.dtype] for g, m in enumerate(gw.Ms))
+        shape = {"group_rows": list(gw.Ms), "group_k": [gw.k_of(g) for g in range(len(gw.Ms))], "N": gw.N}
+    else:
+        in_bytes = (w.M * w.K + w.K * w.N) * ELEM_BYTES[w.dtype]
+        shape = {"M": w.M, "N": w.N, "K": w.K}
     desc = {"bf16_8192": "bf16-input GEMM M=N=K=8192, A,B ~ N(0,1) rounded to bf16 (seed 3), fp32 accumulate "
                          "and output, row-major, persistent tcgen05 path",
             "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
                          "accumulate and output, row-major, persistent tcgen05 path",
             "fp32_4096": "fp32 GEMM M=N=K=4096, A,B ~ N(0,1) (seed 2), exact fp32 on the CUDA cores (SIMT)"}
-    desc.setdefault(args.workload, f"{w.name}, row-major, fp32 output")
+    wkey = f"grouped_{args.grouped}" if gw is not None else args.workload
+    desc.setdefault(wkey, f"{w.name}, row-major, fp32 output" +
+                    (", one gemm_run_grouped launch per step" if gw is not None else ""))
     if w.dtype == "fp32":
         sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
         roof = roofline_alu(res["flops"], res["launch_ms_mean"], sm_mhz)
     else:
         roof = roofline_for_dtype(w.dtype, res["flops"], res["launch_ms_mean"], peaks, peak_src,
+                                  None if gw is not None else
                                   profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else "")))
         if w.dtype in ("bf16", "fp16"):
             roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
@@ -499,9 +530,10 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": desc[args.workload] + (f"; fused epilogue {FUSED_EPILOGUES[args.epilogue]} "
-                                                        "through gemm_run_ex" if args.epilogue else ""),
-                   "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}" if world > 1 else "single",
+        "config": {"workload": desc[wkey] + (f"; fused epilogue {FUSED_EPILOGUES[args.epilogue]} "
+                                               "through gemm_run_ex" if args.epilogue else ""),
+                   **shape, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "options": args.option,
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of operands vs 129 MB L2); no flush",
                    "plan": res["plan"]},
         "roofline": roof,
@@ -554,30 +586,30 @@ def run_ours(args):
         # schedule), and the same GEMMs one by one
         from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16, GROUPED_BF16_SKEWK
         # (tc_sched: 1 static, 2 dynamic)
-        for key, gw, obo, sched in (("grouped_bf16_16", GROUPED_BF16, False, 1),
+        for key, gwl, obo, sched in (("grouped_bf16_16", GROUPED_BF16, False, 1),
                                     ("grouped_bf16_16_dynamic_schedule", GROUPED_BF16, False, 2),
                                     ("grouped_bf16_16_one_by_one", GROUPED_BF16, True, 1),
                                     ("grouped_bf16_16_skewed_k_static_schedule", GROUPED_BF16_SKEWK, False, 1),
                                     ("grouped_bf16_16_skewed_k", GROUPED_BF16_SKEWK, False, 0)):
             with with_option(tg, "tc_sched", sched):
-                r = time_grouped(tg, gw, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
-            rl = roofline_for_dtype("bf16", gw.flops, r["ms"], peaks, peak_src, None)
-            paths[key] = {"workload": gw.name + (", as 16 gemm_run calls" if obo else
+                r = time_grouped(tg, gwl, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
+            rl = roofline_for_dtype("bf16", gwl.flops, r["ms"], peaks, peak_src, None)
+            paths[key] = {"workload": gwl.name + (", as 16 gemm_run calls" if obo else
                                                  ", one gemm_run_grouped launch") +
                                       {0: ", automatic schedule (dynamic: K differs by 2x or more)", 1: "",
                                        2: ", Cluster Launch Control schedule"}[sched],
-                          "group_rows": list(gw.Ms), "group_k": [gw.k_of(g) for g in range(len(gw.Ms))],
+                          "group_rows": list(gwl.Ms), "group_k": [gwl.k_of(g) for g in range(len(gwl.Ms))],
                           "tflops": round(r["tflops"], 2), "steps": n_side,
                           "ms_per_step": round(r["ms"], 4), "launches_per_step": r["launches_per_step"],
                           "l2": "inputs larger than L2", "roofline": rl}
         out["paths"] = paths
 
-    if not args.no_e2e:
+    if not args.no_e2e and gw is None:
         ms, h2d, d2h = time_e2e(tg, w, max(3, min(args.steps, 50)), stream, device)
         out["e2e"] = {"value": round(world * 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
                       "how": "pinned host A,B -> device, gemm_run, C -> pinned host, on one stream, CUDA events"}
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and gw is None:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(out), flush=True)
     if dist is not None:
