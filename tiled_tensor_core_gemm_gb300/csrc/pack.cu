@@ -16,6 +16,8 @@
 // Both are HBM-bound: one read and one write of the operand.  The grid is a multiple of
 // the SM count; each warp walks whole rows so both sides stay coalesced even
 // though the source rows start at arbitrary 2- or 4-byte offsets.
+#include <cstring>
+
 #include "epilogue.cuh"
 #include "internal.h"
 #include "tile_order.cuh"
@@ -192,6 +194,9 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
                                                     int tile_rows, int tile_cols, int full_tiles, int tiles_m,
                                                     int tiles_n, int group_m, void *__restrict__ Cv, int64_t ldc,
                                                     int64_t M, int64_t N, const EpiParams epi) {
+    // Launched as a programmatic dependent of the GEMM: wait until the GEMM's
+    // slab writes are complete and visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t quads_per_row = tile_cols / 4;
     const int64_t per_tile = (int64_t)tile_rows * quads_per_row;
     const int64_t total = (int64_t)tail_tiles * per_tile;
@@ -206,14 +211,25 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
         const int64_t m = (int64_t)tm * tile_rows + r, n = (int64_t)tn * tile_cols + c;
         if (m >= M || n >= N) continue;
         const float *w = W + (int64_t)i * slab + (int64_t)r * tile_cols + c;
-        float4 acc = *reinterpret_cast<const float4 *>(w);
-        for (int s = 1; s < splits; ++s) {
-            const float4 v = *reinterpret_cast<const float4 *>(w + (int64_t)s * tail_tiles * slab);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        const int64_t stride = (int64_t)tail_tiles * slab;   // from one split's slab to the next
+        auto ld = [&](int sp) { return __ldcs(reinterpret_cast<const float4 *>(w + sp * stride)); };
+        auto add = [](float4 &a, const float4 &v) {
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        };
+        // Four slabs' loads in flight at a time; the sums still run in split order.
+        float4 acc = ld(0);
+        int sp = 1;
+        for (; sp + 3 < splits; sp += 4) {
+            const float4 v1 = ld(sp), v2 = ld(sp + 1), v3 = ld(sp + 2), v4 = ld(sp + 3);
+            add(acc, v1);
+            add(acc, v2);
+            add(acc, v3);
+            add(acc, v4);
         }
+        for (; sp < splits; ++sp) add(acc, ld(sp));
         if (epi.active) {
             const float v[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
@@ -292,13 +308,23 @@ cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int 
     const int64_t want = (quads + 255) / 256;
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
     const bool vec = (ldc % 4 == 0) && ((uintptr_t)C % 16 == 0);
+    // Programmatic stream serialisation: the launch may overlap the GEMM's
+    // tail; the kernel's griddepcontrol.wait keeps the reads after its writes.
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (vec)
-        split_reduce<true><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                                                        tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
-    else
-        split_reduce<false><<<blocks, 256, 0, stream>>>(W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                                                         tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, split_reduce<true>, W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
+                                  tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
+    return cudaLaunchKernelEx(&cfg, split_reduce<false>, W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
+                              tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
 }
 
 cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, const EpiParams &epi,

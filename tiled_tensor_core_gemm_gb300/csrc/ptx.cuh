@@ -226,6 +226,11 @@ __device__ __forceinline__ uint32_t clc_query(uint32_t resp, uint32_t &first_x) 
     return ok;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream (launched
+// with programmatic stream serialisation) be scheduled before this one ends;
+// it waits in griddepcontrol.wait until this grid's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // MMA kinds: 16-bit inputs, TF32 inputs, 8-bit (FP8) inputs.
 enum MmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 

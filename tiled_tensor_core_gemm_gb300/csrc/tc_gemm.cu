@@ -462,7 +462,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            if (p.debug_stall && !wait_bar<kPair>(never_bar, 0u, abort_flag, p.timeout_ns)) {
+            // Test hook: wait on a barrier nothing arrives at, for half the bound, so
+            // that this wait (and not the producer's, stalled behind it) expires first.
+            if (p.debug_stall && !wait_bar<kPair>(never_bar, 0u, abort_flag, p.timeout_ns / 2)) {
                 record_failure(kRoleMma, unit, abort_flag);
                 ok = false;
             }
@@ -758,6 +760,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 
     // ------------------------------------------------------------ teardown
+    // The split-K reduction (launched next, when tiles were split) may be
+    // scheduled now; it waits for this grid's slab writes before reading them.
+    if (p.tail_tiles > 0 && threadIdx.x == 0) ptx::pdl_launch_dependents();
     ptx::tc_fence_before();
     if (kPair) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
