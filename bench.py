@@ -340,42 +340,68 @@ def time_grouped(tg, workload, steps, warmup, stream, device, one_by_one=False, 
 
 
 def time_e2e(tg, workload, steps, stream, device):
-    """Same GEMM through gemm_run with the operands in pinned host memory: each
-    step copies A and B host->device, runs, and copies C device->host."""
+    """Same GEMM through gemm_run with the operands in pinned host memory: every
+    step copies its A and B host->device, runs the GEMM, and copies C
+    device->host.  Steps are pipelined over three streams with two device
+    buffer sets -- step i's inputs copy in while step i-1 computes and step
+    i-2's C copies out -- the way a serving loop overlaps transfers with
+    compute; events order each buffer's reuse.  Time = first copy-in to last
+    copy-out, divided by the steps."""
     import torch
     from tiled_tensor_core_gemm_gb300.inputs import workload_operands
     A_h, B_h = workload_operands(workload)
     A_h, B_h = A_h.pin_memory(), B_h.pin_memory()
     M, N, K = workload.M, workload.N, workload.K
-    C_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    A = torch.empty_like(A_h, device=device)
-    B = torch.empty_like(B_h, device=device)
-    C = torch.empty((M, N), dtype=torch.float32, device=device)
     code = tg.DTYPES[workload.dtype]
-    s = stream.cuda_stream
+    sets = []
+    for _ in range(2):
+        sets.append({"A": torch.empty_like(A_h, device=device), "B": torch.empty_like(B_h, device=device),
+                     "C": torch.empty((M, N), dtype=torch.float32, device=device),
+                     "C_h": torch.empty((M, N), dtype=torch.float32).pin_memory(),
+                     "in": torch.cuda.Event(), "done": torch.cuda.Event(), "out": torch.cuda.Event(),
+                     "used": False})
+    h2d, comp, d2h = stream, torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    def step():
-        A.copy_(A_h, non_blocking=True)
-        B.copy_(B_h, non_blocking=True)
-        rc = tg.gemm_run(M, N, K, code, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s)
+    def step(i):
+        st = sets[i % 2]
+        with torch.cuda.stream(h2d):
+            if st["used"]:
+                h2d.wait_event(st["done"])              # the GEMM that read this set has finished
+            st["A"].copy_(A_h, non_blocking=True)
+            st["B"].copy_(B_h, non_blocking=True)
+            st["in"].record(h2d)
+        comp.wait_event(st["in"])
+        if st["used"]:
+            comp.wait_event(st["out"])                  # this set's previous C has been copied out
+        rc = tg.gemm_run(M, N, K, code, st["A"].data_ptr(), K, st["B"].data_ptr(), N, st["C"].data_ptr(), N,
+                         comp.cuda_stream)
         if rc != tg.GEMM_OK:
             raise RuntimeError(tg.gemm_last_error())
-        C_h.copy_(C, non_blocking=True)
+        st["done"].record(comp)
+        d2h.wait_event(st["done"])
+        with torch.cuda.stream(d2h):
+            st["C_h"].copy_(st["C"], non_blocking=True)
+            st["out"].record(d2h)
+        st["used"] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(h2d)
+    comp.wait_event(e0)
+    d2h.wait_event(e0)
+    for i in range(steps):
+        step(i)
+    e1.record(d2h)                                      # after the last copy-out, which follows every step
+    torch.cuda.synchronize()
+    st = tg.gemm_get_status(comp.cuda_stream)
+    if st != tg.GEMM_OK:
+        raise RuntimeError(f"e2e status {st}: {tg.gemm_last_error()}")
     ms = e0.elapsed_time(e1) / steps
-    h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()
-    d2h = C_h.numel() * 4
-    return ms, h2d, d2h
+    h2d_b = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()
+    d2h_b = M * N * 4
+    return ms, h2d_b, d2h_b
 
 
 def cpu_baseline(workload, target_s):
@@ -608,7 +634,9 @@ def run_ours(args):
         ms, h2d, d2h = time_e2e(tg, w, max(3, min(args.steps, 50)), stream, device)
         out["e2e"] = {"value": round(world * 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-                      "how": "pinned host A,B -> device, gemm_run, C -> pinned host, on one stream, CUDA events"}
+                      "how": "every step: pinned host A,B -> device, gemm_run, C -> pinned host; steps pipelined "
+                             "over three streams with two device buffer sets (copy-in of step i, GEMM of i-1, "
+                             "copy-out of i-2 overlap); CUDA events from the first copy-in to the last copy-out"}
     if not args.no_cpu_baseline and world == 1 and gw is None:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(out), flush=True)

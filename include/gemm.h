@@ -223,9 +223,10 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_splits"      force split-K: K ranges for every output tile (1..32);
  *                    the partial tiles go to a workspace and are summed into
  *                    C in a fixed order by a second kernel
- *   "tc_tail_splits" 0 or 1 off (default), n >= 2: split the tiles of the
- *                    last, partly idle round of the persistent schedule into
- *                    n K ranges (same workspace and reduction)
+ *   "tc_tail_splits" 0 auto (2 for TF32, off otherwise), 1 off, n >= 2: split
+ *                    the tiles of the last, partly idle round of the
+ *                    persistent schedule into n K ranges (same workspace and
+ *                    reduction)
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
  *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8

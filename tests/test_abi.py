@@ -181,9 +181,15 @@ def test_plan_low_tile_count_splits_k():
 
 
 def test_plan_splits_the_last_round_only_on_request():
-    # off by default (measured: no gain)
+    # off by default for 16- and 8-bit inputs (measured: no gain or a loss) ...
     assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["tail_tiles"] == 0
+    assert _plan(4096, 4096, 4096, tg.GEMM_E4M3)["tail_tiles"] == 0
+    # ... on by default, two K ranges, for TF32 (measured +4% at 4096^3)
+    auto = _plan(4096, 4096, 4096, tg.GEMM_TF32)
+    assert auto["tail_tiles"] == 28 and auto["splits"] == 2
     try:
+        assert tg.gemm_set_option("tc_tail_splits", 1) == 0          # 1: off for every dtype
+        assert _plan(4096, 4096, 4096, tg.GEMM_TF32)["tail_tiles"] == 0
         # 1024 pair tiles over 76 pairs: 13 full rounds and 36 tiles left
         assert tg.gemm_set_option("tc_tail_splits", 2) == 0
         p = _plan(8192, 8192, 8192, tg.GEMM_BF16)

@@ -16,7 +16,7 @@ struct Options {
     int tc_group_m = 0;        // 0 auto
     int tc_max_ctas = 0;       // 0 auto
     int tc_splits = 0;         // 0 auto, else K ranges for every tile (split-K)
-    int tc_tail_splits = 0;    // 0 auto, 1 off, else K ranges for the last round's tiles
+    int tc_tail_splits = 0;    // 0 auto (2 for TF32), 1 off, else K ranges for the last round's tiles
     int tc_sched = 0;          // 0 auto, 1 static persistent, 2 Cluster Launch Control
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
