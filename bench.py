@@ -267,7 +267,7 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
     launches = 1 + plan["pack_a"] + plan["pack_b"] if plan["path"] == 1 else 1
     return {"total_ms": total_ms, "launch_ms_mean": statistics.mean(launch_ms),
             "launch_ms_median": statistics.median(launch_ms), "launch_ms_min": min(launch_ms),
-            "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K}
+            "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K, "C": C}
 
 
 class with_option:
@@ -427,6 +427,31 @@ def cpu_baseline(workload, target_s):
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} of {workload.M} rows of C (each a full {workload.N}x{workload.K} row-panel product), "
                       f"fp64 C loops, {dt:.1f} s"}
+
+
+TOL = {"fp32": 1e-5, "tf32": 2e-3, "bf16": 1e-5, "fp16": 1e-5, "e4m3": 1e-5, "e5m2": 1e-5}
+
+
+def oracle_check(workload, C_dev, nrows=32):
+    """The timed run's C against the oracle on `nrows` rows spread over M (the
+    first and last, the rest seeded): max |C - Cref| / (|A|.|B|) per entry."""
+    import numpy as np
+    import oracle
+    from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array, workload_operands
+    A, B = workload_operands(workload)
+    rng = np.random.default_rng(workload.seed)
+    rows = sorted({0, workload.M - 1, *(int(r) for r in rng.integers(0, workload.M, nrows - 2))})
+    fp8 = workload.dtype if workload.dtype in ("e4m3", "e5m2") else None
+    ref, D = oracle.gemm_rows(as_oracle_array(A), as_oracle_array(B), rows, bf16=workload.dtype == "bf16",
+                              fp16=workload.dtype == "fp16", fp8=fp8, with_scale=True)
+    got = C_dev[rows].double().cpu().numpy()
+    finite = bool(np.all(np.isfinite(got)))
+    zero = D == 0
+    exact_zero = bool(np.all(got[zero] == ref[zero]))
+    r = float(np.max(np.abs(got[~zero] - ref[~zero]) / D[~zero])) if np.any(~zero) else 0.0
+    tol = TOL[workload.dtype]
+    return {"rows": len(rows), "max_err_ratio": r, "tol": tol, "ok": finite and exact_zero and r <= tol,
+            "what": "the timed run's C on sampled rows against the fp64 oracle, max |C - Cref| / (|A|.|B|)"}
 
 
 def slowest_rank_ms(total_ms: float, dist=None, device="cpu") -> float:
@@ -639,6 +664,8 @@ def run_ours(args):
                              "copy-out of i-2 overlap); CUDA events from the first copy-in to the last copy-out"}
     if not args.no_cpu_baseline and world == 1 and gw is None:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        if not args.epilogue:
+            out["parity"] = oracle_check(w, res["C"])
     print(json.dumps(out), flush=True)
     if dist is not None:
         dist.barrier()

@@ -31,6 +31,7 @@ def test_headline_line_has_every_contract_key():
     assert d["e2e"]["h2d_bytes_per_step"] == 2 * 8192 * 8192 * 2 and d["e2e"]["d2h_bytes_per_step"] == 8192 * 8192 * 4
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert d["gpu_launches"] == 3 and d["config"]["workload"]
+    assert d["parity"]["ok"] and d["parity"]["rows"] >= 8 and d["parity"]["max_err_ratio"] <= 1e-5
 
 
 def test_grouped_line():
