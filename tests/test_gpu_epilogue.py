@@ -21,7 +21,7 @@ from gemm_check import (epilogue_check, oracle_c_old, oracle_full, oracle_rows, 
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ("fp32", "tf32", "bf16", "fp16")
+DTYPES = ("fp32", "tf32", "bf16", "fp16", "e4m3", "e5m2")
 OUTS = ("f32", "bf16", "f16")
 ACTS = ("none", "relu", "gelu")
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
@@ -97,7 +97,7 @@ def test_small_integers_bit_exact_through_epilogue(dtype, out):
 @pytest.mark.parametrize("store", ("tma", "plain"))
 @pytest.mark.parametrize("out", ("f32", "bf16", "f16"))
 @pytest.mark.parametrize("cg,bn", [(1, 64), (1, 128), (1, 256), (2, 256)])
-@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16"))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16", "e4m3"))
 def test_epilogue_every_tensor_core_variant(dtype, cg, bn, out, store):
     """Every compiled tile with the epilogue in registers ahead of a TMA store
     (old C loaded by TMA) and on the lane = column plain-store path."""
@@ -109,7 +109,7 @@ def test_epilogue_every_tensor_core_variant(dtype, cg, bn, out, store):
 
 
 @pytest.mark.parametrize("splits,tail", [(3, 0), (0, 2)])
-@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16"))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16", "e5m2"))
 def test_epilogue_after_split_k_reduction(dtype, splits, tail):
     if splits:
         tg.gemm_set_option("tc_splits", splits)
