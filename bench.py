@@ -202,8 +202,13 @@ def make_device_operands(workload, device):
 
 
 def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=None, on_end=None, epi=None):
-    """Device-side timing with CUDA events on `stream`: per-launch events for the
-    kernel's average duration, and one pair around all K steps.
+    """Device-side timing with CUDA events on `stream`: one pair around all K
+    steps, launched back to back as a user would (consecutive tensor-core
+    launches overlap their set-up through programmatic dependent launch), so
+    the average launch duration is that time / K; then a short pass with an
+    event pair around each launch for the spread of single-launch times (an
+    event between launches keeps them from overlapping, so these run a little
+    longer).
 
     epi: None (gemm_run, FP32 C) or a fused epilogue for gemm_run_ex, as a dict
     with keys act, out, bias (bool), alpha, beta (seeded old C and bias)."""
@@ -241,7 +246,6 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
         st = tg.gemm_get_status(s)
         if st != tg.GEMM_OK:
             raise RuntimeError(f"warm-up status {st}: {tg.gemm_last_error()}")
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
@@ -249,25 +253,33 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
         if on_begin:
             on_begin()
         e0.record(stream)
-        for a, b in ev:
-            a.record(stream)
+        for _ in range(steps):
             run()
-            b.record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
         if on_end:
             on_end()
         if dist is not None:
             dist.barrier()
-    total_ms = e0.elapsed_time(e1)
+        total_ms = e0.elapsed_time(e1)
+        st = tg.gemm_get_status(s)
+        if st != tg.GEMM_OK:
+            raise RuntimeError(f"timed-region status {st}: {tg.gemm_last_error()}")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(min(steps, 30))]
+        for a, b in ev:
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    st = tg.gemm_get_status(s)
-    if st != tg.GEMM_OK:
-        raise RuntimeError(f"timed-region status {st}: {tg.gemm_last_error()}")
-    launches = 1 + plan["pack_a"] + plan["pack_b"] if plan["path"] == 1 else 1
-    return {"total_ms": total_ms, "launch_ms_mean": statistics.mean(launch_ms),
-            "launch_ms_median": statistics.median(launch_ms), "launch_ms_min": min(launch_ms),
-            "plan": plan, "launches_per_step": launches, "flops": 2.0 * M * N * K, "C": C}
+    # the GEMM, plus the operand packs / B transpose before it and the split-K reduction after it
+    launches = (1 + plan["pack_a"] + plan["pack_b"] + plan["b_kmajor"] + int(plan["tail_tiles"] > 0)
+                if plan["path"] == 1 else 1)
+    return {"total_ms": total_ms, "launch_ms_mean": total_ms / steps,
+            "isolated_ms_mean": statistics.mean(launch_ms), "isolated_ms_median": statistics.median(launch_ms),
+            "isolated_ms_min": min(launch_ms), "plan": plan, "launches_per_step": launches,
+            "flops": 2.0 * M * N * K, "C": C}
 
 
 class with_option:
@@ -588,8 +600,9 @@ def run_ours(args):
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of operands vs 129 MB L2); no flush",
                    "plan": res["plan"]},
         "roofline": roof,
-        "kernel_ms": {"mean": round(res["launch_ms_mean"], 5), "median": round(res["launch_ms_median"], 5),
-                      "min": round(res["launch_ms_min"], 5)},
+        "kernel_ms": {"mean": round(res["launch_ms_mean"], 5),
+                      "isolated_launches": {k: round(res[f"isolated_ms_{k}"], 5) for k in ("mean", "median", "min")}
+                      if "isolated_ms_mean" in res else None},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": clocks,
     }

@@ -99,8 +99,12 @@ typedef enum {
  * reads its B operand K-major.  When there are too few output tiles to occupy
  * every SM and K is long, the tensor-core path splits K: partial tiles go to
  * a workspace and a second kernel sums them into C in a fixed order (results
- * are deterministic).  On request ("tc_tail_splits") the tiles of the last,
- * partly idle round of the persistent schedule are split in K the same way.
+ * are deterministic).  When the tiles of the last, partly idle round of the
+ * persistent schedule would fill at most half of the machine, 16-bit inputs
+ * on short schedules run them as two column halves each (every half over
+ * all of K, straight to C: no workspace, and the same sums as a whole
+ * tile); on request ("tc_tail_splits") they are split in K instead, like
+ * split-K.
  * C leaves through TMA stores when its base, pitch and row length (N
  * elements) are all multiples of 16 bytes, else through ordinary stores.
  *
@@ -223,10 +227,21 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_splits"      force split-K: K ranges for every output tile (1..32);
  *                    the partial tiles go to a workspace and are summed into
  *                    C in a fixed order by a second kernel
- *   "tc_tail_splits" 0 auto (2 for TF32, off otherwise), 1 off, n >= 2: split
- *                    the tiles of the last, partly idle round of the
- *                    persistent schedule into n K ranges (same workspace and
- *                    reduction)
+ *   "tc_tail_splits" 0 auto (2 for TF32 when the column halves below do not
+ *                    apply, off otherwise), 1 off, n >= 2: split the tiles
+ *                    of the last, partly idle round of the persistent
+ *                    schedule into n K ranges (same workspace and reduction)
+ *   "tc_tail_halves" run the last round's tiles as column halves when the
+ *                    halves fit in one round and the tile allows it (BN >=
+ *                    128; B read as stored in whole 128-byte chunks per
+ *                    CTA, or the K-major copy): 0 auto (16-bit inputs on
+ *                    schedules of at most 4 rounds), 1 off, 2 wherever the
+ *                    tile allows it
+ *   "tc_pdl"         0 (default) launch the tensor-core kernel as a
+ *                    programmatic dependent of the previous kernel on the
+ *                    stream: its set-up overlaps that kernel's end, and it
+ *                    waits for that kernel to finish before touching global
+ *                    memory; 1 off
  *   "tc_tma_store"   0 auto, 1 force TMA-store epilogue where legal, 2 force
  *                    ordinary-store epilogue
  *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8
@@ -271,6 +286,8 @@ typedef struct {
     int32_t sched;       /* 0: static persistent stride over work units;
                             1: Cluster Launch Control (one cluster per unit
                             launched, running CTAs steal the rest)         */
+    int32_t half_tiles;  /* tiles run as two column halves (the last ones in
+                            the schedule), each half over all of K         */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

@@ -92,6 +92,9 @@ def test_plan_dynamic_schedule_launches_one_cluster_per_unit():
         assert tg.gemm_set_option("tc_sched", 2) == tg.GEMM_OK
         p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
         assert p["sched"] == 1 and p["cta_group"] == 2 and p["grid"] == 2 * p["tiles"] == 2048
+        # column halves are units too: 256 tiles, the last 28 as two halves each
+        h = _plan(4096, 4096, 4096, tg.GEMM_BF16)
+        assert h["half_tiles"] == 28 and h["grid"] == 2 * (256 + 28)
         q = _plan(128, 8192, 8192, tg.GEMM_BF16)          # split-K units count too
         assert q["grid"] == q["tiles"] * q["splits"]
     finally:
@@ -180,20 +183,76 @@ def test_plan_low_tile_count_splits_k():
     assert p["tail_tiles"] == 32        # every tile is split
 
 
-def test_plan_splits_the_last_round_only_on_request():
-    # off by default for 16- and 8-bit inputs (measured: no gain or a loss) ...
-    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["tail_tiles"] == 0
-    assert _plan(4096, 4096, 4096, tg.GEMM_E4M3)["tail_tiles"] == 0
-    # ... on by default, two K ranges, for TF32 (measured +4% at 4096^3)
-    auto = _plan(4096, 4096, 4096, tg.GEMM_TF32)
-    assert auto["tail_tiles"] == 28 and auto["splits"] == 2
+def test_plan_runs_the_last_round_as_column_halves():
+    # 256 pair tiles over 76 pairs: 3 rounds and 28 tiles left, which as 56
+    # halves fit one round; on by default for 16-bit inputs on short schedules
+    for dt in (tg.GEMM_BF16, tg.GEMM_FP16):
+        q = _plan(4096, 4096, 4096, dt)
+        assert q["half_tiles"] == 28 and q["tail_tiles"] == 0 and q["splits"] == 1 and q["grid"] == 152, (dt, q)
+    assert _plan(16384, 1024, 4096, tg.GEMM_BF16)["half_tiles"] == 28
+    # not by default on 14 rounds (8192^3: neutral) nor for TF32 (its K split is faster)
+    assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["half_tiles"] == 0
+    t = _plan(4096, 4096, 4096, tg.GEMM_TF32)
+    assert t["half_tiles"] == 0 and t["tail_tiles"] == 28
+    try:
+        assert tg.gemm_set_option("tc_tail_halves", 2) == 0          # 2: wherever the tile allows it
+        # 1024 tiles: 13 rounds and 36 left, 72 halves
+        p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
+        assert p["half_tiles"] == 36 and p["tail_tiles"] == 0 and p["grid"] == 152
+        t = _plan(4096, 4096, 4096, tg.GEMM_TF32)                   # the K-major B copy halves too
+        assert t["half_tiles"] == 28 and t["tail_tiles"] == 0
+        # 272 tiles leave 44: 88 halves would not fit one round
+        assert _plan(4097, 4095, 4099, tg.GEMM_BF16)["half_tiles"] == 0
+        # FP8 B as stored comes in one 128-column chunk per CTA: no halves
+        assert _plan(8192, 8192, 8192, tg.GEMM_E4M3)["half_tiles"] == 0
+        # a whole number of rounds: no tail
+        assert _plan(256, 256 * 76, 4096, tg.GEMM_BF16)["half_tiles"] == 0
+    finally:
+        tg.gemm_set_option("tc_tail_halves", 0)
+    # 1-CTA 128 x 256 tiles halve too; 64-column tiles do not
+    try:
+        assert tg.gemm_set_option("tc_cta_group", 1) == 0
+        assert tg.gemm_set_option("tc_max_ctas", 100) == 0
+        r = _plan(128 * 130, 256, 1024, tg.GEMM_BF16)             # 130 tiles on 100 CTAs: 30 left
+        assert r["bn"] == 256 and r["half_tiles"] == 30 and r["grid"] == 100
+        assert tg.gemm_set_option("tc_bn", 64) == 0
+        assert _plan(128 * 130, 64, 1024, tg.GEMM_BF16)["half_tiles"] == 0
+    finally:
+        for k in ("tc_cta_group", "tc_max_ctas", "tc_bn"):
+            tg.gemm_set_option(k, 0)
+    try:
+        assert tg.gemm_set_option("tc_tail_halves", 1) == 0          # 1: off
+        assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["half_tiles"] == 0
+    finally:
+        tg.gemm_set_option("tc_tail_halves", 0)
+    assert tg.gemm_set_option("tc_tail_halves", 3) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_get_option("tc_tail_halves") == 0
+    assert tg.gemm_get_option("tc_pdl") == 0
+    assert tg.gemm_set_option("tc_pdl", 1) == 0 and tg.gemm_get_option("tc_pdl") == 1
+    assert tg.gemm_set_option("tc_pdl", 2) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_set_option("tc_pdl", 0) == 0
+
+
+def test_plan_splits_the_last_round_in_k_only_on_request():
+    try:
+        assert tg.gemm_set_option("tc_tail_halves", 1) == 0
+        # without column halves: off by default for 16- and 8-bit inputs
+        # (measured: no gain or a loss) ...
+        assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["tail_tiles"] == 0
+        assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["tail_tiles"] == 0
+        assert _plan(4096, 4096, 4096, tg.GEMM_E4M3)["tail_tiles"] == 0
+        # ... on, two K ranges, for TF32
+        auto = _plan(4096, 4096, 4096, tg.GEMM_TF32)
+        assert auto["tail_tiles"] == 28 and auto["splits"] == 2 and auto["half_tiles"] == 0
+    finally:
+        tg.gemm_set_option("tc_tail_halves", 0)
     try:
         assert tg.gemm_set_option("tc_tail_splits", 1) == 0          # 1: off for every dtype
         assert _plan(4096, 4096, 4096, tg.GEMM_TF32)["tail_tiles"] == 0
         # 1024 pair tiles over 76 pairs: 13 full rounds and 36 tiles left
-        assert tg.gemm_set_option("tc_tail_splits", 2) == 0
+        assert tg.gemm_set_option("tc_tail_splits", 2) == 0          # a K split takes precedence
         p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
-        assert p["tail_tiles"] == 36 and p["splits"] == 2 and p["grid"] == 152
+        assert p["tail_tiles"] == 36 and p["splits"] == 2 and p["grid"] == 152 and p["half_tiles"] == 0
         # TF32 4096^3: 256 pair tiles, 28 left after 3 rounds
         q = _plan(4096, 4096, 4096, tg.GEMM_TF32)
         assert q["tail_tiles"] == 28 and q["splits"] == 2

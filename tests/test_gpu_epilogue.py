@@ -25,7 +25,7 @@ DTYPES = ("fp32", "tf32", "bf16", "fp16", "e4m3", "e5m2")
 OUTS = ("f32", "bf16", "f16")
 ACTS = ("none", "relu", "gelu")
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-               "debug_stall_mma", "tc_splits", "tc_tail_splits")
+               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -121,6 +121,23 @@ def test_epilogue_after_split_k_reduction(dtype, splits, tail):
     plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N)
     assert plan.tail_tiles > 0 and plan.splits > 1
     _check(A, B, dtype, "f16", -0.5, 1.0, "relu", seed=39)
+
+
+@pytest.mark.parametrize("store", ("tma", "plain"))
+@pytest.mark.parametrize("out", ("f32", "bf16"))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+def test_epilogue_on_column_halves(dtype, out, store):
+    """The last round's tiles run as column halves: each half applies bias,
+    residual and activation to its own columns (1998 x 1440 on 20 CTA pairs:
+    48 tiles, the right-hand column's 8 as halves, one of them part empty)."""
+    tg.gemm_set_option("tc_cta_group", 2)
+    tg.gemm_set_option("tc_max_ctas", 40)
+    tg.gemm_set_option("tc_tail_halves", 2)
+    tg.gemm_set_option("tc_tma_store", 2 if store == "plain" else 0)
+    M, N, K = 1998, 1440, 512
+    A, B = make_operands(M, N, K, dtype, "normal", seed=42)
+    assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).half_tiles == 8
+    _check(A, B, dtype, out, 0.75, -0.5, "gelu", seed=43)
 
 
 @pytest.mark.parametrize("out", OUTS)

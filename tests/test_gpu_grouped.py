@@ -24,7 +24,7 @@ from gemm_check import (TOL, epilogue_check, error_ratio, oracle_full, oracle_ro
 pytestmark = pytest.mark.gpu
 
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-               "debug_stall_mma", "tc_splits", "tc_tail_splits")
+               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves")
 GUARD = 64
 
 

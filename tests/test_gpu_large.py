@@ -15,7 +15,8 @@ from gemm_check import TOL, epilogue_check, error_ratio, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
-OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_max_ctas", "tc_tma_store", "tc_splits", "tc_tail_splits", "tc_sched")
+OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_max_ctas", "tc_tma_store", "tc_splits", "tc_tail_splits", "tc_tail_halves",
+               "tc_sched")
 
 M_BIG = (1 << 18) + 7            # 262151 rows
 N_BIG = 8200                     # M_BIG * N_BIG = 2.15e9 > 2^31 elements

@@ -33,7 +33,7 @@ def lib():
     tgbuild.build()
     tg.load_library()
     for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-              "debug_stall_mma", "tc_splits", "tc_tail_splits"):
+              "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -195,8 +195,56 @@ def test_split_tail_exact(dtype, cg, max_ctas, tail_splits):
         _exact(A, B, dtype)
         _exact(A, B, dtype, ldc_pad=1)
     finally:
-        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas", "tc_tail_splits"):
+        for k in ("tc_cta_group", "tc_bn", "tc_max_ctas", "tc_tail_splits", "tc_tail_halves"):
             tg.gemm_set_option(k, 0)
+
+
+HALF_CASES = [  # dtype, cta_group, BN, tc_b_major, CTAs
+    ("bf16", 2, 256, 0, 40), ("fp16", 2, 256, 0, 40), ("tf32", 2, 256, 0, 40), ("bf16", 2, 256, 1, 40),
+    ("e5m2", 2, 256, 1, 40), ("bf16", 1, 256, 0, 40), ("bf16", 1, 128, 0, 44), ("e4m3", 1, 256, 1, 40)]
+
+
+@pytest.mark.parametrize("store", ("tma", "plain"))
+@pytest.mark.parametrize("dtype,cg,bn,b_major,ctas", HALF_CASES, ids=lambda v: str(v))
+def test_tail_halves_exact(dtype, cg, bn, b_major, ctas, store):
+    """Whole tiles first, then the last round's tiles as two column halves each.
+    1998 x 1440 in tiles of 256 (or 128) rows: the raster's last tiles are the
+    right-hand column, whose tiles hold 160 (or 32) of their columns, so one
+    half there is partly empty and, with BN = 128, the other has no column at
+    all; the bottom row of tiles is ragged too."""
+    M, N, K = 1998, 1440, 1024
+    A, B = make_operands(M, N, K, dtype, "ints", seed=27)
+    opts = {"tc_cta_group": cg, "tc_bn": bn, "tc_max_ctas": ctas, "tc_b_major": b_major,
+            "tc_tma_store": 2 if store == "plain" else 0, "tc_tail_halves": 2}
+    try:
+        for k, v in opts.items():
+            tg.gemm_set_option(k, v)
+        plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).as_dict()
+        assert plan["half_tiles"] > 0 and plan["tail_tiles"] == 0 and plan["tma_store"] == (store == "tma"), plan
+        _exact(A, B, dtype)
+    finally:
+        for k in opts:
+            tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+def test_tail_halves_equal_whole_tiles(dtype):
+    """On random data a tile run as two column halves gives the same bits as
+    the tile run whole: every output's sum takes the same K steps in the same
+    order; only the MMA width differs."""
+    A, B = make_operands(4096, 4096, 1024, dtype, "normal", seed=28)
+    try:
+        tg.gemm_set_option("tc_tail_halves", 2)
+        assert tg.gemm_plan(4096, 4096, 1024, tg.DTYPES[dtype], 0, 1024, 0, 4096, 0, 4096).half_tiles == 28
+        C1 = run_gemm(A, B, dtype)
+        tg.gemm_set_option("tc_tail_halves", 1)
+        tg.gemm_set_option("tc_tail_splits", 1)           # whole tiles (TF32 would split the tail in K)
+        assert tg.gemm_plan(4096, 4096, 1024, tg.DTYPES[dtype], 0, 1024, 0, 4096, 0, 4096).tail_tiles == 0
+        C2 = run_gemm(A, B, dtype)
+    finally:
+        tg.gemm_set_option("tc_tail_halves", 0)
+        tg.gemm_set_option("tc_tail_splits", 0)
+    assert np.array_equal(C1, C2)
 
 
 def test_split_k_deterministic_on_random_data():
@@ -213,6 +261,40 @@ def test_split_k_deterministic_on_random_data():
     finally:
         tg.gemm_set_option("tc_tail_splits", 0)
     assert np.array_equal(C1, C2)
+
+
+@pytest.mark.parametrize("n", (512, 2048))
+def test_back_to_back_launches_read_the_previous_output(n):
+    """A tensor-core launch starts its set-up while the previous kernel on the
+    stream finishes (programmatic dependent launch).  Here each step writes C1
+    (BF16) and the next launch reads C1 as its A; the step after that
+    overwrites C1 while that reader may still be finishing.  Small integers
+    keep every value exact (|C1| <= 256, |D| < 2^24), so a read that came too
+    early, or a write that came too soon, would show as a wrong D."""
+    k1 = 4
+    As = [make_operands(n, n, k1, "bf16", "ints", seed=140 + i)[0] for i in range(2)]
+    B1 = make_operands(n, n, k1, "bf16", "ints", seed=142)[1]
+    B2 = make_operands(n, n, n, "bf16", "ints", seed=143)[1]
+    a_dev = [a.cuda() for a in As]
+    b1, b2 = B1.cuda(), B2.cuda()
+    c1 = torch.empty((n, n), dtype=torch.bfloat16, device="cuda")
+    Ds = [torch.empty((n, n), dtype=torch.float32, device="cuda") for _ in range(8)]
+    s = torch.cuda.current_stream().cuda_stream
+    ep = tg.make_epilogue(out="bf16")
+    assert tg.gemm_get_option("tc_pdl") == 0                      # on
+    for i, D in enumerate(Ds):
+        a = a_dev[i % 2]
+        rc = tg.gemm_run_ex(n, n, k1, tg.GEMM_BF16, a.data_ptr(), k1, b1.data_ptr(), n, c1.data_ptr(), n, ep, s)
+        assert rc == tg.GEMM_OK, tg.gemm_last_error()
+        rc = tg.gemm_run(n, n, n, tg.GEMM_BF16, c1.data_ptr(), n, b2.data_ptr(), n, D.data_ptr(), n, s)
+        assert rc == tg.GEMM_OK, tg.gemm_last_error()
+    assert tg.gemm_get_status(s) == tg.GEMM_OK, tg.gemm_last_error()
+    refs = []
+    for a in As:
+        c_ref, _ = oracle_full(a, B1, "bf16")
+        refs.append(oracle_full(torch.from_numpy(c_ref).to(torch.bfloat16), B2, "bf16")[0])
+    for i, D in enumerate(Ds):
+        assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
 
 
 @pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7))

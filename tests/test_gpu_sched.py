@@ -19,7 +19,7 @@ from gemm_check import oracle_full, run_gemm, run_gemm_ex
 pytestmark = pytest.mark.gpu
 
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_sched")
+               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_sched")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -82,6 +82,17 @@ def test_dynamic_with_split_k(splits, tail):
         tg.gemm_set_option("tc_max_ctas", 7)
     s, d = _both(lambda: run_gemm(A, B, "bf16"))
     assert np.array_equal(s, d)
+
+
+def test_dynamic_with_column_halves():
+    """The last tiles' column halves are units like any other for the stealer."""
+    A, B = make_operands(1998, 1440, 1024, "bf16", "ints", seed=125)
+    tg.gemm_set_option("tc_cta_group", 2)
+    tg.gemm_set_option("tc_max_ctas", 40)
+    assert tg.gemm_plan(1998, 1440, 1024, tg.GEMM_BF16, 0, 1024, 0, 1440, 0, 1440).half_tiles == 8
+    s, d = _both(lambda: run_gemm(A, B, "bf16"))
+    ref, _ = oracle_full(A, B, "bf16")
+    assert np.array_equal(d, ref) and np.array_equal(s, d)
 
 
 def test_dynamic_with_fused_residual_epilogue():

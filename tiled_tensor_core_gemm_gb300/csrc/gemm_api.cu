@@ -119,6 +119,8 @@ constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills
 // Split-K adds a second kernel and a workspace round trip (a few microseconds):
 // only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
 constexpr int64_t kMinSplitWork = 1LL << 31;
+// Column halves for the last round by default only on schedules this short.
+constexpr int64_t kMaxRoundsForHalves = 4;
 
 }  // namespace
 
@@ -237,31 +239,40 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         want = std::max<int64_t>(1, std::min<int64_t>(want, num_kb));
         return (int)cdiv(num_kb, cdiv(num_kb, want));
     };
-    int64_t tail = 0;
+    int64_t tail = 0, half = 0;
     if (splits == 0 && tiles * 2 <= units && M * N * K >= kMinSplitWork)
         splits = (int)std::max<int64_t>(1, std::min<int64_t>({units / tiles, num_kb / kMinKbPerSplit, 16}));
+    const int64_t rem = tiles > units ? tiles % units : 0;   // tiles of the last, partly idle round
     if (splits > 1) {
         // split K for every tile
         splits = exact_splits(splits);
         if (splits > 1) tail = tiles;
-    } else if ((opt.tc_tail_splits >= 2 || (opt.tc_tail_splits == 0 && dtype == GEMM_TF32)) && tiles > units) {
+    } else if (opt.tc_tail_splits < 2 && rem > 0 && 2 * rem <= units && tc_halves_ok(dtype, cg, bn, p.b_kmajor) &&
+               (opt.tc_tail_halves == 2 ||
+                (opt.tc_tail_halves == 0 && elem == 2 && tiles <= kMaxRoundsForHalves * units))) {
+        // The last round's tiles as column halves: twice the units, each over
+        // all of K, so no partial sums to combine.  A half needs 1.5x the
+        // operand bytes per flop of a whole tile, so it takes more than half
+        // as long.  Measured on GB300 (profiles/picker.md): +2% on 16-bit
+        // inputs with 3-4 rounds (4096^3, 16384 x 1024 x 4096), neutral at
+        // 8192^3 (14 power-capped rounds), -3% on TF32 against its K split.
+        half = rem;
+    } else if ((opt.tc_tail_splits >= 2 || (opt.tc_tail_splits == 0 && dtype == GEMM_TF32)) && rem > 0) {
         // Split only the tiles of the last, partly idle round of the persistent
         // schedule, so that round's units each get a share of K.  Measured on
         // GB300 (profiles/picker.md): +4% for TF32 4096^3 (its half-rate MMA
         // makes each tile long against the reduction), 1-9% slower for 16- and
         // 8-bit inputs -- whose units in a partly idle last round already run
         // faster -- so it is on by default for TF32 only.
-        const int64_t rem = tiles % units;
         const int want = opt.tc_tail_splits >= 2 ? opt.tc_tail_splits : 2;
-        if (want >= 2 && rem > 0) {
-            splits = exact_splits(want);
-            if (splits > 1) tail = rem;
-        }
+        splits = exact_splits(want);
+        if (splits > 1) tail = rem;
     }
     if (tail == 0) splits = 1;
     p.splits = splits;
     p.tail_tiles = (int32_t)tail;
-    const int64_t work_units = (tiles - tail) + tail * splits;
+    p.half_tiles = (int32_t)half;
+    const int64_t work_units = (tiles - tail - half) + tail * splits + 2 * half;
     units = std::min<int64_t>(units, work_units);
     // Static unless asked: measured on GB300 the dynamic schedule is within
     // 1% at 8192^3 and 2% slower on 4096-class shapes (profiles/picker.md).
@@ -303,6 +314,12 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_tail_splits")) {
         if (v < 0 || v > 16) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_splits must be in [0, 16]");
         g_opt.tc_tail_splits = (int)v;
+    } else if (!std::strcmp(key, "tc_pdl")) {
+        if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "tc_pdl must be 0 or 1");
+        g_opt.tc_pdl = (int)v;
+    } else if (!std::strcmp(key, "tc_tail_halves")) {
+        if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_halves must be 0, 1 or 2");
+        g_opt.tc_tail_halves = (int)v;
     } else if (!std::strcmp(key, "tc_sched")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_sched must be 0 (auto), 1 (static) or 2 (dynamic)");
         g_opt.tc_sched = (int)v;
@@ -339,6 +356,8 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_tma_store")) return o.tc_tma_store;
     if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
     if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
+    if (!std::strcmp(key, "tc_tail_halves")) return o.tc_tail_halves;
+    if (!std::strcmp(key, "tc_pdl")) return o.tc_pdl;
     if (!std::strcmp(key, "tc_sched")) return o.tc_sched;
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;

@@ -17,6 +17,8 @@ struct Options {
     int tc_max_ctas = 0;       // 0 auto
     int tc_splits = 0;         // 0 auto, else K ranges for every tile (split-K)
     int tc_tail_splits = 0;    // 0 auto (2 for TF32), 1 off, else K ranges for the last round's tiles
+    int tc_pdl = 0;            // 0 auto (on), 1 off: programmatic dependent launch of the tensor-core kernel
+    int tc_tail_halves = 0;    // 0 auto (16-bit inputs, <= 4 rounds), 1 off, 2 wherever the tile allows
     int tc_sched = 0;          // 0 auto, 1 static persistent, 2 Cluster Launch Control
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
@@ -79,6 +81,8 @@ int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem);
 // b_kmajor: 1 = B from a K-major transposed copy, 0 = B as stored.
 int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor);
 int tc_stages(int dtype, int cta_group, int bn, int b_kmajor);
+// 1 if the variant can run a tile as two column halves (plan.half_tiles).
+int tc_halves_ok(int dtype, int cta_group, int bn, int b_kmajor);
 
 // Encodes the tensor maps and launches the persistent kernel.  A/B are the
 // (possibly packed) operands with the leading dimensions the plan reports;

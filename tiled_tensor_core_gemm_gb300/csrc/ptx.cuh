@@ -231,6 +231,10 @@ __device__ __forceinline__ uint32_t clc_query(uint32_t resp, uint32_t &first_x) 
 // it waits in griddepcontrol.wait until this grid's writes are visible.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// The dependent's side: wait until the grids this launch depends on have
+// completed and their memory writes are visible (returns at once otherwise).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // MMA kinds: 16-bit inputs, TF32 inputs, 8-bit (FP8) inputs.
 enum MmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 

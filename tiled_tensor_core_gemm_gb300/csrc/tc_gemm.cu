@@ -105,6 +105,11 @@ struct TcCfg {
     static constexpr uint32_t FMT = DT == kDtTF32 ? 2u : (DT == kDtFP16 || DT == kDtE4M3) ? 0u : 1u;
     static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((BKM ? 0u : 1u) << 16) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((kBM * CG) >> 4) << 24);
+    // The same MMA at half the tile width (a column-half unit).
+    static constexpr uint32_t IDESC_HALF = (IDESC & ~(0x3Fu << 17)) | ((uint32_t)((BN / 2) >> 3) << 17);
+    // A column half reads B as stored in whole 128-byte chunks; a K-major B box
+    // is loaded whole and the MMA reads its first half.
+    static constexpr bool HALVES = (BN / 2) % 16 == 0 && BN / 2 >= 64 && (BKM || B_CHUNKS % 2 == 0);
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N out of range");
     static_assert(BKM || (BN_CTA % CHUNK_COLS == 0 && B_CHUNKS >= 1), "B tile must be whole 128-byte chunks");
     static_assert(BN_CTA <= 256, "TMA box rows");
@@ -122,6 +127,7 @@ struct TcParams {
     int full_tiles;                    // tiles [0, full_tiles) run over all of K and store to C
     int tail_tiles;                    // the remaining tiles run as `splits` K ranges each
     int splits;                        // K ranges per tail tile
+    int half_tiles;                    // or: the last tiles run as two column halves each, over all of K, to C
     int kb_per_split;                  // k-blocks per K range
     int num_units;                     // full_tiles + tail_tiles * splits work units
     int group_m;                       // raster group height, in tile rows
@@ -136,17 +142,21 @@ struct TcParams {
     unsigned long long timeout_ns;
 };
 
-// Work unit u -> output tile (tm, tn), its K range [kb0, kb1) and the slab its
-// partial sum goes to (-1: the unit covers all of K and stores to C).
+// Work unit u -> output tile (tm, tn), its K range [kb0, kb1), the slab its
+// partial sum goes to (-1: the unit covers all of K and stores to C) and the
+// column half it covers (-1: the whole tile width).
 //
-// Units [0, full_tiles) are whole tiles.  The tail tiles -- those that would
-// leave part of the machine idle in the last round of the persistent schedule,
-// or every tile when K is split throughout -- are split into K ranges; the
-// ranges of one split index come together, so units that run at once read the
-// same slices of A and B.  Partial tiles go to slabs (one full tile each) that
-// a second kernel sums in split order.
+// Units [0, full_tiles) are whole tiles.  The tiles that would leave part of
+// the machine idle in the last round of the persistent schedule are either
+// (a) run as two column halves each, over all of K and straight to C, when
+//     the halves fit in one round: that round then takes half as long; or
+// (b) split into K ranges, as is every tile when K is split throughout; the
+//     ranges of one split index come together, so units that run at once read
+//     the same slices of A and B.  Partial tiles go to slabs (one full tile
+//     each) that a second kernel sums in split order.
 __device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, int &tn, int &kb0, int &kb1,
-                                            int &slab) {
+                                            int &slab, int &half) {
+    half = -1;
     if (u < p.full_tiles) {
         tile_coords(u, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         kb0 = 0;
@@ -155,6 +165,14 @@ __device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, i
         return;
     }
     const int v = u - p.full_tiles;
+    if (p.half_tiles > 0) {
+        half = v / p.half_tiles;
+        tile_coords(p.full_tiles + (v - half * p.half_tiles), p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        kb0 = 0;
+        kb1 = p.num_kb;
+        slab = -1;
+        return;
+    }
     const int split = v / p.tail_tiles;
     const int i = v - split * p.tail_tiles;
     tile_coords(p.full_tiles + i, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -169,6 +187,7 @@ __device__ __forceinline__ void unit_coords(int u, const TcParams &p, int &tm, i
 // binary search over the groups' first units).
 struct Unit {
     int tm, tn, kb0, kb1, slab;
+    int half;                          // -1: the whole tile width; 0 / 1: that column half
     int M, N;
     const CUtensorMap *mA, *mB, *mC;
     void *C;
@@ -182,7 +201,7 @@ __device__ __forceinline__ Unit unit_info(int u, const TcParams &p, const CUtens
                                           const CUtensorMap *tmC) {
     Unit U;
     if (p.groups == nullptr) {
-        unit_coords(u, p, U.tm, U.tn, U.kb0, U.kb1, U.slab);
+        unit_coords(u, p, U.tm, U.tn, U.kb0, U.kb1, U.slab, U.half);
         U.M = p.M;
         U.N = p.N;
         U.mA = tmA;
@@ -206,6 +225,7 @@ __device__ __forceinline__ Unit unit_info(int u, const TcParams &p, const CUtens
     U.kb0 = 0;
     U.kb1 = g->num_kb;
     U.slab = -1;
+    U.half = -1;
     U.M = g->M;
     U.N = g->N;
     U.mA = &g->tmA;
@@ -320,6 +340,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (kPair) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream, this CTA may have started before that kernel ended: the set-up
+    // above touched only its own shared and Tensor Memory.  Wait here, before
+    // any global-memory access, for that kernel to finish and its writes to be
+    // visible; then let the next launch start its own set-up (when no split-K
+    // reduction, which reads this grid's slabs, comes next).
+    ptx::pdl_wait();
+    if (p.tail_tiles == 0 && threadIdx.x == 0) ptx::pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -339,15 +367,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::prefetch_tensormap(U.mB);
                     last_group = U.group;
                 }
+                // A column-half unit: this CTA's share is half as wide; B as stored
+                // then comes in half the chunks (a K-major box is loaded whole).
+                const bool halfu = Cf::HALVES && U.half >= 0;
+                const int cta_cols = halfu ? Cf::BN_CTA / 2 : Cf::BN_CTA;
                 const int m0 = U.tm * (kBM * CG) + (int)rank * kBM;
-                const int n0 = U.tn * BN + (int)rank * Cf::BN_CTA;
+                const int n0 = U.tn * BN + (halfu ? U.half * (BN / 2) : 0) + (int)rank * cta_cols;
+                const int nchunks = BKM ? 0 : cta_cols / Cf::CHUNK_COLS;
+                const uint32_t tx_bytes =
+                    (uint32_t)((Cf::A_BYTES + (BKM ? Cf::B_BYTES : nchunks * Cf::B_CHUNK_BYTES)) * CG);
                 for (int kb = U.kb0; kb < U.kb1; ++kb) {
                     if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleProducer, t, abort_flag);
                         return false;
                     }
                     const uint32_t fb = full_bar(stage);
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)(Cf::STAGE_BYTES * CG));
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb, tx_bytes);
                     const uint32_t sa = ptx::smem_addr(stages + stage * Cf::STAGE_BYTES);
                     const uint32_t sb = sa + Cf::A_BYTES;
                     const int k0 = kb * Cf::BK;
@@ -358,7 +393,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         } else {
 #pragma unroll
                             for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                                ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb, n0 + c * Cf::CHUNK_COLS, k0);
+                                if (c < nchunks)
+                                    ptx::tma_load_2d(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb, n0 + c * Cf::CHUNK_COLS, k0);
                         }
                     } else {
                         const uint32_t fb_even = ptx::mapa_shared(fb, 0);
@@ -368,8 +404,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         } else {
 #pragma unroll
                             for (int c = 0; c < Cf::B_CHUNKS; ++c)
-                                ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb_even, n0 + c * Cf::CHUNK_COLS,
-                                                      k0);
+                                if (c < nchunks)
+                                    ptx::tma_load_2d_pair(sb + c * Cf::B_CHUNK_BYTES, U.mB, fb_even,
+                                                          n0 + c * Cf::CHUNK_COLS, k0);
                         }
                     }
                     if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
@@ -491,6 +528,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             while (ok && t >= 0) {
                 const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
                 const int kb0 = U.kb0, kb1 = U.kb1;
+                const uint32_t idesc = (Cf::HALVES && U.half >= 0) ? Cf::IDESC_HALF : Cf::IDESC;
                 if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleMma, t, abort_flag);
                     break;
@@ -516,7 +554,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             BKM ? ptx::sdesc_sw128(sb + 32u * kk, 16u, 1024u)
                                 : ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
                                                    1024u);
-                        ptx::mma<CG, Cf::KIND>(d_tmem, adesc, bdesc, Cf::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        ptx::mma<CG, Cf::KIND>(d_tmem, adesc, bdesc, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else ptx::mma_commit(empty_bar(stage));
@@ -579,7 +617,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const Unit U = unit_info(t, p, &tmA, &tmB, &tmC);
             const int slab = U.slab;
             const int m0 = U.tm * (kBM * CG) + (int)rank * kBM + 32 * (int)q;   // this warp's first row
-            const int n0 = U.tn * BN;
+            const bool halfu = Cf::HALVES && U.half >= 0;
+            const int ucols = halfu ? BN / 2 : BN;                                // columns of this unit
+            const int n0 = U.tn * BN + (halfu ? U.half * (BN / 2) : 0);
             const int srow = (int)rank * kBM + 32 * (int)q;                       // same row inside a slab
             const bool to_slab = slab >= 0;
             const bool use_tma = to_slab || U.tma_store;
@@ -605,7 +645,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tc_fence_after();
             const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-            for (int jb = 0; jb < BN / box_cols; ++jb, ++nchunk) {
+            for (int jb = 0; jb < ucols / box_cols; ++jb, ++nchunk) {
                 uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
                 const int col0 = n0 + box_cols * jb;
                 const bool box_live = m0 < U.M && col0 < U.N;
@@ -637,7 +677,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(box_cols * jb + 32 * h), r);
                     ptx::tmem_wait_ld();
-                    if (jb == BN / box_cols - 1 && h == box_cols / 32 - 1) {
+                    if (jb == ucols / box_cols - 1 && h == box_cols / 32 - 1) {
                         // The accumulator is fully in registers/shared: hand it back to the MMA.
                         ptx::tc_fence_before();
                         __syncwarp();
@@ -856,15 +896,24 @@ int launch_kernel(const gemm_plan_t &plan, const CUtensorMap &ta, const CUtensor
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
     if (CG == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
     }
+    if (options_snapshot().tc_pdl != 1) {
+        // may start while the previous kernel on the stream finishes (the
+        // kernel waits for it before touching global memory)
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
     if (e != cudaSuccess) {
         std::snprintf(err, errlen, "tensor-core kernel launch: %s", cudaGetErrorString(e));
@@ -917,10 +966,11 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = (K + Cf::BK - 1) / Cf::BK;
     p.tail_tiles = plan.tail_tiles;
-    p.full_tiles = p.num_tiles - p.tail_tiles;
+    p.half_tiles = plan.tail_tiles > 0 ? 0 : plan.half_tiles;
+    p.full_tiles = p.num_tiles - p.tail_tiles - p.half_tiles;
     p.splits = p.tail_tiles > 0 ? plan.splits : 1;
     p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
-    p.num_units = p.full_tiles + p.tail_tiles * p.splits;
+    p.num_units = p.full_tiles + p.tail_tiles * p.splits + 2 * p.half_tiles;
     p.C = C;
     p.ldc = ldc;
     return launch_kernel<DT, CG, BN, BMODE>(plan, ta, tb, tc, tw, p, stream, err, errlen);
@@ -966,11 +1016,13 @@ constexpr bool variant_ok() {
     return !(DT == kDtTF32 && BMODE == kBNMajor) && (BMODE == kBKMajor || (BN / CG) % (128 / dt_elem(DT)) == 0);
 }
 
+enum VariantValue : int { kValSmem = 0, kValStages = 1, kValHalves = 2 };
+
 template <int DT, int CG, int BN, int BMODE>
-int variant_value(bool stages) {
+int variant_value(int what) {
     if constexpr (variant_ok<DT, CG, BN, BMODE>()) {
         using Cf = TcCfg<DT, CG, BN, BMODE>;
-        return stages ? Cf::STAGES : Cf::SMEM_BYTES;
+        return what == kValStages ? Cf::STAGES : what == kValHalves ? (Cf::HALVES ? 1 : 0) : Cf::SMEM_BYTES;
     } else {
         return 0;
     }
@@ -984,23 +1036,23 @@ int variant_value(bool stages) {
 // memory twice as often per flop and runs 25-30% slower.
 #define TC_VARIANTS(X) X(1, 64) X(1, 128) X(1, 256) X(2, 256)
 
-static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, bool stages) {
+static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, int what) {
     const int mode = b_kmajor ? kBKMajor : kBNMajor;
 #define X(cg, bn_)                                                                                   \
     if (cta_group == cg && bn == bn_) {                                                               \
         if (dtype == GEMM_TF32)                                                                       \
-            return mode == kBKMajor ? variant_value<kDtTF32, cg, bn_, kBKMajor>(stages) : 0;          \
+            return mode == kBKMajor ? variant_value<kDtTF32, cg, bn_, kBKMajor>(what) : 0;           \
         if (dtype == GEMM_FP16)                                                                       \
-            return mode == kBKMajor ? variant_value<kDtFP16, cg, bn_, kBKMajor>(stages)               \
-                                    : variant_value<kDtFP16, cg, bn_, kBNMajor>(stages);              \
+            return mode == kBKMajor ? variant_value<kDtFP16, cg, bn_, kBKMajor>(what)                \
+                                    : variant_value<kDtFP16, cg, bn_, kBNMajor>(what);               \
         if (dtype == GEMM_E4M3)                                                                       \
-            return mode == kBKMajor ? variant_value<kDtE4M3, cg, bn_, kBKMajor>(stages)               \
-                                    : variant_value<kDtE4M3, cg, bn_, kBNMajor>(stages);              \
+            return mode == kBKMajor ? variant_value<kDtE4M3, cg, bn_, kBKMajor>(what)                \
+                                    : variant_value<kDtE4M3, cg, bn_, kBNMajor>(what);               \
         if (dtype == GEMM_E5M2)                                                                       \
-            return mode == kBKMajor ? variant_value<kDtE5M2, cg, bn_, kBKMajor>(stages)               \
-                                    : variant_value<kDtE5M2, cg, bn_, kBNMajor>(stages);              \
-        return mode == kBKMajor ? variant_value<kDtBF16, cg, bn_, kBKMajor>(stages)                   \
-                                : variant_value<kDtBF16, cg, bn_, kBNMajor>(stages);                  \
+            return mode == kBKMajor ? variant_value<kDtE5M2, cg, bn_, kBKMajor>(what)                \
+                                    : variant_value<kDtE5M2, cg, bn_, kBNMajor>(what);               \
+        return mode == kBKMajor ? variant_value<kDtBF16, cg, bn_, kBKMajor>(what)                    \
+                                : variant_value<kDtBF16, cg, bn_, kBNMajor>(what);                   \
     }
     TC_VARIANTS(X)
 #undef X
@@ -1008,10 +1060,16 @@ static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, bool stages)
 }
 
 int tc_smem_bytes(int dtype, int cta_group, int bn, int b_kmajor) {
-    return tc_value(dtype, cta_group, bn, b_kmajor, false);
+    return tc_value(dtype, cta_group, bn, b_kmajor, kValSmem);
 }
 
-int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) { return tc_value(dtype, cta_group, bn, b_kmajor, true); }
+int tc_stages(int dtype, int cta_group, int bn, int b_kmajor) {
+    return tc_value(dtype, cta_group, bn, b_kmajor, kValStages);
+}
+
+int tc_halves_ok(int dtype, int cta_group, int bn, int b_kmajor) {
+    return tc_value(dtype, cta_group, bn, b_kmajor, kValHalves);
+}
 
 // Calls f(dt, cg, bn, mode) -- each an std::integral_constant -- for the
 // variant the plan names; f returns a gemm_status_t.
