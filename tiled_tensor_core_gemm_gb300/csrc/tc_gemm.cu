@@ -676,7 +676,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int h = 0; h < box_cols / 32; ++h) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(box_cols * jb + 32 * h), r);
-                    ptx::tmem_wait_ld();
+                    ptx::tmem_wait_ld(r);
                     if (jb == ucols / box_cols - 1 && h == box_cols / 32 - 1) {
                         // The accumulator is fully in registers/shared: hand it back to the MMA.
                         ptx::tc_fence_before();
