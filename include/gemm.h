@@ -237,7 +237,7 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    CTA, or the K-major copy): 0 auto (16-bit inputs on
  *                    schedules of at most 4 rounds), 1 off, 2 wherever the
  *                    tile allows it
- *   "tc_pdl"         0 (default) launch the tensor-core kernel as a
+ *   "pdl"            0 (default) launch every kernel of the library as a
  *                    programmatic dependent of the previous kernel on the
  *                    stream: its set-up overlaps that kernel's end, and it
  *                    waits for that kernel to finish before touching global

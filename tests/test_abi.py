@@ -227,10 +227,10 @@ def test_plan_runs_the_last_round_as_column_halves():
         tg.gemm_set_option("tc_tail_halves", 0)
     assert tg.gemm_set_option("tc_tail_halves", 3) == tg.GEMM_ERR_INVALID_ARG
     assert tg.gemm_get_option("tc_tail_halves") == 0
-    assert tg.gemm_get_option("tc_pdl") == 0
-    assert tg.gemm_set_option("tc_pdl", 1) == 0 and tg.gemm_get_option("tc_pdl") == 1
-    assert tg.gemm_set_option("tc_pdl", 2) == tg.GEMM_ERR_INVALID_ARG
-    assert tg.gemm_set_option("tc_pdl", 0) == 0
+    assert tg.gemm_get_option("pdl") == 0
+    assert tg.gemm_set_option("pdl", 1) == 0 and tg.gemm_get_option("pdl") == 1
+    assert tg.gemm_set_option("pdl", 2) == tg.GEMM_ERR_INVALID_ARG
+    assert tg.gemm_set_option("pdl", 0) == 0
 
 
 def test_plan_splits_the_last_round_in_k_only_on_request():

@@ -281,7 +281,7 @@ def test_back_to_back_launches_read_the_previous_output(n):
     Ds = [torch.empty((n, n), dtype=torch.float32, device="cuda") for _ in range(8)]
     s = torch.cuda.current_stream().cuda_stream
     ep = tg.make_epilogue(out="bf16")
-    assert tg.gemm_get_option("tc_pdl") == 0                      # on
+    assert tg.gemm_get_option("pdl") == 0                      # on
     for i, D in enumerate(Ds):
         a = a_dev[i % 2]
         rc = tg.gemm_run_ex(n, n, k1, tg.GEMM_BF16, a.data_ptr(), k1, b1.data_ptr(), n, c1.data_ptr(), n, ep, s)
@@ -293,6 +293,51 @@ def test_back_to_back_launches_read_the_previous_output(n):
     for a in As:
         c_ref, _ = oracle_full(a, B1, "bf16")
         refs.append(oracle_full(torch.from_numpy(c_ref).to(torch.bfloat16), B2, "bf16")[0])
+    for i, D in enumerate(Ds):
+        assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
+
+
+@pytest.mark.parametrize("case", ("packed", "fp32"))
+def test_back_to_back_chain_through_packs_and_simt(case):
+    """The same chain where every kernel of the library takes part: with
+    leading dimensions the TMA cannot address, the first GEMM of each step
+    runs after two pack kernels; in FP32 both GEMMs are the SIMT kernel.
+    Each of them may start while the one before it finishes, and must still
+    read only finished data."""
+    n, k1 = 600, 4
+    dtype = "fp32" if case == "fp32" else "bf16"
+    pad = 1 if case == "packed" else 0
+    As = [make_operands(n, n, k1, dtype, "ints", seed=150 + i)[0] for i in range(2)]
+    B1 = make_operands(n, n, k1, dtype, "ints", seed=152)[1]
+    B2 = make_operands(n, n, n, dtype, "ints", seed=153)[1]
+
+    def padded(t, ld):
+        buf = torch.zeros((t.shape[0], ld), dtype=t.dtype, device="cuda")
+        buf[:, :t.shape[1]] = t.cuda()
+        return buf
+
+    a_dev = [padded(a, k1 + pad) for a in As]
+    b1, b2 = padded(B1, n + pad), B2.cuda()
+    c1 = torch.empty((n, n), dtype=torch.float32 if case == "fp32" else torch.bfloat16, device="cuda")
+    Ds = [torch.empty((n, n), dtype=torch.float32, device="cuda") for _ in range(8)]
+    s = torch.cuda.current_stream().cuda_stream
+    code = tg.DTYPES[dtype]
+    ep = tg.make_epilogue(out="f32" if case == "fp32" else "bf16")
+    if case == "packed":
+        plan = tg.gemm_plan(n, n, k1, code, a_dev[0].data_ptr(), k1 + pad, b1.data_ptr(), n + pad, c1.data_ptr(), n)
+        assert plan.pack_a and plan.pack_b
+    for i, D in enumerate(Ds):
+        a = a_dev[i % 2]
+        rc = tg.gemm_run_ex(n, n, k1, code, a.data_ptr(), k1 + pad, b1.data_ptr(), n + pad, c1.data_ptr(), n, ep, s)
+        assert rc == tg.GEMM_OK, tg.gemm_last_error()
+        rc = tg.gemm_run(n, n, n, code, c1.data_ptr(), n, b2.data_ptr(), n, D.data_ptr(), n, s)
+        assert rc == tg.GEMM_OK, tg.gemm_last_error()
+    assert tg.gemm_get_status(s) == tg.GEMM_OK, tg.gemm_last_error()
+    refs = []
+    for a in As:
+        c_ref, _ = oracle_full(a, B1, dtype)
+        c_in = torch.from_numpy(c_ref).float()
+        refs.append(oracle_full(c_in if case == "fp32" else c_in.to(torch.bfloat16), B2, dtype)[0])
     for i, D in enumerate(Ds):
         assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
 

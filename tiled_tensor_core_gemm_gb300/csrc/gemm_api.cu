@@ -314,9 +314,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_tail_splits")) {
         if (v < 0 || v > 16) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_splits must be in [0, 16]");
         g_opt.tc_tail_splits = (int)v;
-    } else if (!std::strcmp(key, "tc_pdl")) {
-        if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "tc_pdl must be 0 or 1");
-        g_opt.tc_pdl = (int)v;
+    } else if (!std::strcmp(key, "pdl")) {
+        if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "pdl must be 0 or 1");
+        g_opt.pdl = (int)v;
     } else if (!std::strcmp(key, "tc_tail_halves")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_halves must be 0, 1 or 2");
         g_opt.tc_tail_halves = (int)v;
@@ -357,7 +357,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
     if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
     if (!std::strcmp(key, "tc_tail_halves")) return o.tc_tail_halves;
-    if (!std::strcmp(key, "tc_pdl")) return o.tc_pdl;
+    if (!std::strcmp(key, "pdl")) return o.pdl;
     if (!std::strcmp(key, "tc_sched")) return o.tc_sched;
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;

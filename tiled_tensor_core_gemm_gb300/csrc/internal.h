@@ -17,7 +17,7 @@ struct Options {
     int tc_max_ctas = 0;       // 0 auto
     int tc_splits = 0;         // 0 auto, else K ranges for every tile (split-K)
     int tc_tail_splits = 0;    // 0 auto (2 for TF32), 1 off, else K ranges for the last round's tiles
-    int tc_pdl = 0;            // 0 auto (on), 1 off: programmatic dependent launch of the tensor-core kernel
+    int pdl = 0;               // 0 on, 1 off: programmatic dependent launch of every kernel
     int tc_tail_halves = 0;    // 0 auto (16-bit inputs, <= 4 rounds), 1 off, 2 wherever the tile allows
     int tc_sched = 0;          // 0 auto, 1 static persistent, 2 Cluster Launch Control
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
@@ -27,6 +27,39 @@ struct Options {
     int debug_stall_mma = 0;   // test hook: make the MMA thread's first wait expire
 };
 Options options_snapshot();
+
+// Programmatic dependent launch, used by every kernel of the library: a
+// launch may start while the previous kernel on the stream finishes; each
+// kernel waits for that kernel (griddepcontrol.wait) before its first
+// global-memory access, and then lets the next launch start its own set-up.
+// The host side: cudaLaunchKernelEx with programmatic stream serialisation
+// (unless the "pdl" option turns it off).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (options_snapshot().pdl != 1) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+#ifdef __CUDACC__
+// The device side, at the top of a kernel that needs nothing from before it
+// but its arguments: wait for the previous grid, then release the next one.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 // --------------------------------------------------------------- epilogue ---
 // Fused epilogue of one call (gemm_run_ex).  active == 0: C is FP32 and gets

@@ -28,6 +28,7 @@ namespace {
 template <typename T>
 __global__ void __launch_bounds__(256) pack_rows(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
                                                  int64_t ld_dst, int64_t rows, int64_t cols) {
+    pdl_enter();
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -64,6 +65,7 @@ template <int ELEM>
 __global__ void __launch_bounds__(256) pack_rows_vec(const uint8_t *__restrict__ src, int64_t ld_src_bytes,
                                                      uint8_t *__restrict__ dst, int64_t ld_dst_bytes, int64_t rows,
                                                      int64_t row_bytes, uintptr_t lo, uintptr_t hi) {
+    pdl_enter();
     // one thread per destination 16-byte chunk, consecutive threads along a row
     const int64_t chunks = ld_dst_bytes / 16;
     const int64_t total = rows * chunks;
@@ -113,6 +115,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) transpose_tiles(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
                                                        int64_t ld_dst, int64_t rows, int64_t cols) {
     __shared__ T tile[32][33];
+    pdl_enter();
     const int64_t tiles_c = (cols + 31) / 32;
     const int64_t tiles = ((rows + 31) / 32) * tiles_c;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -138,6 +141,7 @@ __global__ void __launch_bounds__(256) transpose64_vec(const uint32_t *__restric
                                                        uint32_t *__restrict__ dst, int64_t ld_dst, int64_t rows,
                                                        int64_t cols) {
     __shared__ uint32_t tile[64][65];
+    pdl_enter();
     const int64_t tiles_c = (cols + 63) / 64;
     const int64_t tiles = ((rows + 63) / 64) * tiles_c;
     const int q = threadIdx.x & 15;    // 16-byte group within a 64-wide row
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
                                                     int64_t M, int64_t N, const EpiParams epi) {
     // Launched as a programmatic dependent of the GEMM: wait until the GEMM's
     // slab writes are complete and visible.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_enter();
     const int64_t quads_per_row = tile_cols / 4;
     const int64_t per_tile = (int64_t)tile_rows * quads_per_row;
     const int64_t total = (int64_t)tail_tiles * per_tile;
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ W,
 
 __global__ void __launch_bounds__(256) epilogue_fill(void *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
                                                      const EpiParams epi) {
+    pdl_enter();
     const int64_t total = M * N;
     for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = x / N, c = x - r * N;
@@ -277,24 +282,21 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
     if (vec) {
         const int64_t tiles64 = ((rows + 63) / 64) * ((cols + 63) / 64);
         const int blocks64 = (int)(tiles64 < (int64_t)sms * 8 ? (tiles64 > 0 ? tiles64 : 1) : (int64_t)sms * 8);
-        transpose64_vec<<<blocks64, 256, 0, stream>>>(static_cast<const uint32_t *>(src), ld_src,
-                                                      static_cast<uint32_t *>(dst), ld_dst, rows, cols);
-        return cudaGetLastError();
+        return launch_pdl(transpose64_vec, dim3(blocks64), dim3(256), 0, stream, static_cast<const uint32_t *>(src),
+                          ld_src, static_cast<uint32_t *>(dst), ld_dst, rows, cols);
     }
     const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-    const int blocks = (int)(tiles < (int64_t)sms * 8 ? (tiles > 0 ? tiles : 1) : (int64_t)sms * 8);
+    const dim3 grid((unsigned)(tiles < (int64_t)sms * 8 ? (tiles > 0 ? tiles : 1) : (int64_t)sms * 8));
     if (elem_bytes == 1)
-        transpose_tiles<uint8_t><<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(src), ld_src,
-                                                             static_cast<uint8_t *>(dst), ld_dst, rows, cols);
-    else if (elem_bytes == 2)
-        transpose_tiles<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
-                                                              static_cast<uint16_t *>(dst), ld_dst, rows, cols);
-    else if (elem_bytes == 4)
-        transpose_tiles<uint32_t><<<blocks, 256, 0, stream>>>(static_cast<const uint32_t *>(src), ld_src,
-                                                              static_cast<uint32_t *>(dst), ld_dst, rows, cols);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(transpose_tiles<uint8_t>, grid, dim3(256), 0, stream, static_cast<const uint8_t *>(src),
+                          ld_src, static_cast<uint8_t *>(dst), ld_dst, rows, cols);
+    if (elem_bytes == 2)
+        return launch_pdl(transpose_tiles<uint16_t>, grid, dim3(256), 0, stream, static_cast<const uint16_t *>(src),
+                          ld_src, static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    if (elem_bytes == 4)
+        return launch_pdl(transpose_tiles<uint32_t>, grid, dim3(256), 0, stream, static_cast<const uint32_t *>(src),
+                          ld_src, static_cast<uint32_t *>(dst), ld_dst, rows, cols);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int tile_rows, int tile_cols,
@@ -308,23 +310,11 @@ cudaError_t split_reduce_launch(const float *W, int tail_tiles, int splits, int 
     const int64_t want = (quads + 255) / 256;
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
     const bool vec = (ldc % 4 == 0) && ((uintptr_t)C % 16 == 0);
-    // Programmatic stream serialisation: the launch may overlap the GEMM's
-    // tail; the kernel's griddepcontrol.wait keeps the reads after its writes.
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (vec)
-        return cudaLaunchKernelEx(&cfg, split_reduce<true>, W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                                  tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
-    return cudaLaunchKernelEx(&cfg, split_reduce<false>, W, tail_tiles, splits, tile_rows, tile_cols, full_tiles,
-                              tiles_m, tiles_n, group_m, C, ldc, M, N, epi);
+    // The launch may overlap the GEMM's tail (which releases it at its
+    // teardown); the kernel's wait keeps the reads after the GEMM's writes.
+    return launch_pdl(vec ? split_reduce<true> : split_reduce<false>, dim3((unsigned)blocks), dim3(256), 0, stream, W,
+                      tail_tiles, splits, tile_rows, tile_cols, full_tiles, tiles_m, tiles_n, group_m, C, ldc, M, N,
+                      epi);
 }
 
 cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, const EpiParams &epi,
@@ -334,8 +324,7 @@ cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, con
     if (e != cudaSuccess) return e;
     const int64_t want = (M * N + 255) / 256;
     const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
-    epilogue_fill<<<blocks, 256, 0, stream>>>(C, ldc, M, N, epi);
-    return cudaGetLastError();
+    return launch_pdl(epilogue_fill, dim3(blocks), dim3(256), 0, stream, C, ldc, M, N, epi);
 }
 
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols,
@@ -344,39 +333,36 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
     const int64_t want = (rows + 7) / 8;   // 8 warps per block, one row per warp per pass
-    const int blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    const dim3 grid((unsigned)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8));
     // The vector form needs a 16-byte aligned destination with 16-byte rows.
     if ((uintptr_t)dst % 16 == 0 && (ld_dst * elem_bytes) % 16 == 0 && src_hi > src_lo) {
         const int64_t chunks = rows * (ld_dst * elem_bytes / 16);
         const int64_t vwant = (chunks + 255) / 256;
-        const int vblocks = (int)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16);
+        const dim3 vgrid((unsigned)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16));
         const uint8_t *s = static_cast<const uint8_t *>(src);
         uint8_t *d = static_cast<uint8_t *>(dst);
+        const uintptr_t lo = (uintptr_t)src_lo, hi = (uintptr_t)src_hi;
+        const int64_t eb = elem_bytes;
         if (elem_bytes == 1)
-            pack_rows_vec<1><<<vblocks, 256, 0, stream>>>(s, ld_src, d, ld_dst, rows, cols, (uintptr_t)src_lo,
-                                                         (uintptr_t)src_hi);
-        else if (elem_bytes == 2)
-            pack_rows_vec<2><<<vblocks, 256, 0, stream>>>(s, ld_src * 2, d, ld_dst * 2, rows, cols * 2,
-                                                         (uintptr_t)src_lo, (uintptr_t)src_hi);
-        else if (elem_bytes == 4)
-            pack_rows_vec<4><<<vblocks, 256, 0, stream>>>(s, ld_src * 4, d, ld_dst * 4, rows, cols * 4,
-                                                         (uintptr_t)src_lo, (uintptr_t)src_hi);
-        else
-            return cudaErrorInvalidValue;
-        return cudaGetLastError();
+            return launch_pdl(pack_rows_vec<1>, vgrid, dim3(256), 0, stream, s, ld_src, d, ld_dst, rows, cols, lo, hi);
+        if (elem_bytes == 2)
+            return launch_pdl(pack_rows_vec<2>, vgrid, dim3(256), 0, stream, s, ld_src * eb, d, ld_dst * eb, rows,
+                              cols * eb, lo, hi);
+        if (elem_bytes == 4)
+            return launch_pdl(pack_rows_vec<4>, vgrid, dim3(256), 0, stream, s, ld_src * eb, d, ld_dst * eb, rows,
+                              cols * eb, lo, hi);
+        return cudaErrorInvalidValue;
     }
     if (elem_bytes == 1)
-        pack_rows<uint8_t><<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(src), ld_src,
-                                                       static_cast<uint8_t *>(dst), ld_dst, rows, cols);
-    else if (elem_bytes == 2)
-        pack_rows<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), ld_src,
-                                                        static_cast<uint16_t *>(dst), ld_dst, rows, cols);
-    else if (elem_bytes == 4)
-        pack_rows<uint32_t><<<blocks, 256, 0, stream>>>(static_cast<const uint32_t *>(src), ld_src,
-                                                        static_cast<uint32_t *>(dst), ld_dst, rows, cols);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(pack_rows<uint8_t>, grid, dim3(256), 0, stream, static_cast<const uint8_t *>(src), ld_src,
+                          static_cast<uint8_t *>(dst), ld_dst, rows, cols);
+    if (elem_bytes == 2)
+        return launch_pdl(pack_rows<uint16_t>, grid, dim3(256), 0, stream, static_cast<const uint16_t *>(src), ld_src,
+                          static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    if (elem_bytes == 4)
+        return launch_pdl(pack_rows<uint32_t>, grid, dim3(256), 0, stream, static_cast<const uint32_t *>(src), ld_src,
+                          static_cast<uint32_t *>(dst), ld_dst, rows, cols);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tcgemm

@@ -19,9 +19,12 @@
 // From "GPU architecture and mapping kernels" (ch. 12) section 12.5: thread x
 // runs along the contiguous axis of every global access (coalescing).
 //
-// Numerics: plain FP32 fmaf with k ascending per output; no fast-math, no
-// TF32.  Every size >= 1 is legal: out-of-range loads read 0 and out-of-range
-// stores are skipped.
+// Numerics: FP32 fused multiply-adds, one rounding each, k ascending per
+// output; no fast-math, no TF32.  The FMAs go two at a time (sm_100's paired
+// FP32 FMA on a float2: outputs j and j+1 of a row share a[i]), which halves
+// the FMA instructions the issue slots must carry and leaves every result
+// bit-identical to fmaf.  Every size >= 1 is legal: out-of-range loads read 0
+// and out-of-range stores are skipped.
 #include <type_traits>
 
 #include "epilogue.cuh"
@@ -84,6 +87,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, MIN_BLOCKS)
 sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
             const float *__restrict__ B, int64_t ldb, void *__restrict__ Cv, int64_t ldc, const EpiParams epi) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, RM = Cfg::RM, RN = Cfg::RN;
+    pdl_enter();
     extern __shared__ float4 smem_f4[];
     float *smem = reinterpret_cast<float *>(smem_f4);
     // sA[buf][k][m] (transposed, padded pitch), then sB[buf][k][n].
@@ -131,11 +135,13 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         }
     };
 
-    float acc[4 * RM][4 * RN];
+    // acc2[i][j] holds outputs (i, 2j) and (i, 2j + 1) of the micro-tile.
+    float2 acc2[4 * RM][2 * RN];
 #pragma unroll
     for (int i = 0; i < 4 * RM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4 * RN; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 2 * RN; ++j) acc2[i][j] = make_float2(0.f, 0.f);
+    auto acc = [&](int i, int j) -> float { return (j & 1) ? acc2[i][j >> 1].y : acc2[i][j >> 1].x; };
 
     const int ktiles = (K + BK - 1) / BK;
     // One K step on buffer BUF (a compile-time constant, so every shared
@@ -158,9 +164,12 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                 b[4 * q + 0] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
             }
 #pragma unroll
-            for (int i = 0; i < 4 * RM; ++i)
+            for (int i = 0; i < 4 * RM; ++i) {
+                const float2 ai = make_float2(a[i], a[i]);
 #pragma unroll
-                for (int j = 0; j < 4 * RN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 2 * RN; ++j)
+                    acc2[i][j] = __ffma2_rn(ai, make_float2(b[2 * j], b[2 * j + 1]), acc2[i][j]);
+            }
         }
         // The other buffer was last read before the previous barrier, so it can
         // be refilled now; the barrier below publishes it and also keeps this
@@ -188,7 +197,7 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
 #pragma unroll
             for (int j = 0; j < 4 * RN; ++j) {
                 const int64_t col = n0 + (j / 4) * (BN / RN) + tx * 4 + (j % 4);
-                if (col < N) epi_write(epi, Cv, row * ldc + col, acc[i][j], bias[j]);
+                if (col < N) epi_write(epi, Cv, row * ldc + col, acc(i, j), bias[j]);
             }
         }
         return;
@@ -199,8 +208,8 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         const int64_t row = m0 + (i / 4) * (BM / RM) + ty * 4 + (i % 4);
 #pragma unroll
         for (int q = 0; q < RN; ++q)
-            store_row4<VEC>(C, row, n0 + q * (BN / RN) + tx * 4, ldc, M, N, acc[i][4 * q + 0], acc[i][4 * q + 1],
-                            acc[i][4 * q + 2], acc[i][4 * q + 3]);
+            store_row4<VEC>(C, row, n0 + q * (BN / RN) + tx * 4, ldc, M, N, acc(i, 4 * q + 0), acc(i, 4 * q + 1),
+                            acc(i, 4 * q + 2), acc(i, 4 * q + 3));
     }
 }
 
@@ -214,14 +223,13 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
     }
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(M, N, K, A, lda, B, ldb, C, ldc, epi);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, s, M, N, K, A, lda, B, ldb, C, ldc, epi);
 }
 
 // The compiled variants: id, tile, K step, quads per thread, min resident blocks.
 #define SIMT_VARIANTS(X)          \
     X(1, 128, 128, 8, 2, 2, 2)    \
-    X(2, 128, 128, 16, 2, 2, 2)   \
+    X(2, 128, 128, 16, 2, 2, 1)   \
     X(3, 128, 256, 8, 2, 4, 1)    \
     X(4, 256, 128, 8, 4, 2, 1)    \
     X(5, 64, 64, 8, 2, 2, 4)      \

@@ -905,7 +905,7 @@ int launch_kernel(const gemm_plan_t &plan, const CUtensorMap &ta, const CUtensor
         attr[n_attr].val.clusterDim.z = 1;
         ++n_attr;
     }
-    if (options_snapshot().tc_pdl != 1) {
+    if (options_snapshot().pdl != 1) {
         // may start while the previous kernel on the stream finishes (the
         // kernel waits for it before touching global memory)
         attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
