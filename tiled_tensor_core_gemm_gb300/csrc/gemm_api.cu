@@ -112,9 +112,10 @@ int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 
 
 // Measured on GB300 (profiles/picker.md): at 4096^3 the 128 x 128 tile with a
 // K step of 16 beats K step 8 and the 8 x 16 register tiles; when 128 x 128
-// tiles leave SMs idle (1024^3) the 64 x 64 tile with a K step of 8 is best.
+// tiles leave SMs idle (1024^3, 256^3) the 64 x 64 tile with a K step of 16
+// is best.
 constexpr int kSimtLarge = 2;   // 128 x 128 x 16, 8 x 8 per thread
-constexpr int kSimtSmall = 5;   // 64 x 64 x 8
+constexpr int kSimtSmall = 7;   // 64 x 64 x 16
 constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills the ring several times
 // Split-K adds a second kernel and a workspace round trip (a few microseconds):
 // only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
