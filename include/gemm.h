@@ -103,8 +103,9 @@ typedef enum {
  * persistent schedule would fill at most half of the machine, 16-bit inputs
  * on short schedules run them as two column halves each (every half over
  * all of K, straight to C: no workspace, and the same sums as a whole
- * tile); on request ("tc_tail_splits") they are split in K instead, like
- * split-K.
+ * tile; the launch ends sooner because each half's epilogue drains half the
+ * accumulator); on request ("tc_tail_splits") they are split in K instead,
+ * like split-K.
  * C leaves through TMA stores when its base, pitch and row length (N
  * elements) are all multiples of 16 bytes, else through ordinary stores.
  *

@@ -252,11 +252,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
                (opt.tc_tail_halves == 2 ||
                 (opt.tc_tail_halves == 0 && elem == 2 && tiles <= kMaxRoundsForHalves * units))) {
         // The last round's tiles as column halves: twice the units, each over
-        // all of K, so no partial sums to combine.  A half needs 1.5x the
-        // operand bytes per flop of a whole tile, so it takes more than half
-        // as long.  Measured on GB300 (profiles/picker.md): +2% on 16-bit
-        // inputs with 3-4 rounds (4096^3, 16384 x 1024 x 4096), neutral at
-        // 8192^3 (14 power-capped rounds), -3% on TF32 against its K split.
+        // all of K, so no partial sums to combine.  A half's main loop takes
+        // as many cycles as a whole tile's (the K-block cadence, about 545
+        // cycles, not the MMA, sets its pace), but its epilogue drains half
+        // the accumulator, which shortens the end of the launch.  Measured on
+        // GB300 (profiles/picker.md): +2% on 16-bit inputs with 3-4 rounds
+        // (4096^3, 16384 x 1024 x 4096), neutral at 8192^3 (14 power-capped
+        // rounds), -3% on TF32 against its K split.
         half = rem;
     } else if ((opt.tc_tail_splits >= 2 || (opt.tc_tail_splits == 0 && dtype == GEMM_TF32)) && rem > 0) {
         // Split only the tiles of the last, partly idle round of the persistent

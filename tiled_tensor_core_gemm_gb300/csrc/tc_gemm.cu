@@ -149,7 +149,10 @@ struct TcParams {
 // Units [0, full_tiles) are whole tiles.  The tiles that would leave part of
 // the machine idle in the last round of the persistent schedule are either
 // (a) run as two column halves each, over all of K and straight to C, when
-//     the halves fit in one round: that round then takes half as long; or
+//     the halves fit in one round (each half drains half the accumulator, so
+//     the launch's last epilogue is shorter; the main loop of a half takes
+//     as many cycles as a whole tile's: the K-block cadence, not the MMA,
+//     sets it); or
 // (b) split into K ranges, as is every tile when K is split throughout; the
 //     ranges of one split index come together, so units that run at once read
 //     the same slices of A and B.  Partial tiles go to slabs (one full tile
