@@ -263,8 +263,9 @@ def test_split_k_deterministic_on_random_data():
     assert np.array_equal(C1, C2)
 
 
+@pytest.mark.parametrize("pdl", (0, 1), ids=("pdl_on", "pdl_off"))
 @pytest.mark.parametrize("n", (512, 2048))
-def test_back_to_back_launches_read_the_previous_output(n):
+def test_back_to_back_launches_read_the_previous_output(n, pdl):
     """A tensor-core launch starts its set-up while the previous kernel on the
     stream finishes (programmatic dependent launch).  Here each step writes C1
     (BF16) and the next launch reads C1 as its A; the step after that
@@ -281,14 +282,17 @@ def test_back_to_back_launches_read_the_previous_output(n):
     Ds = [torch.empty((n, n), dtype=torch.float32, device="cuda") for _ in range(8)]
     s = torch.cuda.current_stream().cuda_stream
     ep = tg.make_epilogue(out="bf16")
-    assert tg.gemm_get_option("pdl") == 0                      # on
-    for i, D in enumerate(Ds):
-        a = a_dev[i % 2]
-        rc = tg.gemm_run_ex(n, n, k1, tg.GEMM_BF16, a.data_ptr(), k1, b1.data_ptr(), n, c1.data_ptr(), n, ep, s)
-        assert rc == tg.GEMM_OK, tg.gemm_last_error()
-        rc = tg.gemm_run(n, n, n, tg.GEMM_BF16, c1.data_ptr(), n, b2.data_ptr(), n, D.data_ptr(), n, s)
-        assert rc == tg.GEMM_OK, tg.gemm_last_error()
-    assert tg.gemm_get_status(s) == tg.GEMM_OK, tg.gemm_last_error()
+    assert tg.gemm_set_option("pdl", pdl) == tg.GEMM_OK
+    try:
+        for i, D in enumerate(Ds):
+            a = a_dev[i % 2]
+            rc = tg.gemm_run_ex(n, n, k1, tg.GEMM_BF16, a.data_ptr(), k1, b1.data_ptr(), n, c1.data_ptr(), n, ep, s)
+            assert rc == tg.GEMM_OK, tg.gemm_last_error()
+            rc = tg.gemm_run(n, n, n, tg.GEMM_BF16, c1.data_ptr(), n, b2.data_ptr(), n, D.data_ptr(), n, s)
+            assert rc == tg.GEMM_OK, tg.gemm_last_error()
+        assert tg.gemm_get_status(s) == tg.GEMM_OK, tg.gemm_last_error()
+    finally:
+        tg.gemm_set_option("pdl", 0)
     refs = []
     for a in As:
         c_ref, _ = oracle_full(a, B1, "bf16")
