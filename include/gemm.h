@@ -248,7 +248,9 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "simt_variant"   force a SIMT variant: 1 = 128x128 tile, K step 8, 8x8
  *                    outputs per thread; 2 = same with K step 16; 3 = 128x256,
  *                    8x16 per thread; 4 = 256x128, 16x8 per thread; 5 = 64x64;
- *                    6 = 128x256 with K step 16; 7 = 64x64 with K step 16
+ *                    6 = 128x256 with K step 16; 7 = 64x64 with K step 16;
+ *                    8 = 128x64 and 9 = 64x128 with K step 16, 8x8 per
+ *                    thread in 128-thread blocks (9 is the default)
  *   "tc_b_major"     0 auto (BF16, FP16, FP8: B read as stored, N-major, except
  *                    FP8 tiles of 64 columns per CTA; TF32: B read from a
  *                    K-major transposed copy), 1 force the transposed copy,

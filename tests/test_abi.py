@@ -119,12 +119,14 @@ def test_plan_tf32_and_fp32_4096():
     assert p["path"] == 1 and p["bk"] == 32 and p["b_kmajor"] == 1 and p["pack_b"] == 0
     assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["b_kmajor"] == 0
     s = _plan(4096, 4096, 4096, tg.GEMM_FP32)
-    assert s["path"] == 0 and s["bm"] == 128 and s["bk"] == 16 and s["vec"] == 1 and s["grid"] == 32 * 32
+    assert s["path"] == 0 and s["bm"] == 64 and s["bn"] == 128 and s["bk"] == 16 and s["vec"] == 1
+    assert s["grid"] == 64 * 32
 
 
-def test_plan_small_fp32_shrinks_tile_to_fill_machine():
-    assert _plan(1024, 1024, 1024, tg.GEMM_FP32)["bm"] == 64
-    assert _plan(256, 256, 256, tg.GEMM_FP32)["bm"] == 64
+def test_plan_fp32_uses_64x128_tiles_at_every_size():
+    for n in (256, 1024, 4096):
+        p = _plan(n, n, n, tg.GEMM_FP32)
+        assert (p["bm"], p["bn"], p["bk"]) == (64, 128, 16), p
 
 
 def test_plan_ragged_packs_and_plain_epilogue():

@@ -346,7 +346,7 @@ def test_back_to_back_chain_through_packs_and_simt(case):
         assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
 
 
-@pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7))
+@pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7, 8, 9))
 @pytest.mark.parametrize("shape", [(513, 389, 1027), (300, 520, 64), (1, 1000, 17)], ids=lambda s: "x".join(map(str, s)))
 def test_simt_variants_exact(variant, shape):
     M, N, K = shape

@@ -110,12 +110,11 @@ bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
 
 int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 2 : is_fp8(dtype) ? 1 : 4; }
 
-// Measured on GB300 (profiles/picker.md): at 4096^3 the 128 x 128 tile with a
-// K step of 16 beats K step 8 and the 8 x 16 register tiles; when 128 x 128
-// tiles leave SMs idle (1024^3, 256^3) the 64 x 64 tile with a K step of 16
-// is best.
-constexpr int kSimtLarge = 2;   // 128 x 128 x 16, 8 x 8 per thread
-constexpr int kSimtSmall = 7;   // 64 x 64 x 16
+// Measured on GB300 (profiles/picker.md): with the paired FP32 FMAs the
+// 64 x 128 tile with a K step of 16 (128 threads of 8 x 8 outputs, three
+// blocks and 12 warps per SM) beats the 256-thread 128 x 128 tile (8 warps per
+// SM) at 4096^3, 1024^3 and 256^3.
+constexpr int kSimtDefault = 9;   // 64 x 128 x 16, 8 x 8 per thread
 constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills the ring several times
 // Split-K adds a second kernel and a workspace round trip (a few microseconds):
 // only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
@@ -138,9 +137,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     out->ldb_eff = ldb;
     if (num_sms <= 0) num_sms = 1;
     if (dtype == GEMM_FP32) {
-        // Large problems: the 128 x 128 tile; if that leaves SMs idle, 64 x 64.
         int id = opt.simt_variant;
-        if (id == 0) id = cdiv(M, 128) * cdiv(N, 128) >= num_sms ? kSimtLarge : kSimtSmall;
+        if (id == 0) id = kSimtDefault;
         int bm = 0, bn = 0, bk = 0, smem = 0;
         if (!simt_variant_tile(id, &bm, &bn, &bk, &smem))
             return fail(GEMM_ERR_UNSUPPORTED, "no SIMT variant %d", id);

@@ -234,7 +234,9 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
     X(4, 256, 128, 8, 4, 2, 1)    \
     X(5, 64, 64, 8, 2, 2, 4)      \
     X(6, 128, 256, 16, 2, 4, 1)   \
-    X(7, 64, 64, 16, 2, 2, 4)
+    X(7, 64, 64, 16, 2, 2, 4)     \
+    X(8, 128, 64, 16, 2, 2, 3)    \
+    X(9, 64, 128, 16, 2, 2, 3)
 
 }  // namespace
 
