@@ -228,6 +228,11 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *   "tc_splits"      force split-K: K ranges for every output tile (1..32);
  *                    the partial tiles go to a workspace and are summed into
  *                    C in a fixed order by a second kernel
+ *   "simt_splits"    FP32 (SIMT): 0 auto -- when the tiles cannot give every
+ *                    SM about six blocks, K is cut into up to 8 ranges of
+ *                    at least 32, their partial sums kept in a stream-ordered
+ *                    workspace and added in order by a second kernel (the
+ *                    result does not depend on timing); 1 off; n force n
  *   "tc_tail_splits" 0 auto (2 for TF32 when the column halves below do not
  *                    apply, off otherwise), 1 off, n >= 2: split the tiles
  *                    of the last, partly idle round of the persistent
@@ -283,7 +288,8 @@ typedef struct {
     int32_t vec;         /* SIMT: 16-byte vector loads/stores legal        */
     int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
     int32_t b_kmajor;    /* B staged K-major from a transposed copy (TF32)  */
-    int32_t splits;      /* K ranges per split tile; 1 = no tile split       */
+    int32_t splits;      /* K ranges per split tile (tensor cores) or per
+                            SIMT block (FP32); 1 = no split                */
     int32_t tail_tiles;  /* tiles split into K ranges (the last ones in the
                             schedule; all tiles under full split-K)       */
     int32_t sched;       /* 0: static persistent stride over work units;

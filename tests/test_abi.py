@@ -129,6 +129,28 @@ def test_plan_fp32_uses_64x128_tiles_at_every_size():
         assert (p["bm"], p["bn"], p["bk"]) == (64, 128, 16), p
 
 
+def test_plan_fp32_splits_k_when_tiles_are_few():
+    # target 6 x 152 blocks: 1024^3 has 128 tiles -> 8 K ranges; 256^3 8 tiles,
+    # capped at 8; 2048^3 512 tiles -> 2; 4096^3 fills the machine
+    assert _plan(1024, 1024, 1024, tg.GEMM_FP32)["splits"] == 8
+    assert _plan(1024, 1024, 1024, tg.GEMM_FP32)["grid"] == 1024
+    assert _plan(256, 256, 256, tg.GEMM_FP32)["splits"] == 8
+    assert _plan(2048, 2048, 2048, tg.GEMM_FP32)["splits"] == 2
+    assert _plan(4096, 4096, 4096, tg.GEMM_FP32)["splits"] == 1
+    assert _plan(1000, 1000, 100, tg.GEMM_FP32)["splits"] == 3          # ranges of at least 32
+    assert _plan(1000, 1000, 50, tg.GEMM_FP32)["splits"] == 1           # K too short
+    assert _plan(513, 389, 1027, tg.GEMM_FP32)["splits"] == 8           # capped at 8
+    try:
+        assert tg.gemm_set_option("simt_splits", 1) == 0
+        assert _plan(1024, 1024, 1024, tg.GEMM_FP32)["splits"] == 1
+        assert tg.gemm_set_option("simt_splits", 3) == 0
+        assert _plan(4096, 4096, 4096, tg.GEMM_FP32)["splits"] == 3
+        assert _plan(64, 64, 16, tg.GEMM_FP32)["splits"] == 1           # never more ranges than K steps
+    finally:
+        tg.gemm_set_option("simt_splits", 0)
+    assert tg.gemm_set_option("simt_splits", 9) == tg.GEMM_ERR_INVALID_ARG
+
+
 def test_plan_ragged_packs_and_plain_epilogue():
     p = _plan(4097, 4095, 4099, tg.GEMM_BF16)
     assert p["pack_a"] and p["pack_b"] and not p["tma_store"]

@@ -346,6 +346,24 @@ def test_back_to_back_chain_through_packs_and_simt(case):
         assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
 
 
+@pytest.mark.parametrize("splits", (0, 2, 3, 8))
+@pytest.mark.parametrize("shape", [(513, 389, 1027), (256, 256, 256), (1, 1000, 17), (1000, 7, 1000), (300, 520, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_simt_split_k_exact(shape, splits):
+    """FP32 K cut into ranges (automatic, or forced), partials added in order by
+    a second kernel: small integers stay exact; the result is the same run to run."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "fp32", "ints", seed=170)
+    try:
+        tg.gemm_set_option("simt_splits", splits)
+        _exact(A, B, "fp32")
+        _exact(A, B, "fp32", ldc_pad=3)
+        An, Bn = make_operands(M, N, K, "fp32", "normal", seed=171)
+        assert np.array_equal(run_gemm(An, Bn, "fp32"), run_gemm(An, Bn, "fp32"))
+    finally:
+        tg.gemm_set_option("simt_splits", 0)
+
+
 @pytest.mark.parametrize("variant", (1, 2, 3, 4, 5, 6, 7, 8, 9))
 @pytest.mark.parametrize("shape", [(513, 389, 1027), (300, 520, 64), (1, 1000, 17)], ids=lambda s: "x".join(map(str, s)))
 def test_simt_variants_exact(variant, shape):

@@ -115,6 +115,11 @@ int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 
 // blocks and 12 warps per SM) beats the 256-thread 128 x 128 tile (8 warps per
 // SM) at 4096^3, 1024^3 and 256^3.
 constexpr int kSimtDefault = 9;   // 64 x 128 x 16, 8 x 8 per thread
+// SIMT split-K target: about two waves of the three resident 128-thread
+// blocks per SM, K ranges of at least 32 (measured on GB300, picker.md:
+// 8 ranges at 1024^3 and 256^3, 2 at 2048^3, none at 4096^3).
+constexpr int kSimtBlocksPerSm = 6;
+constexpr int64_t kSimtMinKPerSplit = 32;
 constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills the ring several times
 // Split-K adds a second kernel and a workspace round trip (a few microseconds):
 // only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
@@ -150,7 +155,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         p.cta_group = 1;
         p.group_m = 1;
         p.tiles = (int32_t)(cdiv(M, bm) * cdiv(N, bn));
-        p.grid = p.tiles;
+        // Too few tiles for about two waves of three blocks per SM (each
+        // block's K loop is latency-bound): cut K into up to 8 ranges of at
+        // least 32, summed in order by a second kernel.
+        int64_t splits = opt.simt_splits > 0 ? opt.simt_splits : 1;
+        if (opt.simt_splits == 0 && p.tiles < kSimtBlocksPerSm * num_sms && K >= 2 * kSimtMinKPerSplit)
+            splits = std::min<int64_t>({cdiv(kSimtBlocksPerSm * num_sms, p.tiles), K / kSimtMinKPerSplit, 8});
+        p.splits = (int32_t)std::max<int64_t>(1, std::min<int64_t>(splits, std::max<int64_t>(1, cdiv(K, bk))));
+        p.grid = p.tiles * p.splits;
         p.vec = (lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && a_addr % 16 == 0 && b_addr % 16 == 0 &&
                  c_addr % 16 == 0);
         p.smem_bytes = smem;
@@ -318,6 +330,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "pdl")) {
         if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "pdl must be 0 or 1");
         g_opt.pdl = (int)v;
+    } else if (!std::strcmp(key, "simt_splits")) {
+        if (v < 0 || v > 8) return fail(GEMM_ERR_INVALID_ARG, "simt_splits must be in [0, 8]");
+        g_opt.simt_splits = (int)v;
     } else if (!std::strcmp(key, "tc_tail_halves")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_halves must be 0, 1 or 2");
         g_opt.tc_tail_halves = (int)v;
@@ -358,6 +373,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
     if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
     if (!std::strcmp(key, "tc_tail_halves")) return o.tc_tail_halves;
+    if (!std::strcmp(key, "simt_splits")) return o.simt_splits;
     if (!std::strcmp(key, "pdl")) return o.pdl;
     if (!std::strcmp(key, "tc_sched")) return o.tc_sched;
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
@@ -482,8 +498,22 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
     const gemm_plan_t &p = plan.pub;
 
     if (p.path == 0) {
+        // K ranges: their partial sums live in a stream-ordered workspace.
+        void *sw = nullptr;
+        if (p.splits > 1) {
+            const size_t bytes = (size_t)p.splits * (size_t)M * (size_t)N * 4;
+            e = cudaMallocAsync(&sw, bytes, stream);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(GEMM_ERR_NO_MEMORY, "workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+            }
+        }
         e = simt_fp32_launch(p, (int)M, (int)N, (int)K, static_cast<const float *>(A), lda,
-                             static_cast<const float *>(B), ldb, C, ldc, epi, stream);
+                             static_cast<const float *>(B), ldb, C, ldc, epi, static_cast<float *>(sw), stream);
+        if (sw) {
+            const cudaError_t f = cudaFreeAsync(sw, stream);
+            if (e == cudaSuccess) e = f;
+        }
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_CUDA, "SIMT kernel launch: %s", cudaGetErrorString(e));
     }
     // Tensor-core path: pack operands TMA cannot address, then launch.

@@ -18,6 +18,7 @@ struct Options {
     int tc_splits = 0;         // 0 auto, else K ranges for every tile (split-K)
     int tc_tail_splits = 0;    // 0 auto (2 for TF32), 1 off, else K ranges for the last round's tiles
     int pdl = 0;               // 0 on, 1 off: programmatic dependent launch of every kernel
+    int simt_splits = 0;       // 0 auto, 1 off, n: K ranges for the SIMT kernel
     int tc_tail_halves = 0;    // 0 auto (16-bit inputs, <= 4 rounds), 1 off, 2 wherever the tile allows
     int tc_sched = 0;          // 0 auto, 1 static persistent, 2 Cluster Launch Control
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
@@ -100,10 +101,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype,
 
 // ------------------------------------------------------------------- SIMT ---
 // C = A.B in exact FP32 with the tile the plan chose, written through `epi`
-// (C's element type is epi.out when epi.active, else FP32).
+// (C's element type is epi.out when epi.active, else FP32).  With
+// plan.splits > 1, K is cut into that many ranges whose partial sums go to W
+// (plan.splits x M x N floats) and a second kernel adds them in order.
 cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K,
                              const float *A, int64_t lda, const float *B, int64_t ldb,
-                             void *C, int64_t ldc, const EpiParams &epi, cudaStream_t stream);
+                             void *C, int64_t ldc, const EpiParams &epi, float *W, cudaStream_t stream);
 
 // Tile of SIMT variant `id` (bm, bn, bk, dynamic shared bytes); 0 if unknown.
 int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem);

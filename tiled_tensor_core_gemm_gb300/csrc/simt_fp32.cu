@@ -85,7 +85,8 @@ __device__ __forceinline__ void store_row4(float *__restrict__ p, int64_t row, i
 template <class Cfg, int MIN_BLOCKS, bool VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, MIN_BLOCKS)
 sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
-            const float *__restrict__ B, int64_t ldb, void *__restrict__ Cv, int64_t ldc, const EpiParams epi) {
+            const float *__restrict__ B, int64_t ldb, void *__restrict__ Cv, int64_t ldc, const EpiParams epi,
+            int kps, float *__restrict__ W) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, RM = Cfg::RM, RN = Cfg::RN;
     pdl_enter();
     extern __shared__ float4 smem_f4[];
@@ -98,6 +99,10 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
     const int tx = tid % Cfg::TX, ty = tid / Cfg::TX;
     const int64_t m0 = (int64_t)blockIdx.y * BM;
     const int64_t n0 = (int64_t)blockIdx.x * BN;
+    // Split K: block z sums k in [kb, ke) (kps a multiple of BK, so vector
+    // loads stay aligned) and leaves its partial in W[z]; otherwise all of K.
+    const int kb = kps > 0 ? (int)blockIdx.z * kps : 0;
+    const int ke = kps > 0 ? min(K, kb + kps) : K;
 
     float4 ra[Cfg::A_VEC], rb[Cfg::B_VEC];
 
@@ -107,13 +112,13 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         for (int i = 0; i < Cfg::A_VEC; ++i) {
             const int f = tid + i * Cfg::THREADS;
             const int r = f / (BK / 4), kq = f % (BK / 4);
-            ra[i] = load_row4<VEC>(A, m0 + r, (int64_t)k0 + 4 * kq, lda, M, K);
+            ra[i] = load_row4<VEC>(A, m0 + r, (int64_t)kb + k0 + 4 * kq, lda, M, ke);
         }
 #pragma unroll
         for (int i = 0; i < Cfg::B_VEC; ++i) {
             const int f = tid + i * Cfg::THREADS;
             const int kr = f / (BN / 4), c4 = f % (BN / 4);
-            rb[i] = load_row4<VEC>(B, (int64_t)k0 + kr, n0 + 4 * c4, ldb, K, N);
+            rb[i] = load_row4<VEC>(B, (int64_t)kb + k0 + kr, n0 + 4 * c4, ldb, ke, N);
         }
     };
     // Registers -> shared buffer `buf`: A transposed to [k][m], B as is.
@@ -143,7 +148,7 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         for (int j = 0; j < 2 * RN; ++j) acc2[i][j] = make_float2(0.f, 0.f);
     auto acc = [&](int i, int j) -> float { return (j & 1) ? acc2[i][j >> 1].y : acc2[i][j >> 1].x; };
 
-    const int ktiles = (K + BK - 1) / BK;
+    const int ktiles = ke > kb ? (ke - kb + BK - 1) / BK : 0;
     // One K step on buffer BUF (a compile-time constant, so every shared
     // address below is a fixed offset from one base register).
     auto step = [&](auto buf_c, int kt) {
@@ -185,6 +190,26 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         if (kt + 1 < ktiles) step(std::integral_constant<int, 1>{}, kt + 1);
     }
 
+    if (W != nullptr) {
+        // A K range's partial sums, raw: W[z] is M x N, row-major.
+        float *w = W + (int64_t)blockIdx.z * M * N;
+        const bool wvec = VEC && (N % 4 == 0);
+#pragma unroll
+        for (int i = 0; i < 4 * RM; ++i) {
+            const int64_t row = m0 + (i / 4) * (BM / RM) + ty * 4 + (i % 4);
+#pragma unroll
+            for (int q = 0; q < RN; ++q) {
+                const int64_t col = n0 + q * (BN / RN) + tx * 4;
+                if (wvec)
+                    store_row4<true>(w, row, col, N, M, N, acc(i, 4 * q + 0), acc(i, 4 * q + 1), acc(i, 4 * q + 2),
+                                     acc(i, 4 * q + 3));
+                else
+                    store_row4<false>(w, row, col, N, M, N, acc(i, 4 * q + 0), acc(i, 4 * q + 1), acc(i, 4 * q + 2),
+                                      acc(i, 4 * q + 3));
+            }
+        }
+        return;
+    }
     if (epi.active) {
         // Fused epilogue: element by element, each column's bias read once.
         float bias[4 * RN];
@@ -213,17 +238,37 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
     }
 }
 
+// Sums the K ranges' partials W[0..splits) in order (so the result does not
+// depend on which block finished first) and writes C through the epilogue.
+__global__ void __launch_bounds__(256) simt_split_reduce(const float *__restrict__ W, int splits, int64_t M,
+                                                         int64_t N, void *__restrict__ C, int64_t ldc,
+                                                         const EpiParams epi) {
+    pdl_enter();
+    const int64_t total = M * N;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+        float v = W[x];
+        for (int z = 1; z < splits; ++z) v += W[(int64_t)z * total + x];
+        const int64_t r = x / N, c = x - r * N;
+        if (epi.active) epi_write(epi, C, r * ldc + c, v, epi_bias(epi, c, N));
+        else static_cast<float *>(C)[r * ldc + c] = v;
+    }
+}
+
 template <class Cfg, int MIN_BLOCKS>
 cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, void *C, int64_t ldc, const EpiParams &epi, cudaStream_t s) {
-    const dim3 grid((unsigned)((N + Cfg::BN - 1) / Cfg::BN), (unsigned)((M + Cfg::BM - 1) / Cfg::BM));
-    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+                        int64_t ldb, void *C, int64_t ldc, const EpiParams &epi, int splits, float *W,
+                        cudaStream_t s) {
+    const int kps = splits > 1 ? (((K + splits - 1) / splits + Cfg::BK - 1) / Cfg::BK) * Cfg::BK : 0;
+    const dim3 grid((unsigned)((N + Cfg::BN - 1) / Cfg::BN), (unsigned)((M + Cfg::BM - 1) / Cfg::BM),
+                    (unsigned)(splits > 1 ? splits : 1));
+    if (grid.y > 65535u || (splits > 1 && !W)) return cudaErrorInvalidConfiguration;
     auto kern = vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true> : sgemm_tiled<Cfg, MIN_BLOCKS, false>;
     if (Cfg::SMEM_BYTES > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, s, M, N, K, A, lda, B, ldb, C, ldc, epi);
+    return launch_pdl(kern, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, s, M, N, K, A, lda, B, ldb, C, ldc, epi, kps,
+                      splits > 1 ? W : nullptr);
 }
 
 // The compiled variants: id, tile, K step, quads per thread, min resident blocks.
@@ -241,15 +286,26 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
 }  // namespace
 
 cudaError_t simt_fp32_launch(const gemm_plan_t &plan, int M, int N, int K, const float *A, int64_t lda,
-                             const float *B, int64_t ldb, void *C, int64_t ldc, const EpiParams &epi,
+                             const float *B, int64_t ldb, void *C, int64_t ldc, const EpiParams &epi, float *W,
                              cudaStream_t stream) {
+    const int splits = plan.splits > 1 ? plan.splits : 1;
+    cudaError_t e = cudaErrorInvalidValue;
+    // if (variant 1) e = ...; else if (variant 2) e = ...; ... else return (no such tile)
 #define X(id_, bm_, bn_, bk_, rm_, rn_, minb_)                                                        \
     if (plan.bm == bm_ && plan.bn == bn_ && plan.bk == bk_)                                             \
-        return launch_tile<SimtCfg<bm_, bn_, bk_, rm_, rn_>, minb_>(plan.vec != 0, M, N, K, A, lda, B, ldb, \
-                                                                    C, ldc, epi, stream);
+        e = launch_tile<SimtCfg<bm_, bn_, bk_, rm_, rn_>, minb_>(plan.vec != 0, M, N, K, A, lda, B, ldb, C, \
+                                                                 ldc, epi, splits, W, stream);          \
+    else
     SIMT_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
+    if (e != cudaSuccess || splits == 1) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t want = ((int64_t)M * N + 255) / 256;
+    const dim3 grid((unsigned)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8));
+    return launch_pdl(simt_split_reduce, grid, dim3(256), 0, stream, W, splits, (int64_t)M, (int64_t)N, C, ldc, epi);
 }
 
 int simt_variant_tile(int id, int *bm, int *bn, int *bk, int *smem) {
