@@ -27,7 +27,7 @@
  * 0.  Every product of two such values is exact in double as well.
  *
  * Besides C, every entry point can also return D[i][j] = sum_k |A[i][k]|*|B[k][j]|,
- * the scale against which an error in C[i][j] is judged (max |dC| / D).
+ * the scale against which an error in C[i][j] is measured (max |dC| / D).
  *
  * Loop orders: the main routine runs i-k-j with a per-row accumulator and an
  * OpenMP loop over rows.  A second, independent j-i-k routine exists only so the
