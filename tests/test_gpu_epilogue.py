@@ -140,6 +140,19 @@ def test_epilogue_on_column_halves(dtype, out, store):
     _check(A, B, dtype, out, 0.75, -0.5, "gelu", seed=43)
 
 
+@pytest.mark.parametrize("splits", (2, 8))
+@pytest.mark.parametrize("out", ("f32", "bf16"))
+def test_fp32_epilogue_after_simt_split_k(out, splits):
+    """FP32 K cut into ranges: the second kernel applies alpha, the residual,
+    the bias and the activation once, to the in-order sum of the ranges."""
+    tg.gemm_set_option("simt_splits", splits)
+    try:
+        A, B = make_operands(333, 257, 515, "fp32", "normal", seed=49)
+        _check(A, B, "fp32", out, 0.5, -0.75, "gelu", seed=50, ldc_pad=1)
+    finally:
+        tg.gemm_set_option("simt_splits", 0)
+
+
 @pytest.mark.parametrize("out", OUTS)
 def test_epilogue_with_k_zero(out):
     M, N = 70, 90

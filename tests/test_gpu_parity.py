@@ -227,6 +227,24 @@ def test_tail_halves_exact(dtype, cg, bn, b_major, ctas, store):
             tg.gemm_set_option(k, 0)
 
 
+@pytest.mark.parametrize("K", (1, 65, 129))
+@pytest.mark.parametrize("dtype,cg,bn,b_major,ctas", [HALF_CASES[0], HALF_CASES[2], HALF_CASES[6]],
+                         ids=lambda v: str(v))
+def test_tail_halves_short_k(dtype, cg, bn, b_major, ctas, K):
+    """Column halves whose K loop is one or two k-blocks (the ring never fills)."""
+    M, N = 1998, 1440
+    A, B = make_operands(M, N, K, dtype, "ints", seed=29)
+    opts = {"tc_cta_group": cg, "tc_bn": bn, "tc_max_ctas": ctas, "tc_b_major": b_major, "tc_tail_halves": 2}
+    try:
+        for k, v in opts.items():
+            tg.gemm_set_option(k, v)
+        assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).half_tiles > 0
+        _exact(A, B, dtype)
+    finally:
+        for k in opts:
+            tg.gemm_set_option(k, 0)
+
+
 @pytest.mark.parametrize("dtype", ("bf16", "tf32"))
 def test_tail_halves_equal_whole_tiles(dtype):
     """On random data a tile run as two column halves gives the same bits as
@@ -347,7 +365,8 @@ def test_back_to_back_chain_through_packs_and_simt(case):
 
 
 @pytest.mark.parametrize("splits", (0, 2, 3, 8))
-@pytest.mark.parametrize("shape", [(513, 389, 1027), (256, 256, 256), (1, 1000, 17), (1000, 7, 1000), (300, 520, 64)],
+@pytest.mark.parametrize("shape", [(513, 389, 1027), (256, 256, 256), (1, 1000, 17), (1000, 7, 1000), (300, 520, 64),
+                                   (200, 300, 65), (130, 129, 100), (64, 64, 257)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_simt_split_k_exact(shape, splits):
     """FP32 K cut into ranges (automatic, or forced), partials added in order by
