@@ -82,7 +82,7 @@ __device__ __forceinline__ void store_row4(float *__restrict__ p, int64_t row, i
     if (col + 3 < cols) q[3] = d;
 }
 
-template <class Cfg, int MIN_BLOCKS, bool VEC>
+template <class Cfg, int MIN_BLOCKS, bool VEC, bool SPLIT>
 __global__ void __launch_bounds__(Cfg::THREADS, MIN_BLOCKS)
 sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
             const float *__restrict__ B, int64_t ldb, void *__restrict__ Cv, int64_t ldc, const EpiParams epi,
@@ -99,10 +99,11 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
     const int tx = tid % Cfg::TX, ty = tid / Cfg::TX;
     const int64_t m0 = (int64_t)blockIdx.y * BM;
     const int64_t n0 = (int64_t)blockIdx.x * BN;
-    // Split K: block z sums k in [kb, ke) (kps a multiple of BK, so vector
-    // loads stay aligned) and leaves its partial in W[z]; otherwise all of K.
-    const int kb = kps > 0 ? (int)blockIdx.z * kps : 0;
-    const int ke = kps > 0 ? min(K, kb + kps) : K;
+    // Split K (a separate instance, so the whole-K kernel carries none of
+    // it): block z sums k in [kb, ke) (kps a multiple of BK, so vector loads
+    // stay aligned) and leaves its partial in W[z].
+    const int kb = SPLIT ? (int)blockIdx.z * kps : 0;
+    const int ke = SPLIT ? min(K, kb + kps) : K;
 
     float4 ra[Cfg::A_VEC], rb[Cfg::B_VEC];
 
@@ -190,7 +191,7 @@ sgemm_tiled(int M, int N, int K, const float *__restrict__ A, int64_t lda,
         if (kt + 1 < ktiles) step(std::integral_constant<int, 1>{}, kt + 1);
     }
 
-    if (W != nullptr) {
+    if constexpr (SPLIT) {
         // A K range's partial sums, raw: W[z] is M x N, row-major.
         float *w = W + (int64_t)blockIdx.z * M * N;
         const bool wvec = VEC && (N % 4 == 0);
@@ -262,7 +263,8 @@ cudaError_t launch_tile(bool vec, int M, int N, int K, const float *A, int64_t l
     const dim3 grid((unsigned)((N + Cfg::BN - 1) / Cfg::BN), (unsigned)((M + Cfg::BM - 1) / Cfg::BM),
                     (unsigned)(splits > 1 ? splits : 1));
     if (grid.y > 65535u || (splits > 1 && !W)) return cudaErrorInvalidConfiguration;
-    auto kern = vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true> : sgemm_tiled<Cfg, MIN_BLOCKS, false>;
+    auto kern = splits > 1 ? (vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true, true> : sgemm_tiled<Cfg, MIN_BLOCKS, false, true>)
+                           : (vec ? sgemm_tiled<Cfg, MIN_BLOCKS, true, false> : sgemm_tiled<Cfg, MIN_BLOCKS, false, false>);
     if (Cfg::SMEM_BYTES > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
