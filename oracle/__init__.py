@@ -27,6 +27,8 @@ second independent loop order at tiny sizes, float64 library matmul, and the
 BF16, FP16 and FP8 widenings against the library's own conversions; the epilogue
 against the library's addmm, ReLU and GELU, printed values of the normal CDF,
 GELU's odd-part identity, and per-column bias broadcasting.
+tests/test_oracle_mutants.py plants one plausible mistake at a time in a copy
+of gemm_oracle.c and checks that some pin fails on each.
 """
 from __future__ import annotations
 
@@ -47,43 +49,55 @@ _i64 = ctypes.c_int64
 _ptr = ctypes.c_void_p
 
 
+def compile_library(src: str, out: str) -> str:
+    """Compile one C source of the oracle's form into the shared library `out`
+    (gcc, OpenMP, no -march flags, so x86 and Arm hosts give the same bits)."""
+    os.makedirs(os.path.dirname(os.path.abspath(out)), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+           "-std=c11", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle shared library (gcc, OpenMP, no -march flags)."""
+    """Compile the oracle shared library."""
     with _lock:
         if (not force and os.path.exists(_LIB_PATH)
                 and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
             return _LIB_PATH
-        os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
-               "-std=c11", _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
-        return _LIB_PATH
+        return compile_library(_SRC, _LIB_PATH)
+
+
+def bind(path: str):
+    """Load a library built by compile_library and declare its entry points.
+    The module's functions use the library `_load` returns; the mutation
+    tests bind a copy of the source with one planted mistake the same way."""
+    lib = ctypes.CDLL(os.path.abspath(path))
+    full = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
+    rows = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]
+    jik = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
+    kinds = ("f32", "bf16", "f16", "e4m3", "e5m2")
+    table = [(f"oracle_gemm_{k}", full) for k in kinds] + [(f"oracle_gemm_rows_{k}", rows) for k in kinds]
+    table += [(f"oracle_gemm_{k}_jik", jik) for k in kinds]
+    table += [(f"oracle_widen_{k}", [_ptr, _ptr, _i64]) for k in ("bf16", "f16", "e4m3", "e5m2")]
+    for name, args in table:
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = None
+    lib.oracle_epilogue.argtypes = [_i64, _i64, _ptr, _i64, ctypes.c_double, ctypes.c_double, _ptr,
+                                    ctypes.c_int, _i64, _ptr, ctypes.c_int, _ptr, _i64]
+    lib.oracle_epilogue.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
 
 
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        full = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
-        rows = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]
-        jik = [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64]
-        kinds = ("f32", "bf16", "f16", "e4m3", "e5m2")
-        table = [(f"oracle_gemm_{k}", full) for k in kinds] + [(f"oracle_gemm_rows_{k}", rows) for k in kinds]
-        table += [(f"oracle_gemm_{k}_jik", jik) for k in kinds]
-        table += [(f"oracle_widen_{k}", [_ptr, _ptr, _i64]) for k in ("bf16", "f16", "e4m3", "e5m2")]
-        for name, args in table:
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = None
-        lib.oracle_epilogue.argtypes = [_i64, _i64, _ptr, _i64, ctypes.c_double, ctypes.c_double, _ptr,
-                                        ctypes.c_int, _i64, _ptr, ctypes.c_int, _ptr, _i64]
-        lib.oracle_epilogue.restype = None
-        lib.oracle_num_threads.argtypes = []
-        lib.oracle_num_threads.restype = ctypes.c_int
-        _lib = lib
+        _lib = bind(build())
     return _lib
 
 

@@ -130,6 +130,16 @@ def test_rows_variant_matches_full():
     assert np.array_equal(Cr, C[rows]) and np.array_equal(Dr, D[rows])
 
 
+def test_rows_variant_f32_matches_full():
+    # rows in any order, repeated, first and last; padded leading dimensions
+    A, B = make_operands(41, 30, 52, "fp32", "normal", 12, lda_pad=3, ldb_pad=2)
+    a, b = as_oracle_array(A), as_oracle_array(B)
+    C, D = oracle.gemm(a, b, with_scale=True)
+    rows = [40, 3, 3, 0, 17]
+    Cr, Dr = oracle.gemm_rows(a, b, rows)
+    assert np.array_equal(Cr, C[rows]) and np.array_equal(Dr, D[rows])
+
+
 def test_empty_sum_and_empty_shapes():
     C = oracle.gemm(np.zeros((4, 0), np.float32), np.zeros((0, 6), np.float32))
     assert C.shape == (4, 6) and np.all(C == 0)
