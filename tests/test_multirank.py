@@ -37,7 +37,7 @@ def _worker(rank, world, port, local_ms, out):
 def test_slowest_rank_and_replica_throughput_gloo_world2():
     world = 2
     local_ms = [120.0, 150.5]
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), local_ms, out), nprocs=world, join=True)
     assert out[0] == out[1] == 150.5
     flops = 2.0 * 8192 ** 3
