@@ -431,3 +431,37 @@ def test_grouped_argument_checks_before_cuda():
     mis = [_grp(8, 8, 8, 1 << 24, 8, 1 << 25, 8, 1 << 26, 8, bias=(1 << 27) + 2)]
     assert tg.gemm_run_grouped(BF, mis) == tg.GEMM_ERR_INVALID_ARG and "aligned" in tg.gemm_last_error()
     assert tg.gemm_run_grouped(9, [ok]) == tg.GEMM_ERR_INVALID_ARG and "dtype" in tg.gemm_last_error()
+
+
+def test_torch_wrappers_check_their_tensors_before_the_library():
+    """The torch-level calls reject host tensors, a C of the wrong type or
+    shape, a malformed bias and mismatched group lists with a Python error,
+    before anything reaches the C ABI (these tensors live on the CPU)."""
+    import torch
+    A = torch.zeros(8, 16)
+    B = torch.zeros(16, 4)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        tg.gemm(A, B)
+    with pytest.raises(TypeError, match="float32 tensor"):
+        tg.gemm(A, B, C=torch.zeros(8, 5))
+    with pytest.raises(TypeError, match="float32 tensor"):
+        tg.gemm(A, B, C=torch.zeros(8, 4, dtype=torch.float16))
+    with pytest.raises(ValueError, match="inner dimensions"):
+        tg.gemm(A, torch.zeros(15, 4))
+    with pytest.raises(TypeError, match="operands"):
+        tg.gemm(A, B, dtype="bf16")
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        tg.gemm_ex(A, B, bias=torch.zeros(4))
+    with pytest.raises(TypeError, match="bias"):
+        tg.gemm_ex(A, B, bias=torch.zeros(5))
+    with pytest.raises(TypeError, match="bias"):
+        tg.gemm_ex(A, B, bias=torch.zeros(4, dtype=torch.float64))
+    with pytest.raises(ValueError, match="differ in length"):
+        tg.gemm_grouped([A, A], [B])
+    with pytest.raises(ValueError, match="differ in length"):
+        tg.gemm_grouped([A], [B], Cs=[torch.zeros(8, 4), torch.zeros(8, 4)])
+    with pytest.raises(TypeError, match="bias"):
+        tg.gemm_grouped([A], [B], biases=[torch.zeros(3)])
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        tg.gemm_grouped([A], [B])
+    assert tg.gemm_grouped([], []) == []

@@ -190,6 +190,21 @@ def _ld(t) -> int:
     return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
 
+def _same_cuda_device(*tensors):
+    """Every tensor given (None entries skipped) is a CUDA tensor on one device."""
+    live = [t for t in tensors if t is not None]
+    for t in live:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors (this library has no CPU path)")
+        if t.device != live[0].device:
+            raise ValueError(f"tensors on different devices: {live[0].device} and {t.device}")
+
+
+def _check_bias(torch, bias, n):
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != n or not bias.is_contiguous()):
+        raise TypeError(f"bias must be {n} contiguous float32 values")
+
+
 def _operand_types(torch):
     """dtype code -> torch element type of A and B."""
     return {GEMM_BF16: torch.bfloat16, GEMM_FP16: torch.float16, GEMM_E4M3: torch.float8_e4m3fn,
@@ -221,6 +236,9 @@ def gemm(A, B, C=None, dtype=None, stream=None):
     K2, N = B.shape
     if K != K2:
         raise ValueError("inner dimensions differ")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise TypeError(f"C must be a ({M}, {N}) float32 tensor")
+    _same_cuda_device(A, B, C)
     if C is None:
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if stream is None:
@@ -256,8 +274,8 @@ def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act="none", out="f32",
         C = torch.empty((M, N), dtype=cdt, device=A.device)
     elif C.dtype != cdt or tuple(C.shape) != (M, N):
         raise TypeError(f"C must be a ({M}, {N}) {cdt} tensor")
-    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous()):
-        raise TypeError(f"bias must be {N} contiguous float32 values")
+    _check_bias(torch, bias, N)
+    _same_cuda_device(A, B, C, bias)
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
     ep = make_epilogue(alpha, beta, bias.data_ptr() if bias is not None else 0, act, out)
@@ -276,8 +294,8 @@ def gemm_grouped(As, Bs, Cs=None, biases=None, alpha=1.0, beta=0.0, act="none", 
     """
     import torch
 
-    if len(As) != len(Bs):
-        raise ValueError("As and Bs differ in length")
+    if len(As) != len(Bs) or (Cs is not None and len(Cs) != len(As)) or (biases is not None and len(biases) != len(As)):
+        raise ValueError("As, Bs, Cs and biases differ in length")
     if not As:
         return []
     if dtype is None:
@@ -296,6 +314,8 @@ def gemm_grouped(As, Bs, Cs=None, biases=None, alpha=1.0, beta=0.0, act="none", 
         if a.shape[1] != b.shape[0] or tuple(c.shape) != (a.shape[0], b.shape[1]) or c.dtype != cdt:
             raise ValueError(f"group {i}: shapes or C type do not match")
         bias = biases[i] if biases is not None else None
+        _check_bias(torch, bias, b.shape[1])
+        _same_cuda_device(As[0], a, b, c, bias)
         groups.append(GemmGroup(a.shape[0], b.shape[1], a.shape[1], a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
                                 c.data_ptr(), _ld(c), bias.data_ptr() if bias is not None else None))
     if stream is None:
