@@ -1,6 +1,6 @@
 """Maximum sizes: outputs of more than 2^31 elements, so that every element
 offset in the store paths (TMA stores, ordinary stores, the fused epilogue,
-the split-K reduction, the SIMT kernel) must be 64-bit.  K is short to keep
+the split-K reductions, the SIMT kernel) must be 64-bit.  K is short to keep
 the runs quick; rows past the 2^31-element mark are checked against the
 oracle one by one."""
 import numpy as np
@@ -16,7 +16,7 @@ from gemm_check import TOL, epilogue_check, error_ratio, oracle_rows
 pytestmark = pytest.mark.gpu
 
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_max_ctas", "tc_tma_store", "tc_splits", "tc_tail_splits", "tc_tail_halves",
-               "tc_sched")
+               "tc_sched", "simt_splits")
 
 M_BIG = (1 << 18) + 7            # 262151 rows
 N_BIG = 8200                     # M_BIG * N_BIG = 2.15e9 > 2^31 elements
@@ -89,3 +89,20 @@ def test_simt_fp32_past_2_31_elements():
     assert tg.gemm_get_status(torch.cuda.current_stream().cuda_stream) == tg.GEMM_OK
     _check(C, A, B, "fp32", _rows(M_BIG, N_BIG))
     del C
+
+
+def test_simt_split_k_past_2_31_elements():
+    """Two K ranges forced: each range's partial sums fill an M x N slab of the
+    workspace (the second starts past 2^31 elements), and the in-order
+    reduction reads both and writes C."""
+    tg.gemm_set_option("simt_splits", 2)
+    A, B = make_operands(M_BIG, N_BIG, 64, "fp32", "uniform", seed=135)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = torch.empty((M_BIG, N_BIG), dtype=torch.float32, device="cuda")
+    plan = tg.gemm_plan(M_BIG, N_BIG, 64, tg.GEMM_FP32, Ad.data_ptr(), 64, Bd.data_ptr(), N_BIG, Cd.data_ptr(),
+                        N_BIG)
+    assert plan.splits == 2
+    C = tg.gemm(Ad, Bd, C=Cd, dtype="fp32")
+    assert tg.gemm_get_status(torch.cuda.current_stream().cuda_stream) == tg.GEMM_OK
+    _check(C, A, B, "fp32", _rows(M_BIG, N_BIG))
+    del C, Cd
