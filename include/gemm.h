@@ -89,30 +89,36 @@ typedef enum {
  *   stream      the CUDA stream to enqueue on.
  *
  * Paths: GEMM_FP32 runs the tiled SIMT kernel; every other dtype runs the
- * persistent TMA + tcgen05 kernel.  Operands whose layout the TMA engine
- * cannot address (base not 16-byte aligned, or a row pitch that is not a
- * multiple of 16 bytes) are first copied into a stream-ordered workspace with
- * a padded pitch; that workspace is allocated and freed on the stream
+ * persistent TMA + tcgen05 kernel.  When its tiles are too few to give every
+ * SM about six blocks, the SIMT path cuts K into up to 8 ranges: their partial
+ * sums go to a stream-ordered workspace of (ranges x M x N) floats, and a
+ * second kernel adds them in range order (results are deterministic). That
+ * workspace is allocated and freed on the stream like the ones below, and is
+ * reported as GEMM_ERR_NO_MEMORY if unavailable.  Operands whose layout the
+ * TMA engine cannot address (base not 16-byte aligned, or a row pitch that is
+ * not a multiple of 16 bytes) are first copied into a stream-ordered workspace
+ * with a padded pitch; that workspace is allocated and freed on the stream
  * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
  * unavailable.  For GEMM_TF32 (and FP8 tiles narrower than 128 columns), B is
- * first transposed into the same kind of workspace, because the MMA then
- * reads its B operand K-major.  When there are too few output tiles to occupy
- * every SM and K is long, the tensor-core path splits K: partial tiles go to
- * a workspace and a second kernel sums them into C in a fixed order (results
- * are deterministic).  When the tiles of the last, partly idle round of the
- * persistent schedule would fill at most half of the machine, 16-bit inputs
- * on short schedules run them as two column halves each (every half over
- * all of K, straight to C: no workspace, and the same sums as a whole
- * tile; the launch ends sooner because each half's epilogue drains half the
+ * first transposed into the same kind of workspace, because the MMA then reads
+ * its B operand K-major.  When there are too few output tiles to occupy every
+ * SM and K is long, the tensor-core path splits K: partial tiles go to a
+ * workspace and a second kernel sums them into C in a fixed order (results are
+ * deterministic).  When the tiles of the last, partly idle round of the
+ * persistent schedule would fill at most half of the machine, 16-bit inputs on
+ * short schedules run them as two column halves each (every half over all of
+ * K, straight to C: no workspace, and the same sums as a whole tile; the
+ * launch ends sooner because each half's epilogue drains half the
  * accumulator); on request ("tc_tail_splits") they are split in K instead,
- * like split-K.
- * C leaves through TMA stores when its base, pitch and row length (N
- * elements) are all multiples of 16 bytes, else through ordinary stores.
+ * like split-K. C leaves through TMA stores when its base, pitch and row
+ * length (N elements) are all multiples of 16 bytes, else through ordinary
+ * stores.
  *
  * Errors: GEMM_ERR_INVALID_ARG for negative sizes, lda < K, ldb < N, ldc < N,
  * a NULL pointer with a non-empty extent, an unknown dtype, a pointer not
- * aligned to its element, or C overlapping A or B in memory.  A kernel whose bounded wait expires records
- * GEMM_ERR_TIMEOUT in a device status word that gemm_get_status() reads.
+ * aligned to its element, or C overlapping A or B in memory.  A kernel whose
+ * bounded wait expires records GEMM_ERR_TIMEOUT in a device status word that
+ * gemm_get_status() reads.
  */
 GEMM_API int gemm_run(int64_t M, int64_t N, int64_t K, int dtype,
              const void *A, int64_t lda, const void *B, int64_t ldb,
