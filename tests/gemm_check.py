@@ -68,6 +68,26 @@ def run_gemm(A: torch.Tensor, B: torch.Tensor, dtype: str, ldc_pad: int = 0, a_o
     return C[:, :N].copy()
 
 
+def tf32_round(x: np.ndarray, mode: str) -> np.ndarray:
+    """FP32 values cut to TF32's 10 mantissa bits, as FP32: "rz" drops the
+    13 low bits (toward zero), "rn" rounds to the nearest TF32 value with
+    ties to an even last bit.  The pages give only the format (FP32 range,
+    10-bit mantissa), not how the tensor cores reduce an FP32 operand to it;
+    the two diagnostic oracles built from these inputs tell which one a
+    kernel's output follows.  Finite inputs only."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if mode == "rz":
+        r = u & np.uint32(0xFFFFE000)
+    elif mode == "rn":
+        # add just under half of the dropped part's range, plus the kept last bit
+        # (so an exact half rounds to even), then drop; a carry moves into the
+        # exponent as it should, and the sign bit is untouched
+        r = (u + np.uint32(0x0FFF) + ((u >> np.uint32(13)) & np.uint32(1))) & np.uint32(0xFFFFE000)
+    else:
+        raise ValueError(f"unknown rounding mode {mode!r}")
+    return r.view(np.float32)
+
+
 def error_ratio(C: np.ndarray, Cref: np.ndarray, D: np.ndarray) -> float:
     C = C.astype(np.float64)
     if not np.all(np.isfinite(C)):

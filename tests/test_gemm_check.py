@@ -151,3 +151,38 @@ def test_epilogue_gate_takes_the_rounded_value_and_rejects_two_steps_beyond(out)
     assert epilogue_check(bad, Cref, D, *args)[0] > 1.0
     bad[i, j] = np.nan
     assert epilogue_check(bad, Cref, D, *args)[0] == float("inf")
+
+
+# ------------------------------------------------------ TF32 input rounding --
+# The diagnostic TF32 oracles take their inputs through tf32_round.  Pinned by
+# hand-worked ties and by a brute-force nearest-neighbour search in fp64.
+from gemm_check import tf32_round
+
+
+def test_tf32_round_worked_values():
+    u = 2.0 ** -10                       # TF32 spacing in [1, 2)
+    x = np.array([1.0, 1 + u, 1 + u / 2, 1 + u / 2 + 2 ** -23, 1 + 1.5 * u, 2 - u / 2, -(1 + u / 2 + 2 ** -23)],
+                 np.float32)
+    rn = [1.0, 1 + u, 1.0, 1 + u, 1 + 2 * u, 2.0, -(1 + u)]       # ties go to the even last bit
+    rz = [1.0, 1 + u, 1.0, 1.0, 1 + u, 2 - u, -1.0]
+    assert list(tf32_round(x, "rn").astype(np.float64)) == rn
+    assert list(tf32_round(x, "rz").astype(np.float64)) == rz
+
+
+def test_tf32_round_is_nearest_and_toward_zero():
+    rng = np.random.default_rng(33)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-60, 60, 200000))).astype(np.float32)
+    x[:1000] = rng.integers(-4096, 4096, 1000).astype(np.float32) * np.float32(2.0 ** -11)   # many exact ties
+    for mode in ("rn", "rz"):
+        r = tf32_round(x, mode)
+        assert np.all((r.view(np.uint32) & np.uint32(0x1FFF)) == 0)
+    xd = x.astype(np.float64)
+    _, e = np.frexp(xd)
+    ulp = np.ldexp(1.0, e - 11)                  # TF32 spacing at x (normal inputs)
+    lo = np.trunc(xd / ulp) * ulp                # toward zero
+    hi = lo + np.sign(xd) * ulp
+    assert np.array_equal(tf32_round(x, "rz").astype(np.float64), lo)
+    d_lo, d_hi = np.abs(xd - lo), np.abs(hi - xd)
+    lo_even = (np.abs(lo / ulp) % 2) == 0
+    want = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo_even, lo, hi)))
+    assert np.array_equal(tf32_round(x, "rn").astype(np.float64), want)
