@@ -105,14 +105,17 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(key: str):
+def profiled_traffic(key: str, plan: dict):
     """DRAM bytes per launch from a committed ncu summary (profiles/ncu_traffic.json),
-    or None if the kernel's sources changed since that capture."""
+    or None if the kernel's sources changed since that capture or this run's
+    plan (tile, CTA group, K ranges, B staging, tail handling, schedule)
+    differs from the one captured."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)[key]
-        if d.get("source_digest") == source_digest(d["source_files"]):
+        if (d.get("source_digest") == source_digest(d["source_files"]) and "plan" in d
+                and all(plan.get(k) == v for k, v in d["plan"].items())):
             return float(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -586,7 +589,8 @@ def run_ours(args):
     else:
         roof = roofline_for_dtype(w.dtype, res["flops"], res["launch_ms_mean"], peaks, peak_src,
                                   None if gw is not None else
-                                  profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else "")))
+                                  profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else ""),
+                                                   res["plan"]))
         if w.dtype in ("bf16", "fp16"):
             roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     out = {
@@ -625,13 +629,13 @@ def run_ours(args):
                 rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
             else:
                 rl = roofline_for_dtype(wl.dtype, r["flops"], r["launch_ms_mean"], peaks, peak_src,
-                                        profiled_traffic(key))
+                                        profiled_traffic(key, r["plan"]))
                 # the low-tile-count shape streams B once: bandwidth is its binding roofline
                 if key == "bf16_128x8192x8192":
                     in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 4
                     gbs = in_bytes / (r["launch_ms_mean"] * 1e-3) / 1e9
                     rl = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(key),
+                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(key, r["plan"]),
                           "peak_source": f"hbm_gbs, {peak_src}", "tensor_tflops": rl["achieved"]}
             in_b = (wl.M * wl.K + wl.K * wl.N) * ELEM_BYTES[wl.dtype]
             paths[key] = {"workload": wl.name + (f", fused epilogue {fused[key]}" if key in fused else ""),

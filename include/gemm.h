@@ -104,9 +104,11 @@ typedef enum {
  * its B operand K-major.  When there are too few output tiles to occupy every
  * SM and K is long, the tensor-core path splits K: partial tiles go to a
  * workspace and a second kernel sums them into C in a fixed order (results are
- * deterministic).  When the tiles of the last, partly idle round of the
- * persistent schedule would fill at most half of the machine, 16-bit inputs on
- * short schedules run them as two column halves each (every half over all of
+ * deterministic).  With 16-bit inputs, at most 256 rows and a B of 64 MiB or
+ * more (B streaming from HBM), those tiles are 128 columns wide instead of
+ * 256.  When the tiles of the last, partly idle round of the persistent
+ * schedule would fill at most half of the machine, 16-bit inputs on short
+ * schedules run them as two column halves each (every half over all of
  * K, straight to C: no workspace, and the same sums as a whole tile; the
  * launch ends sooner because each half's epilogue drains half the
  * accumulator); on request ("tc_tail_splits") they are split in K instead,

@@ -196,15 +196,35 @@ def test_plan_misaligned_base_packs():
 
 def test_plan_low_tile_count_splits_k():
     # 32 tiles of 128x256 for 152 SMs and 128 k-blocks: 4 K ranges per tile
-    p = _plan(128, 8192, 8192, tg.GEMM_BF16)
-    assert p["cta_group"] == 1 and p["bn"] == 256 and p["splits"] == 4 and p["grid"] == 128
-    assert p["tma_store"] == 1
+    p = _plan(1024, 2048, 8192, tg.GEMM_BF16)
+    assert p["cta_group"] == 1 and p["bn"] == 256 and p["splits"] == 2 and p["grid"] == 128
+    assert p["tma_store"] == 1 and p["tail_tiles"] == 64        # every tile is split
     # short K: no split, narrow tiles instead
     q = _plan(128, 8192, 256, tg.GEMM_BF16)
     assert q["splits"] == 1 and q["bn"] == 64
     # small problems never split (the reduce would cost more than it saves)
     assert _plan(1000, 1000, 1000, tg.GEMM_BF16)["splits"] == 1
-    assert p["tail_tiles"] == 32        # every tile is split
+
+
+@pytest.mark.parametrize("M,N,K,bn,splits", [
+    # B streams from HBM past at most 256 rows of A: 128-column tiles, K split to fill the SMs
+    (128, 8192, 8192, 128, 2), (64, 8192, 8192, 128, 2), (256, 8192, 8192, 128, 1), (128, 4096, 16384, 128, 4),
+    # B of 32 MB, or 512 and more rows: 256-column tiles (measured faster there)
+    (256, 4096, 4096, 256, 4), (512, 4096, 8192, 256, 2), (1024, 2048, 8192, 256, 2)])
+def test_plan_streaming_b_takes_128_column_tiles(M, N, K, bn, splits):
+    for dt in (tg.GEMM_BF16, tg.GEMM_FP16):
+        p = _plan(M, N, K, dt)
+        assert (p["cta_group"], p["bn"], p["splits"]) == (1, bn, splits), (M, N, K, p)
+        assert p["grid"] == p["tiles"] * p["splits"]
+    # 8-bit and TF32 inputs keep the 256-column tiles
+    assert _plan(M, N, K, tg.GEMM_E4M3)["bn"] == 256
+    assert _plan(M, N, K, tg.GEMM_TF32)["bn"] == 256
+    # a forced tile width is kept
+    try:
+        tg.gemm_set_option("tc_bn", 256)
+        assert _plan(M, N, K, tg.GEMM_BF16)["bn"] == 256
+    finally:
+        tg.gemm_set_option("tc_bn", 0)
 
 
 def test_plan_runs_the_last_round_as_column_halves():

@@ -126,6 +126,14 @@ constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills
 constexpr int64_t kMinSplitWork = 1LL << 31;
 // Column halves for the last round by default only on schedules this short.
 constexpr int64_t kMaxRoundsForHalves = 4;
+// Split-K shapes that stream B from HBM: at most this many rows of A (below the
+// BF16 ridge point of about 280 flop per byte) against a 16-bit B of at least
+// this many bytes (half of L2 and up) take 128-column tiles, twice as many
+// tiles over shallower K ranges (measured on GB300, picker.md: +5% to +10% at
+// 64..256 x 8192 x 8192 and 128 x 4096 x 16384; B of 32 MB, or 512 rows and
+// more, lose with them).
+constexpr int64_t kStreamBMaxRows = 256;
+constexpr int64_t kStreamBMinBytes = 64LL << 20;
 
 }  // namespace
 
@@ -207,9 +215,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         } else if (splits != 1 && M * N * K >= kMinSplitWork &&
                    std::min<int64_t>(num_sms / tiles_of(1, 256), num_kb / kMinKbPerSplit) >= 2) {
             // Too few 128x256 tiles for the SMs, but K is long: split K instead of
-            // shrinking the tile (a narrow tile re-reads A once per column tile).
+            // shrinking the tile (a narrow tile re-reads A once per column tile),
+            // except where B streams from HBM past a few rows of A: there the
+            // re-read A is small and more, narrower tiles keep more SMs reading B.
             cg = 1;
-            bn = 256;
+            bn = (elem == 2 && M <= kStreamBMaxRows && K * N * elem >= kStreamBMinBytes) ? 128 : 256;
         } else if (tiles_of(1, 128) >= num_sms) {
             cg = 1;
             bn = 128;
