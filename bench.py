@@ -62,6 +62,23 @@ def workload_by_key(key):
     return table[key]
 
 
+SHAPE_DTYPES = ("fp32", "tf32", "bf16", "fp16", "e4m3", "e5m2")
+
+
+def shape_workload(spec: str, dtype: str):
+    """A workload of any shape "MxNxK" (sizes >= 1) in one of the library's
+    input types, operands U[-1,1] drawn from seed 4 like the ragged published
+    shapes, for timing planner choices through the same path as the rest."""
+    from tiled_tensor_core_gemm_gb300.inputs import Workload
+    parts = spec.lower().split("x")
+    if len(parts) != 3 or not all(p.isdigit() and int(p) >= 1 for p in parts):
+        raise ValueError(f"--shape wants MxNxK with sizes >= 1, got {spec!r}")
+    if dtype not in SHAPE_DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    M, N, K = (int(p) for p in parts)
+    return Workload(f"{dtype} {M}x{N}x{K} U[-1,1] seed 4", M, N, K, dtype, "uniform", 4)
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -70,6 +87,9 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_KEYS), default="bf16_8192",
                     help="timed workload (default: the headline 8192^3 BF16 GEMM)")
+    ap.add_argument("--shape", default=None, metavar="MxNxK",
+                    help="time this shape instead of --workload (operands U[-1,1], seed 4; type from --dtype)")
+    ap.add_argument("--dtype", choices=SHAPE_DTYPES, default="bf16", help="input type for --shape")
     ap.add_argument("--epilogue", choices=tuple(FUSED_EPILOGUES), default=None,
                     help="time the workload through gemm_run_ex with this fused epilogue")
     ap.add_argument("--grouped", choices=("equal_k", "skewed_k"), default=None,
@@ -543,8 +563,15 @@ def run_ours(args):
 
     from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16, GROUPED_BF16_SKEWK
     gw = {"equal_k": GROUPED_BF16, "skewed_k": GROUPED_BF16_SKEWK}.get(args.grouped)
-    w = gw if gw is not None else workload_by_key(args.workload)
-    headline = args.workload == "bf16_8192" and not args.epilogue and gw is None
+    if gw is not None:
+        w = gw
+    elif args.shape:
+        w = shape_workload(args.shape, args.dtype)
+    else:
+        w = workload_by_key(args.workload)
+    wkey = (f"grouped_{args.grouped}" if gw is not None else
+            f"{args.dtype}_{args.shape.lower()}" if args.shape else args.workload)
+    headline = wkey == "bf16_8192" and not args.epilogue
     sampler = ClockSampler(gpu_uuid(device)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -580,7 +607,6 @@ def run_ours(args):
             "tf32_4096": "fp32 GEMM M=N=K=4096 read as TF32 by the tensor cores, A,B ~ N(0,1) (seed 2), fp32 "
                          "accumulate and output, row-major, persistent tcgen05 path",
             "fp32_4096": "fp32 GEMM M=N=K=4096, A,B ~ N(0,1) (seed 2), exact fp32 on the CUDA cores (SIMT)"}
-    wkey = f"grouped_{args.grouped}" if gw is not None else args.workload
     desc.setdefault(wkey, f"{w.name}, row-major, fp32 output" +
                     (", one gemm_run_grouped launch per step" if gw is not None else ""))
     if w.dtype == "fp32":
@@ -589,7 +615,7 @@ def run_ours(args):
     else:
         roof = roofline_for_dtype(w.dtype, res["flops"], res["launch_ms_mean"], peaks, peak_src,
                                   None if gw is not None else
-                                  profiled_traffic(args.workload + (f"_{args.epilogue}" if args.epilogue else ""),
+                                  profiled_traffic(wkey + (f"_{args.epilogue}" if args.epilogue else ""),
                                                    res["plan"]))
         if w.dtype in ("bf16", "fp16"):
             roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)

@@ -47,3 +47,13 @@ def test_traffic_reported_only_for_the_captured_plan(key):
 
 def test_headline_capture_matches_the_current_plan_and_sources():
     assert bench.profiled_traffic("bf16_8192", _plan(8192, 8192, 8192, tg.GEMM_BF16)) is not None
+
+
+def test_shape_workload_parses_and_rejects():
+    w = bench.shape_workload("128x8192X8192", "bf16")
+    assert (w.M, w.N, w.K, w.dtype, w.dist, w.seed) == (128, 8192, 8192, "bf16", "uniform", 4)
+    for bad in ("128x8192", "0x8x8", "ax8x8", "8x8x8x8", "-1x8x8"):
+        with pytest.raises(ValueError):
+            bench.shape_workload(bad, "bf16")
+    with pytest.raises(ValueError):
+        bench.shape_workload("8x8x8", "int8")
