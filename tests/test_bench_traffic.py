@@ -1,8 +1,11 @@
-"""The DRAM traffic that bench.py puts in its roofline comes from committed
-ncu captures (profiles/ncu_traffic.json).  A figure is only reported while
-the kernel sources still hash to the captured digest and the run's plan is the
-captured one; otherwise the roofline carries traffic null.  No GPU: plans come
-from the library's planner for a 152-SM GB300."""
+"""bench.py's host-side arithmetic, without a GPU.
+
+The DRAM traffic in its roofline comes from committed ncu captures
+(profiles/ncu_traffic.json).  A figure is only reported while the kernel
+sources still hash to the captured digest and the run's plan is the captured
+one; otherwise the roofline carries traffic null.  Plans come from the
+library's planner for a 152-SM GB300.  Also: the --shape parser, and the
+tensor and ALU roofline formulas on worked numbers."""
 import json
 import os
 
@@ -57,3 +60,31 @@ def test_shape_workload_parses_and_rejects():
             bench.shape_workload(bad, "bf16")
     with pytest.raises(ValueError):
         bench.shape_workload("8x8x8", "int8")
+
+
+# ----------------------------------------------------- roofline arithmetic --
+PEAKS = {"hbm_gbs": 6778.0, "bf16_tflops": 1905.1, "bf16_tflops_sustained": 1693.7, "sm_max_mhz": 2070.0}
+
+
+def test_tensor_roofline_worked_headline():
+    # 2 * 8192^3 flop in 0.6598 ms per launch is 1666.4 TFLOP/s, 0.8747 of the 1905.1 burst peak
+    r = bench.roofline_for_dtype("bf16", 2 * 8192 ** 3, 0.6598, PEAKS, "measured", 1.37e9)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] == 1.37e9
+    assert r["achieved"] == pytest.approx(1666.4, abs=0.1) and r["peak"] == 1905.1
+    assert r["frac"] == pytest.approx(0.8747, abs=1e-4)
+    assert r["frac_of_nominal_dense"] == pytest.approx(1666.4 / 2250, abs=1e-4)
+
+
+@pytest.mark.parametrize("dtype,peak", [("fp16", 1905.1), ("tf32", 931.4), ("e4m3", 3810.2), ("e5m2", 3810.2)])
+def test_tensor_peak_per_input_type(dtype, peak):
+    # the measured BF16 burst peak scaled by the nominal dense ratio (TF32 1100/2250, FP8 4500/2250)
+    r = bench.roofline_for_dtype(dtype, 1e12, 1.0, PEAKS, "measured", None)
+    assert r["peak"] == pytest.approx(peak, abs=0.05)
+    assert r["achieved"] == pytest.approx(1000.0) and r["frac"] == pytest.approx(1000.0 / peak, abs=1e-4)
+
+
+def test_alu_roofline_worked_fp32():
+    # 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz = 80.55 TFLOP/s; 4096^3 in 2.466 ms is 55.7 of it
+    r = bench.roofline_alu(2 * 4096 ** 3, 2.466, 2070.0)
+    assert r["bound"] == "alu" and r["peak"] == pytest.approx(80.55, abs=0.01)
+    assert r["achieved"] == pytest.approx(55.73, abs=0.01) and r["frac"] == pytest.approx(0.6919, abs=1e-4)
