@@ -88,3 +88,22 @@ def test_alu_roofline_worked_fp32():
     r = bench.roofline_alu(2 * 4096 ** 3, 2.466, 2070.0)
     assert r["bound"] == "alu" and r["peak"] == pytest.approx(80.55, abs=0.01)
     assert r["achieved"] == pytest.approx(55.73, abs=0.01) and r["frac"] == pytest.approx(0.6919, abs=1e-4)
+
+
+def test_cpu_baseline_leg_times_the_oracle_and_checks_sampled_rows():
+    import torch
+    import oracle
+    from tiled_tensor_core_gemm_gb300.inputs import Workload, as_oracle_array, workload_operands
+    w = Workload("bf16 96x80x64 U[-1,1] seed 4", 96, 80, 64, "bf16", "uniform", 4)
+    A, B = workload_operands(w)
+    good = torch.from_numpy(oracle.gemm(as_oracle_array(A), as_oracle_array(B), bf16=True).astype("float32"))
+    base, parity = bench.cpu_baseline_leg(w, 0.05, good)
+    assert base["kind"] == "oracle" and base["unit"] == "TFLOP/s" and base["value"] > 0 and base["cores"] >= 1
+    assert parity["ok"] and parity["max_err_ratio"] <= 1e-7 and parity["rows"] >= 2
+    bad = good.clone()
+    bad[0, 5] += 1.0                   # row 0 is always sampled
+    assert not bench.cpu_baseline_leg(w, 0.05, bad)[1]["ok"]
+    nan = good.clone()
+    nan[w.M - 1, 0] = float("nan")     # and so is the last row
+    assert not bench.cpu_baseline_leg(w, 0.05, nan)[1]["ok"]
+    assert bench.cpu_baseline_leg(w, 0.05, None)[1] is None
