@@ -3,15 +3,20 @@
 
 One step = one C = A.B through the C ABI (gemm_run) on the headline workload,
 a BF16-input GEMM with M = N = K = 8192 (N(0,1) operands rounded to BF16, seed
-3, FP32 accumulation and output) on the persistent tcgen05 path.  The FP32
-SIMT and TF32 tensor-core paths are timed on the 4096^3 FP32 workload in the
-same run and reported under "paths".
+3, FP32 accumulation and output) on the persistent tcgen05 path.  In the same
+run, each of the other published workloads (FP32 SIMT and TF32 at 256^3 to
+4096^3, the ragged BF16 shapes) is timed and checked against the oracle on
+sampled rows; their compact records end the JSON line ("configs").  A
+"sustained" leg repeats the headline back to back for over a second, against
+the sustained peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
-independent replica of the same GEMM (the path has no exchange step); value
-= all ranks' flops / the slowest rank's time.  --impl reference times the
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): the GEMM is sharded by
+rows -- each rank computes an 8192-row slab of a (ranks x 8192) x 8192 x 8192
+product against its own copy of B, broadcast from rank 0 once before timing;
+nothing crosses ranks inside the timed region (weak scaling); value = all
+ranks' flops / the slowest rank's time.  --impl reference times the
 fp64 oracle on the host cores on bounded samples of the same workload.
 """
 from __future__ import annotations
@@ -37,7 +42,6 @@ L2_BYTES = 129e6
 NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0, "fp8": 4500.0}   # GB300 per-GPU dense, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
-SMS = 152
 FP32_LANES_PER_SM = 128
 # bench keys of the published workloads (tiled_tensor_core_gemm_gb300/inputs.py)
 WORKLOAD_KEYS = ("bf16_8192", "tf32_4096", "fp32_4096", "fp32_1024", "tf32_1024", "fp32_256",
@@ -237,6 +241,12 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
     with keys act, out, bias (bool), alpha, beta (seeded old C and bias)."""
     import torch
     _, _, A, B = make_device_operands(workload, device)
+    if dist is not None:
+        # row-sharded across ranks: this rank's slab of A is its own; B comes
+        # from rank 0 once, into this rank's own buffer, before any timing
+        from tiled_tensor_core_gemm_gb300.sharded import broadcast_b
+        broadcast_b(B, 0)
+        torch.cuda.synchronize(device)
     M, N, K = workload.M, workload.N, workload.K
     code = tg.DTYPES[workload.dtype]
     s = stream.cuda_stream
@@ -297,7 +307,8 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
         torch.cuda.synchronize()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     # the GEMM, plus the operand packs / B transpose before it and the split-K reduction after it
-    launches = (1 + plan["pack_a"] + plan["pack_b"] + plan["b_kmajor"] + int(plan["tail_tiles"] > 0)
+    launches = (1 + int(plan["pack_a"] or plan["pack_b"]) + plan["b_kmajor"]
+                + int(plan["tail_tiles"] > 0 and not plan.get("cluster_split"))
                 if plan["path"] == 1 else 1)
     return {"total_ms": total_ms, "launch_ms_mean": total_ms / steps,
             "isolated_ms_mean": statistics.mean(launch_ms), "isolated_ms_median": statistics.median(launch_ms),
@@ -501,6 +512,12 @@ def _parity_rows(workload, C_dev, nrows=32):
             "what": "the timed run's C on sampled rows against the fp64 oracle, max |C - Cref| / (|A|.|B|)"}
 
 
+def configs_parity(workload, C_dev, nrows=16):
+    """A published workload's timed C against the oracle on sampled rows (part
+    of the cpu_baseline leg: skipped with --no-cpu-baseline)."""
+    return _parity_rows(workload, C_dev, nrows)
+
+
 def slowest_rank_ms(total_ms: float, dist=None, device="cpu") -> float:
     """The timed region's length on the slowest rank (every rank gets the max)."""
     if dist is None:
@@ -536,19 +553,64 @@ def roofline_for_dtype(dtype, flops, launch_ms, peaks, peak_src, traffic):
     return roofline_tensor(flops, launch_ms, peaks["bf16_tflops"] * ratio, src, NOMINAL_DENSE_TFLOPS[fam], traffic)
 
 
-def roofline_alu(flops, launch_ms, sm_mhz):
+def roofline_alu(flops, launch_ms, sm_mhz, sms):
+    """FP32 SIMT roofline: the FP32 FMA pipes of `sms` SMs (read from the
+    device) at `sm_mhz`."""
     achieved = flops / (launch_ms * 1e-3) / 1e12
-    peak = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
     return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": UNIT,
             "frac": round(achieved / peak, 4), "traffic": None,
-            "peak_source": f"derived: {SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {sm_mhz:.0f} MHz"}
+            "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {sm_mhz:.0f} MHz"}
+
+
+def roofline_hbm(workload, launch_ms, peaks, peak_src, traffic):
+    """HBM roofline of a GEMM too short and wide to be compute-bound: its
+    compulsory bytes (A and B read once, C written once) per call."""
+    in_bytes = (workload.M * workload.K + workload.K * workload.N) * ELEM_BYTES[workload.dtype]
+    gbs = (in_bytes + workload.M * workload.N * 4) / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic, "peak_source": f"hbm_gbs, {peak_src}",
+            "tensor_tflops": round(2.0 * workload.M * workload.N * workload.K / (launch_ms * 1e-3) / 1e12, 2)}
+
+
+# The published workloads other than the headline, timed beside it; their
+# compact records end the JSON line (key: the workload's id and shape).
+CONFIG_WORKLOADS = (("c1_fp32_256", "fp32_256"), ("c2_fp32_1024", "fp32_1024"), ("c2_tf32_1024", "tf32_1024"),
+                    ("c3_fp32_4096", "fp32_4096"), ("c3_tf32_4096", "tf32_4096"), ("c5_bf16_1000", "bf16_1000"),
+                    ("c5_bf16_4097x4095x4099", "bf16_4097x4095x4099"),
+                    ("c5_bf16_16384x1024x4096", "bf16_16384x1024x4096"),
+                    ("c5_bf16_128x8192x8192", "bf16_128x8192x8192"))
+# HBM-bound among them (B streams once past a few rows of A)
+HBM_BOUND = {"bf16_128x8192x8192"}
+
+
+def config_record(roof, parity):
+    """Compact record of one published workload: throughput, the roofline it
+    is judged against, and the timed run's C against the oracle on sampled rows."""
+    rec = {"tflops": roof.get("tensor_tflops", roof["achieved"]), "bound": roof["bound"],
+           "achieved": roof["achieved"], "peak": round(roof["peak"], 1), "unit": roof["unit"],
+           "frac": round(roof["frac"], 3)}
+    if parity is not None:
+        rec["parity"] = float(f"{parity['max_err_ratio']:.2e}")
+        rec["tol"] = parity["tol"]
+        rec["ok"] = parity["ok"]
+    return rec
+
+
+def ordered_line(out):
+    """The JSON line with the contract keys first and the compact per-config
+    records last, so that the end of the line (the part of stdout a driver
+    keeps) holds every published workload's figure."""
+    last = ("paths", "sustained", "configs")
+    d = {k: v for k, v in out.items() if k not in last}
+    d.update({k: out[k] for k in last if k in out})
+    return json.dumps(d, separators=(",", ":"))
 
 
 def run_ours(args):
     import torch
     import tiled_tensor_core_gemm_gb300 as tg
     from tiled_tensor_core_gemm_gb300 import build as tgbuild
-    from tiled_tensor_core_gemm_gb300.inputs import C3_FP32_4096, C3_TF32_4096, C4_BF16_8192
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -621,23 +683,33 @@ def run_ours(args):
             "fp32_4096": "fp32 GEMM M=N=K=4096, A,B ~ N(0,1) (seed 2), exact fp32 on the CUDA cores (SIMT)"}
     desc.setdefault(wkey, f"{w.name}, row-major, fp32 output" +
                     (", one gemm_run_grouped launch per step" if gw is not None else ""))
-    if w.dtype == "fp32":
-        sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
-        roof = roofline_alu(res["flops"], res["launch_ms_mean"], sm_mhz)
-    else:
-        roof = roofline_for_dtype(w.dtype, res["flops"], res["launch_ms_mean"], peaks, peak_src,
-                                  None if gw is not None else
-                                  profiled_traffic(wkey + (f"_{args.epilogue}" if args.epilogue else ""),
-                                                   res["plan"]))
-        if w.dtype in ("bf16", "fp16"):
-            roof["frac_of_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
+
+    def roofline_of(key, wl, r):
+        """The roofline a workload is judged against: FP32 FMA pipes (SIMT),
+        HBM (short and wide shapes), else the tensor cores of its input type."""
+        if wl.dtype == "fp32":
+            return roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz, sms)
+        traffic = None if r["plan"] is None else profiled_traffic(key, r["plan"])
+        if key in HBM_BOUND:
+            return roofline_hbm(wl, r["launch_ms_mean"], peaks, peak_src, traffic)
+        rl = roofline_for_dtype(wl.dtype, r["flops"], r["launch_ms_mean"], peaks, peak_src, traffic)
+        if wl.dtype in ("bf16", "fp16"):
+            rl["frac_of_sustained"] = round(rl["achieved"] / peaks["bf16_tflops_sustained"], 4)
+        return rl
+
+    roof = roofline_of(wkey + (f"_{args.epilogue}" if args.epilogue else ""), w, res)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": desc[wkey] + (f"; fused epilogue {FUSED_EPILOGUES[args.epilogue]} "
                                                "through gemm_run_ex" if args.epilogue else ""),
-                   **shape, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   **shape, "parallelism": (f"rows x{world}: each rank the M-row slab above of a "
+                                            f"{world * shape.get('M', 0)}-row GEMM, B broadcast once before timing"
+                                            if world > 1 and gw is None else
+                                            f"replicas x{world}" if world > 1 else "single"),
                    "options": args.option,
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of operands vs 129 MB L2); no flush",
                    "plan": res["plan"]},
@@ -648,83 +720,102 @@ def run_ours(args):
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": clocks,
     }
+    check = not args.no_cpu_baseline and world == 1
     if not args.no_paths and headline:
-        sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks["sm_max_mhz"]
-        paths = {}
         n_side = max(3, min(args.steps, 100))
-        side = [("fp32_simt_4096", C3_FP32_4096), ("tf32_4096", C3_TF32_4096)]
-        side += [(k, workload_by_key(k)) for k in ("fp32_256", "fp32_1024", "tf32_1024", "bf16_1000",
-                                                    "bf16_4097x4095x4099", "bf16_16384x1024x4096",
-                                                    "bf16_128x8192x8192", "fp16_4096", "fp16_8192",
-                                                    "e4m3_4096", "e4m3_8192", "e5m2_8192")]
-        # the fused epilogues on the headline shape
+        side_warm = max(3, min(args.warmup, 10))
+        # the other published workloads: compact records with parity on sampled rows
+        configs = {}
+        for cid, key in CONFIG_WORKLOADS:
+            wl = workload_by_key(key)
+            r = time_gemm(tg, wl, n_side, side_warm, stream, device)
+            rl = roofline_of(key, wl, r)
+            configs[cid] = config_record(rl, configs_parity(wl, r["C"]) if check else None)
+            configs[cid]["plan"] = plan_tag(r["plan"])
+            del r
+        # more input types, fused epilogues and schedules on the pages' benchmark sizes
+        paths = {}
         fused = {f"bf16_8192_{k}": v for k, v in FUSED_EPILOGUES.items()}
-        side += [(k, workload_by_key("bf16_8192")) for k in fused]
-        for key, wl in side:
-            r = time_gemm(tg, wl, n_side, max(3, min(args.warmup, 10)), stream, device, epi=fused.get(key))
-            tf = r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12
-            if wl.dtype == "fp32":
-                rl = roofline_alu(r["flops"], r["launch_ms_mean"], sm_mhz)
-            else:
-                rl = roofline_for_dtype(wl.dtype, r["flops"], r["launch_ms_mean"], peaks, peak_src,
-                                        profiled_traffic(key, r["plan"]))
-                # the low-tile-count shape streams B once: bandwidth is its binding roofline
-                if key == "bf16_128x8192x8192":
-                    in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2 + wl.M * wl.N * 4
-                    gbs = in_bytes / (r["launch_ms_mean"] * 1e-3) / 1e9
-                    rl = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(key, r["plan"]),
-                          "peak_source": f"hbm_gbs, {peak_src}", "tensor_tflops": rl["achieved"]}
-            in_b = (wl.M * wl.K + wl.K * wl.N) * ELEM_BYTES[wl.dtype]
-            paths[key] = {"workload": wl.name + (f", fused epilogue {fused[key]}" if key in fused else ""),
-                          "tflops": round(tf, 2), "steps": n_side,
-                          "l2": "inputs larger than L2" if in_b > L2_BYTES else "inputs fit in L2 (no flush)",
-                          "kernel_ms_mean": round(r["launch_ms_mean"], 4), "roofline": rl, "plan": r["plan"]}
-        # the headline shape under the dynamic schedule (Cluster Launch Control)
+        extra = [(k, workload_by_key(k), None) for k in ("fp16_4096", "fp16_8192", "e4m3_4096", "e4m3_8192",
+                                                        "e5m2_8192")]
+        extra += [(k, workload_by_key("bf16_8192"), v) for k, v in fused.items()]
+        for key, wl, epi in extra:
+            r = time_gemm(tg, wl, n_side, side_warm, stream, device, epi=epi)
+            rl = roofline_of(key, wl, r)
+            paths[key] = {"tflops": rl["achieved"], "frac": round(rl["frac"], 3)}
         with with_option(tg, "tc_sched", 2):
-            r = time_gemm(tg, w, n_side, max(3, min(args.warmup, 10)), stream, device)
-        paths["bf16_8192_dynamic_schedule"] = {
-            "workload": w.name + ", Cluster Launch Control schedule", "steps": n_side,
-            "tflops": round(r["flops"] / (r["total_ms"] / n_side * 1e-3) / 1e12, 2),
-            "kernel_ms_mean": round(r["launch_ms_mean"], 4), "plan": r["plan"],
-            "roofline": roofline_for_dtype("bf16", r["flops"], r["launch_ms_mean"], peaks, peak_src, None)}
-        # the skewed 16-group workload: one grouped launch (static and dynamic
-        # schedule), and the same GEMMs one by one
+            r = time_gemm(tg, w, n_side, side_warm, stream, device)
+        rl = roofline_of("bf16_8192_dynamic_schedule", w, r)
+        paths["bf16_8192_dynamic_schedule"] = {"tflops": rl["achieved"], "frac": round(rl["frac"], 3)}
         from tiled_tensor_core_gemm_gb300.inputs import GROUPED_BF16, GROUPED_BF16_SKEWK
-        # (tc_sched: 1 static, 2 dynamic)
+        # 16-group workloads: one grouped launch (static / dynamic / automatic schedule), and as 16 calls
         for key, gwl, obo, sched in (("grouped_bf16_16", GROUPED_BF16, False, 1),
                                     ("grouped_bf16_16_dynamic_schedule", GROUPED_BF16, False, 2),
                                     ("grouped_bf16_16_one_by_one", GROUPED_BF16, True, 1),
                                     ("grouped_bf16_16_skewed_k_static_schedule", GROUPED_BF16_SKEWK, False, 1),
                                     ("grouped_bf16_16_skewed_k", GROUPED_BF16_SKEWK, False, 0)):
             with with_option(tg, "tc_sched", sched):
-                r = time_grouped(tg, gwl, n_side, max(3, min(args.warmup, 10)), stream, device, obo)
+                r = time_grouped(tg, gwl, n_side, side_warm, stream, device, obo)
             rl = roofline_for_dtype("bf16", gwl.flops, r["ms"], peaks, peak_src, None)
-            paths[key] = {"workload": gwl.name + (", as 16 gemm_run calls" if obo else
-                                                 ", one gemm_run_grouped launch") +
-                                      {0: ", automatic schedule (dynamic: K differs by 2x or more)", 1: "",
-                                       2: ", Cluster Launch Control schedule"}[sched],
-                          "group_rows": list(gwl.Ms), "group_k": [gwl.k_of(g) for g in range(len(gwl.Ms))],
-                          "tflops": round(r["tflops"], 2), "steps": n_side,
-                          "ms_per_step": round(r["ms"], 4), "launches_per_step": r["launches_per_step"],
-                          "l2": "inputs larger than L2", "roofline": rl}
+            paths[key] = {"tflops": rl["achieved"], "frac": round(rl["frac"], 3)}
         out["paths"] = paths
+        # the headline again, back to back for at least a second: the clock the
+        # power cap settles at, against the sustained peak
+        sus_steps = max(args.steps, int(1.2 / max(ms_per_step * 1e-3, 1e-6)) + 1)
+        sus_sampler = ClockSampler(gpu_uuid(device))
+        sus_sampler.start()
+        try:
+            r = time_gemm(tg, w, sus_steps, 3, stream, device, on_begin=sus_sampler.mark_begin,
+                          on_end=sus_sampler.mark_end)
+        finally:
+            sus_clocks = sus_sampler.stop()
+        sus_tf = r["flops"] / (r["launch_ms_mean"] * 1e-3) / 1e12
+        out["sustained"] = {"tflops": round(sus_tf, 2), "steps": sus_steps, "seconds": round(r["total_ms"] / 1e3, 2),
+                            "peak": peaks["bf16_tflops_sustained"],
+                            "frac": round(sus_tf / peaks["bf16_tflops_sustained"], 4),
+                            "frac_of_burst": round(sus_tf / peaks["bf16_tflops"], 4), "clocks": sus_clocks}
+        del r
+        out["configs"] = configs
 
     if not args.no_e2e and gw is None:
         ms, h2d, d2h = time_e2e(tg, w, max(3, min(args.steps, 50)), stream, device)
         out["e2e"] = {"value": round(world * 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-                      "how": "every step: pinned host A,B -> device, gemm_run, C -> pinned host; steps pipelined "
-                             "over three streams with two device buffer sets (copy-in of step i, GEMM of i-1, "
-                             "copy-out of i-2 overlap); CUDA events from the first copy-in to the last copy-out"}
-    if not args.no_cpu_baseline and world == 1 and gw is None:
+                      "how": "pinned host A,B -> device, gemm_run, C -> pinned host each step, pipelined over "
+                             "three streams; events from the first copy-in to the last copy-out"}
+    if check and gw is None:
         out["cpu_baseline"], parity = cpu_baseline_leg(w, args.cpu_seconds, None if args.epilogue else res["C"])
         if parity is not None:
             out["parity"] = parity
-    print(json.dumps(out), flush=True)
+            if "configs" in out:
+                out["configs"] = {"c4_bf16_8192": config_record(roof, parity) | {"plan": plan_tag(res["plan"])},
+                                  **out["configs"]}
+    print(ordered_line(out), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def plan_tag(plan):
+    """The plan in a few characters: CTA group x tile width, K ranges or
+    column halves, B staging, packs and store path."""
+    if plan is None:
+        return None
+    if plan["path"] == 0:
+        return f"simt{plan['bm']}x{plan['bn']}" + (f"/k{plan['splits']}" if plan["splits"] > 1 else "")
+    t = f"cg{plan['cta_group']}x{plan['bn']}"
+    if plan["tail_tiles"]:
+        t += f"/k{plan['splits']}" + ("" if plan["tail_tiles"] == plan["tiles"] else "tail")
+        t += "dsm" if plan.get("cluster_split") else ""
+    if plan["half_tiles"]:
+        t += "/halves"
+    if plan["b_kmajor"]:
+        t += "/bT"
+    if plan["pack_a"] or plan["pack_b"]:
+        t += "/pack" + ("A" if plan["pack_a"] else "") + ("B" if plan["pack_b"] else "")
+    if not plan["tma_store"]:
+        t += "/st"
+    return t
 
 
 # -------------------------------------------------------- reference arm ---

@@ -245,6 +245,12 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    apply, off otherwise), 1 off, n >= 2: split the tiles
  *                    of the last, partly idle round of the persistent
  *                    schedule into n K ranges (same workspace and reduction)
+ *   "tc_split_reduce" how the K ranges of split-K tiles are summed: 0 auto
+ *                    (in cluster shared memory when every tile is split
+ *                    into 2 ranges on single-CTA tiles and the tiles fit one
+ *                    round of clusters, else the workspace and second
+ *                    kernel), 1 always the workspace and second kernel,
+ *                    2 in cluster shared memory where legal
  *   "tc_tail_halves" run the last round's tiles as column halves when the
  *                    halves fit in one round and the tile allows it (BN >=
  *                    128; B read as stored in whole 128-byte chunks per
@@ -305,6 +311,10 @@ typedef struct {
                             launched, running CTAs steal the rest)         */
     int32_t half_tiles;  /* tiles run as two column halves (the last ones in
                             the schedule), each half over all of K         */
+    int32_t cluster_split; /* 0, or the K ranges (2) of every split tile run by
+                            the CTAs of one cluster, their partial sums
+                            added in cluster shared memory: no workspace and
+                            no second kernel                                */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
@@ -331,10 +341,13 @@ GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
  *   - N * roundup(K, 4) must not exceed GEMM_TF32_STATIC_SCRATCH_BYTES / 4
  *     floats (GEMM_ERR_INVALID_ARG);
  *   - A must start on a 16-byte boundary with lda a multiple of 4
- *     (GEMM_ERR_UNSUPPORTED): there is no scratch for a copy of A.
+ *     (GEMM_ERR_UNSUPPORTED): there is no scratch for a copy of A.  So a
+ *     contiguous A (lda == K) with K not a multiple of 4 is rejected; pad lda
+ *     to a multiple of 4, or call gemm_run.
  * The first call on each device looks up the scratch array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the array and it keeps the last call's
+ * (cudaGetSymbolAddress) with that device current, and a call looks it up
+ * again when the device's context has changed since (after cudaDeviceReset);
+ * make such a call before any stream capture.  All calls share the array and it keeps the last call's
  * contents (no call needs it zeroed); calls whose GPU work overlaps -- e.g. on
  * two unordered streams -- race on it, so order them.
  */

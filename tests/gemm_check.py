@@ -125,14 +125,17 @@ def sample_rows(M: int, tile: int = 128, extra: int = 8, seed: int = 0):
 
 # ----------------------------------------------------------- fused epilogue --
 # Acceptance for C = act(alpha * A.B + beta * C_old + bias) stored as `out`:
-# the stored value must lie between the output type's grid points at or
-# beyond y - b and y + b (rounded down and up), where y is the oracle's fp64
-# value and b bounds the error of the FP32 result before the cast:
+# the stored value must lie in [RN(y - b), RN(y + b)], RN being round to
+# nearest (ties to even) onto the output type's grid, y the oracle's fp64
+# value and b a bound on the error of the FP32 result before the cast:
 #   b = (1.13 * tol + 1e-6) * S,  S = |alpha| D + |beta C_old| + |bias|,
 # i.e. the GEMM's own bound on alpha * A.B, times the largest slope of the
 # activation (GELU's is below 1.13, ReLU's is 1), plus a few FP32 roundings of
-# the three-term sum and of the activation.  Any correctly rounded cast of a
-# value within b of y passes; an off-by-one-ulp cast of a value outside fails.
+# the three-term sum and of the activation.  A round-to-nearest cast is
+# monotone, so the cast of any FP32 value within b of y lands in that
+# interval; where b is small against the output's spacing the interval is the
+# single grid point RN(y), and a cast that rounds up, truncates or lands one
+# grid step away falls outside it.
 OUT_P = {"f32": 24, "bf16": 8, "f16": 11}          # significand bits
 OUT_EMIN = {"f32": -126, "bf16": -126, "f16": -14}  # smallest normal exponent
 
@@ -145,6 +148,16 @@ def grid_round(x: np.ndarray, out: str, up: bool) -> np.ndarray:
     ulp = np.ldexp(1.0, e - (OUT_P[out] - 1))
     q = x / ulp
     return (np.ceil(q) if up else np.floor(q)) * ulp
+
+
+def grid_round_nearest(x: np.ndarray, out: str) -> np.ndarray:
+    """x rounded to the nearest point of the output type's grid, ties to the
+    point with an even last significand bit (values in the type's range)."""
+    x = np.asarray(x, np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e - 1, OUT_EMIN[out])
+    ulp = np.ldexp(1.0, e - (OUT_P[out] - 1))
+    return np.rint(x / ulp) * ulp
 
 
 OUT_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
@@ -193,8 +206,10 @@ def oracle_c_old(c_old: torch.Tensor | None, out: str):
 
 def epilogue_check(C: np.ndarray, acc: np.ndarray, D: np.ndarray, dtype: str, out: str, alpha: float, beta: float,
                    c_old, bias, act: str):
-    """Worst |out - y| / (distance from y to the allowed edge on that side);
-    <= 1 passes.  Also returns y."""
+    """Worst |out - mid| / half over the elements, where [lo, hi] = [RN(y - b),
+    RN(y + b)] is the allowed interval, mid its centre and half its half
+    width; <= 1 passes (inside the interval), and an element whose interval is
+    a single grid point must equal it (else inf).  Also returns y."""
     old = oracle_c_old(c_old, out)
     b = bias.numpy() if bias is not None else None
     y = oracle.epilogue(acc, alpha, beta, old, out, b, act)
@@ -204,13 +219,14 @@ def epilogue_check(C: np.ndarray, acc: np.ndarray, D: np.ndarray, dtype: str, ou
     if b is not None:
         S = S + np.abs(b.astype(np.float64))[None, :]
     slack = (1.13 * TOL[dtype] + 1e-6) * S
-    lo = grid_round(y - slack, out, up=False)
-    hi = grid_round(y + slack, out, up=True)
+    lo = grid_round_nearest(y - slack, out)
+    hi = grid_round_nearest(y + slack, out)
     if not np.all(np.isfinite(C)):
         return float("inf"), y
-    room = np.where(C >= y, hi - y, y - lo)
-    diff = np.abs(C - y)
-    if np.any(diff[room == 0] != 0):
+    mid, half = (lo + hi) / 2, (hi - lo) / 2
+    diff = np.abs(C - mid)
+    point = half == 0
+    if np.any(diff[point] != 0):
         return float("inf"), y
-    live = room > 0
-    return (float(np.max(diff[live] / room[live])) if np.any(live) else 0.0), y
+    live = ~point
+    return (float(np.max(diff[live] / half[live])) if np.any(live) else 0.0), y

@@ -116,8 +116,11 @@ def test_plan_8192_bf16_uses_cta_pairs_full_machine():
 
 def test_plan_tf32_and_fp32_4096():
     p = _plan(4096, 4096, 4096, tg.GEMM_TF32)
-    assert p["path"] == 1 and p["bk"] == 32 and p["b_kmajor"] == 1 and p["pack_b"] == 0
+    assert p["path"] == 1 and p["bk"] == 32 and p["b_kmajor"] == 0 and p["pack_b"] == 0   # B read as stored
     assert _plan(4096, 4096, 4096, tg.GEMM_BF16)["b_kmajor"] == 0
+    # a row pitch that is not a multiple of 16 bytes is packed, not transposed
+    r = _plan(512, 1023, 512, tg.GEMM_TF32)
+    assert r["b_kmajor"] == 0 and r["pack_b"] == 1
     s = _plan(4096, 4096, 4096, tg.GEMM_FP32)
     assert s["path"] == 0 and s["bm"] == 64 and s["bn"] == 128 and s["bk"] == 16 and s["vec"] == 1
     assert s["grid"] == 64 * 32
@@ -243,7 +246,7 @@ def test_plan_runs_the_last_round_as_column_halves():
         # 1024 tiles: 13 rounds and 36 left, 72 halves
         p = _plan(8192, 8192, 8192, tg.GEMM_BF16)
         assert p["half_tiles"] == 36 and p["tail_tiles"] == 0 and p["grid"] == 152
-        t = _plan(4096, 4096, 4096, tg.GEMM_TF32)                   # the K-major B copy halves too
+        t = _plan(4096, 4096, 4096, tg.GEMM_TF32)                   # TF32 B as stored halves too
         assert t["half_tiles"] == 28 and t["tail_tiles"] == 0
         # 272 tiles leave 44: 88 halves would not fit one round
         assert _plan(4097, 4095, 4099, tg.GEMM_BF16)["half_tiles"] == 0
@@ -325,10 +328,10 @@ def test_plan_forced_options():
     try:
         assert tg.gemm_set_option("tc_b_major", 1) == 0
         assert _plan(512, 512, 512, tg.GEMM_BF16)["b_kmajor"] == 1
+        assert _plan(512, 512, 512, tg.GEMM_TF32)["b_kmajor"] == 1
         assert tg.gemm_set_option("tc_b_major", 2) == 0
         assert _plan(512, 512, 512, tg.GEMM_BF16)["b_kmajor"] == 0
-        with pytest.raises(tg.GemmError, match="K-major copy"):
-            _plan(512, 512, 512, tg.GEMM_TF32)
+        assert _plan(512, 512, 512, tg.GEMM_TF32)["b_kmajor"] == 0
         assert tg.gemm_set_option("tc_b_major", 0) == 0
         assert tg.gemm_set_option("tc_cta_group", 1) == 0
         assert tg.gemm_set_option("tc_bn", 128) == 0

@@ -85,7 +85,7 @@ def test_tensor_peak_per_input_type(dtype, peak):
 
 def test_alu_roofline_worked_fp32():
     # 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz = 80.55 TFLOP/s; 4096^3 in 2.466 ms is 55.7 of it
-    r = bench.roofline_alu(2 * 4096 ** 3, 2.466, 2070.0)
+    r = bench.roofline_alu(2 * 4096 ** 3, 2.466, 2070.0, 152)
     assert r["bound"] == "alu" and r["peak"] == pytest.approx(80.55, abs=0.01)
     assert r["achieved"] == pytest.approx(55.73, abs=0.01) and r["frac"] == pytest.approx(0.6919, abs=1e-4)
 
@@ -107,3 +107,37 @@ def test_cpu_baseline_leg_times_the_oracle_and_checks_sampled_rows():
     nan[w.M - 1, 0] = float("nan")     # and so is the last row
     assert not bench.cpu_baseline_leg(w, 0.05, nan)[1]["ok"]
     assert bench.cpu_baseline_leg(w, 0.05, None)[1] is None
+
+
+def test_hbm_roofline_worked_short_wide_shape():
+    # 128 x 8192 x 8192 BF16: (128*8192 + 8192*8192) * 2 + 128*8192*4 bytes = 140.5 MB in 26.0 us is 5404 GB/s
+    from tiled_tensor_core_gemm_gb300.inputs import C5_BF16_RAGGED
+    r = bench.roofline_hbm(C5_BF16_RAGGED[3], 0.026, PEAKS, "measured", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6778.0
+    assert r["achieved"] == pytest.approx(140.5e6 / 26.0e-6 / 1e9, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6778.0, abs=1e-4)
+    assert r["tensor_tflops"] == pytest.approx(2 * 128 * 8192 * 8192 / 26.0e-6 / 1e12, abs=0.01)
+
+
+def test_configs_record_ends_the_line_within_a_short_tail():
+    """A line shaped like the headline run's, with every published workload:
+    the per-config object comes last, so the last 2000 characters of stdout
+    (all a driver may keep) hold it whole."""
+    import json
+    roof = bench.roofline_for_dtype("bf16", 2 * 8192 ** 3, 0.5763, PEAKS, "measured", 1373747080.0)
+    parity = {"rows": 32, "max_err_ratio": 9.3e-7, "tol": 1e-5, "ok": True, "what": "x" * 80}
+    plan = {"path": 1, "cta_group": 2, "bn": 256, "tail_tiles": 64, "tiles": 64, "splits": 2, "half_tiles": 0,
+            "b_kmajor": 0, "pack_a": 1, "pack_b": 1, "tma_store": 0, "bm": 128}
+    configs = {cid: bench.config_record(roof, parity) | {"plan": bench.plan_tag(plan)}
+               for cid, _ in (("c4_bf16_8192", 0),) + bench.CONFIG_WORKLOADS}
+    out = {"metric": bench.METRIC, "value": 1907.8, "config": {"workload": "w" * 300, "plan": plan},
+           "configs": configs, "roofline": roof, "paths": {f"p{i}": {"tflops": 1.0, "frac": 0.5} for i in range(12)},
+           "sustained": {"tflops": 1666.0, "clocks": {"sm_mhz": 1515.0, "reasons": ["sw_power_cap"]}},
+           "cpu_baseline": {"value": 0.04, "sample": "s" * 120}, "e2e": {"value": 662.8}, "parity": parity}
+    line = bench.ordered_line(out)
+    d = json.loads(line)
+    assert list(d)[-1] == "configs" and list(d)[:2] == ["metric", "value"]
+    tail = line[-2000:]
+    assert tail.index('"configs":') >= 0 and line.endswith("}}}")
+    assert json.loads("{" + tail[tail.index('"configs":'):]) == {"configs": configs}
+    assert bench.plan_tag(plan) == "cg2x256/k2/packAB/st"

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gemm_check import TOL, epilogue_check, error_ratio, grid_round
+from gemm_check import TOL, epilogue_check, error_ratio, grid_round, grid_round_nearest
 from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array, make_operands
 
 
@@ -133,7 +133,7 @@ def _grid_steps_up(x, out, n):
 
 
 @pytest.mark.parametrize("out", ["bf16", "f16"])
-def test_epilogue_gate_takes_the_rounded_value_and_rejects_two_steps_beyond(out):
+def test_epilogue_gate_takes_the_rounded_value_and_rejects_one_step_beyond(out):
     A, B, Cref, D = _ref()
     bias = torch.linspace(-1, 1, N, dtype=torch.float32)
     args = ("fp32", out, 0.5, 0.0, None, bias, "gelu")
@@ -144,13 +144,63 @@ def test_epilogue_gate_takes_the_rounded_value_and_rejects_two_steps_beyond(out)
     good = v.to(OUT[out]).double().numpy()
     worst, y2 = epilogue_check(good, Cref, D, *args)
     assert np.array_equal(y, y2) and worst <= 1.0
-    # the same output with its largest element two grid steps above the rounded value
+    # the same output with its largest element one grid step above the rounded value
     i, j = np.unravel_index(np.argmax(y), y.shape)
     bad = good.copy()
-    bad[i, j] = _grid_steps_up(good[i, j], out, 2)
+    bad[i, j] = _grid_steps_up(good[i, j], out, 1)
     assert epilogue_check(bad, Cref, D, *args)[0] > 1.0
     bad[i, j] = np.nan
     assert epilogue_check(bad, Cref, D, *args)[0] == float("inf")
+
+
+def test_grid_round_nearest_matches_the_library_casts():
+    """Round-to-nearest-even onto each output grid, against the library's own
+    FP32 -> BF16 / FP16 and FP64 -> FP32 conversions (one rounding each), on
+    random values over many binades, FP16 subnormals, and exact ties."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(100000) * np.exp2(rng.integers(-40, 12, 100000))).astype(np.float32)
+    sub = (rng.uniform(-1, 1, 20000) * 2.0 ** -14).astype(np.float32)              # FP16 subnormal range
+    for out, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        grid = torch.from_numpy(x).to(tdt).double().numpy()
+        step = grid_round(np.abs(grid) * (1 + 2.0 ** -(P[out] + 1)), out, True) - np.abs(grid)
+        ties = (np.abs(grid) + step / 2) * np.sign(grid)                            # halfway to the next point
+        ties = ties[np.abs(ties) < (6e4 if out == "f16" else 1e30)].astype(np.float32)
+        assert np.array_equal(ties.astype(np.float64), ties)                        # exact in FP32
+        for vals in (x, sub, ties):
+            vals = vals[np.abs(vals) < (6.5e4 if out == "f16" else 3e38)]
+            want = torch.from_numpy(vals).to(tdt).double().numpy()
+            assert np.array_equal(grid_round_nearest(vals.astype(np.float64), out), want), out
+    xd = rng.standard_normal(100000) * np.exp2(rng.integers(-60, 60, 100000))
+    assert np.array_equal(grid_round_nearest(xd, "f32"), xd.astype(np.float32).astype(np.float64))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_epilogue_gate_rejects_a_cast_that_rounds_up_or_truncates(out):
+    """Values a fraction of one grid step above grid points, with an error
+    bound b far below the spacing: the round-to-nearest cast passes, and a
+    cast that rounds up or truncates fails wherever it differs from it -- one
+    grid step off."""
+    ulp = 2.0 ** -(P[out] - 1)                                     # spacing in [1, 2)
+    frac = np.array([0.1, 0.3, 0.45, 0.55, 0.7, 0.9])
+    y = 1.0 + (np.arange(8)[None, :] + frac[:, None]) * ulp         # 6 x 8 values between grid points
+    b = 1e-5                                                       # the error bound before the cast
+    D = np.full_like(y, b / (1.13 * TOL["fp32"] + 1e-6))           # makes the gate's b exactly this
+    args = ("fp32", out, 1.0, 0.0, None, None, "none")
+    rn, up, down = grid_round_nearest(y, out), grid_round(y, out, True), grid_round(y, out, False)
+    assert epilogue_check(rn, y, D, *args)[0] <= 1.0
+    assert np.any(up != rn) and np.any(down != rn)
+    assert epilogue_check(up, y, D, *args)[0] > 1.0
+    assert epilogue_check(down, y, D, *args)[0] > 1.0
+    # a single element 0.9 grid steps above y (rounded up from 0.1 of a step) fails on its own
+    one = rn.copy()
+    one[0, 0] = up[0, 0]
+    assert one[0, 0] - y[0, 0] > 0.85 * ulp
+    assert epilogue_check(one, y, D, *args)[0] > 1.0
+    # and a value within b of a midpoint may go either way
+    mid = 1.0 + 0.5 * ulp + 0.3 * b
+    y2, D2 = np.array([[mid]]), np.array([[D[0, 0]]])
+    for c in (1.0, 1.0 + ulp):
+        assert epilogue_check(np.array([[c]]), y2, D2, *args)[0] <= 1.0
 
 
 # ------------------------------------------------------ TF32 input rounding --

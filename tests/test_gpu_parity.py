@@ -2,9 +2,10 @@
 
 * exact: small-integer inputs (every product and partial sum an exact small
   integer) at tile-edge shapes must give bit-identical C on every path;
-* the published workloads: 256^3 / 1024^3 FP32 and 1024^3 TF32 in full,
-  4096^3 FP32/TF32, 8192^3 BF16 and the ragged BF16 set on sampled rows, in
-  the launch configuration the benchmark uses (automatic plan);
+* the published workloads, every element of C: 256^3 / 1024^3 FP32, 1024^3
+  TF32, 4096^3 FP32/TF32, 8192^3 BF16 and the four ragged BF16 shapes, in
+  the launch configuration the benchmark uses (automatic plan); the FP16 and
+  FP8 workloads on sampled rows;
 * structure: identity, permutation, all-ones, K = 0, guard bands and padded
   leading dimensions, misaligned bases (operand pack), determinism, and every
   compiled tensor-core variant and epilogue.
@@ -33,7 +34,7 @@ def lib():
     tgbuild.build()
     tg.load_library()
     for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-              "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves"):
+              "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -127,10 +128,10 @@ def test_deterministic(dtype):
 TC_VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 256)]
 
 
-# (dtype, B staging): BF16, FP16 and FP8 read B as stored (N-major) or from the
-# K-major transposed copy; TF32 always uses the K-major copy.
-TC_OPERANDS = [("bf16", 2), ("bf16", 1), ("tf32", 1), ("fp16", 2), ("fp16", 1), ("e4m3", 2), ("e4m3", 1),
-               ("e5m2", 2), ("e5m2", 1)]
+# (dtype, B staging): every input type reads B as stored (N-major; TF32 with
+# the 32-byte-unit swizzle) or from the K-major transposed copy.
+TC_OPERANDS = [("bf16", 2), ("bf16", 1), ("tf32", 2), ("tf32", 1), ("fp16", 2), ("fp16", 1), ("e4m3", 2),
+               ("e4m3", 1), ("e5m2", 2), ("e5m2", 1)]
 
 
 @pytest.mark.parametrize("operands", TC_OPERANDS, ids=lambda o: f"{o[0]}_{'kmajorB' if o[1] == 1 else 'nmajorB'}")
@@ -163,10 +164,12 @@ def test_every_tensor_core_variant_exact(operands, variant, tma_store, shape):
 @pytest.mark.parametrize("variant", TC_VARIANTS, ids=lambda v: f"cg{v[0]}_bn{v[1]}")
 @pytest.mark.parametrize("splits", (2, 3, 7))
 def test_split_k_exact(dtype, variant, splits):
-    """Split-K: partial tiles in the workspace, summed in split order."""
+    """Split-K: partial tiles in the workspace, summed in split order by the
+    reduce kernel."""
     cg, bn = variant
     A, B = make_operands(300, 700, 1100, dtype, "ints", seed=20)
     try:
+        tg.gemm_set_option("tc_split_reduce", 1)
         tg.gemm_set_option("tc_cta_group", cg)
         tg.gemm_set_option("tc_bn", bn)
         tg.gemm_set_option("tc_splits", splits)
@@ -175,7 +178,52 @@ def test_split_k_exact(dtype, variant, splits):
         tg.gemm_set_option("tc_max_ctas", 3 * cg)
         _exact(A, B, dtype)
     finally:
-        for k in ("tc_cta_group", "tc_bn", "tc_splits", "tc_max_ctas", "tc_b_major"):
+        for k in ("tc_cta_group", "tc_bn", "tc_splits", "tc_max_ctas", "tc_b_major", "tc_split_reduce"):
+            tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16", "e4m3"))
+@pytest.mark.parametrize("bn", (64, 128, 256))
+@pytest.mark.parametrize("shape", [(300, 700, 1100), (128, 2048, 4096), (40, 1000, 777)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_split_k_summed_in_cluster_shared_memory_exact(dtype, bn, shape):
+    """Split-K with the two K ranges of a tile on the two CTAs of a cluster,
+    summed through distributed shared memory: exact on small integers, with
+    TMA stores, with plain stores (C not TMA-addressable), and with rows of a
+    lane quarter past M."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dtype, "ints", seed=33)
+    opts = {"tc_cta_group": 1, "tc_bn": bn, "tc_splits": 2, "tc_split_reduce": 2}
+    try:
+        for k, v in opts.items():
+            tg.gemm_set_option(k, v)
+        plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).as_dict()
+        assert plan["cluster_split"] == 2 and plan["splits"] == 2 and plan["grid"] == 2 * plan["tiles"], plan
+        _exact(A, B, dtype)
+        _exact(A, B, dtype, ldc_pad=3)
+    finally:
+        for k in opts:
+            tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+def test_cluster_split_k_gives_the_reduce_kernels_bits(dtype):
+    """On random data the cluster-summed split gives exactly the bits of the
+    workspace-and-reduce-kernel split: both add the K ranges' FP32 partials in
+    range order."""
+    M, N, K = 128, 8192, 8192 if dtype == "bf16" else 4096
+    A, B = make_operands(M, N, K, dtype, "normal", seed=34)
+    try:
+        tg.gemm_set_option("tc_splits", 2)
+        tg.gemm_set_option("tc_split_reduce", 1)
+        assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).cluster_split == 0
+        C1 = run_gemm(A, B, dtype)
+        tg.gemm_set_option("tc_split_reduce", 2)
+        assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).cluster_split == 2
+        C2 = run_gemm(A, B, dtype)
+        assert np.array_equal(C1, C2)
+    finally:
+        for k in ("tc_splits", "tc_split_reduce"):
             tg.gemm_set_option(k, 0)
 
 
@@ -200,7 +248,8 @@ def test_split_tail_exact(dtype, cg, max_ctas, tail_splits):
 
 
 HALF_CASES = [  # dtype, cta_group, BN, tc_b_major, CTAs
-    ("bf16", 2, 256, 0, 40), ("fp16", 2, 256, 0, 40), ("tf32", 2, 256, 0, 40), ("bf16", 2, 256, 1, 40),
+    ("bf16", 2, 256, 0, 40), ("fp16", 2, 256, 0, 40), ("tf32", 2, 256, 0, 40), ("tf32", 2, 256, 1, 40),
+    ("tf32", 1, 128, 0, 44), ("bf16", 2, 256, 1, 40),
     ("e5m2", 2, 256, 1, 40), ("bf16", 1, 256, 0, 40), ("bf16", 1, 128, 0, 44), ("e4m3", 1, 256, 1, 40)]
 
 
@@ -228,7 +277,7 @@ def test_tail_halves_exact(dtype, cg, bn, b_major, ctas, store):
 
 
 @pytest.mark.parametrize("K", (1, 65, 129))
-@pytest.mark.parametrize("dtype,cg,bn,b_major,ctas", [HALF_CASES[0], HALF_CASES[2], HALF_CASES[6]],
+@pytest.mark.parametrize("dtype,cg,bn,b_major,ctas", [("bf16", 2, 256, 0, 40), ("tf32", 2, 256, 0, 40), ("bf16", 1, 128, 0, 44)],
                          ids=lambda v: str(v))
 def test_tail_halves_short_k(dtype, cg, bn, b_major, ctas, K):
     """Column halves whose K loop is one or two k-blocks (the ring never fills)."""
@@ -406,8 +455,34 @@ def test_workload_full(w):
     assert r <= TOL[w.dtype], r
 
 
-@pytest.mark.parametrize("w", [C3_FP32_4096, C3_TF32_4096, C4_BF16_8192] + list(C5_BF16_RAGGED[1:]) +
-                         [FP16_4096, FP16_8192, E4M3_4096, E4M3_8192, E5M2_8192], ids=lambda w: w.name)
+# The oracle's C and D of a full-size workload, kept for the process: the FP32
+# and TF32 4096^3 workloads share their inputs (and so one oracle run).
+_ORACLE_CACHE = {}
+
+
+def _oracle_of(w):
+    kind = "f32" if w.dtype in ("fp32", "tf32") else w.dtype
+    key = (w.M, w.N, w.K, kind, w.dist, w.seed)
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE.clear()          # one full-size product held at a time (8192^3: 1 GiB of C and D)
+        A, B = workload_operands(w)
+        _ORACLE_CACHE[key] = oracle_full(A, B, w.dtype)
+    return _ORACLE_CACHE[key]
+
+
+@pytest.mark.parametrize("w", [C3_FP32_4096, C3_TF32_4096, C4_BF16_8192] + list(C5_BF16_RAGGED[1:]),
+                         ids=lambda w: w.name)
+def test_workload_full_size_every_element(w):
+    """The published full-size workloads, every element of C against the
+    oracle, in the launch configuration the benchmark times (automatic plan)."""
+    A, B = workload_operands(w)
+    C = run_gemm(A, B, w.dtype)
+    Cref, D = _oracle_of(w)
+    r = error_ratio(C, Cref, D)
+    assert r <= TOL[w.dtype], r
+
+
+@pytest.mark.parametrize("w", [FP16_4096, FP16_8192, E4M3_4096, E4M3_8192, E5M2_8192], ids=lambda w: w.name)
 def test_workload_sampled_rows(w):
     A, B = workload_operands(w)
     C = run_gemm(A, B, w.dtype)

@@ -110,26 +110,26 @@ bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
 
 int elem_bytes(int dtype) { return (dtype == GEMM_BF16 || dtype == GEMM_FP16) ? 2 : is_fp8(dtype) ? 1 : 4; }
 
-// Measured on GB300 (profiles/picker.md): with the paired FP32 FMAs the
+// Measured on GB300 (CUDA-event sweeps): with the paired FP32 FMAs the
 // 64 x 128 tile with a K step of 16 (128 threads of 8 x 8 outputs, three
 // blocks and 12 warps per SM) beats the 256-thread 128 x 128 tile (8 warps per
 // SM) at 4096^3, 1024^3 and 256^3.
 constexpr int kSimtDefault = 9;   // 64 x 128 x 16, 8 x 8 per thread
 // SIMT split-K target: about two waves of the three resident 128-thread
-// blocks per SM, K ranges of at least 32 (measured on GB300, picker.md:
+// blocks per SM, K ranges of at least 32 (measured on GB300:
 // 8 ranges at 1024^3 and 256^3, 2 at 2048^3, none at 4096^3).
 constexpr int kSimtBlocksPerSm = 6;
 constexpr int64_t kSimtMinKPerSplit = 32;
 constexpr int kMinKbPerSplit = 8;   // k-blocks per K range, so each range fills the ring several times
 // Split-K adds a second kernel and a workspace round trip (a few microseconds):
-// only worth it from about 4 GFLOP up (measured on GB300, profiles/picker.md).
+// only worth it from about 4 GFLOP up (measured on GB300).
 constexpr int64_t kMinSplitWork = 1LL << 31;
 // Column halves for the last round by default only on schedules this short.
 constexpr int64_t kMaxRoundsForHalves = 4;
 // Split-K shapes that stream B from HBM: at most this many rows of A (below the
 // BF16 ridge point of about 280 flop per byte) against a 16-bit B of at least
 // this many bytes (half of L2 and up) take 128-column tiles, twice as many
-// tiles over shallower K ranges (measured on GB300, picker.md: +5% to +10% at
+// tiles over shallower K ranges (measured on GB300: +5% to +10% at
 // 64..256 x 8192 x 8192 and 128 x 4096 x 16384; B of 32 MB, or 512 rows and
 // more, lose with them).
 constexpr int64_t kStreamBMaxRows = 256;
@@ -182,11 +182,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.bk = 128 / elem;
     p.pack_a = (a_addr % 16 != 0) || ((lda * elem) % 16 != 0);
     if (p.pack_a) out->lda_eff = round_up(K, 16 / elem);
-    // B is read as stored (N-major) for BF16; TF32 always reads a K-major
-    // transposed copy (the N-major TF32 form gave wrong results on GB300).
-    if (dtype == GEMM_TF32 && opt.tc_b_major == 2)
-        return fail(GEMM_ERR_UNSUPPORTED, "TF32 cannot read B as stored; it needs the K-major copy (tc_b_major 0 or 1)");
-    p.b_kmajor = opt.tc_b_major == 1 ? 1 : opt.tc_b_major == 2 ? 0 : (dtype == GEMM_TF32 ? 1 : 0);
+    // B is read as stored (N-major) unless a K-major transposed copy is asked
+    // for (or, below, an FP8 tile is too narrow for B's 128-byte chunks).
+    p.b_kmajor = opt.tc_b_major == 1 ? 1 : 0;
     if (p.b_kmajor) {
         p.pack_b = 0;
         out->ldb_eff = round_up(K, 16 / elem);
@@ -276,14 +274,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         // as many cycles as a whole tile's (the K-block cadence, about 545
         // cycles, not the MMA, sets its pace), but its epilogue drains half
         // the accumulator, which shortens the end of the launch.  Measured on
-        // GB300 (profiles/picker.md): +2% on 16-bit inputs with 3-4 rounds
+        // GB300: +2% on 16-bit inputs with 3-4 rounds
         // (4096^3, 16384 x 1024 x 4096), neutral at 8192^3 (14 power-capped
         // rounds), -3% on TF32 against its K split.
         half = rem;
     } else if ((opt.tc_tail_splits >= 2 || (opt.tc_tail_splits == 0 && dtype == GEMM_TF32)) && rem > 0) {
         // Split only the tiles of the last, partly idle round of the persistent
         // schedule, so that round's units each get a share of K.  Measured on
-        // GB300 (profiles/picker.md): +4% for TF32 4096^3 (its half-rate MMA
+        // GB300: +4% for TF32 4096^3 (its half-rate MMA
         // makes each tile long against the reduction), 1-9% slower for 16- and
         // 8-bit inputs -- whose units in a partly idle last round already run
         // faster -- so it is on by default for TF32 only.
@@ -295,10 +293,22 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     p.splits = splits;
     p.tail_tiles = (int32_t)tail;
     p.half_tiles = (int32_t)half;
+    // Split K on every tile, two ranges, single-CTA tiles, one round of
+    // clusters: the ranges of a tile run on the two CTAs of a cluster and are
+    // summed in cluster shared memory (no workspace round trip, no second
+    // kernel).  Measured on GB300: 128 x 8192 x 8192 (B streams from HBM).
+    if (opt.tc_split_reduce != 1 && splits == 2 && tail == tiles && cg == 1 && opt.tc_sched != 2 &&
+        max_clusters_2cta > 0 && tiles <= max_clusters_2cta && 2 * tiles <= units)
+        p.cluster_split = 2;
+    else if (opt.tc_split_reduce == 2 && tail > 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "split-K in cluster shared memory needs every tile split in 2 on single-CTA tiles, at most %d "
+                    "tiles and the static schedule (tiles=%lld splits=%d cta_group=%d)",
+                    max_clusters_2cta, (long long)tiles, splits, cg);
     const int64_t work_units = (tiles - tail - half) + tail * splits + 2 * half;
     units = std::min<int64_t>(units, work_units);
     // Static unless asked: measured on GB300 the dynamic schedule is within
-    // 1% at 8192^3 and 2% slower on 4096-class shapes (profiles/picker.md).
+    // 1% at 8192^3 and 2% slower on 4096-class shapes.
     p.sched = opt.tc_sched == 2 ? 1 : 0;
     // dynamic schedule: one cluster per work unit, the running ones steal the rest
     p.grid = (int32_t)((p.sched ? work_units : units) * cg);
@@ -343,6 +353,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "simt_splits")) {
         if (v < 0 || v > 8) return fail(GEMM_ERR_INVALID_ARG, "simt_splits must be in [0, 8]");
         g_opt.simt_splits = (int)v;
+    } else if (!std::strcmp(key, "tc_split_reduce")) {
+        if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_split_reduce must be 0, 1 or 2");
+        g_opt.tc_split_reduce = (int)v;
     } else if (!std::strcmp(key, "tc_tail_halves")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_halves must be 0, 1 or 2");
         g_opt.tc_tail_halves = (int)v;
@@ -383,6 +396,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_splits")) return o.tc_splits;
     if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
     if (!std::strcmp(key, "tc_tail_halves")) return o.tc_tail_halves;
+    if (!std::strcmp(key, "tc_split_reduce")) return o.tc_split_reduce;
     if (!std::strcmp(key, "simt_splits")) return o.simt_splits;
     if (!std::strcmp(key, "pdl")) return o.pdl;
     if (!std::strcmp(key, "tc_sched")) return o.tc_sched;
@@ -533,10 +547,12 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
     const uint64_t b_bytes = p.b_kmajor ? (uint64_t)N * plan.ldb_eff * eb
                              : p.pack_b ? (uint64_t)K * plan.ldb_eff * eb : 0;
     const uint64_t a_off = 0, b_off = (a_bytes + 255) / 256 * 256;
-    // Partial tiles of split tiles: tail_tiles x splits slabs of (128 * cta_group) x bn floats.
-    const uint64_t w_bytes = p.tail_tiles > 0 ? (uint64_t)p.tail_tiles * p.splits * 128 * p.cta_group * p.bn * 4 : 0;
+    // Partial tiles of split tiles: tail_tiles x splits slabs of (128 * cta_group) x bn floats
+    // (none when the K ranges are summed in cluster shared memory).
+    const bool slabs = p.tail_tiles > 0 && !p.cluster_split;
+    const uint64_t w_bytes = slabs ? (uint64_t)p.tail_tiles * p.splits * 128 * p.cta_group * p.bn * 4 : 0;
     const uint64_t w_off = (b_off + b_bytes + 255) / 256 * 256;
-    if (p.pack_a || p.pack_b || p.b_kmajor || p.tail_tiles > 0) {
+    if (p.pack_a || p.pack_b || p.b_kmajor || slabs) {
         e = cudaMallocAsync(&ws, (size_t)(w_off + w_bytes), stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -544,11 +560,19 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
                         cudaGetErrorString(e));
         }
         uint8_t *w = static_cast<uint8_t *>(ws);
-        if (p.pack_a) {
+        if (p.pack_a && p.pack_b) {
+            // both operands in one launch
+            e = pack_two_launch(A, lda, w + a_off, plan.lda_eff, M, K, a_lo, a_hi, B, ldb, w + b_off, plan.ldb_eff, K,
+                                N, b_lo, b_hi, eb, stream);
+            Ause = w + a_off;
+            Buse = w + b_off;
+        } else if (p.pack_a) {
             e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, a_lo, a_hi, stream);
             Ause = w + a_off;
         }
-        if (e == cudaSuccess && p.b_kmajor) {
+        if (e == cudaSuccess && p.pack_a && p.pack_b) {
+            // done above
+        } else if (e == cudaSuccess && p.b_kmajor) {
             e = transpose_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
             Buse = w + b_off;
         } else if (e == cudaSuccess && p.pack_b) {
@@ -561,7 +585,7 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
         }
     }
     char err[256] = {0};
-    float *Wp = p.tail_tiles > 0 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
+    float *Wp = slabs ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w_off) : nullptr;
     rc = tc_launch(p, dtype, (int)M, (int)N, (int)K, Ause, plan.lda_eff, Buse, plan.ldb_eff, C, ldc, Wp, epi,
                    (uint32_t)opt.wait_timeout_ms, stream, err, sizeof err);
     if (rc == GEMM_OK && Wp) {

@@ -229,9 +229,7 @@ int run_grouped(int dtype, int64_t G, const gemm_group_t *groups, const EpiParam
         bn = 256;
     }
     if (cg == 2 && clusters <= 0) return api_error(GEMM_ERR_UNSUPPORTED, "2-CTA tiles need cluster support");
-    if (dtype == GEMM_TF32 && opt.tc_b_major == 2)
-        return api_error(GEMM_ERR_UNSUPPORTED, "TF32 cannot read B as stored; it needs the K-major copy");
-    int b_kmajor = opt.tc_b_major == 1 ? 1 : opt.tc_b_major == 2 ? 0 : (dtype == GEMM_TF32 ? 1 : 0);
+    int b_kmajor = opt.tc_b_major == 1 ? 1 : 0;
     const bool fp8 = dtype == GEMM_E4M3 || dtype == GEMM_E5M2;
     if (fp8 && !b_kmajor && (bn / cg) % 128 != 0) {
         if (opt.tc_b_major == 2) return api_error(GEMM_ERR_UNSUPPORTED, "FP8 B as stored needs 128 columns per CTA");

@@ -23,7 +23,8 @@ struct Options {
     int tc_sched = 0;          // 0 auto, 1 static persistent, 2 Cluster Launch Control
     int tc_tma_store = 0;      // 0 auto, 1 force TMA store, 2 force plain stores
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
-    int tc_b_major = 0;        // 0 auto (BF16 as stored, TF32 transposed), 1 K-major copy, 2 as stored
+    int tc_b_major = 0;        // 0 auto (as stored; FP8 narrow tiles transposed), 1 K-major copy, 2 as stored
+    int tc_split_reduce = 0;   // 0 auto, 1 workspace + reduce kernel, 2 cluster shared memory
     int wait_timeout_ms = 2000;
     int debug_stall_mma = 0;   // test hook: make the MMA thread's first wait expire
 };
@@ -159,6 +160,12 @@ int tc_max_active_clusters(int device);
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int elem_bytes, uint64_t src_lo, uint64_t src_hi,
                              cudaStream_t stream);
+
+// Both operands' packs (as pack_rows_launch) in one launch.
+cudaError_t pack_two_launch(const void *a, int64_t lda, void *a_dst, int64_t lda_dst, int64_t a_rows, int64_t a_cols,
+                            uint64_t a_lo, uint64_t a_hi, const void *b, int64_t ldb, void *b_dst, int64_t ldb_dst,
+                            int64_t b_rows, int64_t b_cols, uint64_t b_lo, uint64_t b_hi, int elem_bytes,
+                            cudaStream_t stream);
 
 // For each split tile i (tile index full_tiles + i in the raster order), sums
 // its `splits` slabs W[(s * tail_tiles + i) * tile_rows * tile_cols ...] in

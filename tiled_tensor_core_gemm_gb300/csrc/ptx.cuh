@@ -79,6 +79,20 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// 16-byte store into shared memory named by a shared::cluster address
+// (possibly another CTA's of the cluster).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -177,15 +191,23 @@ __device__ __forceinline__ void tc_fence_after() {
 // ------------------------------------------------------------------- MMA ---
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all in 16-byte units), descriptor version 1 in bits
-// 46-47, base offset 0, and the 128-byte swizzle layout (value 2 in bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+// 46-47, base offset 0, and the layout type in bits 61-63: 2 = the 128-byte
+// swizzle of 16-byte units (8 rows of 128 bytes, 1024-byte pattern), 1 = the
+// 128-byte swizzle of 32-byte units (4 rows of 128 bytes, 512-byte pattern).
+enum SmemLayout : uint32_t { kLayoutSw128Atom32 = 1, kLayoutSw128 = 2 };
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(layout & 7u) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    return sdesc(saddr, lbo_bytes, sbo_bytes, kLayoutSw128);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; accumulate when `acc` is non-zero.

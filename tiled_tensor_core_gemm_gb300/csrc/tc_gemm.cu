@@ -64,9 +64,15 @@ constexpr int kUQ = 4;                         // unit-queue slots (dynamic sche
 
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
-// How B is staged: as stored (N-major, "MN-major" for the MMA; BF16 only --
-// with TF32 operands this form gave wrong results on GB300), or from a K-major
-// transposed copy.
+// How B is staged: as stored (N-major, "MN-major" for the MMA), or from a
+// K-major transposed copy.  B as stored comes in 128-byte column chunks of BK
+// K-rows.  For 16- and 8-bit operands each chunk uses the 128-byte swizzle of
+// 16-byte units (atoms of 8 K-rows, 1024 bytes).  The TF32 MMA reads an
+// MN-major operand only with the 128-byte swizzle of 32-byte units (measured
+// on GB300 by reading back which shared-memory element each (k, n) of one MMA
+// took: with 16-byte units it reads nothing valid): atoms of 4 K-rows, 512
+// bytes apart, in which row r holds its four 32-byte units in the order
+// u ^ (r % 4) -- the layout the TMA engine writes for that swizzle mode.
 enum BMode : int { kBNMajor = 0, kBKMajor = 1 };
 
 // Operand element type of a variant.
@@ -93,7 +99,12 @@ struct TcCfg {
     // B MN-major (as stored, K x N): B_CHUNKS boxes of BK rows x 128 bytes.
     static constexpr int B_BYTES = BKM ? BN_CTA * 128 : B_CHUNKS * B_CHUNK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int B_KSTEP_BYTES = (UMMA_K / 8) * 1024;  // 8 K-rows per 1024-byte swizzle atom
+    static constexpr int B_KSTEP_BYTES = (UMMA_K / 8) * 1024;  // one MMA's K-rows of a 128-byte chunk
+    // B as stored: TF32 takes the 32-byte-unit swizzle (4-row atoms 512 B apart),
+    // other types the 16-byte-unit one (8-row atoms 1024 B apart).
+    static constexpr bool B_ATOM32 = TF32 && !BKM;
+    static constexpr uint32_t B_SBO = B_ATOM32 ? 512u : 1024u;
+    static constexpr uint32_t B_LAYOUT = B_ATOM32 ? ptx::kLayoutSw128Atom32 : ptx::kLayoutSw128;
     static constexpr int STAGES_FIT = (kSmemBudget - 1024 - kEpiBytes - kBarBytes) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + kEpiBytes + kBarBytes;
@@ -116,8 +127,10 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
-    static_assert((2 * STAGES + 29) * 8 <= kBarBytes, "barrier area too small");
-    static_assert(!(TF32 && BMODE == kBNMajor), "TF32 reads B from the K-major copy");
+    static_assert((2 * STAGES + 37) * 8 <= kBarBytes, "barrier area too small");
+    // Split K reduced across a cluster: the partials a CTA receives (one per
+    // other K range, for its lane quarters) fit in its idle ring.
+    static_assert(kBM * BN * 4 <= STAGES * STAGE_BYTES, "ring too small for the cluster split-K partials");
 };
 
 struct TcParams {
@@ -139,6 +152,8 @@ struct TcParams {
     const GroupDesc *groups;           // grouped launch: per-group sizes, maps and C (nullptr: one GEMM)
     int group_count;
     int sched;                         // 0: static stride over units; 1: Cluster Launch Control
+    int csplit;                        // 0, or the K ranges of each tile reduced across a cluster of that
+                                       // many CTAs (one tile per cluster; cta_group 1)
     unsigned long long timeout_ns;
 };
 
@@ -281,7 +296,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t *epi = smem + Cf::STAGES * Cf::STAGE_BYTES;
     // Barrier area, in 8-byte words: full[S], empty[S], acc_full[2], acc_empty[2],
     // never, old_c[8], unit queue full[4] / empty[4], clc_full, clc_used, pad,
-    // CLC response (2 words), unit queue (2 words), TMEM slot + abort flag.
+    // CLC response (2 words), unit queue (2 words), TMEM slot + abort flag,
+    // cluster split-K ready[4] / partials-in[4].
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi + kEpiBytes);
     constexpr int kW = 2 * Cf::STAGES;
     uint8_t *clc_resp = reinterpret_cast<uint8_t *>(bars + kW + 24);          // 16-byte aligned
@@ -302,11 +318,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto uq_empty = [&](int i) { return bar0 + 8u * (uint32_t)(kW + 17 + i); };
     const uint32_t clc_full = bar0 + 8u * (uint32_t)(kW + 21);
     const uint32_t clc_used = bar0 + 8u * (uint32_t)(kW + 22);   // leader: both CTAs read the response
+    // cluster split-K, per TMEM lane quarter: ready (the owning CTA's ring is
+    // free to receive) and in (every other K range's partial has arrived)
+    auto csr_ready = [&](uint32_t q) { return bar0 + 8u * (uint32_t)(kW + 29) + 8u * q; };
+    auto csr_in = [&](uint32_t q) { return bar0 + 8u * (uint32_t)(kW + 33) + 8u * q; };
     const bool dyn = p.sched != 0;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
-    const int unit = (int)blockIdx.x / CG, nunits = (int)gridDim.x / CG;
+    // Cluster split-K: CTA crank of each cluster takes K range crank of the
+    // cluster's one tile (work unit crank * tiles + tile); no further units.
+    const uint32_t csplit = (uint32_t)p.csplit;
+    const uint32_t crank = csplit ? ptx::cluster_ctarank() : 0u;
+    const int unit = csplit ? (int)(crank * (uint32_t)p.tail_tiles + blockIdx.x / csplit) : (int)blockIdx.x / CG;
+    const int nunits = csplit ? p.num_units : (int)gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cf::STAGES; ++s) {
@@ -326,6 +351,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         ptx::mbar_init(clc_full, 1);
         ptx::mbar_init(clc_used, CG);
+        for (uint32_t i = 0; i < 4; ++i) {
+            ptx::mbar_init(csr_ready(i), 1);                                  // the owner's one arrival
+            ptx::mbar_init(csr_in(i), 32u * (csplit > 1 ? csplit - 1 : 1));  // every lane of each sender warp
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -340,7 +369,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
-    if (kPair) ptx::cluster_sync(); else __syncthreads();
+    if (kPair || csplit) ptx::cluster_sync(); else __syncthreads();   // peers' barriers ready before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Launched as a programmatic dependent of the previous kernel on the
@@ -350,7 +379,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // visible; then let the next launch start its own set-up (when no split-K
     // reduction, which reads this grid's slabs, comes next).
     ptx::pdl_wait();
-    if (p.tail_tiles == 0 && threadIdx.x == 0) ptx::pdl_launch_dependents();
+    if ((p.tail_tiles == 0 || csplit) && threadIdx.x == 0) ptx::pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -552,11 +581,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         // A: K-major, 8-row groups 1024 B apart; K advances 32 B inside the swizzle row.
                         const uint64_t adesc = ptx::sdesc_sw128(sa + 32u * kk, 16u, 1024u);
                         // B K-major: laid out like A.  B MN-major: 128-byte column chunks
-                        // B_CHUNK_BYTES apart (leading), 8-row K groups 1024 B apart (stride).
+                        // B_CHUNK_BYTES apart (leading), swizzle atoms of K-rows B_SBO apart (stride).
                         const uint64_t bdesc =
                             BKM ? ptx::sdesc_sw128(sb + 32u * kk, 16u, 1024u)
-                                : ptx::sdesc_sw128(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
-                                                   1024u);
+                                : ptx::sdesc(sb + (uint32_t)(Cf::B_KSTEP_BYTES * kk), (uint32_t)Cf::B_CHUNK_BYTES,
+                                             Cf::B_SBO, Cf::B_LAYOUT);
                         ptx::mma<CG, Cf::KIND>(d_tmem, adesc, bdesc, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
@@ -624,7 +653,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int ucols = halfu ? BN / 2 : BN;                                // columns of this unit
             const int n0 = U.tn * BN + (halfu ? U.half * (BN / 2) : 0);
             const int srow = (int)rank * kBM + 32 * (int)q;                       // same row inside a slab
-            const bool to_slab = slab >= 0;
+            const bool to_slab = slab >= 0 && !csplit;
             const bool use_tma = to_slab || U.tma_store;
             if (U.group != last_group) {
                 if (lane == 0 && U.tma_store) {
@@ -647,6 +676,58 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             ptx::tc_fence_after();
             const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
+            // Split K reduced across the cluster ("Learn CuTeDSL" section 9:
+            // distributed shared memory of a thread-block cluster).  Lane
+            // quarter q of the tile belongs to CTA q / (4 / csplit): the other
+            // CTAs store their partial of it, 32 rows x BN FP32, into the
+            // owner's ring (idle now: each CTA has run its only unit), and
+            // the owner adds them to its own in K-range order before the
+            // epilogue.
+            bool csr_owner = false;                    // this warp sums its quarter's K ranges
+            uint32_t csr_base = 0;                     // where the other ranges' partials of it land
+            if (csplit) {
+                const uint32_t per = 4u / csplit, owner = q / per, qloc = q % per;
+                const uint32_t part_bytes = 32u * (uint32_t)BN * 4u;
+                if (owner != crank) {
+                    const bool rdy = wait_bar<true>(csr_ready(q), 0u, abort_flag, p.timeout_ns);
+                    if (!__all_sync(0xffffffffu, rdy)) {
+                        if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                        break;
+                    }
+                    const uint32_t j = crank < owner ? crank : crank - 1;
+                    const uint32_t dst = ptx::mapa_shared(ptx::smem_addr(stages) + (j * per + qloc) * part_bytes, owner);
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(32 * c), r);
+                        ptx::tmem_wait_ld(r);
+                        const uint32_t row = dst + (uint32_t)c * 4096u + lane * 128u;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            ptx::st_cluster_v4(row + (((uint32_t)k ^ (lane & 7u)) * 16u), r[4 * k], r[4 * k + 1],
+                                               r[4 * k + 2], r[4 * k + 3]);
+                    }
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(csr_in(q), owner));   // release: this lane's stores
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                    if (ok && !next_unit(t, t)) {
+                        if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                        break;
+                    }
+                    continue;
+                }
+                if (lane < csplit && lane != crank) ptx::mbar_arrive_cluster(ptx::mapa_shared(csr_ready(q), lane));
+                const bool got = wait_bar<true>(csr_in(q), 0u, abort_flag, p.timeout_ns);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                    break;
+                }
+                csr_base = ptx::smem_addr(stages) + qloc * part_bytes;
+                csr_owner = true;
+            }
 #pragma unroll 1
             for (int jb = 0; jb < ucols / box_cols; ++jb, ++nchunk) {
                 uint8_t *buf = bufs + (nchunk & 1u) * kEpiBufBytes;
@@ -680,6 +761,33 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(box_cols * jb + 32 * h), r);
                     ptx::tmem_wait_ld(r);
+                    if (csr_owner) {
+                        // this quarter's K ranges summed in range order, this CTA's own at crank
+                        const uint32_t per = 4u / csplit, part_bytes = 32u * (uint32_t)BN * 4u;
+                        const uint32_t row = csr_base + (uint32_t)((box_cols * jb + 32 * h) / 32) * 4096u + lane * 128u;
+                        float sum[32];
+#pragma unroll 1
+                        for (uint32_t s = 0; s < csplit; ++s) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float4 v;
+                                if (s == crank) {
+                                    v = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                    __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                                } else {
+                                    const uint32_t j = s < crank ? s : s - 1;
+                                    v = ptx::ld_shared_v4f(row + j * per * part_bytes + (((uint32_t)k ^ (lane & 7u)) * 16u));
+                                }
+                                if (s == 0) {
+                                    sum[4 * k] = v.x; sum[4 * k + 1] = v.y; sum[4 * k + 2] = v.z; sum[4 * k + 3] = v.w;
+                                } else {
+                                    sum[4 * k] += v.x; sum[4 * k + 1] += v.y; sum[4 * k + 2] += v.z; sum[4 * k + 3] += v.w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(sum[c]);
+                    }
                     if (jb == ucols / box_cols - 1 && h == box_cols / 32 - 1) {
                         // The accumulator is fully in registers/shared: hand it back to the MMA.
                         ptx::tc_fence_before();
@@ -805,9 +913,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------------------ teardown
     // The split-K reduction (launched next, when tiles were split) may be
     // scheduled now; it waits for this grid's slab writes before reading them.
-    if (p.tail_tiles > 0 && threadIdx.x == 0) ptx::pdl_launch_dependents();
+    if (p.tail_tiles > 0 && !csplit && threadIdx.x == 0) ptx::pdl_launch_dependents();
     ptx::tc_fence_before();
-    if (kPair) ptx::cluster_sync(); else __syncthreads();
+    // (a cluster split's peers stay until no CTA of the cluster touches another's shared memory)
+    if (kPair || csplit) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cf::TMEM_COLS);
 }
@@ -828,9 +937,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Row-major matrix of `rows` x `cols` elements with a pitch of `ld` elements,
-// tiled in boxes of box_cols x box_rows with the 128-byte swizzle.
+// tiled in boxes of box_cols x box_rows with a 128-byte swizzle (of 16-byte
+// units unless `swizzle` says otherwise).
 CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base, int64_t cols, int64_t rows,
-                   int64_t ld, int box_cols, int box_rows) {
+                   int64_t ld, int box_cols, int box_rows,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = tensor_map_encoder();
     if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -838,7 +949,7 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const voi
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // FP32 slabs [count][rows][cols], dense, stored in 32 x 32 x 1 boxes with
@@ -871,7 +982,8 @@ CUresult encode_operands(int M, int N, int K, const void *A, int64_t lda, const 
     CUresult r = encode_2d(ta, dt, Cf::ELEM, A, K, M, lda, Cf::BK, kBM);
     if (r == CUDA_SUCCESS)
         r = Cf::BKM ? encode_2d(tb, dt, Cf::ELEM, B, K, N, ldb, Cf::BK, Cf::BN_CTA)   // B^T: N x K
-                    : encode_2d(tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK);
+                    : encode_2d(tb, dt, Cf::ELEM, B, N, K, ldb, Cf::CHUNK_COLS, Cf::BK,
+                                Cf::B_ATOM32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
     if (r == CUDA_SUCCESS && tma_store) {
         if (out == GEMM_OUT_F32)
             r = encode_2d(tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc, 32, 32);
@@ -901,9 +1013,10 @@ int launch_kernel(const gemm_plan_t &plan, const CUtensorMap &ta, const CUtensor
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n_attr = 0;
-    if (CG == 2) {
+    if (CG == 2 || p.csplit) {
+        // a CTA pair, or the CTAs of one tile's K ranges
         attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.x = CG == 2 ? 2 : (unsigned)p.csplit;
         attr[n_attr].val.clusterDim.y = 1;
         attr[n_attr].val.clusterDim.z = 1;
         ++n_attr;
@@ -949,7 +1062,7 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     CUresult r = encode_operands<DT, CG, BN, BMODE>(M, N, K, A, lda, B, ldb, C, ldc,
                                                     epi.active ? epi.out : GEMM_OUT_F32, plan.tma_store != 0, &ta,
                                                     &tb, &tc);
-    if (r == CUDA_SUCCESS && plan.tail_tiles > 0) {
+    if (r == CUDA_SUCCESS && plan.tail_tiles > 0 && !plan.cluster_split) {
         if (!W) {
             std::snprintf(err, errlen, "split tail without a workspace");
             return GEMM_ERR_INVALID_ARG;
@@ -976,6 +1089,14 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.num_units = p.full_tiles + p.tail_tiles * p.splits + 2 * p.half_tiles;
     p.C = C;
     p.ldc = ldc;
+    if (plan.cluster_split) {
+        if (CG != 1 || plan.cluster_split != p.splits || p.full_tiles != 0 || plan.sched != 0 ||
+            plan.grid != p.num_units) {
+            std::snprintf(err, errlen, "cluster split-K plan is inconsistent");
+            return GEMM_ERR_INVALID_ARG;
+        }
+        p.csplit = plan.cluster_split;
+    }
     return launch_kernel<DT, CG, BN, BMODE>(plan, ta, tb, tc, tw, p, stream, err, errlen);
 }
 
@@ -1012,11 +1133,11 @@ int launch_grouped_variant(const gemm_plan_t &plan, const GroupDesc *groups, int
 }
 
 // A (dtype, CTA group, BN, B mode) combination is compiled only if it is legal:
-// TF32 always reads the K-major copy of B, and B read as stored needs every
-// CTA's share of the tile width to be whole 128-byte column chunks.
+// B read as stored needs every CTA's share of the tile width to be whole
+// 128-byte column chunks.
 template <int DT, int CG, int BN, int BMODE>
 constexpr bool variant_ok() {
-    return !(DT == kDtTF32 && BMODE == kBNMajor) && (BMODE == kBKMajor || (BN / CG) % (128 / dt_elem(DT)) == 0);
+    return BMODE == kBKMajor || (BN / CG) % (128 / dt_elem(DT)) == 0;
 }
 
 enum VariantValue : int { kValSmem = 0, kValStages = 1, kValHalves = 2 };
@@ -1044,7 +1165,8 @@ static int tc_value(int dtype, int cta_group, int bn, int b_kmajor, int what) {
 #define X(cg, bn_)                                                                                   \
     if (cta_group == cg && bn == bn_) {                                                               \
         if (dtype == GEMM_TF32)                                                                       \
-            return mode == kBKMajor ? variant_value<kDtTF32, cg, bn_, kBKMajor>(what) : 0;           \
+            return mode == kBKMajor ? variant_value<kDtTF32, cg, bn_, kBKMajor>(what)                \
+                                    : variant_value<kDtTF32, cg, bn_, kBNMajor>(what);               \
         if (dtype == GEMM_FP16)                                                                       \
             return mode == kBKMajor ? variant_value<kDtFP16, cg, bn_, kBKMajor>(what)                \
                                     : variant_value<kDtFP16, cg, bn_, kBNMajor>(what);               \
@@ -1084,10 +1206,9 @@ static int dispatch_variant(const gemm_plan_t &plan, int dtype, F &&f, char *err
       integral_constant<int, MODE_>{})
 #define X(cg, bn_)                                                                                       \
     if (plan.cta_group == cg && plan.bn == bn_) {                                                         \
-        if (dtype == GEMM_TF32) {                                                                         \
-            if (plan.b_kmajor != kBKMajor) break;                                                         \
-            return TC_CALL(kDtTF32, kBKMajor, cg, bn_);                                                   \
-        }                                                                                                 \
+        if (dtype == GEMM_TF32)                                                                           \
+            return plan.b_kmajor == kBKMajor ? TC_CALL(kDtTF32, kBKMajor, cg, bn_)                        \
+                                             : TC_CALL(kDtTF32, kBNMajor, cg, bn_);                       \
         if (dtype == GEMM_FP16)                                                                           \
             return plan.b_kmajor == kBKMajor ? TC_CALL(kDtFP16, kBKMajor, cg, bn_)                        \
                                              : TC_CALL(kDtFP16, kBNMajor, cg, bn_);                       \

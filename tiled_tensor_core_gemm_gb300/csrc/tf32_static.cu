@@ -14,7 +14,11 @@
 // Host code cannot use the array's name as a device address, so on the first
 // call on each device (with that device current) the entry point asks the
 // runtime for the array's device address with cudaGetSymbolAddress and keeps
-// it for that device.  That first call should come before any stream capture.
+// it for that device, tagged with the unique id of the context it was looked
+// up in.  When the device's current context is another one (after
+// cudaDeviceReset, the module -- and with it the array -- is loaded anew), the
+// address is looked up again.  A call that does this look-up should come
+// before any stream capture.
 //
 // Every call shares the one array, and it keeps the previous call's contents.
 // Nothing in it needs to start at zero: each call's transpose writes every
@@ -24,6 +28,8 @@
 //
 // Beyond the scratch it runs exactly what gemm_run runs for GEMM_TF32: the
 // same argument checks, planner, transpose kernel and tensor-core kernel.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -37,14 +43,43 @@ constexpr int64_t kScratchElems = GEMM_TF32_STATIC_SCRATCH_BYTES / 4;
 static __device__ __align__(256) float g_tf32_bt_scratch[kScratchElems];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[64] = {nullptr};
+struct ScratchSlot {
+    unsigned long long ctx_id = 0;   // unique id of the context the address belongs to
+    void *ptr = nullptr;
+};
+ScratchSlot g_scratch[64];
 
-// Device address of the scratch array on device `dev` (which must be current).
+// Unique id of the calling thread's current context; false if none is current
+// or the driver entry points are unavailable.
+bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array on device `dev` (which must be current),
+// looked up once per context.
 int scratch_address(int dev, void **out) {
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchSlot &slot = g_scratch[dev];
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
+    if (!slot.ptr || !have_id || slot.ctx_id != id) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_tf32_bt_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_tf32_bt_scratch);   // also makes the context current
         if (e != cudaSuccess || p == nullptr) {
             cudaGetLastError();
             char msg[256];
@@ -52,9 +87,12 @@ int scratch_address(int dev, void **out) {
                           cudaGetErrorString(e));
             return api_error(GEMM_ERR_CUDA, msg);
         }
-        g_scratch_ptr[dev] = p;
+        if (!have_id) have_id = current_context_id(&id);
+        if (!have_id) return api_error(GEMM_ERR_CUDA, "no current CUDA context after the scratch look-up");
+        slot.ptr = p;
+        slot.ctx_id = id;
     }
-    *out = g_scratch_ptr[dev];
+    *out = slot.ptr;
     return GEMM_OK;
 }
 
