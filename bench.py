@@ -101,6 +101,9 @@ def parse_args():
     ap.add_argument("--option", action="append", default=[], metavar="KEY=VALUE",
                     help="set a library option (gemm_set_option) for the whole run, e.g. tc_sched=2")
     ap.add_argument("--no-paths", action="store_true", help="skip the FP32/TF32 side paths")
+    ap.add_argument("--trace", default=None, metavar="FILE",
+                    help="after timing, trace one call of the workload in the kernel (per-unit, per-role time "
+                         "stamps) and write it as Chrome-trace JSON to FILE; its summary joins the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
@@ -307,7 +310,7 @@ def time_gemm(tg, workload, steps, warmup, stream, device, dist=None, on_begin=N
         torch.cuda.synchronize()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     # the GEMM, plus the operand packs / B transpose before it and the split-K reduction after it
-    launches = (1 + int(plan["pack_a"] or plan["pack_b"]) + plan["b_kmajor"]
+    launches = (1 + plan["pack_a"] + plan["pack_b"] + plan["b_kmajor"]
                 + int(plan["tail_tiles"] > 0 and not plan.get("cluster_split"))
                 if plan["path"] == 1 else 1)
     return {"total_ms": total_ms, "launch_ms_mean": total_ms / steps,
@@ -720,6 +723,23 @@ def run_ours(args):
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": clocks,
     }
+    if args.trace and gw is None and rank == 0:
+        from tiled_tensor_core_gemm_gb300 import trace as tt
+        _, _, At, Bt = make_device_operands(w, device)
+        Ct = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+
+        def one_call():
+            with torch.cuda.stream(stream):
+                rc = tg.gemm_run(w.M, w.N, w.K, tg.DTYPES[w.dtype], At.data_ptr(), w.K, Bt.data_ptr(), w.N,
+                                 Ct.data_ptr(), w.N, stream.cuda_stream)
+                if rc != tg.GEMM_OK:
+                    raise RuntimeError(tg.gemm_last_error())
+        one_call()                                     # warm
+        recs, count = tt.capture(one_call)
+        with open(args.trace, "w") as f:
+            json.dump(tt.chrome_trace(recs), f)
+        out["trace"] = {"file": args.trace, "records": int(count), **{k: round(v, 2) for k, v in tt.summary(recs).items()}}
+        del At, Bt, Ct
     check = not args.no_cpu_baseline and world == 1
     if not args.no_paths and headline:
         n_side = max(3, min(args.steps, 100))

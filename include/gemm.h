@@ -250,7 +250,8 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    into 2 ranges on single-CTA tiles and the tiles fit one
  *                    round of clusters, else the workspace and second
  *                    kernel), 1 always the workspace and second kernel,
- *                    2 in cluster shared memory where legal
+ *                    2 in cluster shared memory where legal (every tile
+ *                    split into 2 or 4 ranges, one CTA per range)
  *   "tc_tail_halves" run the last round's tiles as column halves when the
  *                    halves fit in one round and the tile allows it (BN >=
  *                    128; B read as stored in whole 128-byte chunks per
@@ -276,6 +277,9 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    2 force reading B as stored (a TF32 call, or an FP8 call
  *                    with 64 columns per CTA, then fails with
  *                    GEMM_ERR_UNSUPPORTED)
+ *   "trace_addr"     device address of a trace buffer, 0 = off (see
+ *                    gemm_trace_record_t below); "trace_records" its
+ *                    capacity in records
  *   "wait_timeout_ms" bound on every in-kernel wait (default 2000)
  *   "debug_stall_mma" test hook: 1 makes the tensor-core kernel's MMA thread
  *                    first wait on a barrier nothing arrives at, so the wait
@@ -311,10 +315,10 @@ typedef struct {
                             launched, running CTAs steal the rest)         */
     int32_t half_tiles;  /* tiles run as two column halves (the last ones in
                             the schedule), each half over all of K         */
-    int32_t cluster_split; /* 0, or the K ranges (2) of every split tile run by
-                            the CTAs of one cluster, their partial sums
-                            added in cluster shared memory: no workspace and
-                            no second kernel                                */
+    int32_t cluster_split; /* 0, or the K ranges (2; 4 on request) of every
+                            split tile, run by the CTAs of one cluster and
+                            summed in cluster shared memory: no workspace
+                            and no second kernel                            */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
@@ -355,6 +359,33 @@ GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,
 GEMM_API int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K,
                                   const float *A, int64_t lda, const float *B, int64_t ldb,
                                   float *C, int64_t ldc, struct CUstream_st *stream);
+
+/*
+ * Timeline trace of the tensor-core kernel ("Learn CuTeDSL" section 7: the
+ * kernel stamps %globaltimer at points of interest into a global buffer,
+ * which the host turns into a timeline).  Off unless the option "trace_addr"
+ * holds the device address of a caller-owned buffer of 32 + 32 *
+ * "trace_records" bytes (8-byte aligned, device memory of the calling
+ * device).  Its first 32 bytes are a header whose first uint32 the kernel
+ * increments once per record it writes (records beyond "trace_records" are
+ * dropped but still counted); zero the header before a traced call.  Records
+ * follow the header, in no particular order.  The buffer is read only after
+ * the stream is synchronised; concurrent traced calls share the buffer.
+ */
+typedef struct {
+    uint64_t t_begin_ns;  /* %globaltimer at the start of the span           */
+    uint64_t t_end_ns;    /* %globaltimer at its end                          */
+    int32_t unit;         /* work unit (-1: the CTA's whole life)             */
+    int16_t role;         /* 1 TMA producer: the unit's loads issued;
+                             2 MMA issuer: accumulator free -> last commit;
+                             3 epilogue warp: accumulator full -> stored;
+                             4 CTA: start -> teardown                         */
+    int16_t sm;           /* %smid                                            */
+    int32_t cta;          /* blockIdx.x                                       */
+    int32_t sub;          /* roles 1-2: k-blocks of the unit; role 3: lane
+                             quarter (+4 when it sends its partial to a
+                             cluster peer instead of storing)                 */
+} gemm_trace_record_t;
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 GEMM_API int gemm_version(void);

@@ -297,14 +297,17 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     // clusters: the ranges of a tile run on the two CTAs of a cluster and are
     // summed in cluster shared memory (no workspace round trip, no second
     // kernel).  Measured on GB300: 128 x 8192 x 8192 (B streams from HBM).
-    if (opt.tc_split_reduce != 1 && splits == 2 && tail == tiles && cg == 1 && opt.tc_sched != 2 &&
-        max_clusters_2cta > 0 && tiles <= max_clusters_2cta && 2 * tiles <= units)
+    // On request, 4 ranges in clusters of 4 CTAs.
+    const bool cs_shape = tail == tiles && cg == 1 && opt.tc_sched != 2 && (int64_t)splits * tiles <= units;
+    if (opt.tc_split_reduce != 1 && cs_shape && splits == 2 && max_clusters_2cta > 0 && tiles <= max_clusters_2cta)
         p.cluster_split = 2;
+    else if (opt.tc_split_reduce == 2 && cs_shape && splits == 4)
+        p.cluster_split = 4;
     else if (opt.tc_split_reduce == 2 && tail > 0)
         return fail(GEMM_ERR_UNSUPPORTED,
-                    "split-K in cluster shared memory needs every tile split in 2 on single-CTA tiles, at most %d "
-                    "tiles and the static schedule (tiles=%lld splits=%d cta_group=%d)",
-                    max_clusters_2cta, (long long)tiles, splits, cg);
+                    "split-K in cluster shared memory needs every tile split in 2 (or 4) on single-CTA tiles, "
+                    "ranges x tiles <= %lld CTAs and the static schedule (tiles=%lld splits=%d cta_group=%d)",
+                    (long long)units, (long long)tiles, splits, cg);
     const int64_t work_units = (tiles - tail - half) + tail * splits + 2 * half;
     units = std::min<int64_t>(units, work_units);
     // Static unless asked: measured on GB300 the dynamic schedule is within
@@ -376,6 +379,12 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "debug_stall_mma")) {
         if (v < 0 || v > 1) return fail(GEMM_ERR_INVALID_ARG, "debug_stall_mma must be 0 or 1");
         g_opt.debug_stall_mma = (int)v;
+    } else if (!std::strcmp(key, "trace_addr")) {
+        if (v < 0 || v % 8 != 0) return fail(GEMM_ERR_INVALID_ARG, "trace_addr must be 0 or an 8-byte aligned address");
+        g_opt.trace_addr = v;
+    } else if (!std::strcmp(key, "trace_records")) {
+        if (v < 0 || v > (1 << 24)) return fail(GEMM_ERR_INVALID_ARG, "trace_records must be in [0, 2^24]");
+        g_opt.trace_records = (int)v;
     } else if (!std::strcmp(key, "wait_timeout_ms")) {
         if (v < 1 || v > 600000) return fail(GEMM_ERR_INVALID_ARG, "wait_timeout_ms must be in [1, 600000]");
         g_opt.wait_timeout_ms = (int)v;
@@ -403,6 +412,8 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "simt_variant")) return o.simt_variant;
     if (!std::strcmp(key, "tc_b_major")) return o.tc_b_major;
     if (!std::strcmp(key, "wait_timeout_ms")) return o.wait_timeout_ms;
+    if (!std::strcmp(key, "trace_addr")) return o.trace_addr;
+    if (!std::strcmp(key, "trace_records")) return o.trace_records;
     if (!std::strcmp(key, "debug_stall_mma")) return o.debug_stall_mma;
     return -1;
 }
@@ -508,6 +519,7 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
     if ((rc = check_device_span("B", B, (uint64_t)((K - 1) * ldb + N) * eb, dev, &b_lo, &b_hi))) return rc;
 
     const Options opt = options_snapshot();
+    if ((rc = api_check_trace(opt, dev))) return rc;
     Plan plan;
     rc = make_plan(M, N, K, dtype, (uint64_t)(uintptr_t)A, lda, (uint64_t)(uintptr_t)B, ldb, c0, ldc, d.sms,
                    d.max_clusters, opt, &plan);
@@ -560,19 +572,12 @@ int run(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, 
                         cudaGetErrorString(e));
         }
         uint8_t *w = static_cast<uint8_t *>(ws);
-        if (p.pack_a && p.pack_b) {
-            // both operands in one launch
-            e = pack_two_launch(A, lda, w + a_off, plan.lda_eff, M, K, a_lo, a_hi, B, ldb, w + b_off, plan.ldb_eff, K,
-                                N, b_lo, b_hi, eb, stream);
-            Ause = w + a_off;
-            Buse = w + b_off;
-        } else if (p.pack_a) {
+        // (one launch per operand: measured faster than one launch over both)
+        if (p.pack_a) {
             e = pack_rows_launch(A, lda, w + a_off, plan.lda_eff, M, K, eb, a_lo, a_hi, stream);
             Ause = w + a_off;
         }
-        if (e == cudaSuccess && p.pack_a && p.pack_b) {
-            // done above
-        } else if (e == cudaSuccess && p.b_kmajor) {
+        if (e == cudaSuccess && p.b_kmajor) {
             e = transpose_launch(B, ldb, w + b_off, plan.ldb_eff, K, N, eb, stream);
             Buse = w + b_off;
         } else if (e == cudaSuccess && p.pack_b) {
@@ -658,6 +663,12 @@ int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int6
 
 int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev) {
     return check_device_span(name, p, bytes, dev);
+}
+
+int api_check_trace(const Options &opt, int dev) {
+    if (!opt.trace_addr) return GEMM_OK;
+    return check_device_span("trace buffer", reinterpret_cast<const void *>((uintptr_t)opt.trace_addr),
+                             32ull + 32ull * (uint64_t)opt.trace_records, dev);
 }
 
 int api_check_device_span_range(const char *name, const void *p, uint64_t bytes, int dev, uint64_t *lo,

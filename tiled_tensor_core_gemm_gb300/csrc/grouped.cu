@@ -204,6 +204,7 @@ int run_grouped(int dtype, int64_t G, const gemm_group_t *groups, const EpiParam
     EpiParams epi = epi_in;
     if (any_bias) epi.active = 1;      // NULL-bias groups then add 0
     const Options opt = options_snapshot();
+    if ((rc = api_check_trace(opt, dev))) return rc;
 
     // ---- one plan for every group, from the total tile count
     gemm_plan_t plan;

@@ -26,6 +26,8 @@ struct Options {
     int tc_b_major = 0;        // 0 auto (as stored; FP8 narrow tiles transposed), 1 K-major copy, 2 as stored
     int tc_split_reduce = 0;   // 0 auto, 1 workspace + reduce kernel, 2 cluster shared memory
     int wait_timeout_ms = 2000;
+    int64_t trace_addr = 0;    // device address of a trace buffer (0: off)
+    int trace_records = 0;     // its capacity in records
     int debug_stall_mma = 0;   // test hook: make the MMA thread's first wait expire
 };
 Options options_snapshot();
@@ -161,12 +163,6 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
                              int64_t rows, int64_t cols, int elem_bytes, uint64_t src_lo, uint64_t src_hi,
                              cudaStream_t stream);
 
-// Both operands' packs (as pack_rows_launch) in one launch.
-cudaError_t pack_two_launch(const void *a, int64_t lda, void *a_dst, int64_t lda_dst, int64_t a_rows, int64_t a_cols,
-                            uint64_t a_lo, uint64_t a_hi, const void *b, int64_t ldb, void *b_dst, int64_t ldb_dst,
-                            int64_t b_rows, int64_t b_cols, uint64_t b_lo, uint64_t b_hi, int elem_bytes,
-                            cudaStream_t stream);
-
 // For each split tile i (tile index full_tiles + i in the raster order), sums
 // its `splits` slabs W[(s * tail_tiles + i) * tile_rows * tile_cols ...] in
 // split order into C (clipped to M x N), through `epi`.
@@ -191,6 +187,8 @@ void api_clear_error();
 int api_validate(int64_t M, int64_t N, int64_t K, int dtype, const void *A, int64_t lda, const void *B,
                  int64_t ldb, const void *C, int64_t ldc);
 int api_check_device_span(const char *name, const void *p, uint64_t bytes, int dev);
+// The trace buffer named by the options, if any, is device memory of `dev` with room for its records.
+int api_check_trace(const Options &opt, int dev);
 // The same, also reporting the allocation [*lo, *hi) that holds the span.
 int api_check_device_span_range(const char *name, const void *p, uint64_t bytes, int dev, uint64_t *lo,
                                 uint64_t *hi);

@@ -61,32 +61,15 @@ __device__ __forceinline__ uint32_t keep_bytes(uint32_t w, int nbytes) {
     return nbytes >= 4 ? w : nbytes <= 0 ? 0u : (w & ((1u << (8 * nbytes)) - 1u));
 }
 
-// One matrix of a vector pack launch (bytes throughout).
-struct PackJob {
-    const uint8_t *src;
-    int64_t ld_src, ld_dst, rows, row_bytes;
-    uint8_t *dst;
-    uintptr_t lo, hi;                  // the source allocation: words outside it are not read
-};
-
-// Packs `a`, then `b` (b.rows may be 0), in one launch: the grid strides over
-// the destination chunks of both.
 template <int ELEM>
-__global__ void __launch_bounds__(256) pack_rows_vec(const PackJob ja, const PackJob jb) {
+__global__ void __launch_bounds__(256) pack_rows_vec(const uint8_t *__restrict__ src, int64_t ld_src_bytes,
+                                                     uint8_t *__restrict__ dst, int64_t ld_dst_bytes, int64_t rows,
+                                                     int64_t row_bytes, uintptr_t lo, uintptr_t hi) {
     pdl_enter();
     // one thread per destination 16-byte chunk, consecutive threads along a row
-    const int64_t total_a = ja.rows * (ja.ld_dst / 16);
-    const int64_t total = total_a + jb.rows * (jb.ld_dst / 16);
-    for (int64_t xx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; xx < total; xx += (int64_t)gridDim.x * blockDim.x) {
-        // the fields of this chunk's matrix, selected by value (no indexing into the parameters)
-        const bool in_a = xx < total_a;
-        const int64_t x = in_a ? xx : xx - total_a;
-        const uint8_t *__restrict__ src = in_a ? ja.src : jb.src;
-        uint8_t *__restrict__ dst = in_a ? ja.dst : jb.dst;
-        const int64_t ld_src_bytes = in_a ? ja.ld_src : jb.ld_src, ld_dst_bytes = in_a ? ja.ld_dst : jb.ld_dst;
-        const int64_t row_bytes = in_a ? ja.row_bytes : jb.row_bytes;
-        const uintptr_t lo = in_a ? ja.lo : jb.lo, hi = in_a ? ja.hi : jb.hi;
-        const int64_t chunks = ld_dst_bytes / 16;
+    const int64_t chunks = ld_dst_bytes / 16;
+    const int64_t total = rows * chunks;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = x / chunks, c = x - r * chunks;
         const uintptr_t s = reinterpret_cast<uintptr_t>(src) + (uintptr_t)(r * ld_src_bytes);
         const uintptr_t a = s & ~(uintptr_t)15;
@@ -344,39 +327,6 @@ cudaError_t epilogue_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, con
     return launch_pdl(epilogue_fill, dim3(blocks), dim3(256), 0, stream, C, ldc, M, N, epi);
 }
 
-namespace {
-
-// The vector pack needs a 16-byte aligned destination with 16-byte rows.
-bool pack_vec_ok(const void *dst, int64_t ld_dst, int elem_bytes, uint64_t src_lo, uint64_t src_hi) {
-    return (uintptr_t)dst % 16 == 0 && (ld_dst * elem_bytes) % 16 == 0 && src_hi > src_lo &&
-           (elem_bytes == 1 || elem_bytes == 2 || elem_bytes == 4);
-}
-
-PackJob pack_job(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols,
-                 int elem_bytes, uint64_t src_lo, uint64_t src_hi) {
-    PackJob j;
-    j.src = static_cast<const uint8_t *>(src);
-    j.ld_src = ld_src * elem_bytes;
-    j.dst = static_cast<uint8_t *>(dst);
-    j.ld_dst = ld_dst * elem_bytes;
-    j.rows = rows;
-    j.row_bytes = cols * elem_bytes;
-    j.lo = (uintptr_t)src_lo;
-    j.hi = (uintptr_t)src_hi;
-    return j;
-}
-
-cudaError_t pack_vec_launch(const PackJob &a, const PackJob &b, int elem_bytes, int sms, cudaStream_t stream) {
-    const int64_t chunks = a.rows * (a.ld_dst / 16) + b.rows * (b.ld_dst / 16);
-    const int64_t vwant = (chunks + 255) / 256;
-    const dim3 vgrid((unsigned)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16));
-    if (elem_bytes == 1) return launch_pdl(pack_rows_vec<1>, vgrid, dim3(256), 0, stream, a, b);
-    if (elem_bytes == 2) return launch_pdl(pack_rows_vec<2>, vgrid, dim3(256), 0, stream, a, b);
-    return launch_pdl(pack_rows_vec<4>, vgrid, dim3(256), 0, stream, a, b);
-}
-
-}  // namespace
-
 cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows, int64_t cols,
                              int elem_bytes, uint64_t src_lo, uint64_t src_hi, cudaStream_t stream) {
     cudaError_t e;
@@ -384,10 +334,24 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
     if (e != cudaSuccess) return e;
     const int64_t want = (rows + 7) / 8;   // 8 warps per block, one row per warp per pass
     const dim3 grid((unsigned)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8));
-    if (pack_vec_ok(dst, ld_dst, elem_bytes, src_lo, src_hi)) {
-        PackJob none = pack_job(nullptr, 0, nullptr, 16 / elem_bytes, 0, 0, elem_bytes, 0, 0);
-        return pack_vec_launch(pack_job(src, ld_src, dst, ld_dst, rows, cols, elem_bytes, src_lo, src_hi), none,
-                               elem_bytes, sms, stream);
+    // The vector form needs a 16-byte aligned destination with 16-byte rows.
+    if ((uintptr_t)dst % 16 == 0 && (ld_dst * elem_bytes) % 16 == 0 && src_hi > src_lo) {
+        const int64_t chunks = rows * (ld_dst * elem_bytes / 16);
+        const int64_t vwant = (chunks + 255) / 256;
+        const dim3 vgrid((unsigned)(vwant < (int64_t)sms * 16 ? (vwant > 0 ? vwant : 1) : (int64_t)sms * 16));
+        const uint8_t *s = static_cast<const uint8_t *>(src);
+        uint8_t *d = static_cast<uint8_t *>(dst);
+        const uintptr_t lo = (uintptr_t)src_lo, hi = (uintptr_t)src_hi;
+        const int64_t eb = elem_bytes;
+        if (elem_bytes == 1)
+            return launch_pdl(pack_rows_vec<1>, vgrid, dim3(256), 0, stream, s, ld_src, d, ld_dst, rows, cols, lo, hi);
+        if (elem_bytes == 2)
+            return launch_pdl(pack_rows_vec<2>, vgrid, dim3(256), 0, stream, s, ld_src * eb, d, ld_dst * eb, rows,
+                              cols * eb, lo, hi);
+        if (elem_bytes == 4)
+            return launch_pdl(pack_rows_vec<4>, vgrid, dim3(256), 0, stream, s, ld_src * eb, d, ld_dst * eb, rows,
+                              cols * eb, lo, hi);
+        return cudaErrorInvalidValue;
     }
     if (elem_bytes == 1)
         return launch_pdl(pack_rows<uint8_t>, grid, dim3(256), 0, stream, static_cast<const uint8_t *>(src), ld_src,
@@ -399,23 +363,6 @@ cudaError_t pack_rows_launch(const void *src, int64_t ld_src, void *dst, int64_t
         return launch_pdl(pack_rows<uint32_t>, grid, dim3(256), 0, stream, static_cast<const uint32_t *>(src), ld_src,
                           static_cast<uint32_t *>(dst), ld_dst, rows, cols);
     return cudaErrorInvalidValue;
-}
-
-cudaError_t pack_two_launch(const void *a, int64_t lda, void *a_dst, int64_t lda_dst, int64_t a_rows, int64_t a_cols,
-                            uint64_t a_lo, uint64_t a_hi, const void *b, int64_t ldb, void *b_dst, int64_t ldb_dst,
-                            int64_t b_rows, int64_t b_cols, uint64_t b_lo, uint64_t b_hi, int elem_bytes,
-                            cudaStream_t stream) {
-    cudaError_t e;
-    const int sms = sm_count(&e);
-    if (e != cudaSuccess) return e;
-    if (!pack_vec_ok(a_dst, lda_dst, elem_bytes, a_lo, a_hi) || !pack_vec_ok(b_dst, ldb_dst, elem_bytes, b_lo, b_hi)) {
-        e = pack_rows_launch(a, lda, a_dst, lda_dst, a_rows, a_cols, elem_bytes, a_lo, a_hi, stream);
-        return e != cudaSuccess ? e : pack_rows_launch(b, ldb, b_dst, ldb_dst, b_rows, b_cols, elem_bytes, b_lo, b_hi,
-                                                       stream);
-    }
-    return pack_vec_launch(pack_job(a, lda, a_dst, lda_dst, a_rows, a_cols, elem_bytes, a_lo, a_hi),
-                           pack_job(b, ldb, b_dst, ldb_dst, b_rows, b_cols, elem_bytes, b_lo, b_hi), elem_bytes, sms,
-                           stream);
 }
 
 }  // namespace tcgemm

@@ -155,6 +155,9 @@ struct TcParams {
     int csplit;                        // 0, or the K ranges of each tile reduced across a cluster of that
                                        // many CTAs (one tile per cluster; cta_group 1)
     unsigned long long timeout_ns;
+    uint32_t *trace_count;             // timeline trace: record counter (nullptr: off)
+    gemm_trace_record_t *trace;        // and the records after it
+    int trace_cap;
 };
 
 // Work unit u -> output tile (tm, tn), its K range [kb0, kb1), the slab its
@@ -257,6 +260,21 @@ __device__ __forceinline__ Unit unit_info(int u, const TcParams &p, const CUtens
     return U;
 }
 
+// One timeline record (when tracing is on): a span of `role` on `unit`.
+__device__ __noinline__ void trace_put(const TcParams &p, int role, int unit, int sub, uint64_t t0, uint64_t t1) {
+    const uint32_t i = atomicAdd(p.trace_count, 1u);
+    if (i >= (uint32_t)p.trace_cap) return;
+    gemm_trace_record_t r;
+    r.t_begin_ns = t0;
+    r.t_end_ns = t1;
+    r.unit = unit;
+    r.role = (int16_t)role;
+    r.sm = (int16_t)ptx::smid();
+    r.cta = (int32_t)blockIdx.x;
+    r.sub = sub;
+    p.trace[i] = r;
+}
+
 __device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
     *abort_flag = 1;
     if (atomicCAS(&g_tc_status[0], 0u, (uint32_t)GEMM_ERR_TIMEOUT) == 0u) {
@@ -288,6 +306,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     using Cf = TcCfg<DT, CG, BN, BMODE>;
     constexpr bool kPair = CG == 2;
     constexpr bool BKM = Cf::BKM;
+    const bool tracing = p.trace_count != nullptr;
+    const uint64_t t_start = tracing ? ptx::globaltimer_ns() : 0;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -408,6 +428,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int nchunks = BKM ? 0 : cta_cols / Cf::CHUNK_COLS;
                 const uint32_t tx_bytes =
                     (uint32_t)((Cf::A_BYTES + (BKM ? Cf::B_BYTES : nchunks * Cf::B_CHUNK_BYTES)) * CG);
+                const uint64_t t_unit = tracing ? ptx::globaltimer_ns() : 0;
                 for (int kb = U.kb0; kb < U.kb1; ++kb) {
                     if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                         record_failure(kRoleProducer, t, abort_flag);
@@ -443,6 +464,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (tracing) trace_put(p, 1, t, U.kb1 - U.kb0, t_unit, ptx::globaltimer_ns());
                 return true;
             };
             if (!dyn) {
@@ -566,6 +588,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
+                const uint64_t t_unit = tracing ? ptx::globaltimer_ns() : 0;
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
@@ -595,6 +618,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!ok) break;
                 if (kPair) ptx::mma_commit_pair(accf_bar(acc), 0x3);
                 else ptx::mma_commit(accf_bar(acc));
+                if (tracing) trace_put(p, 2, t, kb1 - kb0, t_unit, ptx::globaltimer_ns());
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
                 if (!next_unit(t, t)) {
@@ -675,6 +699,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 break;
             }
             ptx::tc_fence_after();
+            const uint64_t t_unit = tracing ? ptx::globaltimer_ns() : 0;
             const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
             // Split K reduced across the cluster ("Learn CuTeDSL" section 9:
             // distributed shared memory of a thread-block cluster).  Lane
@@ -711,6 +736,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                    if (tracing && lane == 0) trace_put(p, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
                     if (ok && !next_unit(t, t)) {
@@ -875,6 +901,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                     const int col = col0 + (int)lane;
                     const uint32_t cchunk = lane >> 2, cword = lane & 3u;
+                    if (!fused) {
+                        // The box's 32 rows: every shared load first, then the
+                        // stores, with the row and column tests and the address
+                        // arithmetic done once (the last round's epilogue runs
+                        // exposed at the end of the launch).
+                        const int nrows = min(32, U.M - m0);
+                        const bool col_ok = col < U.N;
+                        float *dst = static_cast<float *>(U.C) + (int64_t)m0 * U.ldc + col;
+                        const uint8_t *src = buf + cword * 4u;
+                        float v[32];
+#pragma unroll
+                        for (int rr = 0; rr < 32; ++rr)
+                            v[rr] = *reinterpret_cast<const float *>(src + rr * 128 + ((cchunk ^ (uint32_t)(rr & 7)) * 16u));
+                        if (col_ok) {
+#pragma unroll
+                            for (int rr = 0; rr < 32; ++rr) {
+                                if (rr < nrows) *dst = v[rr];
+                                dst += U.ldc;
+                            }
+                        }
+                        __syncwarp();
+                        continue;
+                    }
                     const float bias = epi_bias(e, col, U.N);
 #pragma unroll 1
                     for (int r0 = 0; r0 < 32; r0 += 8) {
@@ -899,6 +948,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                 }
             }
+            if (tracing && lane == 0) trace_put(p, 3, t, (int)q, t_unit, ptx::globaltimer_ns());
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
             if (ok && !next_unit(t, t)) {
@@ -919,6 +969,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (kPair || csplit) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cf::TMEM_COLS);
+    if (tracing && threadIdx.x == 0) trace_put(p, 4, -1, 0, t_start, ptx::globaltimer_ns());
 }
 
 // ------------------------------------------------------------------ host ---
@@ -1049,6 +1100,12 @@ TcParams base_params(const gemm_plan_t &plan, const EpiParams &epi, uint32_t tim
     p.groups = nullptr;
     p.sched = plan.sched;
     p.timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+    const Options o = options_snapshot();
+    if (o.trace_addr) {
+        p.trace_count = reinterpret_cast<uint32_t *>((uintptr_t)o.trace_addr);
+        p.trace = reinterpret_cast<gemm_trace_record_t *>((uintptr_t)o.trace_addr + 32);
+        p.trace_cap = o.trace_records;
+    }
     return p;
 }
 

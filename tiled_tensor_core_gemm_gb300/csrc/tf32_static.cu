@@ -138,6 +138,7 @@ extern "C" int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K, const float
     if ((rc = api_check_device_span("B", B, (uint64_t)((K - 1) * ldb + N) * 4u, dev))) return rc;
 
     Options opt = options_snapshot();
+    if ((rc = api_check_trace(opt, dev))) return rc;
     opt.tc_b_major = 1;   // B always goes through the transposed copy in the scratch
     opt.tc_splits = 1;    // no workspace for partial sums of split tiles
     opt.tc_tail_splits = 1;
