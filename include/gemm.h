@@ -379,7 +379,15 @@ typedef struct {
     int16_t role;         /* 1 TMA producer: the unit's loads issued;
                              2 MMA issuer: accumulator free -> last commit;
                              3 epilogue warp: accumulator full -> stored;
-                             4 CTA: start -> teardown                         */
+                             4 CTA: start -> teardown;
+                             5 CTA set-up: sub 0 start -> barriers, Tensor
+                               Memory and CTA/cluster barrier done, sub 1
+                               -> the previous grid's wait done;
+                             6 epilogue detail: sub 0-2 an owning warp of a
+                               cluster split (accumulator full -> first
+                               partial chunk in -> last chunk in -> last
+                               store issued), sub 3 last store issued ->
+                               its shared-memory reads done                */
     int16_t sm;           /* %smid                                            */
     int32_t cta;          /* blockIdx.x                                       */
     int32_t sub;          /* roles 1-2: k-blocks of the unit; role 3: lane

@@ -373,6 +373,41 @@ def test_back_to_back_launches_read_the_previous_output(n, pdl):
         assert np.array_equal(D.cpu().double().numpy(), refs[i % 2]), f"step {i}"
 
 
+def test_back_to_back_chain_through_the_cluster_split():
+    """Each step: C1 = A_i . B1 through split-K summed in cluster shared
+    memory (its owners' TMA stores are the last writes of that launch), then
+    D = C1 . B2 reads C1 as its A (TF32).  The next step overwrites C1 while
+    that reader may still be finishing.  Entries in {-1, 0, 1} keep every
+    value exact (|C1| <= 512, |D| < 2^24)."""
+    M, N1, K1, N2 = 128, 2048, 512, 256
+    As = [make_operands(M, N1, K1, "bf16", "ints", seed=160 + i, lo_hi=1)[0] for i in range(2)]
+    B1 = make_operands(M, N1, K1, "bf16", "ints", seed=162, lo_hi=1)[1]
+    B2 = make_operands(N1, N2, N1, "tf32", "ints", seed=163, lo_hi=1)[1]
+    a_dev = [a.cuda() for a in As]
+    b1, b2 = B1.cuda(), B2.cuda()
+    c1 = torch.empty((M, N1), dtype=torch.float32, device="cuda")
+    Ds = [torch.empty((M, N2), dtype=torch.float32, device="cuda") for _ in range(8)]
+    s = torch.cuda.current_stream().cuda_stream
+    try:
+        tg.gemm_set_option("tc_splits", 2)
+        assert tg.gemm_plan(M, N1, K1, tg.GEMM_BF16, 0, K1, 0, N1, 0, N1).cluster_split == 2
+        for i, D in enumerate(Ds):
+            a = a_dev[i % 2]
+            rc = tg.gemm_run(M, N1, K1, tg.GEMM_BF16, a.data_ptr(), K1, b1.data_ptr(), N1, c1.data_ptr(), N1, s)
+            assert rc == tg.GEMM_OK, tg.gemm_last_error()
+            rc = tg.gemm_run(M, N2, N1, tg.GEMM_TF32, c1.data_ptr(), N1, b2.data_ptr(), N2, D.data_ptr(), N2, s)
+            assert rc == tg.GEMM_OK, tg.gemm_last_error()
+        assert tg.gemm_get_status(s) == tg.GEMM_OK, tg.gemm_last_error()
+    finally:
+        tg.gemm_set_option("tc_splits", 0)
+    refs = []
+    for a in As:
+        c_ref, _ = oracle_full(a, B1, "bf16")
+        refs.append(oracle_full(torch.from_numpy(c_ref.astype(np.float32)), B2, "tf32")[0])
+    for i, D in enumerate(Ds):
+        assert np.array_equal(D.cpu().numpy().astype(np.float64), refs[i % 2]), i
+
+
 @pytest.mark.parametrize("case", ("packed", "fp32"))
 def test_back_to_back_chain_through_packs_and_simt(case):
     """The same chain where every kernel of the library takes part: with

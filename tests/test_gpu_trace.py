@@ -52,7 +52,11 @@ def test_trace_records_every_unit_and_role(lib):
     assert plan["tail_tiles"] == 0 and plan["half_tiles"] == 0 and plan["cta_group"] == 1, plan
     out, go = _run(A, B, "bf16")
     recs, count = tt.capture(go)
-    assert count == len(recs) == 2 * units + 4 * units + plan["grid"]
+    assert count == len(recs)
+    per_role = np.bincount(recs["role"], minlength=7)
+    assert per_role[1] == per_role[2] == units and per_role[3] == 4 * units
+    assert per_role[4] == plan["grid"] and per_role[5] == 2 * plan["grid"]
+    assert per_role[6] == 4 * plan["grid"]           # each epilogue warp's last store -> its reads done
     for role, per_unit in ((1, 1), (2, 1), (3, 4)):
         sel = recs[recs["role"] == role]
         assert sorted(np.bincount(sel["unit"], minlength=units).tolist()) == [per_unit] * units, role
@@ -64,6 +68,7 @@ def test_trace_records_every_unit_and_role(lib):
         u = int(r["unit"])
         assert by[(1, u)]["t_begin_ns"] <= by[(2, u)]["t_end_ns"] <= r["t_end_ns"]
     # every unit span lies inside its CTA's life
+    assert np.sum(recs["role"] == 5) == 2 * plan["grid"]
     life = {int(r["cta"]): r for r in recs[recs["role"] == 4]}
     assert len(life) == plan["grid"]
     for r in recs[recs["role"] != 4]:
@@ -90,6 +95,9 @@ def test_trace_shows_cluster_split_senders(lib):
     epi = recs[recs["role"] == 3]
     # each CTA sends two lane quarters to its peer and stores the other two
     assert np.sum(epi["sub"] >= 4) == np.sum(epi["sub"] < 4) == 2 * plan["grid"]
+    # an owning warp's detail: to the first partial chunk, to the last, to its last store
+    detail = recs[(recs["role"] == 6) & (recs["sub"] < 3)]
+    assert len(detail) == 3 * 2 * plan["grid"] and np.all(detail["t_end_ns"] >= detail["t_begin_ns"])
 
 
 @pytest.mark.gpu

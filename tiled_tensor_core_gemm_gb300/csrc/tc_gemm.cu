@@ -59,7 +59,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;         // 32 rows x 32 fp32, 128-byte swizzled
 constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
 constexpr int kSmemBudget = 232448;            // 227 KB opt-in dynamic shared memory
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 1024;
 constexpr int kUQ = 4;                         // unit-queue slots (dynamic schedule)
 
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
@@ -127,10 +127,12 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for a ring");
     static_assert(2 * BN <= 512, "two accumulators must fit in Tensor Memory");
     static_assert(SMEM_BYTES <= kSmemBudget, "shared memory budget exceeded");
-    static_assert((2 * STAGES + 37) * 8 <= kBarBytes, "barrier area too small");
+    static_assert((2 * STAGES + 65) * 8 <= kBarBytes, "barrier area too small");
     // Split K reduced across a cluster: the partials a CTA receives (one per
-    // other K range, for its lane quarters) fit in its idle ring.
-    static_assert(kBM * BN * 4 <= STAGES * STAGE_BYTES, "ring too small for the cluster split-K partials");
+    // other K range, for its lane quarters) and the ones it stages to send
+    // (its other lane quarters) fit in its idle ring: at most 6 quarter-tiles.
+    static_assert(6 * 32 * BN * 4 <= STAGES * STAGE_BYTES, "ring too small for the cluster split-K partials");
+    // (with 2 ranges: 2 received + 2 staged to send + 2 of the owner's own = 6 as well)
 };
 
 struct TcParams {
@@ -339,9 +341,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t clc_full = bar0 + 8u * (uint32_t)(kW + 21);
     const uint32_t clc_used = bar0 + 8u * (uint32_t)(kW + 22);   // leader: both CTAs read the response
     // cluster split-K, per TMEM lane quarter: ready (the owning CTA's ring is
-    // free to receive) and in (every other K range's partial has arrived)
+    // free to receive) and, per 32-column chunk, in (every other K range's
+    // partial of that chunk has arrived)
     auto csr_ready = [&](uint32_t q) { return bar0 + 8u * (uint32_t)(kW + 29) + 8u * q; };
-    auto csr_in = [&](uint32_t q) { return bar0 + 8u * (uint32_t)(kW + 33) + 8u * q; };
+    auto csr_in = [&](uint32_t q, uint32_t c) { return bar0 + 8u * (uint32_t)(kW + 33) + 8u * (q * 8u + c); };
     const bool dyn = p.sched != 0;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -372,8 +375,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::mbar_init(clc_full, 1);
         ptx::mbar_init(clc_used, CG);
         for (uint32_t i = 0; i < 4; ++i) {
-            ptx::mbar_init(csr_ready(i), 1);                                  // the owner's one arrival
-            ptx::mbar_init(csr_in(i), 32u * (csplit > 1 ? csplit - 1 : 1));  // every lane of each sender warp
+            ptx::mbar_init(csr_ready(i), 1);               // the owner's one arrival
+            for (uint32_t c = 0; c < 8; ++c) ptx::mbar_init(csr_in(i, c), 1);   // the owner's, plus the bytes
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -398,8 +401,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // any global-memory access, for that kernel to finish and its writes to be
     // visible; then let the next launch start its own set-up (when no split-K
     // reduction, which reads this grid's slabs, comes next).
+    const uint64_t t_synced = tracing ? ptx::globaltimer_ns() : 0;
     ptx::pdl_wait();
     if ((p.tail_tiles == 0 || csplit) && threadIdx.x == 0) ptx::pdl_launch_dependents();
+    if (tracing && threadIdx.x == 0) {
+        // set-up: barriers, Tensor Memory and the CTA (or cluster) barrier; then the wait for the previous grid
+        trace_put(p, 5, -1, 0, t_start, t_synced);
+        trace_put(p, 5, -1, 1, t_synced, ptx::globaltimer_ns());
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -644,6 +653,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc_phase = 0;
         uint32_t nchunk = 0;                 // boxes staged so far (buffer nchunk & 1)
         uint32_t old_phase = 0;              // parity of each buffer's old-C barrier
+        uint64_t t_last_issue = 0;           // (traced) when this warp issued its last TMA store
         bool ok = true;
         int last_group = -1;
         // The unit sequence: the static stride, or the producer's unit queue
@@ -700,14 +710,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             ptx::tc_fence_after();
             const uint64_t t_unit = tracing ? ptx::globaltimer_ns() : 0;
+            uint64_t t_first_in = 0, t_last_in = 0;     // cluster split-K owner: partials' arrival (traced)
             const uint32_t trow = tmem_base + ((32u * q) << 16) + (uint32_t)(acc * BN);
             // Split K reduced across the cluster ("Learn CuTeDSL" section 9:
             // distributed shared memory of a thread-block cluster).  Lane
-            // quarter q of the tile belongs to CTA q / (4 / csplit): the other
-            // CTAs store their partial of it, 32 rows x BN FP32, into the
-            // owner's ring (idle now: each CTA has run its only unit), and
-            // the owner adds them to its own in K-range order before the
-            // epilogue.
+            // quarter q of the tile belongs to CTA q / (4 / csplit).  Each
+            // other CTA stages its partial of it, 32 rows x BN FP32, in its
+            // own ring (idle now: each CTA has run its only unit) and moves
+            // it to the owner's ring with one bulk copy per 32-column chunk,
+            // whose bytes complete the owner's barrier of that chunk.  The
+            // owner adds each chunk to its own, in K-range order, as soon as
+            // it has arrived.  Ring layout: the received quarter-tiles first,
+            // (csplit - 1) * 4 / csplit of them, then the ones staged to send.
             bool csr_owner = false;                    // this warp sums its quarter's K ranges
             uint32_t csr_base = 0;                     // where the other ranges' partials of it land
             if (csplit) {
@@ -721,18 +735,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     const uint32_t j = crank < owner ? crank : crank - 1;
                     const uint32_t dst = ptx::mapa_shared(ptx::smem_addr(stages) + (j * per + qloc) * part_bytes, owner);
+                    // staged after the received quarter-tiles, one region per quarter this CTA sends
+                    const uint32_t sent = q < crank * per ? q : q - per;
+                    uint8_t *local = stages + ((csplit - 1) * per + sent) * part_bytes;
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(32 * c), r);
                         ptx::tmem_wait_ld(r);
-                        const uint32_t row = dst + (uint32_t)c * 4096u + lane * 128u;
+                        uint8_t *row = local + c * 4096 + lane * 128u;
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            ptx::st_cluster_v4(row + (((uint32_t)k ^ (lane & 7u)) * 16u), r[4 * k], r[4 * k + 1],
-                                               r[4 * k + 2], r[4 * k + 3]);
+                            *reinterpret_cast<uint4 *>(row + (((uint32_t)k ^ (lane & 7u)) * 16u)) =
+                                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::bulk_copy_to_peer(dst + (uint32_t)c * 4096u, ptx::smem_addr(local + c * 4096), 4096u,
+                                                   ptx::mapa_shared(csr_in(q, (uint32_t)c), owner));
                     }
-                    ptx::mbar_arrive_cluster(ptx::mapa_shared(csr_in(q), owner));   // release: this lane's stores
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
@@ -745,14 +766,89 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     continue;
                 }
-                if (lane < csplit && lane != crank) ptx::mbar_arrive_cluster(ptx::mapa_shared(csr_ready(q), lane));
-                const bool got = wait_bar<true>(csr_in(q), 0u, abort_flag, p.timeout_ns);
-                if (!__all_sync(0xffffffffu, got)) {
-                    if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
-                    break;
+                if (lane == 0) {
+                    // the bytes each chunk will receive, then the go-ahead to the senders
+                    for (uint32_t c = 0; c < (uint32_t)(BN / 32); ++c)
+                        ptx::mbar_arrive_expect_tx(csr_in(q, c), 4096u * (csplit - 1));
+                    for (uint32_t s = 0; s < csplit; ++s)
+                        if (s != crank) ptx::mbar_arrive_cluster(ptx::mapa_shared(csr_ready(q), s));
                 }
                 csr_base = ptx::smem_addr(stages) + qloc * part_bytes;
                 csr_owner = true;
+            }
+            // A plain FP32 C stored by TMA: the owner writes each summed chunk
+            // back into the first received slot (already in the 128-byte
+            // swizzled box layout) and stores it from there, no staging buffer.
+            const bool csr_direct = csr_owner && !fused && U.tma_store && box_cols == 32;
+            if (csr_direct && csplit == 2) {
+                // Two ranges: copy this warp's own accumulator into the ring
+                // right away (after the received and the sent quarter-tiles),
+                // so that while the peer's chunks arrive the sums need only
+                // shared memory; Tensor Memory is handed back at once.
+                const uint32_t per = 2u, part_bytes = 32u * (uint32_t)BN * 4u;
+                uint8_t *own = stages + (2u * per + (q % per)) * part_bytes;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(32 * c), r);
+                    ptx::tmem_wait_ld(r);
+                    uint8_t *row = own + c * 4096 + lane * 128u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4 *>(row + (((uint32_t)k ^ (lane & 7u)) * 16u)) =
+                            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                uint8_t *slot = stages + (size_t)(csr_base - ptx::smem_addr(stages));   // the peer's partial
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const bool got = wait_bar<true>(csr_in(q, (uint32_t)c), 0u, abort_flag, p.timeout_ns);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    if (tracing) {
+                        t_last_in = ptx::globaltimer_ns();
+                        if (c == 0) t_first_in = t_last_in;
+                    }
+                    uint8_t *srow = slot + c * 4096 + lane * 128u;
+                    const uint8_t *orow = own + c * 4096 + lane * 128u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = ((uint32_t)k ^ (lane & 7u)) * 16u;
+                        const float4 a = *reinterpret_cast<const float4 *>(orow + off);
+                        const float4 b = *reinterpret_cast<const float4 *>(srow + off);
+                        // K-range order: range 0 + range 1, whichever CTA holds which
+                        *reinterpret_cast<float4 *>(srow + off) =
+                            crank == 0 ? make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w)
+                                       : make_float4(b.x + a.x, b.y + a.y, b.z + a.z, b.w + a.w);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    const int col0 = n0 + 32 * c;
+                    if (lane == 0 && m0 < U.M && col0 < U.N) {
+                        ptx::tma_store_2d(U.mC, csr_base + (uint32_t)c * 4096u, col0, m0);
+                        ptx::bulk_commit_group();
+                        if (tracing) t_last_issue = ptx::globaltimer_ns();
+                    }
+                }
+                if (tracing && lane == 0) {
+                    const uint64_t t_end = ptx::globaltimer_ns();
+                    trace_put(p, 3, t, (int)q, t_unit, t_end);
+                    trace_put(p, 6, t, 0, t_unit, t_first_in);
+                    trace_put(p, 6, t, 1, t_first_in, t_last_in);
+                    trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                }
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+                if (ok && !next_unit(t, t)) {
+                    if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                    break;
+                }
+                continue;
             }
 #pragma unroll 1
             for (int jb = 0; jb < ucols / box_cols; ++jb, ++nchunk) {
@@ -760,7 +856,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int col0 = n0 + box_cols * jb;
                 const bool box_live = m0 < U.M && col0 < U.N;
                 // The TMA store that last read this buffer (two boxes ago) must be done.
-                if (nchunk >= 2) {
+                if (nchunk >= 2 && !csr_direct) {
                     if (lane == 0) ptx::bulk_wait_group_read<1>();
                     __syncwarp();
                 }
@@ -790,7 +886,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (csr_owner) {
                         // this quarter's K ranges summed in range order, this CTA's own at crank
                         const uint32_t per = 4u / csplit, part_bytes = 32u * (uint32_t)BN * 4u;
-                        const uint32_t row = csr_base + (uint32_t)((box_cols * jb + 32 * h) / 32) * 4096u + lane * 128u;
+                        const uint32_t chunk = (uint32_t)((box_cols * jb + 32 * h) / 32);
+                        const bool got = wait_bar<true>(csr_in(q, chunk), 0u, abort_flag, p.timeout_ns);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        if (tracing) {
+                            t_last_in = ptx::globaltimer_ns();
+                            if (chunk == 0) t_first_in = t_last_in;
+                        }
+                        const uint32_t row = csr_base + chunk * 4096u + lane * 128u;
                         float sum[32];
 #pragma unroll 1
                         for (uint32_t s = 0; s < csplit; ++s) {
@@ -813,6 +920,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
 #pragma unroll
                         for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(sum[c]);
+                        if (csr_direct) {
+                            // the sum, in place of the first received partial
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                *reinterpret_cast<uint4 *>(stages + (row - ptx::smem_addr(stages)) +
+                                                           (((uint32_t)k ^ (lane & 7u)) * 16u)) =
+                                    make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                        }
                     }
                     if (jb == ucols / box_cols - 1 && h == box_cols / 32 - 1) {
                         // The accumulator is fully in registers/shared: hand it back to the MMA.
@@ -876,7 +991,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 *reinterpret_cast<float4 *>(row_base + (((uint32_t)c ^ (lane & 7u)) * 16u)) =
                                     make_float4(y[4 * c + 0], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
                         }
-                    } else {
+                    } else if (!csr_direct) {
                         // Row `lane`, 16-byte chunk c stored at position c ^ (row % 8): the
                         // 128-byte swizzle the TMA store expects, and conflict-free here.
 #pragma unroll
@@ -886,13 +1001,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                             __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
                     }
                 }
+                if (!ok) break;   // a cluster peer's partial never arrived (recorded above)
                 if (use_tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (to_slab) ptx::tma_store_3d(&tmW, ptx::smem_addr(buf), 32 * jb, srow, slab);
-                        else if (box_live) ptx::tma_store_2d(U.mC, ptx::smem_addr(buf), col0, m0);
+                        const uint32_t src =
+                            csr_direct ? csr_base + (uint32_t)jb * 4096u : ptx::smem_addr(buf);   // box = chunk jb
+                        if (to_slab) ptx::tma_store_3d(&tmW, src, 32 * jb, srow, slab);
+                        else if (box_live) ptx::tma_store_2d(U.mC, src, col0, m0);
                         ptx::bulk_commit_group();
+                        if (tracing) t_last_issue = ptx::globaltimer_ns();
                     }
                 } else {
                     // C not addressable by TMA: lane = column, each row of the box
@@ -948,7 +1067,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                 }
             }
-            if (tracing && lane == 0) trace_put(p, 3, t, (int)q, t_unit, ptx::globaltimer_ns());
+            if (tracing && lane == 0) {
+                const uint64_t t_end = ptx::globaltimer_ns();
+                trace_put(p, 3, t, (int)q, t_unit, t_end);
+                if (t_first_in) {
+                    // owner of a cluster split: to the first partial chunk, to the last, to the last store
+                    trace_put(p, 6, t, 0, t_unit, t_first_in);
+                    trace_put(p, 6, t, 1, t_first_in, t_last_in);
+                    trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                }
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
             if (ok && !next_unit(t, t)) {
@@ -956,7 +1084,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 break;
             }
         }
-        if (lane == 0) ptx::bulk_wait_group<0>();
+        // Before the CTA's shared memory goes away, its TMA stores must have
+        // read it; their global writes complete on their own and are
+        // visible once the grid has completed (which the next kernel on
+        // the stream waits for in griddepcontrol.wait).
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        if (tracing && lane == 0 && t_last_issue) trace_put(p, 6, -1, 3, t_last_issue, ptx::globaltimer_ns());
         __syncwarp();
     }
 

@@ -16,7 +16,7 @@ import numpy as np
 
 RECORD = np.dtype([("t_begin_ns", "<u8"), ("t_end_ns", "<u8"), ("unit", "<i4"), ("role", "<i2"), ("sm", "<i2"),
                    ("cta", "<i4"), ("sub", "<i4")])
-ROLES = {1: "TMA loads", 2: "MMA", 3: "epilogue", 4: "CTA"}
+ROLES = {1: "TMA loads", 2: "MMA", 3: "epilogue", 4: "CTA", 5: "set-up", 6: "epilogue detail"}
 HEADER_BYTES = 32
 
 
@@ -58,7 +58,7 @@ def chrome_trace(records) -> dict:
     for r in records:
         role = int(r["role"])
         name = ROLES.get(role, f"role {role}")
-        tid = role * 10 + (int(r["sub"]) if role == 3 else 0)
+        tid = role * 10 + (int(r["sub"]) if role in (3, 5, 6) else 0)
         if role == 3 and int(r["sub"]) >= 4:
             name = "epilogue (to peer)"
         events.append({"name": name if role == 4 else f"{name} u{int(r['unit'])}", "ph": "X", "pid": int(r["sm"]),
@@ -77,6 +77,9 @@ def summary(records) -> dict:
     if len(cta):
         out["launch_us"] = (int(cta["t_end_ns"].max()) - int(cta["t_begin_ns"].min())) / 1e3
         out["cta_life_us_mean"] = float(np.mean(cta["t_end_ns"].astype(np.int64) - cta["t_begin_ns"].astype(np.int64))) / 1e3
+    setup = records[(records["role"] == 5) & (records["sub"] == 0)]
+    if len(setup):
+        out["setup_us_mean"] = float(np.mean(setup["t_end_ns"].astype(np.int64) - setup["t_begin_ns"].astype(np.int64))) / 1e3
     for role, name in ((1, "loads"), (2, "mma"), (3, "epilogue")):
         sel = records[records["role"] == role]
         if len(sel):
