@@ -25,7 +25,7 @@ DTYPES = ("fp32", "tf32", "bf16", "fp16", "e4m3", "e5m2")
 OUTS = ("f32", "bf16", "f16")
 ACTS = ("none", "relu", "gelu")
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves")
+               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -121,6 +121,40 @@ def test_epilogue_after_split_k_reduction(dtype, splits, tail):
     plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N)
     assert plan.tail_tiles > 0 and plan.splits > 1
     _check(A, B, dtype, "f16", -0.5, 1.0, "relu", seed=39)
+
+
+@pytest.mark.parametrize("splits", (2, 4))
+@pytest.mark.parametrize("store", ("tma", "plain"))
+@pytest.mark.parametrize("out", ("f32", "bf16"))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "fp16", "e4m3"))
+def test_epilogue_after_split_k_in_cluster_shared_memory(dtype, out, store, splits):
+    """The K ranges summed across a cluster, then the whole epilogue (alpha,
+    the old C, bias, GELU, the output cast) by the owning CTA's warps, with
+    TMA stores and with ordinary stores."""
+    for k, v in (("tc_cta_group", 1), ("tc_bn", 128), ("tc_splits", splits), ("tc_split_reduce", 2),
+                 ("tc_tma_store", 2 if store == "plain" else 0)):
+        tg.gemm_set_option(k, v)
+    M, N, K = 300, 520, 2048
+    plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N)
+    assert plan.cluster_split == splits and plan.splits == splits
+    A, B = make_operands(M, N, K, dtype, "normal", seed=40)
+    _check(A, B, dtype, out, -0.5, 1.0, "gelu", seed=41)
+
+
+@pytest.mark.parametrize("splits", (2, 4))
+@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
+def test_small_integers_bit_exact_through_cluster_split_epilogue(dtype, splits):
+    M, N, K = 200, 300, 256
+    A, B = make_operands(M, N, K, dtype, "ints", seed=42, lo_hi=1)      # |A.B| <= 256
+    gen = torch.Generator().manual_seed(43)
+    c_old = torch.randint(-8, 9, (M, N), generator=gen).to(torch.float32)
+    bias = torch.randint(-8, 9, (N,), generator=gen).to(torch.float32)
+    for k, v in (("tc_cta_group", 1), ("tc_bn", 64), ("tc_splits", splits), ("tc_split_reduce", 2)):
+        tg.gemm_set_option(k, v)
+    assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).cluster_split == splits
+    C = run_gemm_ex(A, B, dtype, "f32", 1.0, -1.0, c_old, bias, "relu")
+    acc, _ = oracle_full(A, B, dtype)
+    assert np.array_equal(C, np.maximum(acc - c_old.double().numpy() + bias.double().numpy()[None, :], 0.0))
 
 
 @pytest.mark.parametrize("store", ("tma", "plain"))
