@@ -827,6 +827,7 @@ def plan_tag(plan):
     if plan["tail_tiles"]:
         t += f"/k{plan['splits']}" + ("" if plan["tail_tiles"] == plan["tiles"] else "tail")
         t += "dsm" if plan.get("cluster_split") else ""
+        t += f"{plan['kb_split']}" if plan.get("kb_split") else ""
     if plan["half_tiles"]:
         t += "/halves"
     if plan["b_kmajor"]:

@@ -252,6 +252,14 @@ GEMM_API int gemm_get_status(struct CUstream_st *stream);
  *                    kernel), 1 always the workspace and second kernel,
  *                    2 in cluster shared memory where legal (every tile
  *                    split into 2 or 4 ranges, one CTA per range)
+ *   "tc_split_lead"  with every tile split into 2 K ranges summed in
+ *                    cluster shared memory (or the same shape forced
+ *                    through the workspace), 128 columns or fewer and C
+ *                    stored by TMA: the percent of k-blocks in the first
+ *                    range (the plan's kb_split).  0 auto and 50: an even
+ *                    split with the lane quarters shared out (measured
+ *                    faster); 51..95 that share, the first range's CTA
+ *                    owning the whole tile
  *   "tc_tail_halves" run the last round's tiles as column halves when the
  *                    halves fit in one round and the tile allows it (BN >=
  *                    128; B read as stored in whole 128-byte chunks per
@@ -319,6 +327,12 @@ typedef struct {
                             split tile, run by the CTAs of one cluster and
                             summed in cluster shared memory: no workspace
                             and no second kernel                            */
+    int32_t kb_split;    /* 0: K ranges of equal length; else, with 2 ranges,
+                            the k-blocks (bk deep) of the first.  Summed in
+                            cluster shared memory, the first range's CTA
+                            then owns the whole tile and the other sends
+                            its partial to it (plain FP32 C stored by TMA;
+                            with a fused epilogue each CTA owns half)     */
 } gemm_plan_t;
 
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype,

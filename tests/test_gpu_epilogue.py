@@ -25,7 +25,7 @@ DTYPES = ("fp32", "tf32", "bf16", "fp16", "e4m3", "e5m2")
 OUTS = ("f32", "bf16", "f16")
 ACTS = ("none", "relu", "gelu")
 OPTION_KEYS = ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce")
+               "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce", "tc_split_lead")
 
 
 @pytest.fixture(scope="module", autouse=True)

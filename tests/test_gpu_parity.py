@@ -34,7 +34,7 @@ def lib():
     tgbuild.build()
     tg.load_library()
     for k in ("tc_bn", "tc_cta_group", "tc_group_m", "tc_max_ctas", "tc_tma_store", "simt_variant", "tc_b_major",
-              "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce"):
+              "debug_stall_mma", "tc_splits", "tc_tail_splits", "tc_tail_halves", "tc_split_reduce", "tc_split_lead"):
         tg.gemm_set_option(k, 0)
     yield
 
@@ -211,14 +211,43 @@ def test_split_k_summed_in_cluster_shared_memory_exact(dtype, bn, shape, splits)
             tg.gemm_set_option(k, 0)
 
 
-@pytest.mark.parametrize("dtype", ("bf16", "tf32"))
-def test_cluster_split_k_gives_the_reduce_kernels_bits(dtype):
+@pytest.mark.parametrize("dtype", ("bf16", "tf32", "e4m3"))
+@pytest.mark.parametrize("bn", (64, 128))
+@pytest.mark.parametrize("lead", (51, 75, 95))
+@pytest.mark.parametrize("shape", [(300, 700, 1100), (40, 1000, 777), (128, 2048, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cluster_split_one_owner_exact(dtype, bn, lead, shape):
+    """Two K ranges of uneven length on the CTAs of a cluster: CTA 0 runs the
+    first range, receives CTA 1's partial past its ring and stores the whole
+    tile.  Exact on small integers for first ranges from just over half to
+    95% of the k-blocks, with rows of a lane quarter past M and ragged
+    columns."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dtype, "ints", seed=35)
+    opts = {"tc_cta_group": 1, "tc_bn": bn, "tc_splits": 2, "tc_split_reduce": 2, "tc_split_lead": lead}
+    try:
+        for k, v in opts.items():
+            tg.gemm_set_option(k, v)
+        plan = tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).as_dict()
+        if plan["splits"] != 2 or plan["tiles"] * 2 > 152:
+            pytest.skip("K does not cut into 2 ranges here, or too many CTAs")
+        assert plan["cluster_split"] == 2 and plan["kb_split"] > 0, plan
+        _exact(A, B, dtype)
+    finally:
+        for k in opts:
+            tg.gemm_set_option(k, 0)
+
+
+@pytest.mark.parametrize("dtype,lead", [("bf16", 0), ("bf16", 56), ("bf16", 80), ("tf32", 0)])
+def test_cluster_split_k_gives_the_reduce_kernels_bits(dtype, lead):
     """On random data the cluster-summed split gives exactly the bits of the
-    workspace-and-reduce-kernel split: both add the K ranges' FP32 partials in
-    range order."""
+    workspace-and-reduce-kernel split: both cut K at the same k-block (even,
+    or the one-owner split) and add the K ranges' FP32 partials in range
+    order."""
     M, N, K = 128, 8192, 8192 if dtype == "bf16" else 4096
     A, B = make_operands(M, N, K, dtype, "normal", seed=34)
     try:
+        tg.gemm_set_option("tc_split_lead", lead)
         tg.gemm_set_option("tc_splits", 2)
         tg.gemm_set_option("tc_split_reduce", 1)
         assert tg.gemm_plan(M, N, K, tg.DTYPES[dtype], 0, K, 0, N, 0, N).cluster_split == 0
@@ -228,7 +257,7 @@ def test_cluster_split_k_gives_the_reduce_kernels_bits(dtype):
         C2 = run_gemm(A, B, dtype)
         assert np.array_equal(C1, C2)
     finally:
-        for k in ("tc_splits", "tc_split_reduce"):
+        for k in ("tc_splits", "tc_split_reduce", "tc_split_lead"):
             tg.gemm_set_option(k, 0)
 
 

@@ -81,23 +81,38 @@ def test_trace_records_every_unit_and_role(lib):
 
 
 @pytest.mark.gpu
-def test_trace_shows_cluster_split_senders(lib):
+@pytest.mark.parametrize("lead", (0, 56), ids=("quarters_shared", "one_owner"))
+def test_trace_shows_cluster_split_senders(lib, lead):
     M, N, K = 128, 2048, 4096
     A, B = make_operands(M, N, K, "bf16", "ints", seed=42)
     try:
         tg.gemm_set_option("tc_splits", 2)
+        tg.gemm_set_option("tc_split_lead", lead)
         plan = tg.gemm_plan(M, N, K, tg.GEMM_BF16, 0, K, 0, N, 0, N).as_dict()
-        assert plan["cluster_split"] == 2
+        assert plan["cluster_split"] == 2 and (plan["kb_split"] > 0) == (lead > 50), plan
         out, go = _run(A, B, "bf16")
         recs, count = tt.capture(go)
     finally:
         tg.gemm_set_option("tc_splits", 0)
+        tg.gemm_set_option("tc_split_lead", 0)
     epi = recs[recs["role"] == 3]
-    # each CTA sends two lane quarters to its peer and stores the other two
-    assert np.sum(epi["sub"] >= 4) == np.sum(epi["sub"] < 4) == 2 * plan["grid"]
+    sends, stores = epi[epi["sub"] >= 4], epi[epi["sub"] < 4]
+    # four lane quarters per tile are sent and four stored, per cluster of two CTAs
+    assert len(sends) == len(stores) == 2 * plan["grid"]
+    if lead <= 50:
+        # each CTA sends two lane quarters to its peer and stores the other two
+        for half in (sends, stores):
+            assert np.all(np.bincount(half["cta"], minlength=plan["grid"]) == 2)
+    else:
+        # CTA 1 of each cluster sends all four, CTA 0 stores all four
+        assert np.all(sends["cta"] % 2 == 1) and np.all(stores["cta"] % 2 == 0)
     # an owning warp's detail: to the first partial chunk, to the last, to its last store
     detail = recs[(recs["role"] == 6) & (recs["sub"] < 3)]
     assert len(detail) == 3 * 2 * plan["grid"] and np.all(detail["t_end_ns"] >= detail["t_begin_ns"])
+    import oracle
+    from tiled_tensor_core_gemm_gb300.inputs import as_oracle_array
+    assert np.array_equal(out["C"].cpu().numpy().astype(np.float64),
+                          oracle.gemm(as_oracle_array(A), as_oracle_array(B), bf16=True))
 
 
 @pytest.mark.gpu

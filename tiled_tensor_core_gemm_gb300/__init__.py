@@ -58,7 +58,7 @@ class GemmPlan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "path", "bm", "bn", "bk", "stages", "cta_group", "group_m", "grid", "tiles",
         "pack_a", "pack_b", "tma_store", "vec", "smem_bytes", "b_kmajor", "splits", "tail_tiles", "sched",
-        "half_tiles", "cluster_split")]
+        "half_tiles", "cluster_split", "kb_split")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -308,6 +308,23 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
                     "split-K in cluster shared memory needs every tile split in 2 (or 4) on single-CTA tiles, "
                     "ranges x tiles <= %lld CTAs and the static schedule (tiles=%lld splits=%d cta_group=%d)",
                     (long long)units, (long long)tiles, splits, cg);
+    // On request, two K ranges of a tile on the CTAs of a cluster, 128
+    // columns or fewer, C stored by TMA: CTA 0 takes the longer first range
+    // and owns the whole tile, CTA 1 takes the shorter second range and sends
+    // its partial while CTA 0 still streams (the kernel keeps a receive
+    // region for it past a shorter ring).  The workspace path, when forced,
+    // cuts K at the same k-block, so both give the same partial sums.
+    // Measured on GB300 (128 x 8192 x 8192): 29.0 us with ranges of equal
+    // length and the lane quarters shared out, 30.4 / 32.0 / 36.1 us with
+    // 53 / 56 / 75% in the first range -- a CTA's stream rate is capped, so
+    // the owners alone do not keep HBM busy -- hence off by default.
+    if (cs_shape && splits == 2 && max_clusters_2cta > 0 && tiles <= max_clusters_2cta && bn <= 128 &&
+        p.tma_store && opt.tc_split_lead > 50) {
+        const int lead = opt.tc_split_lead;
+        const int64_t even = cdiv(num_kb, 2);
+        const int64_t kb = std::min<int64_t>(num_kb - 1, std::max<int64_t>(even, (num_kb * lead + 50) / 100));
+        if (kb >= even && kb < num_kb) p.kb_split = (int32_t)kb;
+    }
     const int64_t work_units = (tiles - tail - half) + tail * splits + 2 * half;
     units = std::min<int64_t>(units, work_units);
     // Static unless asked: measured on GB300 the dynamic schedule is within
@@ -359,6 +376,9 @@ int gemm_set_option(const char *key, int64_t v) {
     } else if (!std::strcmp(key, "tc_split_reduce")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_split_reduce must be 0, 1 or 2");
         g_opt.tc_split_reduce = (int)v;
+    } else if (!std::strcmp(key, "tc_split_lead")) {
+        if (v != 0 && (v < 50 || v > 95)) return fail(GEMM_ERR_INVALID_ARG, "tc_split_lead must be 0 or in [50, 95]");
+        g_opt.tc_split_lead = (int)v;
     } else if (!std::strcmp(key, "tc_tail_halves")) {
         if (v < 0 || v > 2) return fail(GEMM_ERR_INVALID_ARG, "tc_tail_halves must be 0, 1 or 2");
         g_opt.tc_tail_halves = (int)v;
@@ -406,6 +426,7 @@ int64_t gemm_get_option(const char *key) {
     if (!std::strcmp(key, "tc_tail_splits")) return o.tc_tail_splits;
     if (!std::strcmp(key, "tc_tail_halves")) return o.tc_tail_halves;
     if (!std::strcmp(key, "tc_split_reduce")) return o.tc_split_reduce;
+    if (!std::strcmp(key, "tc_split_lead")) return o.tc_split_lead;
     if (!std::strcmp(key, "simt_splits")) return o.simt_splits;
     if (!std::strcmp(key, "pdl")) return o.pdl;
     if (!std::strcmp(key, "tc_sched")) return o.tc_sched;

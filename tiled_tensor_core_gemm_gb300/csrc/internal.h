@@ -25,6 +25,7 @@ struct Options {
     int simt_variant = 0;      // 0 auto, else a compiled SIMT variant id (1..6)
     int tc_b_major = 0;        // 0 auto (as stored; FP8 narrow tiles transposed), 1 K-major copy, 2 as stored
     int tc_split_reduce = 0;   // 0 auto, 1 workspace + reduce kernel, 2 cluster shared memory
+    int tc_split_lead = 0;     // two K ranges: percent of k-blocks in the first (0 auto, 50 even)
     int wait_timeout_ms = 2000;
     int64_t trace_addr = 0;    // device address of a trace buffer (0: off)
     int trace_records = 0;     // its capacity in records

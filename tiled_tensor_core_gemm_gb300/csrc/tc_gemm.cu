@@ -156,6 +156,10 @@ struct TcParams {
     int sched;                         // 0: static stride over units; 1: Cluster Launch Control
     int csplit;                        // 0, or the K ranges of each tile reduced across a cluster of that
                                        // many CTAs (one tile per cluster; cta_group 1)
+    int csr_rx;                        // 0: each CTA of the cluster owns some lane quarters of the tile;
+                                       // else (2 ranges) CTA 0 owns the whole tile and receives CTA 1's
+                                       // partial at this byte offset of its shared memory, past the ring
+    int ring;                          // ring stages in use (0: all STAGES); fewer leave csr_rx free
     unsigned long long timeout_ns;
     uint32_t *trace_count;             // timeline trace: record counter (nullptr: off)
     gemm_trace_record_t *trace;        // and the records after it
@@ -355,6 +359,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t crank = csplit ? ptx::cluster_ctarank() : 0u;
     const int unit = csplit ? (int)(crank * (uint32_t)p.tail_tiles + blockIdx.x / csplit) : (int)blockIdx.x / CG;
     const int nunits = csplit ? p.num_units : (int)gridDim.x / CG;
+    const int ring = p.ring > 0 ? p.ring : Cf::STAGES;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cf::STAGES; ++s) {
@@ -380,6 +385,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        if (csplit == 2 && p.csr_rx && crank == 0)
+            // one owner: the bytes of every chunk of the peer's partial, expected from the start
+            for (uint32_t i = 0; i < 4; ++i)
+                for (uint32_t c = 0; c < (uint32_t)(BN / 32); ++c) ptx::mbar_arrive_expect_tx(csr_in(i, c), 4096u);
     }
     if (warp == 0 && lane == 0 && p.groups == nullptr) {
         ptx::prefetch_tensormap(&tmA);
@@ -471,7 +480,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                           n0 + c * Cf::CHUNK_COLS, k0);
                         }
                     }
-                    if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == ring) { stage = 0; phase ^= 1u; }
                 }
                 if (tracing) trace_put(p, 1, t, U.kb1 - U.kb0, t_unit, ptx::globaltimer_ns());
                 return true;
@@ -545,12 +554,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // Drain: wait until the MMAs have released every slot, so that no
             // tensor-core read of this CTA's shared memory and no commit
             // arrival on its barriers is still outstanding at teardown.
-            for (int i = 0; ok && i < Cf::STAGES; ++i) {
+            for (int i = 0; ok && i < ring; ++i) {
                 if (!wait_bar<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
                     record_failure(kRoleDrain, -1, abort_flag);
                     break;
                 }
-                if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == ring) { stage = 0; phase ^= 1u; }
             }
         }
         __syncwarp();
@@ -622,7 +631,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else ptx::mma_commit(empty_bar(stage));
-                    if (++stage == Cf::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == ring) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 if (kPair) ptx::mma_commit_pair(accf_bar(acc), 0x3);
@@ -722,6 +731,98 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // owner adds each chunk to its own, in K-range order, as soon as
             // it has arrived.  Ring layout: the received quarter-tiles first,
             // (csplit - 1) * 4 / csplit of them, then the ones staged to send.
+            if (csplit == 2 && p.csr_rx) {
+                // Two K ranges, one owner: CTA 0 of the cluster runs the longer
+                // first range and sums and stores the whole tile; CTA 1 runs the
+                // second and sends its partial the moment its MMAs end, while
+                // CTA 0 still streams.  The partial lands past CTA 0's ring
+                // (which runs `ring` stages deep for this), whose chunk barriers
+                // CTA 0 armed at set-up, so the sender needs no go-ahead.  The
+                // layout of a quarter's chunk: 32 rows of 128 bytes, 16-byte
+                // units swizzled by row (the TMA store's box layout).
+                const uint32_t part_bytes = 32u * (uint32_t)BN * 4u;
+                const uint32_t rx = ptx::smem_addr(stages) + (uint32_t)p.csr_rx + q * part_bytes;
+                if (crank != 0) {
+                    uint8_t *local = stages + q * part_bytes;          // this CTA's ring, idle now
+                    const uint32_t dst = ptx::mapa_shared(rx, 0);
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(32 * c), r);
+                        ptx::tmem_wait_ld(r);
+                        uint8_t *row = local + c * 4096 + lane * 128u;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4 *>(row + (((uint32_t)k ^ (lane & 7u)) * 16u)) =
+                                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::bulk_copy_to_peer(dst + (uint32_t)c * 4096u, ptx::smem_addr(local + c * 4096), 4096u,
+                                                   ptx::mapa_shared(csr_in(q, (uint32_t)c), 0));
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                    if (tracing && lane == 0) trace_put(p, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
+                } else {
+                    uint8_t *slot = stages + p.csr_rx + q * part_bytes;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(32 * c), r);
+                        ptx::tmem_wait_ld(r);
+                        if (c == BN / 32 - 1) {
+                            // the accumulator is in registers: hand Tensor Memory back
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                        }
+                        const bool got = wait_bar<true>(csr_in(q, (uint32_t)c), 0u, abort_flag, p.timeout_ns);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        if (tracing) {
+                            t_last_in = ptx::globaltimer_ns();
+                            if (c == 0) t_first_in = t_last_in;
+                        }
+                        uint8_t *srow = slot + c * 4096 + lane * 128u;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t off = ((uint32_t)k ^ (lane & 7u)) * 16u;
+                            const float4 b = *reinterpret_cast<const float4 *>(srow + off);
+                            // K-range order: this CTA's range 0, then the peer's range 1
+                            *reinterpret_cast<float4 *>(srow + off) =
+                                make_float4(__uint_as_float(r[4 * k]) + b.x, __uint_as_float(r[4 * k + 1]) + b.y,
+                                            __uint_as_float(r[4 * k + 2]) + b.z, __uint_as_float(r[4 * k + 3]) + b.w);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        const int col0 = n0 + 32 * c;
+                        if (lane == 0 && m0 < U.M && col0 < U.N) {
+                            ptx::tma_store_2d(U.mC, rx + (uint32_t)c * 4096u, col0, m0);
+                            ptx::bulk_commit_group();
+                            if (tracing) t_last_issue = ptx::globaltimer_ns();
+                        }
+                    }
+                    if (tracing && lane == 0) {
+                        trace_put(p, 3, t, (int)q, t_unit, ptx::globaltimer_ns());
+                        trace_put(p, 6, t, 0, t_unit, t_first_in);
+                        trace_put(p, 6, t, 1, t_first_in, t_last_in);
+                        trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                    }
+                }
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+                if (!ok) break;
+                if (!next_unit(t, t)) {
+                    if (lane == 0) record_failure(kRoleEpilogue, t, abort_flag);
+                    break;
+                }
+                continue;
+            }
             bool csr_owner = false;                    // this warp sums its quarter's K ranges
             uint32_t csr_base = 0;                     // where the other ranges' partials of it land
             if (csplit) {
@@ -1276,9 +1377,18 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
     p.full_tiles = p.num_tiles - p.tail_tiles - p.half_tiles;
     p.splits = p.tail_tiles > 0 ? plan.splits : 1;
     p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
+    if (p.splits == 2 && plan.kb_split > 0) {
+        // an uneven pair of K ranges: the first has kb_split k-blocks
+        if (plan.kb_split < p.kb_per_split || plan.kb_split >= p.num_kb) {
+            std::snprintf(err, errlen, "kb_split %d out of range for %d k-blocks", plan.kb_split, p.num_kb);
+            return GEMM_ERR_INVALID_ARG;
+        }
+        p.kb_per_split = plan.kb_split;
+    }
     p.num_units = p.full_tiles + p.tail_tiles * p.splits + 2 * p.half_tiles;
     p.C = C;
     p.ldc = ldc;
+    p.ring = Cf::STAGES;
     if (plan.cluster_split) {
         if (CG != 1 || plan.cluster_split != p.splits || p.full_tiles != 0 || plan.sched != 0 ||
             plan.grid != p.num_units) {
@@ -1286,6 +1396,17 @@ int launch_variant(const gemm_plan_t &plan, int M, int N, int K, const void *A, 
             return GEMM_ERR_INVALID_ARG;
         }
         p.csplit = plan.cluster_split;
+        // One owner per tile (an uneven split, plain FP32 C stored by TMA): its
+        // receive region, 4 lane quarters x 32 rows x BN FP32, ends where the
+        // epilogue staging area ends and takes as many ring stages as needed
+        // beyond that area.
+        const int rx_bytes = 4 * 32 * BN * 4;
+        const int over = rx_bytes > kEpiBytes ? rx_bytes - kEpiBytes : 0;
+        const int ring = Cf::STAGES - (over + Cf::STAGE_BYTES - 1) / Cf::STAGE_BYTES;
+        if (p.csplit == 2 && plan.kb_split > 0 && !epi.active && plan.tma_store && ring >= 3) {
+            p.ring = ring;
+            p.csr_rx = Cf::STAGES * Cf::STAGE_BYTES + kEpiBytes - rx_bytes;
+        }
     }
     return launch_kernel<DT, CG, BN, BMODE>(plan, ta, tb, tc, tw, p, stream, err, errlen);
 }
