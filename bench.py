@@ -738,7 +738,8 @@ def run_ours(args):
         recs, count = tt.capture(one_call)
         with open(args.trace, "w") as f:
             json.dump(tt.chrome_trace(recs), f)
-        out["trace"] = {"file": args.trace, "records": int(count), **{k: round(v, 2) for k, v in tt.summary(recs).items()}}
+        out["trace"] = {"file": args.trace, "records": int(len(recs)), "slots": int(count),
+                        **{k: round(v, 2) for k, v in tt.summary(recs).items()}}
         del At, Bt, Ct
     check = not args.no_cpu_baseline and world == 1
     if not args.no_paths and headline:

@@ -380,11 +380,14 @@ GEMM_API int gemm_run_tf32_static(int64_t M, int64_t N, int64_t K,
  * which the host turns into a timeline).  Off unless the option "trace_addr"
  * holds the device address of a caller-owned buffer of 32 + 32 *
  * "trace_records" bytes (8-byte aligned, device memory of the calling
- * device).  Its first 32 bytes are a header whose first uint32 the kernel
- * increments once per record it writes (records beyond "trace_records" are
- * dropped but still counted); zero the header before a traced call.  Records
- * follow the header, in no particular order.  The buffer is read only after
- * the stream is synchronised; concurrent traced calls share the buffer.
+ * device).  Its first 32 bytes are a header whose first uint32 counts the
+ * record slots the kernel has reserved: each recording thread reserves 16 at
+ * a time and fills them in turn, so a record costs no atomic of its own.
+ * Records follow the header, in no particular order; slots at or beyond
+ * "trace_records" are dropped but still counted, and reserved slots a
+ * thread did not fill keep the caller's zeros (role 0: skip them).  Zero the
+ * whole buffer before a traced call.  The buffer is read only after the
+ * stream is synchronised; concurrent traced calls share the buffer.
  */
 typedef struct {
     uint64_t t_begin_ns;  /* %globaltimer at the start of the span           */

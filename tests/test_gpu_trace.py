@@ -52,7 +52,7 @@ def test_trace_records_every_unit_and_role(lib):
     assert plan["tail_tiles"] == 0 and plan["half_tiles"] == 0 and plan["cta_group"] == 1, plan
     out, go = _run(A, B, "bf16")
     recs, count = tt.capture(go)
-    assert count == len(recs)
+    assert len(recs) <= count          # (slots are reserved 16 at a time per recording thread)
     per_role = np.bincount(recs["role"], minlength=7)
     assert per_role[1] == per_role[2] == units and per_role[3] == 4 * units
     assert per_role[4] == plan["grid"] and per_role[5] == 2 * plan["grid"]
@@ -120,7 +120,7 @@ def test_trace_overflow_and_bad_buffer(lib):
     A, B = make_operands(1024, 1024, 512, "bf16", "ints", seed=43)
     out, go = _run(A, B, "bf16")
     recs, count = tt.capture(go, capacity=10)
-    assert len(recs) == 10 and count > 10
+    assert 0 < len(recs) <= 10 and count > 10
     host = torch.zeros(64, dtype=torch.uint8).pin_memory()
     assert tg.gemm_set_option("trace_addr", host.data_ptr()) == tg.GEMM_OK
     try:

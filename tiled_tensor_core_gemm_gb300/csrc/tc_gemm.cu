@@ -267,9 +267,20 @@ __device__ __forceinline__ Unit unit_info(int u, const TcParams &p, const CUtens
 }
 
 // One timeline record (when tracing is on): a span of `role` on `unit`.
-__device__ __noinline__ void trace_put(const TcParams &p, int role, int unit, int sub, uint64_t t0, uint64_t t1) {
-    const uint32_t i = atomicAdd(p.trace_count, 1u);
-    if (i >= (uint32_t)p.trace_cap) return;
+// A recording thread reserves record slots kTraceBlock at a time with one
+// atomic on the buffer's counter (slot.x = its next slot, slot.y = the end of
+// its block; returned updated) and fills them with plain stores, so that a
+// record costs no round trip to L2; slots it reserves but does not fill stay
+// as the caller zeroed them (role 0).
+constexpr uint32_t kTraceBlock = 16;
+__device__ __noinline__ uint2 trace_put(const TcParams &p, uint2 slot, int role, int unit, int sub, uint64_t t0,
+                                        uint64_t t1) {
+    if (slot.x == slot.y) {
+        slot.x = atomicAdd(p.trace_count, kTraceBlock);
+        slot.y = slot.x + kTraceBlock;
+    }
+    const uint32_t i = slot.x++;
+    if (i >= (uint32_t)p.trace_cap) return slot;
     gemm_trace_record_t r;
     r.t_begin_ns = t0;
     r.t_end_ns = t1;
@@ -279,6 +290,7 @@ __device__ __noinline__ void trace_put(const TcParams &p, int role, int unit, in
     r.cta = (int32_t)blockIdx.x;
     r.sub = sub;
     p.trace[i] = r;
+    return slot;
 }
 
 __device__ __noinline__ void record_failure(uint32_t role, int tile, volatile int *abort_flag) {
@@ -314,6 +326,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     constexpr bool BKM = Cf::BKM;
     const bool tracing = p.trace_count != nullptr;
     const uint64_t t_start = tracing ? ptx::globaltimer_ns() : 0;
+    uint2 tslot = make_uint2(0u, 0u);   // this thread's reserved trace slots (trace_put)
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment (in the shared window) for the swizzle atoms.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -415,8 +428,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if ((p.tail_tiles == 0 || csplit) && threadIdx.x == 0) ptx::pdl_launch_dependents();
     if (tracing && threadIdx.x == 0) {
         // set-up: barriers, Tensor Memory and the CTA (or cluster) barrier; then the wait for the previous grid
-        trace_put(p, 5, -1, 0, t_start, t_synced);
-        trace_put(p, 5, -1, 1, t_synced, ptx::globaltimer_ns());
+        tslot = trace_put(p, tslot, 5, -1, 0, t_start, t_synced);
+        tslot = trace_put(p, tslot, 5, -1, 1, t_synced, ptx::globaltimer_ns());
     }
 
     if (warp == 0) {
@@ -482,7 +495,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (++stage == ring) { stage = 0; phase ^= 1u; }
                 }
-                if (tracing) trace_put(p, 1, t, U.kb1 - U.kb0, t_unit, ptx::globaltimer_ns());
+                if (tracing) tslot = trace_put(p, tslot, 1, t, U.kb1 - U.kb0, t_unit, ptx::globaltimer_ns());
                 return true;
             };
             if (!dyn) {
@@ -636,7 +649,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!ok) break;
                 if (kPair) ptx::mma_commit_pair(accf_bar(acc), 0x3);
                 else ptx::mma_commit(accf_bar(acc));
-                if (tracing) trace_put(p, 2, t, kb1 - kb0, t_unit, ptx::globaltimer_ns());
+                if (tracing) tslot = trace_put(p, tslot, 2, t, kb1 - kb0, t_unit, ptx::globaltimer_ns());
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
                 if (!next_unit(t, t)) {
@@ -764,7 +777,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
-                    if (tracing && lane == 0) trace_put(p, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
+                    if (tracing && lane == 0) tslot = trace_put(p, tslot, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
                 } else {
                     uint8_t *slot = stages + p.csr_rx + q * part_bytes;
 #pragma unroll 1
@@ -808,10 +821,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                     }
                     if (tracing && lane == 0) {
-                        trace_put(p, 3, t, (int)q, t_unit, ptx::globaltimer_ns());
-                        trace_put(p, 6, t, 0, t_unit, t_first_in);
-                        trace_put(p, 6, t, 1, t_first_in, t_last_in);
-                        trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                        tslot = trace_put(p, tslot, 3, t, (int)q, t_unit, ptx::globaltimer_ns());
+                        tslot = trace_put(p, tslot, 6, t, 0, t_unit, t_first_in);
+                        tslot = trace_put(p, tslot, 6, t, 1, t_first_in, t_last_in);
+                        tslot = trace_put(p, tslot, 6, t, 2, t_last_in, t_last_issue);
                     }
                 }
                 acc ^= 1;
@@ -858,7 +871,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
-                    if (tracing && lane == 0) trace_put(p, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
+                    if (tracing && lane == 0) tslot = trace_put(p, tslot, 3, t, (int)q + 4, t_unit, ptx::globaltimer_ns());
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
                     if (ok && !next_unit(t, t)) {
@@ -938,10 +951,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 if (tracing && lane == 0) {
                     const uint64_t t_end = ptx::globaltimer_ns();
-                    trace_put(p, 3, t, (int)q, t_unit, t_end);
-                    trace_put(p, 6, t, 0, t_unit, t_first_in);
-                    trace_put(p, 6, t, 1, t_first_in, t_last_in);
-                    trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                    tslot = trace_put(p, tslot, 3, t, (int)q, t_unit, t_end);
+                    tslot = trace_put(p, tslot, 6, t, 0, t_unit, t_first_in);
+                    tslot = trace_put(p, tslot, 6, t, 1, t_first_in, t_last_in);
+                    tslot = trace_put(p, tslot, 6, t, 2, t_last_in, t_last_issue);
                 }
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
@@ -1170,12 +1183,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             if (tracing && lane == 0) {
                 const uint64_t t_end = ptx::globaltimer_ns();
-                trace_put(p, 3, t, (int)q, t_unit, t_end);
+                tslot = trace_put(p, tslot, 3, t, (int)q, t_unit, t_end);
                 if (t_first_in) {
                     // owner of a cluster split: to the first partial chunk, to the last, to the last store
-                    trace_put(p, 6, t, 0, t_unit, t_first_in);
-                    trace_put(p, 6, t, 1, t_first_in, t_last_in);
-                    trace_put(p, 6, t, 2, t_last_in, t_last_issue);
+                    tslot = trace_put(p, tslot, 6, t, 0, t_unit, t_first_in);
+                    tslot = trace_put(p, tslot, 6, t, 1, t_first_in, t_last_in);
+                    tslot = trace_put(p, tslot, 6, t, 2, t_last_in, t_last_issue);
                 }
             }
             acc ^= 1;
@@ -1190,7 +1203,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // visible once the grid has completed (which the next kernel on
         // the stream waits for in griddepcontrol.wait).
         if (lane == 0) ptx::bulk_wait_group_read<0>();
-        if (tracing && lane == 0 && t_last_issue) trace_put(p, 6, -1, 3, t_last_issue, ptx::globaltimer_ns());
+        if (tracing && lane == 0 && t_last_issue) tslot = trace_put(p, tslot, 6, -1, 3, t_last_issue, ptx::globaltimer_ns());
         __syncwarp();
     }
 
@@ -1203,7 +1216,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (kPair || csplit) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cf::TMEM_COLS);
-    if (tracing && threadIdx.x == 0) trace_put(p, 4, -1, 0, t_start, ptx::globaltimer_ns());
+    if (tracing && threadIdx.x == 0) tslot = trace_put(p, tslot, 4, -1, 0, t_start, ptx::globaltimer_ns());
 }
 
 // ------------------------------------------------------------------ host ---

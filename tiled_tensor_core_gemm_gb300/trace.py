@@ -22,9 +22,10 @@ HEADER_BYTES = 32
 
 def capture(fn, capacity: int = 1 << 16, device=None):
     """Run ``fn()`` (which enqueues library calls on the current stream) with
-    tracing on, synchronise, and return (records, count): the records as a
-    structured array (at most ``capacity``) and how many the kernels tried to
-    write."""
+    tracing on, synchronise, and return (records, count): the records written
+    as a structured array (at most ``capacity`` slots read; reserved slots a
+    kernel thread did not fill, role 0, are skipped) and how many record
+    slots the kernels reserved (at least the records written)."""
     import torch
 
     from . import GEMM_OK, GemmError, gemm_last_error, gemm_set_option
@@ -45,7 +46,7 @@ def capture(fn, capacity: int = 1 << 16, device=None):
     count = int(host[:4].view(np.uint32)[0])
     n = min(count, capacity)
     recs = host[HEADER_BYTES:HEADER_BYTES + n * RECORD.itemsize].view(RECORD).copy()
-    return recs, count
+    return recs[recs["role"] != 0], count
 
 
 def chrome_trace(records) -> dict:
