@@ -99,14 +99,21 @@ typedef enum {
  * not a multiple of 16 bytes) are first copied into a stream-ordered workspace
  * with a padded pitch; that workspace is allocated and freed on the stream
  * (cudaMallocAsync/cudaFreeAsync) and reported as GEMM_ERR_NO_MEMORY if
- * unavailable.  For GEMM_TF32 (and FP8 tiles narrower than 128 columns), B is
- * first transposed into the same kind of workspace, because the MMA then reads
- * its B operand K-major.  When there are too few output tiles to occupy every
- * SM and K is long, the tensor-core path splits K: partial tiles go to a
- * workspace and a second kernel sums them into C in a fixed order (results are
- * deterministic).  With 16-bit inputs, at most 256 rows and a B of 64 MiB or
- * more (B streaming from HBM), those tiles are 128 columns wide instead of
- * 256.  When the tiles of the last, partly idle round of the persistent
+ * unavailable.  For FP8 tiles narrower than 128 columns (and on request,
+ * option "tc_b_major"), B is first transposed into the same kind of
+ * workspace, because the MMA then reads its B operand K-major; otherwise B is
+ * read as stored.  When there are too few output tiles to occupy every SM
+ * and K is long, the tensor-core path splits K.  Two K ranges of a tile that
+ * fit one round of 2-CTA clusters run on the two CTAs of a cluster and are
+ * summed in distributed shared memory (no workspace, no second kernel); the
+ * planner takes 128-column tiles in two such ranges where they keep as many
+ * CTAs busy as 256-column tiles would (and, for TF32 and 8-bit inputs, in
+ * place of 64-column tiles).  Otherwise partial tiles go to a workspace and a
+ * second kernel sums them into C in a fixed order.  Either way the ranges are
+ * added in order (results are deterministic, and the same both ways).  With
+ * 16-bit inputs, at most 256 rows and a B of 64 MiB or more (B streaming
+ * from HBM), split tiles are 128 columns wide.  When the tiles of the last,
+ * partly idle round of the persistent
  * schedule would fill at most half of the machine, 16-bit inputs on short
  * schedules run them as two column halves each (every half over all of
  * K, straight to C: no workspace, and the same sums as a whole tile; the

@@ -212,16 +212,13 @@ def test_plan_low_tile_count_splits_k():
 @pytest.mark.parametrize("M,N,K,bn,splits", [
     # B streams from HBM past at most 256 rows of A: 128-column tiles, K split to fill the SMs
     (128, 8192, 8192, 128, 2), (64, 8192, 8192, 128, 2), (256, 8192, 8192, 128, 1), (128, 4096, 16384, 128, 4),
-    # B of 32 MB, or 512 and more rows: 256-column tiles (measured faster there)
-    (256, 4096, 4096, 256, 4), (512, 4096, 8192, 256, 2), (1024, 2048, 8192, 256, 2)])
+    # 512 and more rows: 256-column tiles (measured faster there)
+    (512, 4096, 8192, 256, 2), (1024, 2048, 8192, 256, 2)])
 def test_plan_streaming_b_takes_128_column_tiles(M, N, K, bn, splits):
     for dt in (tg.GEMM_BF16, tg.GEMM_FP16):
         p = _plan(M, N, K, dt)
         assert (p["cta_group"], p["bn"], p["splits"]) == (1, bn, splits), (M, N, K, p)
         assert p["grid"] == p["tiles"] * p["splits"]
-    # 8-bit and TF32 inputs keep the 256-column tiles
-    assert _plan(M, N, K, tg.GEMM_E4M3)["bn"] == 256
-    assert _plan(M, N, K, tg.GEMM_TF32)["bn"] == 256
     # a forced tile width is kept
     try:
         tg.gemm_set_option("tc_bn", 256)
@@ -230,45 +227,33 @@ def test_plan_streaming_b_takes_128_column_tiles(M, N, K, bn, splits):
         tg.gemm_set_option("tc_bn", 0)
 
 
-def test_plan_two_k_ranges_with_one_owner():
-    """Two K ranges summed in cluster shared memory: of equal length unless
-    asked; on request (128-column tiles, C stored by TMA) the first range
-    takes that share of the k-blocks and its CTA owns the tile, and the
-    forced workspace path cuts K at the same k-block."""
-    p = _plan(128, 8192, 8192, tg.GEMM_BF16)
-    assert (p["cluster_split"], p["splits"], p["bn"], p["kb_split"]) == (2, 2, 128, 0), p
+@pytest.mark.parametrize("M,N,K,dt,bn,splits,cluster", [
+    # too few 256-column tiles: two K ranges of 128-column tiles summed in cluster
+    # shared memory where they fit one round of clusters and keep as many CTAs busy
+    (256, 4096, 4096, "bf16", 128, 2, 2), (1024, 1024, 2048, "bf16", 128, 2, 2),
+    (512, 2048, 2048, "fp16", 128, 2, 2), (768, 1536, 3072, "bf16", 128, 2, 2),
+    (512, 2048, 2048, "tf32", 128, 2, 2), (512, 2048, 2048, "e4m3", 128, 2, 2),
+    # ... not where they would not fit one round, or keep fewer CTAs busy
+    (1024, 1536, 4096, "bf16", 256, 3, 0), (256, 2048, 8192, "bf16", 256, 9, 0),
+    (2048, 1024, 2048, "bf16", 256, 2, 2), (1536, 1536, 1536, "bf16", 256, 2, 2),
+    # little work: TF32 and 8-bit inputs take them instead of 64-column tiles, 16-bit inputs do not
+    (1024, 1024, 1024, "tf32", 128, 2, 2), (1024, 1024, 1024, "e4m3", 128, 2, 2),
+    (1024, 1024, 1024, "e5m2", 128, 2, 2), (1024, 1024, 1024, "bf16", 64, 1, 0),
+    (1000, 1000, 1000, "bf16", 64, 1, 0), (1024, 1024, 512, "tf32", 64, 1, 0)])
+def test_plan_two_k_ranges_in_cluster_shared_memory(M, N, K, dt, bn, splits, cluster):
+    p = _plan(M, N, K, tg.DTYPES[dt])
+    assert (p["cta_group"], p["bn"], p["splits"], p["cluster_split"]) == (1, bn, splits, cluster), (M, N, K, dt, p)
+    assert p["b_kmajor"] == 0
     try:
-        tg.gemm_set_option("tc_split_lead", 56)
-        assert _plan(128, 8192, 8192, tg.GEMM_BF16)["kb_split"] == 72
-        assert _plan(128, 8192, 8256, tg.GEMM_BF16)["kb_split"] == 72          # 129 k-blocks
-        assert _plan(128, 8192, 8192, tg.GEMM_BF16, ldc=8195)["kb_split"] == 0  # C by ordinary stores
-        assert _plan(128, 8192, 8192, tg.GEMM_TF32)["kb_split"] == 0           # 256-column tiles
-        assert _plan(128, 4096, 16384, tg.GEMM_BF16)["kb_split"] == 0          # 4 ranges
-        assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["kb_split"] == 0
-        for lead, kb in ((0, 0), (50, 0), (51, 65), (75, 96), (95, 122)):
-            assert tg.gemm_set_option("tc_split_lead", lead) == tg.GEMM_OK
-            assert _plan(128, 8192, 8192, tg.GEMM_BF16)["kb_split"] == kb, lead
-        tg.gemm_set_option("tc_split_lead", 56)
-        tg.gemm_set_option("tc_split_reduce", 1)
-        q = _plan(128, 8192, 8192, tg.GEMM_BF16)
-        assert q["cluster_split"] == 0 and q["kb_split"] == 72, q
-        for bad in (1, 49, 96, -1):
-            assert tg.gemm_set_option("tc_split_lead", bad) == tg.GEMM_ERR_INVALID_ARG
-    finally:
-        tg.gemm_set_option("tc_split_lead", 0)
+        tg.gemm_set_option("tc_split_reduce", 1)           # the workspace path: the old choice stands
+        q = _plan(M, N, K, tg.DTYPES[dt])
+        assert q["cluster_split"] == 0
         tg.gemm_set_option("tc_split_reduce", 0)
-
-
-def test_plan_struct_layout_matches_the_header(tmp_path):
-    src = tmp_path / "plan.c"
-    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\n'
-                   'int main(void) { printf("%zu %zu %zu\\n", sizeof(gemm_plan_t),'
-                   ' offsetof(gemm_plan_t, cluster_split), offsetof(gemm_plan_t, kb_split)); return 0; }\n')
-    exe = tmp_path / "plan"
-    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
-    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
-    P = tg.GemmPlan
-    assert got == [ctypes.sizeof(P), P.cluster_split.offset, P.kb_split.offset]
+        tg.gemm_set_option("tc_splits", 1)                  # no split at all
+        assert _plan(M, N, K, tg.DTYPES[dt])["splits"] == 1
+    finally:
+        tg.gemm_set_option("tc_split_reduce", 0)
+        tg.gemm_set_option("tc_splits", 0)
 
 
 def test_plan_runs_the_last_round_as_column_halves():

@@ -203,6 +203,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
     int splits = opt.tc_splits;
     auto tiles_of = [&](int g, int b) { return cdiv(M, 128 * g) * cdiv(N, b); };
     const int64_t num_kb = cdiv(K, 128 / elem);
+    // Two K ranges of 128-column tiles, summed in cluster shared memory, when
+    // they fit one round of 2-CTA clusters: no workspace, no second kernel.
+    const int64_t t128 = tiles_of(1, 128);
+    const bool two_dsm_fit = splits != 1 && opt.tc_split_reduce != 1 && max_clusters_2cta > 0 &&
+                             2 * t128 <= std::min<int64_t>(num_sms, 2LL * max_clusters_2cta) &&
+                             num_kb >= 2 * kMinKbPerSplit / (elem == 1 ? 4 : 1);
+    bool two_dsm = false;   // chose them: two K ranges below, whatever the work size
     if (cg == 0 && bn == 0) {
         if (max_clusters_2cta > 0 && tiles_of(2, 256) >= max_clusters_2cta) {
             cg = 2;
@@ -218,9 +225,33 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
             // re-read A is small and more, narrower tiles keep more SMs reading B.
             cg = 1;
             bn = (elem == 2 && M <= kStreamBMaxRows && K * N * elem >= kStreamBMinBytes) ? 128 : 256;
+            // 128-column tiles in two K ranges summed in cluster shared memory
+            // beat 256-column tiles whose ranges go through the workspace (3 or
+            // more of them), or that keep fewer CTAs busy.  Measured on GB300
+            // (alternating blocks, µs per call, 256-column plan -> this one):
+            // BF16 1024x1024x2048 15.1 -> 11.7, 512x2048x2048 15.1 -> 11.7,
+            // 768x1536x3072 16.5 -> 14.0, 256x4096x4096 17.7 -> 16.1; FP16 and
+            // TF32 alike; E4M3 512x2048x2048 11.3 -> 9.5 (twice the CTAs).  Not
+            // where it keeps fewer CTAs busy (256x2048x8192: 18.6 -> 24.0).
+            const int64_t t256 = tiles_of(1, 256);
+            const int64_t s256 = std::min<int64_t>({num_sms / t256, num_kb / kMinKbPerSplit, 16});
+            if (bn == 256 && two_dsm_fit && (s256 >= 3 ? 2 * t128 >= t256 * s256 : 2 * t128 > t256 * s256)) {
+                bn = 128;
+                two_dsm = true;
+            }
         } else if (tiles_of(1, 128) >= num_sms) {
             cg = 1;
             bn = 128;
+        } else if ((dtype == GEMM_TF32 || is_fp8(dtype)) && two_dsm_fit && 2 * t128 >= tiles_of(1, 64) &&
+                   K >= 1024) {
+            // TF32 and 8-bit inputs, too little work for the split above: two K
+            // ranges of 128-column tiles in cluster shared memory rather than
+            // 64-column tiles (for 8-bit inputs those also need B's K-major
+            // copy).  Measured on GB300: TF32 1024^3 12.9 -> 12.1 µs, E4M3 /
+            // E5M2 1024^3 10.3 -> 8.4; 16-bit inputs lose at that size.
+            cg = 1;
+            bn = 128;
+            two_dsm = true;
         } else {
             cg = 1;
             bn = 64;
@@ -259,7 +290,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, uint64_t a_addr, int64
         return (int)cdiv(num_kb, cdiv(num_kb, want));
     };
     int64_t tail = 0, half = 0;
-    if (splits == 0 && tiles * 2 <= units && M * N * K >= kMinSplitWork)
+    if (splits == 0 && two_dsm)
+        splits = 2;
+    else if (splits == 0 && tiles * 2 <= units && M * N * K >= kMinSplitWork)
         splits = (int)std::max<int64_t>(1, std::min<int64_t>({units / tiles, num_kb / kMinKbPerSplit, 16}));
     const int64_t rem = tiles > units ? tiles % units : 0;   // tiles of the last, partly idle round
     if (splits > 1) {
