@@ -85,22 +85,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-// 16-byte store into shared memory named by a shared::cluster address
-// (possibly another CTA's of the cluster).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// 16-byte asynchronous store into another CTA's shared memory (addr and bar
-// are shared::cluster addresses); its bytes count toward the transaction
-// count of the mbarrier `bar` in that CTA.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar) : "memory");
-}
-
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
 // another CTA's of the cluster (dst and bar are shared::cluster addresses);
 // its bytes count toward the transaction count of `bar` in that CTA.
@@ -163,11 +147,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
