@@ -87,6 +87,22 @@ def test_options_roundtrip_and_validation():
     assert tg.gemm_set_option("tc_sched", 3) == tg.GEMM_ERR_INVALID_ARG
 
 
+def test_every_documented_option_is_implemented_and_no_other():
+    """The option keys the header documents (each at the head of a line in
+    the gemm_set_option comment, plus "trace_records", described with
+    "trace_addr") are exactly the keys gemm_get_option answers and
+    gemm_api.cu reads."""
+    import re
+    header = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    documented = set(re.findall(r'^ \*   "([a-z_0-9]+)"', header, re.M)) | {"trace_records"}
+    api = open(os.path.join(ROOT, "tiled_tensor_core_gemm_gb300", "csrc", "gemm_api.cu")).read()
+    implemented = set(re.findall(r'if \(!std::strcmp\(key, "([a-z_0-9]+)"\)\) return o\.', api))
+    assert documented == implemented, (documented ^ implemented)
+    for key in documented:
+        assert tg.gemm_get_option(key) != -1, key
+    assert tg.gemm_get_option("tc_bn_x") == -1
+
+
 def test_plan_dynamic_schedule_launches_one_cluster_per_unit():
     try:
         assert tg.gemm_set_option("tc_sched", 2) == tg.GEMM_OK
