@@ -272,6 +272,48 @@ def test_plan_two_k_ranges_in_cluster_shared_memory(M, N, K, dt, bn, splits, clu
         tg.gemm_set_option("tc_splits", 0)
 
 
+def test_plan_two_k_ranges_with_one_owner():
+    """Two K ranges summed in cluster shared memory: of equal length unless
+    asked; on request (128-column tiles, C stored by TMA) the first range
+    takes that share of the k-blocks and its CTA owns the tile, and the
+    forced workspace path cuts K at the same k-block."""
+    p = _plan(128, 8192, 8192, tg.GEMM_BF16)
+    assert (p["cluster_split"], p["splits"], p["bn"], p["kb_split"]) == (2, 2, 128, 0), p
+    try:
+        tg.gemm_set_option("tc_split_lead", 56)
+        assert _plan(128, 8192, 8192, tg.GEMM_BF16)["kb_split"] == 72
+        assert _plan(128, 8192, 8256, tg.GEMM_BF16)["kb_split"] == 72          # 129 k-blocks
+        assert _plan(128, 8192, 8192, tg.GEMM_BF16, ldc=8195)["kb_split"] == 0  # C by ordinary stores
+        assert _plan(128, 8192, 8192, tg.GEMM_TF32)["kb_split"] == 143         # 256 k-blocks
+        assert _plan(1024, 2048, 8192, tg.GEMM_BF16)["kb_split"] == 0          # 256-column tiles
+        assert _plan(128, 4096, 16384, tg.GEMM_BF16)["kb_split"] == 0          # 4 ranges
+        assert _plan(8192, 8192, 8192, tg.GEMM_BF16)["kb_split"] == 0
+        for lead, kb in ((0, 0), (50, 0), (51, 65), (75, 96), (95, 122)):
+            assert tg.gemm_set_option("tc_split_lead", lead) == tg.GEMM_OK
+            assert _plan(128, 8192, 8192, tg.GEMM_BF16)["kb_split"] == kb, lead
+        tg.gemm_set_option("tc_split_lead", 56)
+        tg.gemm_set_option("tc_split_reduce", 1)
+        q = _plan(128, 8192, 8192, tg.GEMM_BF16)
+        assert q["cluster_split"] == 0 and q["kb_split"] == 72, q
+        for bad in (1, 49, 96, -1):
+            assert tg.gemm_set_option("tc_split_lead", bad) == tg.GEMM_ERR_INVALID_ARG
+    finally:
+        tg.gemm_set_option("tc_split_lead", 0)
+        tg.gemm_set_option("tc_split_reduce", 0)
+
+
+def test_plan_struct_layout_matches_the_header(tmp_path):
+    src = tmp_path / "plan.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\n'
+                   'int main(void) { printf("%zu %zu %zu\\n", sizeof(gemm_plan_t),'
+                   ' offsetof(gemm_plan_t, cluster_split), offsetof(gemm_plan_t, kb_split)); return 0; }\n')
+    exe = tmp_path / "plan"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = tg.GemmPlan
+    assert got == [ctypes.sizeof(P), P.cluster_split.offset, P.kb_split.offset]
+
+
 def test_plan_runs_the_last_round_as_column_halves():
     # 256 pair tiles over 76 pairs: 3 rounds and 28 tiles left, which as 56
     # halves fit one round; on by default for 16-bit inputs on short schedules
